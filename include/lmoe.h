@@ -1,0 +1,162 @@
+/*
+ * lmoe.h -- C ABI of liblmoe.so: the LatentMoE expert layer forward on one B300 (sm_103a).
+ *
+ * The layer (shengxinai.com Nemotron 3 blog, section 2.2 "LatentMoE：在潜空间中重构专家网络",
+ * steps 1-3; "Nemotron 3 Super" page, section "潜在MoE"):
+ *     z  = bf16(x Wd^T)                       down-projection d -> l (l = d/4), BF16
+ *     route x to the top-k of E experts       (NVIDIA AI releases Nemotron 3 Ultra: 512 / top-22)
+ *     per selected expert, in latent space:   u = zq W1q_e^T, h = bf16(relu(u)^2), o = hq W2q_e^T
+ *                                             (NVFP4 weights and activations)
+ *     c  = bf16(sum_j w_j o_j)                routing-weighted combine
+ *     y  = bf16(c Wu^T)                       up-projection l -> d, BF16
+ * NVFP4 (same blog, section 3.1.1): E2M1 elements, one E4M3 scale per 16 contiguous
+ * contraction-axis elements, one FP32 tensor scale.
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are DEVICE pointers unless the argument says "host".
+ *  - Matrices are row-major; weights follow y = x W^T (rows = output features), so every
+ *    operand is contiguous along its contraction axis.
+ *  - NVFP4 codes are packed two per byte, the even element in the low nibble; block scales
+ *    are E4M3 bytes, one per 16 elements along the contraction axis.
+ *  - Calls return a status and never abort, exit or throw.  Argument errors are detected on
+ *    the host before anything is launched.  Launched work is asynchronous on `stream`;
+ *    device-side errors (a bounded wait that ran out) latch into the context's error word and
+ *    are reported by lmoe_check() and by the next call on that context.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *  - The caller owns every buffer it passes; the context owns the quantized weights.
+ *  - A context must not run two forwards at once on overlapping workspaces.
+ */
+#ifndef LMOE_H
+#define LMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *lmoe_stream;   /* == cudaStream_t */
+
+typedef enum {
+    LMOE_OK = 0,
+    LMOE_EINVAL = 1,        /* bad argument (detected on the host, nothing launched)      */
+    LMOE_ENOMEM = 2,        /* device allocation failed, or workspace too small           */
+    LMOE_ECUDA = 3,         /* a CUDA runtime/driver call failed                          */
+    LMOE_EUNSUPPORTED = 4,  /* device is not sm_103a / sm_100-family, or shape unsupported */
+    LMOE_ETIMEOUT = 5,      /* a bounded device-side wait ran out (kernel returned early) */
+    LMOE_EDEVICE = 6        /* a device-side check failed (error word set)                */
+} lmoe_status;
+
+typedef enum { LMOE_BF16 = 0, LMOE_FP32 = 1 } lmoe_dtype;
+
+typedef struct lmoe_ctx lmoe_ctx;   /* opaque, owned by the library */
+
+/* Weights handed to lmoe_create.  All DEVICE pointers, caller-owned, read only during
+ * lmoe_create (the context keeps its own quantized / copied versions). */
+typedef struct {
+    const void  *w_down;    /* bf16 [l][d]        z = x w_down^T            (BF16, kept)      */
+    const void  *w_up;      /* bf16 [d][l]        y = c w_up^T              (BF16, kept)      */
+    const float *w_router;  /* fp32 [E][d]        logits = x w_router^T + b                   */
+    const float *b_router;  /* fp32 [E] or NULL   router bias (used for selection and weights)*/
+    const void  *w1;        /* bf16 [E][ffn][l]   latent-up expert masters, quantized at create */
+    const void  *w2;        /* bf16 [E][l][ffn]   latent-down expert masters, quantized at create */
+    float amax_z;           /* static amax of z (calibration); > 0                           */
+    float amax_h;           /* static amax of h (calibration); > 0                           */
+} lmoe_weights;
+
+/* Create a layer context: validates the dims, allocates the context buffers, quantizes every
+ * expert matrix to NVFP4 (one FP32 tensor scale per expert per matrix, computed from its amax)
+ * and lays the block scales out for the tensor cores; synchronizes `stream` once at the end.
+ * Dims: d, l and ffn multiples of 64; 1 <= k <= 32; k <= E <= 1024.
+ * (The Ultra layer: d = 8192, l = 2048, E = 512, k = 22; ffn is not given by the pages.)
+ * Errors: LMOE_EINVAL (dims / NULL pointers / amax <= 0), LMOE_ENOMEM, LMOE_ECUDA,
+ * LMOE_EUNSUPPORTED (device is not compute capability 10.3). */
+lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights *w,
+                        lmoe_stream stream, lmoe_ctx **out);
+
+/* NVFP4 quantization (blog section 3.1.1) of a row-major [rows][K] tensor along K.
+ *   src          device, bf16 or fp32 per `dt`
+ *   amax         tensor amax; < 0: computed on the device from src
+ *   codes        device uint8 [rows][K/2]    (even element in the low nibble)
+ *   sf           device uint8 [rows][K/16]   E4M3 block scales, row-major
+ *   tensor_scale device float [1]            the FP32 decode scale amax/2688 (1 if amax == 0)
+ * Arithmetic (fp32, round-to-nearest-even): s_enc = 2688/amax, s_dec = amax/2688;
+ * sf = e4m3_satfinite(amax_block * (s_enc/6)); q = e2m1_satfinite(x * (1/(value(sf)*s_dec))),
+ * q = +-0 where value(sf)*s_dec == 0.  K % 16 == 0, rows >= 0 (0 is a no-op). */
+lmoe_status lmoe_quantize_nvfp4(const void *src, lmoe_dtype dt, int64_t rows, int64_t K,
+                                float amax, uint8_t *codes, uint8_t *sf, float *tensor_scale,
+                                lmoe_stream stream);
+
+/* Routing alone (top-k of E per token, NVIDIA AI releases Nemotron 3 Ultra, architecture):
+ *   x       device bf16 [T][d]
+ *   idx     device int32 [T][k]  selected experts, ascending expert id per token
+ *   w       device float [T][k]  softmax over the k selected logits, same order as idx
+ *   counts  device int32 [E]     tokens per expert (may be NULL)
+ * Logits are computed in the canonical fp32 order (64-element fma chunks, chunk partials added
+ * left to right, then the bias), so idx and counts are exact.  Uses context-owned scratch
+ * (grown with cudaMallocAsync on first use for a larger T).  T >= 0. */
+lmoe_status lmoe_route(lmoe_ctx *ctx, const void *x, int64_t T, int32_t *idx, float *w,
+                       int32_t *counts, lmoe_stream stream);
+
+/* Bytes of device workspace lmoe_forward needs for T tokens (256-byte aligned pointer). */
+size_t lmoe_workspace_size(const lmoe_ctx *ctx, int64_t T);
+
+/* The layer forward: x device bf16 [T][d] -> y device bf16 [T][d].  No host synchronization
+ * and no host read of device data; every launch is on `stream`, so the call can be captured
+ * in a CUDA graph.  ws: device workspace of at least lmoe_workspace_size(ctx, T) bytes.
+ * Errors: LMOE_EINVAL (NULL / T < 0), LMOE_ENOMEM (ws_bytes too small), LMOE_ECUDA. */
+lmoe_status lmoe_forward(lmoe_ctx *ctx, const void *x, int64_t T, void *y, void *ws,
+                         size_t ws_bytes, lmoe_stream stream);
+
+/* Bytes of device workspace lmoe_forward_host needs (lmoe_workspace_size + x and y staging). */
+size_t lmoe_host_workspace_size(const lmoe_ctx *ctx, int64_t T);
+
+/* The forward from and to HOST memory: copies x_host (bf16 [T][d], pinned for best speed) to
+ * the device, runs lmoe_forward, copies y back to y_host and synchronizes `stream`. */
+lmoe_status lmoe_forward_host(lmoe_ctx *ctx, const void *x_host, int64_t T, void *y_host,
+                              void *ws, size_t ws_bytes, lmoe_stream stream);
+
+/* Intermediates of the last lmoe_forward, as byte ranges of its workspace (for parity checks).
+ * Stage ids: see lmoe_stage.  Returns LMOE_EINVAL for an unknown stage. */
+typedef enum {
+    LMOE_STAGE_IDX = 0,      /* int32 [T][k]                                           */
+    LMOE_STAGE_W = 1,        /* float [T][k]                                           */
+    LMOE_STAGE_COUNTS = 2,   /* int32 [E]                                              */
+    LMOE_STAGE_ZQ_CODES = 3, /* uint8 [T][l/2]                                         */
+    LMOE_STAGE_ZQ_SF = 4,    /* uint8 [T][l/16]   row-major E4M3                       */
+    LMOE_STAGE_C = 5,        /* bf16  [T][l]      combine output                       */
+    LMOE_STAGE_Z = 6,        /* bf16  [T][l]      debug mode only                       */
+    LMOE_STAGE_ROWS = 7,     /* int32 [R] slot (token*k + j) of each permuted row, -1 = pad */
+    LMOE_STAGE_H = 8,        /* bf16  [R][ffn]    debug mode only, permuted rows        */
+    LMOE_STAGE_HQ_CODES = 9, /* uint8 [R][ffn/2]  permuted rows                         */
+    LMOE_STAGE_HQ_SF = 10,   /* uint8 [R/128][ffn/64][512] tensor-core scale atoms      */
+    LMOE_STAGE_NROWS = 11    /* int32 [1]         R actually used                       */
+} lmoe_stage;
+lmoe_status lmoe_workspace_range(const lmoe_ctx *ctx, int64_t T, int stage, size_t *offset,
+                                 size_t *bytes);
+
+/* Debug mode (0/1): when on, lmoe_forward also writes z and h (bf16) into its workspace,
+ * which then needs lmoe_workspace_size() bytes computed after this call. */
+lmoe_status lmoe_set_debug(lmoe_ctx *ctx, int on);
+
+/* Copy expert e's quantized matrix (which = 1: W1 [ffn][l], which = 2: W2 [l][ffn]) out of the
+ * context in the canonical layout: codes device uint8 [N][K/2], sf device uint8 [N][K/16]
+ * row-major, *s_dec (host) its FP32 tensor scale.  Synchronizes `stream`. */
+lmoe_status lmoe_get_expert_nvfp4(const lmoe_ctx *ctx, int which, int e, uint8_t *codes,
+                                  uint8_t *sf, float *s_dec, lmoe_stream stream);
+
+/* Synchronize `stream` and report (and clear) the context's device error word. */
+lmoe_status lmoe_check(lmoe_ctx *ctx, lmoe_stream stream);
+
+/* Static description of a status code. */
+const char *lmoe_status_string(lmoe_status s);
+
+/* Free the context (synchronizes the device once).  NULL is a no-op. */
+void lmoe_destroy(lmoe_ctx *ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

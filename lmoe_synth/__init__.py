@@ -1,0 +1,127 @@
+"""Seeded synthetic inputs for the LatentMoE expert layer.
+
+This module only draws random numbers; it holds none of the layer's arithmetic.  Both the
+CPU oracle (through the tests) and the CUDA library receive the very same tensors from it.
+
+Recipe (every tensor from its own torch Philox / CPU generator stream, seeded from the
+config seed and a fixed tag, so any one expert can be regenerated alone):
+  x         [T][d]          ~ N(0, 1)            rounded to bf16
+  w_down    [l][d]          ~ N(0, 1/d)          rounded to bf16    (z = x w_down^T)
+  w_up      [d][l]          ~ N(0, 1/l)          rounded to bf16    (y = c w_up^T)
+  w_router  [E][d]          ~ N(0, 1/d)          fp32
+  b_router  [E]             0 ("uniform") or Zipf: b[pi(r)] = -s ln r, r = 1..E, pi a seeded
+                            permutation (so expert popularity follows a Zipf(s) law)
+  w1[e]     [ffn][l]        ~ N(0, 1/l)          rounded to bf16    (u = zq w1_e^T)
+  w2[e]     [l][ffn]        ~ N(0, 1/ffn)        rounded to bf16    (o = hq w2_e^T)
+  x_cal     [T_cal][d]      ~ N(0, 1) bf16, seed + 1: the calibration batch
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Dims:
+    d: int
+    l: int
+    E: int
+    k: int
+    ffn: int
+
+
+TINY = Dims(d=256, l=64, E=16, k=4, ffn=128)
+ULTRA = Dims(d=8192, l=2048, E=512, k=22, ffn=2048)
+
+_TAG = {"x": 1, "w_down": 2, "w_up": 3, "w_router": 4, "perm": 5, "w1": 1000, "w2": 2000000,
+        "x_cal": 7}
+
+
+def _gen(device, seed: int, tag: int) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed((seed * 1_000_003 + tag) % (2 ** 63))
+    return g
+
+
+def _normal(shape, std, device, seed, tag, dtype):
+    g = _gen(device, seed, tag)
+    t = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    return t.to(dtype)
+
+
+def tokens(T: int, d: int, seed: int, device="cpu", tag: str = "x") -> torch.Tensor:
+    """x ~ N(0,1) as bf16 [T][d]."""
+    return _normal((T, d), 1.0, device, seed, _TAG[tag], torch.bfloat16)
+
+
+def projections(dims: Dims, seed: int, device="cpu"):
+    wd = _normal((dims.l, dims.d), 1.0 / math.sqrt(dims.d), device, seed, _TAG["w_down"],
+                 torch.bfloat16)
+    wu = _normal((dims.d, dims.l), 1.0 / math.sqrt(dims.l), device, seed, _TAG["w_up"],
+                 torch.bfloat16)
+    return wd, wu
+
+
+def router(dims: Dims, seed: int, device="cpu", zipf_s: float = 0.0):
+    wr = _normal((dims.E, dims.d), 1.0 / math.sqrt(dims.d), device, seed, _TAG["w_router"],
+                 torch.float32)
+    if zipf_s <= 0.0:
+        b = torch.zeros(dims.E, dtype=torch.float32, device=device)
+    else:
+        g = _gen("cpu", seed, _TAG["perm"])
+        perm = torch.randperm(dims.E, generator=g)
+        r = torch.arange(1, dims.E + 1, dtype=torch.float64)
+        b = torch.empty(dims.E, dtype=torch.float64)
+        b[perm] = -zipf_s * torch.log(r)
+        b = b.to(torch.float32).to(device)
+    return wr, b
+
+
+def expert(dims: Dims, seed: int, e: int, device="cpu"):
+    """(w1_e [ffn][l], w2_e [l][ffn]) bf16 for expert e."""
+    w1 = _normal((dims.ffn, dims.l), 1.0 / math.sqrt(dims.l), device, seed, _TAG["w1"] + e,
+                 torch.bfloat16)
+    w2 = _normal((dims.l, dims.ffn), 1.0 / math.sqrt(dims.ffn), device, seed, _TAG["w2"] + e,
+                 torch.bfloat16)
+    return w1, w2
+
+
+def experts(dims: Dims, seed: int, device="cpu"):
+    """All experts stacked: (w1 [E][ffn][l], w2 [E][l][ffn]) bf16."""
+    w1 = torch.empty((dims.E, dims.ffn, dims.l), dtype=torch.bfloat16, device=device)
+    w2 = torch.empty((dims.E, dims.l, dims.ffn), dtype=torch.bfloat16, device=device)
+    for e in range(dims.E):
+        a, b = expert(dims, seed, e, device)
+        w1[e].copy_(a)
+        w2[e].copy_(b)
+    return w1, w2
+
+
+@dataclasses.dataclass
+class Layer:
+    """All inputs of one layer instance (tensors on `device`)."""
+    dims: Dims
+    seed: int
+    zipf_s: float
+    w_down: torch.Tensor
+    w_up: torch.Tensor
+    w_router: torch.Tensor
+    b_router: torch.Tensor
+    w1: torch.Tensor
+    w2: torch.Tensor
+
+
+def layer(dims: Dims, seed: int, device="cpu", zipf_s: float = 0.0) -> Layer:
+    wd, wu = projections(dims, seed, device)
+    wr, b = router(dims, seed, device, zipf_s)
+    w1, w2 = experts(dims, seed, device)
+    return Layer(dims, seed, zipf_s, wd, wu, wr, b, w1, w2)
+
+
+def calibration_tokens(T: int, d: int, seed: int, device="cpu") -> torch.Tensor:
+    """The calibration batch: N(0,1) bf16 tokens drawn with seed + 1."""
+    return tokens(T, d, seed + 1, device, tag="x_cal")

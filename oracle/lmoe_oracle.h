@@ -1,0 +1,112 @@
+/*
+ * lmoe_oracle.h -- plain, slow CPU oracle for the LatentMoE expert layer forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU-baseline
+ * leg of the benchmark may load or call this library.  It shares no code, header,
+ * table or helper with the CUDA library under nvfp4_latentmoe_fwd_02_b300/csrc.
+ *
+ * Every function states the passage it follows.  Page names used below:
+ *   [BLOG]  shengxinai.com blog on Nemotron 3 ("Nemotron 3 不止是模型 ... 可复现的工业级蓝图"),
+ *           section 2.2 "LatentMoE：在潜空间中重构专家网络" and section 3.1.1 "NVFP4 格式解析",
+ *           section 3.1.3 mixed-precision table (latent projections kept in BF16).
+ *   [NEWS]  "NVIDIA AI釋出Nemotron 3 Ultra：一個開放的550B混合專家混合Mamba-Transformer..."
+ *           (architecture paragraph: d = 8192, 512 experts, top-22; quantization paragraph:
+ *           native FP4 math on Blackwell).
+ *   [CARD]  "nvidia/NVIDIA-Nemotron-3-Ultra-550B-A55B-NVFP4 · Hugging Face", Description.
+ *   [SUPER] "Nemotron 3 Super：面向智能体推理的混合Mamba-Transformer MoE模型", section "潜在MoE".
+ *   [HEIDI] "Heidi 在 Fireworks 上训练并部署 NVIDIA Nemotron 3 Ultra", NVFP4 quantization paragraph
+ *           (post-training quantization calibrated on synthetic prompts).
+ *
+ * Parity status: every function here is pinned by a CPU test (see tests/test_oracle_*.py)
+ * except the composition of the whole quantized layer, which is pinned only through its
+ * parts and through the special cases (l = d identity projections -> standard MoE;
+ * E = k = 1 -> plain squared-ReLU FFN) in unquantized mode: "parity unpinned" for the
+ * end-to-end quantized composition beyond those pins; the pages print no worked example.
+ */
+#ifndef LMOE_ORACLE_H
+#define LMOE_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- number formats ([BLOG] 3.1.1: E2M1 elements, E4M3 block scale) ---- */
+double  oracle_e2m1_value(uint8_t code);       /* low 4 bits used; bit 3 = sign            */
+double  oracle_e4m3_value(uint8_t code);       /* NaN for 0x7F / 0xFF                      */
+uint8_t oracle_f32_to_e2m1(float v);           /* round-to-nearest-even, saturate to +-6   */
+uint8_t oracle_f32_to_e4m3(float v);           /* round-to-nearest-even, saturate to +-448 */
+double  oracle_round_bf16(double v);           /* round-to-nearest-even to bfloat16        */
+void    oracle_f32_to_e2m1_array(const float *v, int64_t n, uint8_t *out, int nthreads);
+void    oracle_f32_to_e4m3_array(const float *v, int64_t n, uint8_t *out, int nthreads);
+
+/* NVFP4 quantization of a row-major [R][K] fp32 array along K (16-element blocks).
+ * amax < 0: the tensor amax is computed from src.  codes: [R][K/2] (even element in
+ * the low nibble), sf: [R][K/16] E4M3 bytes, *s_dec: the FP32 tensor (decode) scale.
+ * nthreads <= 0: all host cores. */
+void oracle_quantize_nvfp4(const float *src, int64_t R, int64_t K, float amax,
+                           uint8_t *codes, uint8_t *sf, float *s_dec, int nthreads);
+
+/* Exact NVFP4 x NVFP4 dot product over K elements (K % 16 == 0), block scales applied,
+ * tensor scales NOT applied. */
+double oracle_nvfp4_dot(const uint8_t *qa, const uint8_t *sfa,
+                        const uint8_t *qb, const uint8_t *sfb, int64_t K);
+
+/* Router: canonical fp32 logits, top-k by (logit desc, index asc), softmax over the
+ * k selected logits (fp64, rounded to float).  x: [T][d] values, Wr: [E][d], b: [E] or NULL.
+ * idx/w: [T][k] in ascending expert id; logits [T][E] and counts [E] optional. */
+void oracle_router(const float *x, int64_t T, int d, const float *Wr, const float *b,
+                   int E, int k, float *logits, int32_t *idx, float *w, int32_t *counts,
+                   int nthreads);
+
+/* The layer. Weight layouts follow y = x * W^T (rows = output features). */
+typedef struct {
+    int d, l, E, k, ffn;
+    const float *w_down;    /* [l][d]  bf16 values                                  */
+    const float *w_up;      /* [d][l]  bf16 values                                  */
+    const float *w_router;  /* [E][d]  fp32                                         */
+    const float *b_router;  /* [E] or NULL                                          */
+    /* quantized experts (quant mode); per-expert pointers, NULL = not available     */
+    const uint8_t *const *w1_codes; /* [E] -> [ffn][l/2]   */
+    const uint8_t *const *w1_sf;    /* [E] -> [ffn][l/16]  */
+    const float *w1_sdec;           /* [E]                  */
+    const uint8_t *const *w2_codes; /* [E] -> [l][ffn/2]   */
+    const uint8_t *const *w2_sf;    /* [E] -> [l][ffn/16]  */
+    const float *w2_sdec;           /* [E]                  */
+    /* master experts (unquantized mode); per-expert pointers                         */
+    const float *const *w1;         /* [E] -> [ffn][l]     */
+    const float *const *w2;         /* [E] -> [l][ffn]     */
+    float amax_z, amax_h;           /* static activation amax (calibration)          */
+} oracle_layer;
+
+typedef struct {               /* every pointer optional (NULL = not wanted)          */
+    float   *z;        /* [T][l]            bf16 values (quant) / fp64 rounded to float (unquant) */
+    uint8_t *zq_codes; /* [T][l/2]          */
+    uint8_t *zq_sf;    /* [T][l/16]         */
+    float   *logits;   /* [T][E]            */
+    int32_t *idx;      /* [T][k]            */
+    float   *w;        /* [T][k]            */
+    int32_t *counts;   /* [E]               */
+    float   *h;        /* [T][k][ffn]       bf16 values, slots in ascending expert id */
+    uint8_t *hq_codes; /* [T][k][ffn/2]     */
+    uint8_t *hq_sf;    /* [T][k][ffn/16]    */
+    double  *c64;      /* [T][l]            combine before rounding */
+    float   *c;        /* [T][l]            bf16 values              */
+    double  *y64;      /* [T][d]            before the final rounding */
+    float   *y;        /* [T][d]            bf16 values              */
+} oracle_out;
+
+/* quant = 1: the NVFP4 layer.  quant = 0: the same layer in plain fp64 with the master
+ * weights and no rounding of any intermediate (used by the structural pins).
+ * Returns 0, or -1 if an expert that a token selects has no weights. */
+int oracle_layer_forward(const oracle_layer *L, const float *x, int64_t T, int quant,
+                         oracle_out *out, int nthreads);
+
+/* Static activation calibration ([HEIDI]): amax of z and of h over a calibration batch. */
+int oracle_calibrate(const oracle_layer *L, const float *x, int64_t T,
+                     float *amax_z, float *amax_h, int nthreads);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
