@@ -1,0 +1,370 @@
+// gemm.cuh -- the tensor-core GEMMs of the layer (tcgen05, TMEM accumulators, TMA operands).
+//
+// One persistent, warp-specialized kernel template serves
+//   * the BF16 latent projections d -> l and l -> d (kind::f16, fp32 accumulate) -- the
+//     projections stay in BF16 (shengxinai.com Nemotron 3 blog, section 3.1.3 table), and
+//   * the NVFP4 expert GEMMs latent-up and latent-down (kind::mxf4nvf4.block_scale with
+//     UE4M3 scales, one per 16 K, E2M1 operands; blog section 3.1.1), grouped per expert.
+// D[m][n] = sum_k A[m][k] * B[n][k]: A = activations (rows = tokens), B = weights (rows = output
+// features); both K-major.  Tile 128 x 128, one SW128 row of 128 bytes per operand per stage
+// (64 bf16 or 256 e2m1 elements of K).
+//
+// Warp roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer (one elected lane): operand tiles + scale atoms -> smem ring
+//   warp 1      TMEM allocator and MMA issuer (one lane): scale atoms smem -> TMEM with
+//               tcgen05.cp, tcgen05.mma into one of two 128-column accumulators
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads lane quadrant w % 4),
+//               fused output transform, global stores / reductions
+// Barriers: full/empty per smem stage, tmem_full/tmem_empty per accumulator.  Every wait is
+// bounded (common.cuh); on a timeout the CTA records LMOE_ETIMEOUT, the roles leave their
+// loops, outstanding tensor-core work is drained with a bounded wait and TMEM is freed.
+#pragma once
+#include "common.cuh"
+#include "nvfp4.cuh"
+
+namespace lmoe {
+
+enum EpiMode : int {
+    EPI_STORE_BF16 = 0,   // out bf16 [M][ld] = acc
+    EPI_RED_F32 = 1,      // out fp32 [M][ld] += acc (split-K partial)
+    EPI_Z_QUANT = 2,      // z = bf16(acc); zq = NVFP4(z) row-major; dbg = z
+    EPI_H_QUANT = 3,      // h = bf16(relu(alpha_e acc)^2); hq = NVFP4(h) (scale atoms); dbg = h
+    EPI_COMBINE = 4       // c_acc[token] += w_slot * alpha_e * acc
+};
+
+constexpr int kBM = 128, kBN = 128;
+constexpr int kTileBytes = kBM * 128;     // 16 KB per operand per stage
+constexpr int kSfStageBytes = 4 * 512;    // 4 scale atoms (4 x K64) per operand per stage
+
+struct GemmArgs {
+    int M, N, K;                 // dense: rows of A, rows of B (= output cols), depth (elements)
+    int m_tiles, n_tiles, k_tiles, k_splits, kt_per_split;
+    int grouped, E;              // grouped: per-expert segments from the device tables
+    const int32_t *mt_start;     // [E+1] prefix of M tiles
+    const int32_t *seg_start;    // [E+1] first row of each expert's segment (multiple of 128)
+    const int32_t *counts;       // [E]
+    const uint8_t *sfa;          // activation scale atoms [rows/128][K/64][512]
+    const uint8_t *sfb;          // weight scale atoms [E][NB][K/64][512]
+    int NB;                      // ceil(N / 128)
+    int epi;
+    void *out;                   // see EpiMode
+    int64_t ld_out;
+    QScale q;                    // quantizer of z or h
+    uint8_t *q_codes;            // [rows][N/2]
+    uint8_t *q_sf;               // z: [rows][N/16] row-major; h: atoms [rows/128][N/64][512]
+    __nv_bfloat16 *dbg;          // optional bf16 copy of z or h, [rows][N]
+    const float *alpha;          // [E] per-expert tensor-scale product
+    const int32_t *row_slot;     // [rows] routing slot of a permuted row (combine)
+    const float *route_w;        // [T*k]
+    int topk;
+    unsigned *err;
+};
+
+struct Tile {
+    int e, a_row0, rows, b_row0, n0, cols, kt0, kt1;
+};
+
+__device__ __forceinline__ Tile decode_tile(const GemmArgs &g, int t) {
+    Tile tl;
+    if (g.grouped) {
+        const int key = t / g.n_tiles;
+        int lo = 0, hi = g.E - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(g.mt_start + mid) <= key) lo = mid; else hi = mid - 1;
+        }
+        const int e = lo;
+        const int mt0 = __ldg(g.mt_start + e);
+        const int mt_e = __ldg(g.mt_start + e + 1) - mt0;
+        const int local = t - mt0 * g.n_tiles;
+        const int m = local % mt_e, n = local / mt_e;
+        tl.e = e;
+        tl.a_row0 = __ldg(g.seg_start + e) + m * kBM;
+        tl.rows = min(kBM, __ldg(g.counts + e) - m * kBM);
+        tl.n0 = n * kBN;
+        tl.b_row0 = e * g.N + n * kBN;
+        tl.cols = min(kBN, g.N - n * kBN);
+        tl.kt0 = 0;
+        tl.kt1 = g.k_tiles;
+    } else {
+        const int m = t % g.m_tiles;
+        const int r = t / g.m_tiles;
+        const int n = r % g.n_tiles, s = r / g.n_tiles;
+        tl.e = 0;
+        tl.a_row0 = m * kBM;
+        tl.rows = min(kBM, g.M - m * kBM);
+        tl.n0 = n * kBN;
+        tl.b_row0 = n * kBN;
+        tl.cols = min(kBN, g.N - n * kBN);
+        tl.kt0 = s * g.kt_per_split;
+        tl.kt1 = min(g.k_tiles, tl.kt0 + g.kt_per_split);
+    }
+    return tl;
+}
+
+// Wait that also gives up when another role of the CTA has aborted.
+__device__ __forceinline__ bool role_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          unsigned *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitLimitCycles) {
+            *abort = 1;
+            raise_error(err, kErrTimeout);
+            return false;
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// epilogue: one thread owns one accumulator row; 32 columns per call
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ void epilogue_chunk(const GemmArgs &g, const Tile &tl, int row,
+                                               int c0, const uint32_t (&r)[32]) {
+    if (row >= tl.rows) return;
+    const int64_t grow = static_cast<int64_t>(tl.a_row0) + row;   // global row of A / output
+    const int col = tl.n0 + c0;                                    // output column
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    switch (g.epi) {
+    case EPI_STORE_BF16: {
+        uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(g.out) + grow * g.ld_out + col);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                              pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+        break;
+    }
+    case EPI_RED_F32: {
+        float *o = static_cast<float *>(g.out) + grow * g.ld_out + col;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) red_add_v4_f32(o + 4 * i, v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        break;
+    }
+    case EPI_Z_QUANT:
+    case EPI_H_QUANT: {
+        if (g.epi == EPI_H_QUANT) {
+            const float a = __ldg(g.alpha + tl.e);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float u = fmaxf(__fmul_rn(a, v[i]), 0.0f);
+                v[i] = __fmul_rn(u, u);
+            }
+        }
+        uint32_t hb[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            hb[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+            v[2 * i] = __uint_as_float(hb[i] << 16);
+            v[2 * i + 1] = __uint_as_float(hb[i] & 0xFFFF0000u);
+        }
+        if (g.dbg) {
+            uint4 *o = reinterpret_cast<uint4 *>(g.dbg + grow * g.N + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[i] = make_uint4(hb[4 * i], hb[4 * i + 1], hb[4 * i + 2], hb[4 * i + 3]);
+        }
+        uint32_t w[4], s[2];
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[i] = v[16 * b + i];
+            s[b] = quant_block16(x, g.q, w[2 * b], w[2 * b + 1]);
+        }
+        *reinterpret_cast<uint4 *>(g.q_codes + grow * (g.N / 2) + col / 2) = make_uint4(w[0], w[1], w[2], w[3]);
+        const uint16_t s2 = static_cast<uint16_t>(s[0] | (s[1] << 8));
+        if (g.epi == EPI_Z_QUANT)
+            *reinterpret_cast<uint16_t *>(g.q_sf + grow * (g.N / 16) + col / 16) = s2;
+        else
+            *reinterpret_cast<uint16_t *>(g.q_sf + sf_atom_offset(grow, col / 16, g.N / 64)) = s2;
+        break;
+    }
+    case EPI_COMBINE: {
+        const int slot = __ldg(g.row_slot + grow);
+        if (slot < 0) break;
+        const int64_t t = slot / g.topk;
+        const float ws = __ldg(g.route_w + slot);
+        const float a = __ldg(g.alpha + tl.e);
+        float *o = static_cast<float *>(g.out) + t * g.ld_out + col;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            red_add_v4_f32(o + 4 * i, __fmul_rn(ws, __fmul_rn(a, v[4 * i])),
+                           __fmul_rn(ws, __fmul_rn(a, v[4 * i + 1])),
+                           __fmul_rn(ws, __fmul_rn(a, v[4 * i + 2])),
+                           __fmul_rn(ws, __fmul_rn(a, v[4 * i + 3])));
+        break;
+    }
+    default: break;
+    }
+}
+
+template <bool NVF4>
+constexpr int gemm_smem_bytes(int stages) {
+    return 1024 + stages * (2 * kTileBytes + (NVF4 ? 2 * kSfStageBytes : 0)) + 256;
+}
+
+template <bool NVF4, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmArgs g) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = sA + STAGES * kTileBytes;
+    uint8_t *sSFA = sB + STAGES * kTileBytes;
+    uint8_t *sSFB = sSFA + (NVF4 ? STAGES * kSfStageBytes : 0);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sSFB + (NVF4 ? STAGES * kSfStageBytes : 0));
+    uint64_t *full = bars, *empty = bars + STAGES;
+    uint64_t *tfull = bars + 2 * STAGES, *tempty = tfull + 2, *drain = tempty + 2;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
+
+    constexpr uint32_t kAccCols = kBN;
+    constexpr uint32_t kTmemCols = NVF4 ? 512 : 256;
+    constexpr uint32_t kSfCol0 = 2 * kAccCols;
+    static_assert(!NVF4 || kSfCol0 + STAGES * 32 <= 512, "TMEM budget");
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4); }
+        mbar_init(drain, 1);
+        *s_abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) { prefetch_tmap(&tmA); prefetch_tmap(&tmB); }
+    if (warp == 1) { tmem_alloc(s_tmem, kTmemCols); tmem_relinquish(); }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+
+    const int num_tiles = g.grouped ? __ldg(g.mt_start + g.E) * g.n_tiles
+                                    : g.m_tiles * g.n_tiles * g.k_splits;
+    const int K64 = g.K / 64;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued = 0, issued_phase = 0;   // per stage: ever issued / phase of last issue
+            for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x) {
+                const Tile tl = decode_tile(g, t);
+                for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
+                    if (!role_wait(&empty[stage], phase ^ 1, s_abort, g.err)) break;
+                    const int nsteps = NVF4 ? min(4, K64 - 4 * kt) : 4;
+                    const uint32_t bytes = 2 * kTileBytes + (NVF4 ? 2 * nsteps * 512 : 0);
+                    mbar_arrive_expect_tx(&full[stage], bytes);
+                    const int kx = NVF4 ? kt * 128 : kt * 64;
+                    tma_load_2d(sA + stage * kTileBytes, &tmA, &full[stage], kx, tl.a_row0);
+                    tma_load_2d(sB + stage * kTileBytes, &tmB, &full[stage], kx, tl.b_row0);
+                    if (NVF4) {
+                        bulk_load(sSFA + stage * kSfStageBytes,
+                                  g.sfa + (static_cast<size_t>(tl.a_row0 >> 7) * K64 + 4 * kt) * 512,
+                                  nsteps * 512, &full[stage]);
+                        bulk_load(sSFB + stage * kSfStageBytes,
+                                  g.sfb + ((static_cast<size_t>(tl.e) * g.NB + (tl.n0 >> 7)) * K64 + 4 * kt) * 512,
+                                  nsteps * 512, &full[stage]);
+                    }
+                    issued |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (*s_abort) {
+                // the last load issued to each stage has landed before the CTA leaves (bounded)
+                for (int s = 0; s < STAGES; ++s) {
+                    if (!((issued >> s) & 1u)) continue;
+                    const uint32_t p = (issued_phase >> s) & 1u;
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(&full[s], p) && clock64() - t0 < kWaitLimitCycles / 8) {}
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = NVF4 ? idesc_nvf4(kBM, kBN) : idesc_bf16(kBM, kBN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x, ++it) {
+                const Tile tl = decode_tile(g, t);
+                const int acc = it & 1;
+                const uint32_t aphase = (it >> 1) & 1;
+                if (!role_wait(&tempty[acc], aphase ^ 1, s_abort, g.err)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + acc * kAccCols;
+                bool ok = true;
+                for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
+                    if (!role_wait(&full[stage], phase, s_abort, g.err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(sA + stage * kTileBytes);
+                    const uint32_t b_base = smem_u32(sB + stage * kTileBytes);
+                    if constexpr (NVF4) {
+                        const int nsteps = min(4, K64 - 4 * kt);
+                        const uint32_t sf_t = tmem + kSfCol0 + stage * 32;
+                        for (int kk = 0; kk < nsteps; ++kk) {
+                            tmem_cp_sf(sf_t + kk * 4, sdesc_sf(smem_u32(sSFA + stage * kSfStageBytes + kk * 512)));
+                            tmem_cp_sf(sf_t + 16 + kk * 4, sdesc_sf(smem_u32(sSFB + stage * kSfStageBytes + kk * 512)));
+                        }
+                        for (int kk = 0; kk < nsteps; ++kk)
+                            mma_nvf4(d_tmem, sdesc_sw128(a_base + kk * 32), sdesc_sw128(b_base + kk * 32),
+                                     idesc, sf_t + kk * 4, sf_t + 16 + kk * 4,
+                                     (kt > tl.kt0 || kk > 0) ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16(d_tmem, sdesc_sw128(a_base + kk * 32), sdesc_sw128(b_base + kk * 32),
+                                     idesc, (kt > tl.kt0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&empty[stage]);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit(&tfull[acc]);
+            }
+            // all tensor-core work of this CTA is complete before TMEM is released
+            mma_commit(drain);
+            const long long t0 = clock64();
+            while (!mbar_try_wait(drain, 0) && clock64() - t0 < kWaitLimitCycles) {}
+        }
+    } else {
+        // ---------------------------------------------------------------- epilogue
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        int it = 0;
+        for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x, ++it) {
+            const Tile tl = decode_tile(g, t);
+            const int acc = it & 1;
+            const uint32_t aphase = (it >> 1) & 1;
+            if (!role_wait(&tfull[acc], aphase, s_abort, g.err)) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem + acc * kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
+#pragma unroll 1
+            for (int ch = 0; ch < kBN / 32; ++ch) {
+                if (ch * 32 >= tl.cols) break;
+                uint32_t r[32];
+                tmem_ld32(taddr + ch * 32, r);
+                tmem_wait_ld();
+                epilogue_chunk(g, tl, row, ch * 32, r);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace lmoe

@@ -1,0 +1,641 @@
+// lmoe_api.cu -- host side of liblmoe.so: the C ABI declared in include/lmoe.h.
+//
+// The LatentMoE expert layer forward (shengxinai.com Nemotron 3 blog, section 2.2, steps 1-3):
+// down-projection d -> l, routing on x, NVFP4 latent experts, weighted combine, up-projection.
+// The host code validates arguments, lays out the workspace, encodes TMA descriptors and
+// launches the kernels of this directory on the caller's stream; it never synchronizes or
+// reads device memory inside lmoe_forward.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "../../include/lmoe.h"
+#include "common.cuh"
+#include "gemm.cuh"
+#include "moe.cuh"
+#include "nvfp4.cuh"
+#include "router.cuh"
+
+using namespace lmoe;
+
+namespace {
+
+constexpr int kStagesF4 = 5;
+constexpr int kStagesBF16 = 6;
+constexpr int kPartialsMaxT = 64;   // router: chunk-partials kernel up to this many tokens
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D K-major operand: `inner` elements per row (contiguous), `rows` rows, row pitch in bytes.
+// Box: one 128-byte swizzle row by 128 rows.
+bool make_map(CUtensorMap *m, bool bf16, const void *ptr, uint64_t inner, uint64_t rows,
+              uint64_t pitch_bytes) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {pitch_bytes};
+    cuuint32_t box[2] = {bf16 ? 64u : 128u, 128u};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                    const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct WsLayout {
+    size_t idx, w, counts, seg, mt, fill, nrows, row_slot, router, zacc, zq_codes, zq_sf, z_dbg,
+        a_codes, a_sf, h_codes, h_sf, h_dbg, c_acc, c, yacc, total;
+    int64_t R;   // row capacity of the permuted buffers (multiple of 128)
+    bool partials, split_down, split_up;
+    int down_splits, up_splits;
+};
+
+}  // namespace
+
+struct lmoe_ctx {
+    int d, l, E, k, ffn;
+    int dev, num_sms;
+    __nv_bfloat16 *w_down, *w_up;
+    float *w_router, *b_router;
+    uint8_t *w1_codes, *w1_sf, *w2_codes, *w2_sf;
+    float *w1_sdec, *w2_sdec, *alpha1, *alpha2;
+    unsigned *amax_bits;   // [2E]
+    float amax_z, amax_h;
+    QScale qz, qh;
+    CUtensorMap tm_wd, tm_wu, tm_w1, tm_w2;
+    unsigned *err;
+    int debug;
+    void *route_ws;
+    size_t route_ws_bytes;
+};
+
+namespace {
+
+lmoe_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return LMOE_OK;
+    if (e == cudaErrorMemoryAllocation) return LMOE_ENOMEM;
+    return LMOE_ECUDA;
+}
+#define LMOE_CUDA(call)                                         \
+    do {                                                        \
+        cudaError_t e_ = (call);                                \
+        if (e_ != cudaSuccess) return cuda_status(e_);          \
+    } while (0)
+#define LMOE_LAUNCH()                                           \
+    do {                                                        \
+        cudaError_t e_ = cudaGetLastError();                    \
+        if (e_ != cudaSuccess) return cuda_status(e_);          \
+    } while (0)
+
+// Split-K plan for a dense projection: spread small-M problems over the SMs.
+int plan_splits(int m_tiles, int n_tiles, int k_tiles, int num_sms) {
+    const int tiles = m_tiles * n_tiles;
+    if (tiles * 2 > num_sms) return 1;
+    int s = std::max(1, num_sms / tiles);
+    s = std::min(s, k_tiles);
+    const int per = static_cast<int>(cdiv(k_tiles, s));
+    return static_cast<int>(cdiv(k_tiles, per));
+}
+
+WsLayout layout(const lmoe_ctx *c, int64_t T) {
+    WsLayout L;
+    std::memset(&L, 0, sizeof(L));
+    const int64_t d = c->d, l = c->l, E = c->E, k = c->k, F = c->ffn;
+    L.R = cdiv(T * k + E * 127, 128) * 128;
+    if (L.R == 0) L.R = 128;
+    L.partials = T <= kPartialsMaxT;
+    const int mt = static_cast<int>(cdiv(T, 128));
+    L.down_splits = plan_splits(mt, static_cast<int>(cdiv(l, 128)), static_cast<int>(d / 64), c->num_sms);
+    L.up_splits = plan_splits(mt, static_cast<int>(cdiv(d, 128)), static_cast<int>(l / 64), c->num_sms);
+    L.split_down = L.down_splits > 1;
+    L.split_up = L.up_splits > 1;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
+    L.idx = take(T * k * 4);
+    L.w = take(T * k * 4);
+    L.counts = take(E * 4);
+    L.seg = take((E + 1) * 4);
+    L.mt = take((E + 1) * 4);
+    L.fill = take(E * 4);
+    L.nrows = take(4);
+    L.row_slot = take(L.R * 4);
+    L.router = take(L.partials ? T * E * (d / kChunk) * 4 : T * E * 4);
+    L.zacc = take(L.split_down ? T * l * 4 : 0);
+    L.zq_codes = take(T * l / 2);
+    L.zq_sf = take(T * l / 16);
+    L.z_dbg = take(c->debug ? T * l * 2 : 0);
+    L.a_codes = take(L.R * l / 2);
+    L.a_sf = take(L.R * l / 16);
+    L.h_codes = take(L.R * F / 2);
+    L.h_sf = take(L.R * F / 16);
+    L.h_dbg = take(c->debug ? L.R * F * 2 : 0);
+    L.c_acc = take(T * l * 4);
+    L.c = take(T * l * 2);
+    L.yacc = take(L.split_up ? T * d * 4 : 0);
+    L.total = off;
+    return L;
+}
+
+template <bool NVF4, int STAGES>
+cudaError_t set_smem_attr() {
+    return cudaFuncSetAttribute(gemm_kernel<NVF4, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                gemm_smem_bytes<NVF4>(STAGES));
+}
+
+template <bool NVF4, int STAGES>
+cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int grid,
+                        cudaStream_t s) {
+    gemm_kernel<NVF4, STAGES><<<grid, 192, gemm_smem_bytes<NVF4>(STAGES), s>>>(ta, tb, g);
+    return cudaGetLastError();
+}
+
+GemmArgs dense_args(int M, int N, int K, int splits, int epi, unsigned *err) {
+    GemmArgs g;
+    std::memset(&g, 0, sizeof(g));
+    g.M = M; g.N = N; g.K = K;
+    g.m_tiles = static_cast<int>(cdiv(M, kBM));
+    g.n_tiles = static_cast<int>(cdiv(N, kBN));
+    g.k_tiles = K / 64;
+    g.kt_per_split = static_cast<int>(cdiv(g.k_tiles, splits));
+    g.k_splits = static_cast<int>(cdiv(g.k_tiles, g.kt_per_split));
+    g.epi = epi;
+    g.err = err;
+    return g;
+}
+
+int grid_for(int64_t tiles, int num_sms) {
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tiles, num_sms)));
+}
+
+lmoe_status check_error_word(lmoe_ctx *c) {
+    unsigned v = 0;
+    if (cudaMemcpy(&v, c->err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return LMOE_ECUDA;
+    if (v) cudaMemset(c->err, 0, sizeof(unsigned));
+    if (v & kErrTimeout) return LMOE_ETIMEOUT;
+    if (v) return LMOE_EDEVICE;
+    return LMOE_OK;
+}
+
+// The router on x: logits (chunk partials or tiled), top-k + softmax + counts.
+lmoe_status launch_router(const lmoe_ctx *c, const __nv_bfloat16 *x, int64_t T, bool partials,
+                          float *scratch, int32_t *idx, float *w, int32_t *counts,
+                          cudaStream_t s) {
+    const int C = c->d / kChunk;
+    if (partials) {
+        dim3 grid(static_cast<unsigned>(cdiv(C, 32)), static_cast<unsigned>(cdiv(c->E, 8)));
+        router_partials_kernel<<<grid, 256, 0, s>>>(x, c->w_router, static_cast<int>(T), c->d, c->E, scratch);
+    } else {
+        dim3 grid(static_cast<unsigned>(cdiv(T, kRT)), static_cast<unsigned>(cdiv(c->E, kRE)));
+        router_logits_kernel<<<grid, 128, 0, s>>>(x, c->w_router, c->b_router, static_cast<int>(T), c->d,
+                                                  c->E, scratch);
+    }
+    LMOE_LAUNCH();
+    router_topk_kernel<<<static_cast<unsigned>(cdiv(T, 8)), 256, 0, s>>>(
+        scratch, partials ? 0 : 1, static_cast<int>(T), c->E, C, c->k,
+        partials ? c->b_router : nullptr, idx, w, counts);
+    LMOE_LAUNCH();
+    return LMOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *lmoe_status_string(lmoe_status s) {
+    switch (s) {
+    case LMOE_OK: return "ok";
+    case LMOE_EINVAL: return "invalid argument";
+    case LMOE_ENOMEM: return "out of device memory or workspace too small";
+    case LMOE_ECUDA: return "CUDA error";
+    case LMOE_EUNSUPPORTED: return "unsupported device or shape";
+    case LMOE_ETIMEOUT: return "a bounded device-side wait timed out";
+    case LMOE_EDEVICE: return "device-side check failed";
+    }
+    return "unknown status";
+}
+
+lmoe_status lmoe_quantize_nvfp4(const void *src, lmoe_dtype dt, int64_t rows, int64_t K, float amax,
+                                uint8_t *codes, uint8_t *sf, float *tensor_scale,
+                                lmoe_stream stream) {
+    if (rows < 0 || K <= 0 || K % 16 != 0 || (dt != LMOE_BF16 && dt != LMOE_FP32)) return LMOE_EINVAL;
+    if (rows == 0) return LMOE_OK;
+    if (!src || !codes || !sf || !tensor_scale) return LMOE_EINVAL;
+    if (amax != amax) return LMOE_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t n = rows * K;
+    const int64_t blocks = rows * (K / 16);
+    const int qgrid = static_cast<int>(std::min<int64_t>(cdiv(blocks, 256), 148 * 16));
+    unsigned *bits = reinterpret_cast<unsigned *>(tensor_scale);   // holds amax bits until the end
+    if (amax < 0.0f) {
+        LMOE_CUDA(cudaMemsetAsync(bits, 0, sizeof(unsigned), s));
+        const int agrid = static_cast<int>(std::min<int64_t>(cdiv(n, 256), 148 * 8));
+        if (dt == LMOE_BF16)
+            amax_kernel<__nv_bfloat16><<<agrid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(src), n, bits);
+        else
+            amax_kernel<float><<<agrid, 256, 0, s>>>(static_cast<const float *>(src), n, bits);
+        LMOE_LAUNCH();
+    } else {
+        unsigned ab;
+        std::memcpy(&ab, &amax, sizeof(ab));
+        LMOE_CUDA(cudaMemcpyAsync(bits, &ab, sizeof(ab), cudaMemcpyHostToDevice, s));
+    }
+    if (dt == LMOE_BF16)
+        quantize_rows_kernel<__nv_bfloat16><<<qgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(src),
+                                                                 rows, K, -1.0f, bits, codes, sf);
+    else
+        quantize_rows_kernel<float><<<qgrid, 256, 0, s>>>(static_cast<const float *>(src), rows, K, -1.0f,
+                                                         bits, codes, sf);
+    LMOE_LAUNCH();
+    tensor_scale_kernel<<<1, 32, 0, s>>>(bits, 1, tensor_scale);
+    LMOE_LAUNCH();
+    return LMOE_OK;
+}
+
+lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights *w,
+                        lmoe_stream stream, lmoe_ctx **out) {
+    if (!out) return LMOE_EINVAL;
+    *out = nullptr;
+    if (!w || !w->w_down || !w->w_up || !w->w_router || !w->w1 || !w->w2) return LMOE_EINVAL;
+    if (d <= 0 || l <= 0 || ffn <= 0 || d % 64 || l % 64 || ffn % 64) return LMOE_EINVAL;
+    if (k < 1 || k > 32 || E < k || E > 1024) return LMOE_EINVAL;
+    if (!(w->amax_z > 0.0f) || !(w->amax_h > 0.0f)) return LMOE_EINVAL;
+    int dev = 0;
+    LMOE_CUDA(cudaGetDevice(&dev));
+    cudaDeviceProp prop;
+    LMOE_CUDA(cudaGetDeviceProperties(&prop, dev));
+    if (prop.major != 10 || prop.minor != 3) return LMOE_EUNSUPPORTED;
+    if (!encode_fn()) return LMOE_ECUDA;
+    {
+        static std::once_flag once;
+        static cudaError_t attr_err = cudaSuccess;
+        std::call_once(once, [] {
+            cudaError_t a = set_smem_attr<true, kStagesF4>();
+            cudaError_t b = set_smem_attr<false, kStagesBF16>();
+            attr_err = a != cudaSuccess ? a : b;
+        });
+        if (attr_err != cudaSuccess) return cuda_status(attr_err);
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    lmoe_ctx *c = new (std::nothrow) lmoe_ctx;
+    if (!c) return LMOE_ENOMEM;
+    std::memset(c, 0, sizeof(*c));
+    c->d = d; c->l = l; c->E = E; c->k = k; c->ffn = ffn;
+    c->dev = dev;
+    c->num_sms = prop.multiProcessorCount;
+    c->amax_z = w->amax_z;
+    c->amax_h = w->amax_h;
+    c->qz = qscale_from_amax(w->amax_z);
+    c->qh = qscale_from_amax(w->amax_h);
+    auto fail = [&](lmoe_status st) { lmoe_destroy(c); return st; };
+#define CREATE_CUDA(call)                                   \
+    do {                                                    \
+        cudaError_t e_ = (call);                            \
+        if (e_ != cudaSuccess) return fail(cuda_status(e_)); \
+    } while (0)
+    const size_t NB1 = cdiv(ffn, 128), NB2 = cdiv(l, 128);
+    const size_t w1_sf_bytes = static_cast<size_t>(E) * NB1 * (l / 64) * 512;
+    const size_t w2_sf_bytes = static_cast<size_t>(E) * NB2 * (ffn / 64) * 512;
+    CREATE_CUDA(cudaMalloc(&c->w_down, static_cast<size_t>(l) * d * 2));
+    CREATE_CUDA(cudaMalloc(&c->w_up, static_cast<size_t>(d) * l * 2));
+    CREATE_CUDA(cudaMalloc(&c->w_router, static_cast<size_t>(E) * d * 4));
+    CREATE_CUDA(cudaMalloc(&c->b_router, static_cast<size_t>(E) * 4));
+    CREATE_CUDA(cudaMalloc(&c->w1_codes, static_cast<size_t>(E) * ffn * l / 2));
+    CREATE_CUDA(cudaMalloc(&c->w2_codes, static_cast<size_t>(E) * l * ffn / 2));
+    CREATE_CUDA(cudaMalloc(&c->w1_sf, w1_sf_bytes));
+    CREATE_CUDA(cudaMalloc(&c->w2_sf, w2_sf_bytes));
+    CREATE_CUDA(cudaMalloc(&c->w1_sdec, E * 4));
+    CREATE_CUDA(cudaMalloc(&c->w2_sdec, E * 4));
+    CREATE_CUDA(cudaMalloc(&c->alpha1, E * 4));
+    CREATE_CUDA(cudaMalloc(&c->alpha2, E * 4));
+    CREATE_CUDA(cudaMalloc(&c->amax_bits, 2 * E * 4));
+    CREATE_CUDA(cudaMalloc(&c->err, sizeof(unsigned)));
+    CREATE_CUDA(cudaMemsetAsync(c->err, 0, sizeof(unsigned), s));
+    CREATE_CUDA(cudaMemcpyAsync(c->w_down, w->w_down, static_cast<size_t>(l) * d * 2, cudaMemcpyDeviceToDevice, s));
+    CREATE_CUDA(cudaMemcpyAsync(c->w_up, w->w_up, static_cast<size_t>(d) * l * 2, cudaMemcpyDeviceToDevice, s));
+    CREATE_CUDA(cudaMemcpyAsync(c->w_router, w->w_router, static_cast<size_t>(E) * d * 4, cudaMemcpyDeviceToDevice, s));
+    if (w->b_router)
+        CREATE_CUDA(cudaMemcpyAsync(c->b_router, w->b_router, E * 4, cudaMemcpyDeviceToDevice, s));
+    else
+        CREATE_CUDA(cudaMemsetAsync(c->b_router, 0, E * 4, s));
+    CREATE_CUDA(cudaMemsetAsync(c->w1_sf, 0, w1_sf_bytes, s));
+    CREATE_CUDA(cudaMemsetAsync(c->w2_sf, 0, w2_sf_bytes, s));
+    CREATE_CUDA(cudaMemsetAsync(c->amax_bits, 0, 2 * E * 4, s));
+    // expert weights: per-expert amax, then quantization into codes + scale atoms
+    const int64_t seg1 = static_cast<int64_t>(ffn) * l, seg2 = static_cast<int64_t>(l) * ffn;
+    amax_segments_kernel<<<dim3(16, E), 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->w1), seg1, c->amax_bits);
+    amax_segments_kernel<<<dim3(16, E), 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->w2), seg2, c->amax_bits + E);
+    CREATE_CUDA(cudaGetLastError());
+    const int qgrid = c->num_sms * 16;
+    quantize_experts_kernel<<<qgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->w1), E, ffn, l,
+                                                  c->amax_bits, c->w1_codes, c->w1_sf);
+    quantize_experts_kernel<<<qgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->w2), E, l, ffn,
+                                                  c->amax_bits + E, c->w2_codes, c->w2_sf);
+    tensor_scale_kernel<<<cdiv(E, 256), 256, 0, s>>>(c->amax_bits, E, c->w1_sdec);
+    tensor_scale_kernel<<<cdiv(E, 256), 256, 0, s>>>(c->amax_bits + E, E, c->w2_sdec);
+    CREATE_CUDA(cudaGetLastError());
+    CREATE_CUDA(cudaStreamSynchronize(s));
+    // alpha_e = s_dec(activation) * s_dec(weight_e), in fp32
+    {
+        float *sd1 = new float[E], *sd2 = new float[E], *a1 = new float[E], *a2 = new float[E];
+        cudaError_t e1 = cudaMemcpy(sd1, c->w1_sdec, E * 4, cudaMemcpyDeviceToHost);
+        cudaError_t e2 = cudaMemcpy(sd2, c->w2_sdec, E * 4, cudaMemcpyDeviceToHost);
+        for (int e = 0; e < E; ++e) {
+            volatile float p1 = c->qz.s_dec * sd1[e];
+            volatile float p2 = c->qh.s_dec * sd2[e];
+            a1[e] = p1; a2[e] = p2;
+        }
+        cudaError_t e3 = cudaMemcpy(c->alpha1, a1, E * 4, cudaMemcpyHostToDevice);
+        cudaError_t e4 = cudaMemcpy(c->alpha2, a2, E * 4, cudaMemcpyHostToDevice);
+        delete[] sd1; delete[] sd2; delete[] a1; delete[] a2;
+        for (cudaError_t e : {e1, e2, e3, e4})
+            if (e != cudaSuccess) return fail(cuda_status(e));
+    }
+    bool ok = make_map(&c->tm_wd, true, c->w_down, d, l, static_cast<uint64_t>(d) * 2) &&
+              make_map(&c->tm_wu, true, c->w_up, l, d, static_cast<uint64_t>(l) * 2) &&
+              make_map(&c->tm_w1, false, c->w1_codes, l / 2, static_cast<uint64_t>(E) * ffn, l / 2) &&
+              make_map(&c->tm_w2, false, c->w2_codes, ffn / 2, static_cast<uint64_t>(E) * l, ffn / 2);
+    if (!ok) return fail(LMOE_ECUDA);
+#undef CREATE_CUDA
+    *out = c;
+    return LMOE_OK;
+}
+
+void lmoe_destroy(lmoe_ctx *c) {
+    if (!c) return;
+    cudaDeviceSynchronize();
+    void *ptrs[] = {c->w_down, c->w_up, c->w_router, c->b_router, c->w1_codes, c->w1_sf,
+                    c->w2_codes, c->w2_sf, c->w1_sdec, c->w2_sdec, c->alpha1, c->alpha2,
+                    c->amax_bits, c->err, c->route_ws};
+    for (void *p : ptrs)
+        if (p) cudaFree(p);
+    delete c;
+}
+
+size_t lmoe_workspace_size(const lmoe_ctx *c, int64_t T) {
+    if (!c || T < 0) return 0;
+    return layout(c, T).total;
+}
+
+size_t lmoe_host_workspace_size(const lmoe_ctx *c, int64_t T) {
+    if (!c || T < 0) return 0;
+    return align256(layout(c, T).total) + 2 * align256(static_cast<size_t>(T) * c->d * 2);
+}
+
+lmoe_status lmoe_workspace_range(const lmoe_ctx *c, int64_t T, int stage, size_t *offset,
+                                 size_t *bytes) {
+    if (!c || T < 0 || !offset || !bytes) return LMOE_EINVAL;
+    const WsLayout L = layout(c, T);
+    const int64_t k = c->k, l = c->l, F = c->ffn;
+    switch (stage) {
+    case LMOE_STAGE_IDX: *offset = L.idx; *bytes = T * k * 4; break;
+    case LMOE_STAGE_W: *offset = L.w; *bytes = T * k * 4; break;
+    case LMOE_STAGE_COUNTS: *offset = L.counts; *bytes = c->E * 4; break;
+    case LMOE_STAGE_ZQ_CODES: *offset = L.zq_codes; *bytes = T * l / 2; break;
+    case LMOE_STAGE_ZQ_SF: *offset = L.zq_sf; *bytes = T * l / 16; break;
+    case LMOE_STAGE_C: *offset = L.c; *bytes = T * l * 2; break;
+    case LMOE_STAGE_Z: *offset = L.z_dbg; *bytes = c->debug ? T * l * 2 : 0; break;
+    case LMOE_STAGE_ROWS: *offset = L.row_slot; *bytes = L.R * 4; break;
+    case LMOE_STAGE_H: *offset = L.h_dbg; *bytes = c->debug ? L.R * F * 2 : 0; break;
+    case LMOE_STAGE_HQ_CODES: *offset = L.h_codes; *bytes = L.R * F / 2; break;
+    case LMOE_STAGE_HQ_SF: *offset = L.h_sf; *bytes = L.R * F / 16; break;
+    case LMOE_STAGE_NROWS: *offset = L.nrows; *bytes = 4; break;
+    default: return LMOE_EINVAL;
+    }
+    return LMOE_OK;
+}
+
+lmoe_status lmoe_set_debug(lmoe_ctx *c, int on) {
+    if (!c) return LMOE_EINVAL;
+    c->debug = on ? 1 : 0;
+    return LMOE_OK;
+}
+
+lmoe_status lmoe_route(lmoe_ctx *c, const void *x, int64_t T, int32_t *idx, float *w,
+                       int32_t *counts, lmoe_stream stream) {
+    if (!c || T < 0) return LMOE_EINVAL;
+    if (T == 0) return LMOE_OK;
+    if (!x || !idx || !w) return LMOE_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool partials = T <= kPartialsMaxT;
+    const size_t need = partials ? static_cast<size_t>(T) * c->E * (c->d / kChunk) * 4
+                                 : static_cast<size_t>(T) * c->E * 4;
+    if (need > c->route_ws_bytes) {
+        if (c->route_ws) LMOE_CUDA(cudaFreeAsync(c->route_ws, s));
+        c->route_ws = nullptr;
+        c->route_ws_bytes = 0;
+        LMOE_CUDA(cudaMallocAsync(&c->route_ws, need, s));
+        c->route_ws_bytes = need;
+    }
+    if (counts) LMOE_CUDA(cudaMemsetAsync(counts, 0, c->E * 4, s));
+    return launch_router(c, static_cast<const __nv_bfloat16 *>(x), T, partials,
+                         static_cast<float *>(c->route_ws), idx, w, counts, s);
+}
+
+lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *ws, size_t ws_bytes,
+                         lmoe_stream stream) {
+    if (!c || T < 0) return LMOE_EINVAL;
+    if (T == 0) return LMOE_OK;
+    if (!x || !y || !ws) return LMOE_EINVAL;
+    if (T > (int64_t(1) << 24)) return LMOE_EINVAL;
+    const WsLayout L = layout(c, T);
+    if (ws_bytes < L.total) return LMOE_ENOMEM;
+    if (reinterpret_cast<uintptr_t>(ws) % 256 || reinterpret_cast<uintptr_t>(x) % 16 ||
+        reinterpret_cast<uintptr_t>(y) % 16)
+        return LMOE_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *W = static_cast<uint8_t *>(ws);
+    auto at = [&](size_t off) { return static_cast<void *>(W + off); };
+    int32_t *idx = static_cast<int32_t *>(at(L.idx));
+    float *rw = static_cast<float *>(at(L.w));
+    int32_t *counts = static_cast<int32_t *>(at(L.counts));
+    int32_t *seg = static_cast<int32_t *>(at(L.seg));
+    int32_t *mt = static_cast<int32_t *>(at(L.mt));
+    int32_t *fill = static_cast<int32_t *>(at(L.fill));
+    int32_t *nrows = static_cast<int32_t *>(at(L.nrows));
+    int32_t *row_slot = static_cast<int32_t *>(at(L.row_slot));
+    float *zacc = static_cast<float *>(at(L.zacc));
+    uint8_t *zq_codes = static_cast<uint8_t *>(at(L.zq_codes));
+    uint8_t *zq_sf = static_cast<uint8_t *>(at(L.zq_sf));
+    __nv_bfloat16 *z_dbg = c->debug ? static_cast<__nv_bfloat16 *>(at(L.z_dbg)) : nullptr;
+    uint8_t *a_codes = static_cast<uint8_t *>(at(L.a_codes));
+    uint8_t *a_sf = static_cast<uint8_t *>(at(L.a_sf));
+    uint8_t *h_codes = static_cast<uint8_t *>(at(L.h_codes));
+    uint8_t *h_sf = static_cast<uint8_t *>(at(L.h_sf));
+    __nv_bfloat16 *h_dbg = c->debug ? static_cast<__nv_bfloat16 *>(at(L.h_dbg)) : nullptr;
+    float *c_acc = static_cast<float *>(at(L.c_acc));
+    __nv_bfloat16 *cb = static_cast<__nv_bfloat16 *>(at(L.c));
+    float *yacc = static_cast<float *>(at(L.yacc));
+    const int d = c->d, l = c->l, E = c->E, k = c->k, F = c->ffn;
+
+    // 0. zero the accumulators and the expert histogram
+    {
+        ZeroRanges z;
+        std::memset(&z, 0, sizeof(z));
+        z.p[0] = reinterpret_cast<uint4 *>(counts); z.n16[0] = cdiv(E * 4, 16);
+        z.p[1] = reinterpret_cast<uint4 *>(c_acc); z.n16[1] = T * l * 4 / 16;
+        if (L.split_down) { z.p[2] = reinterpret_cast<uint4 *>(zacc); z.n16[2] = T * l * 4 / 16; }
+        if (L.split_up) { z.p[3] = reinterpret_cast<uint4 *>(yacc); z.n16[3] = T * d * 4 / 16; }
+        zero_kernel<<<c->num_sms * 4, 256, 0, s>>>(z);
+        LMOE_LAUNCH();
+    }
+    // 1. router
+    {
+        lmoe_status st = launch_router(c, static_cast<const __nv_bfloat16 *>(x), T, L.partials,
+                                       static_cast<float *>(at(L.router)), idx, rw, counts, s);
+        if (st != LMOE_OK) return st;
+    }
+    // 2. per-expert segments
+    segments_kernel<<<1, 1024, 0, s>>>(counts, E, seg, mt, fill, row_slot, nrows);
+    LMOE_LAUNCH();
+    // 3. down-projection z = x Wd^T, quantized to NVFP4
+    {
+        CUtensorMap tx;
+        if (!make_map(&tx, true, x, d, T, static_cast<uint64_t>(d) * 2)) return LMOE_ECUDA;
+        GemmArgs g = dense_args(static_cast<int>(T), l, d, L.down_splits,
+                                L.split_down ? EPI_RED_F32 : EPI_Z_QUANT, c->err);
+        if (L.split_down) {
+            g.out = zacc; g.ld_out = l;
+        } else {
+            g.q = c->qz; g.q_codes = zq_codes; g.q_sf = zq_sf; g.dbg = z_dbg;
+        }
+        LMOE_CUDA((launch_gemm<false, kStagesBF16>(tx, c->tm_wd, g,
+                                                   grid_for(int64_t(g.m_tiles) * g.n_tiles * g.k_splits, c->num_sms), s)));
+        if (L.split_down) {
+            const int grid = static_cast<int>(std::min<int64_t>(cdiv(T * l / 16, 256), c->num_sms * 8));
+            z_finalize_kernel<<<grid, 256, 0, s>>>(zacc, T, l, c->qz, zq_codes, zq_sf, z_dbg);
+            LMOE_LAUNCH();
+        }
+    }
+    // 4. gather the quantized latent tokens into per-expert segments
+    {
+        const int64_t nslots = T * k;
+        scatter_kernel<<<static_cast<unsigned>(cdiv(nslots, 8)), 256, 0, s>>>(
+            idx, nslots, seg, fill, row_slot, k, l, zq_codes, zq_sf, a_codes, a_sf);
+        LMOE_LAUNCH();
+    }
+    // 5. latent-up grouped GEMM + relu^2 + requantize
+    {
+        CUtensorMap ta;
+        if (!make_map(&ta, false, a_codes, l / 2, L.R, l / 2)) return LMOE_ECUDA;
+        GemmArgs g;
+        std::memset(&g, 0, sizeof(g));
+        g.M = static_cast<int>(L.R); g.N = F; g.K = l;
+        g.n_tiles = static_cast<int>(cdiv(F, kBN));
+        g.k_tiles = static_cast<int>(cdiv(l, 256));
+        g.grouped = 1; g.E = E; g.mt_start = mt; g.seg_start = seg; g.counts = counts;
+        g.sfa = a_sf; g.sfb = c->w1_sf; g.NB = static_cast<int>(cdiv(F, 128));
+        g.epi = EPI_H_QUANT; g.q = c->qh; g.q_codes = h_codes; g.q_sf = h_sf; g.dbg = h_dbg;
+        g.alpha = c->alpha1; g.err = c->err;
+        LMOE_CUDA((launch_gemm<true, kStagesF4>(ta, c->tm_w1, g, c->num_sms, s)));
+    }
+    // 6. latent-down grouped GEMM, routing weight, combine into c_acc
+    {
+        CUtensorMap ta;
+        if (!make_map(&ta, false, h_codes, F / 2, L.R, F / 2)) return LMOE_ECUDA;
+        GemmArgs g;
+        std::memset(&g, 0, sizeof(g));
+        g.M = static_cast<int>(L.R); g.N = l; g.K = F;
+        g.n_tiles = static_cast<int>(cdiv(l, kBN));
+        g.k_tiles = static_cast<int>(cdiv(F, 256));
+        g.grouped = 1; g.E = E; g.mt_start = mt; g.seg_start = seg; g.counts = counts;
+        g.sfa = h_sf; g.sfb = c->w2_sf; g.NB = static_cast<int>(cdiv(l, 128));
+        g.epi = EPI_COMBINE; g.out = c_acc; g.ld_out = l;
+        g.alpha = c->alpha2; g.row_slot = row_slot; g.route_w = rw; g.topk = k; g.err = c->err;
+        LMOE_CUDA((launch_gemm<true, kStagesF4>(ta, c->tm_w2, g, c->num_sms, s)));
+    }
+    // 7. c = bf16(c_acc)
+    {
+        const int grid = static_cast<int>(std::min<int64_t>(cdiv(T * l / 8, 256), c->num_sms * 8));
+        f32_to_bf16_kernel<<<grid, 256, 0, s>>>(c_acc, T * l, cb);
+        LMOE_LAUNCH();
+    }
+    // 8. up-projection y = c Wu^T
+    {
+        CUtensorMap tc;
+        if (!make_map(&tc, true, cb, l, T, static_cast<uint64_t>(l) * 2)) return LMOE_ECUDA;
+        GemmArgs g = dense_args(static_cast<int>(T), d, l, L.up_splits,
+                                L.split_up ? EPI_RED_F32 : EPI_STORE_BF16, c->err);
+        g.out = L.split_up ? static_cast<void *>(yacc) : y;
+        g.ld_out = d;
+        LMOE_CUDA((launch_gemm<false, kStagesBF16>(tc, c->tm_wu, g,
+                                                   grid_for(int64_t(g.m_tiles) * g.n_tiles * g.k_splits, c->num_sms), s)));
+        if (L.split_up) {
+            const int grid = static_cast<int>(std::min<int64_t>(cdiv(T * d / 8, 256), c->num_sms * 8));
+            f32_to_bf16_kernel<<<grid, 256, 0, s>>>(yacc, T * d, static_cast<__nv_bfloat16 *>(y));
+            LMOE_LAUNCH();
+        }
+    }
+    return LMOE_OK;
+}
+
+lmoe_status lmoe_forward_host(lmoe_ctx *c, const void *x_host, int64_t T, void *y_host, void *ws,
+                              size_t ws_bytes, lmoe_stream stream) {
+    if (!c || T < 0) return LMOE_EINVAL;
+    if (T == 0) return LMOE_OK;
+    if (!x_host || !y_host || !ws) return LMOE_EINVAL;
+    const size_t main = align256(layout(c, T).total);
+    const size_t io = align256(static_cast<size_t>(T) * c->d * 2);
+    if (ws_bytes < main + 2 * io) return LMOE_ENOMEM;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *W = static_cast<uint8_t *>(ws);
+    void *xd = W + main, *yd = W + main + io;
+    const size_t bytes = static_cast<size_t>(T) * c->d * 2;
+    LMOE_CUDA(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s));
+    lmoe_status st = lmoe_forward(c, xd, T, yd, ws, main, stream);
+    if (st != LMOE_OK) return st;
+    LMOE_CUDA(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s));
+    LMOE_CUDA(cudaStreamSynchronize(s));
+    return LMOE_OK;
+}
+
+lmoe_status lmoe_get_expert_nvfp4(const lmoe_ctx *c, int which, int e, uint8_t *codes, uint8_t *sf,
+                                  float *s_dec, lmoe_stream stream) {
+    if (!c || (which != 1 && which != 2) || e < 0 || e >= c->E || !codes || !sf || !s_dec)
+        return LMOE_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int N = which == 1 ? c->ffn : c->l;
+    const int K = which == 1 ? c->l : c->ffn;
+    const uint8_t *src = (which == 1 ? c->w1_codes : c->w2_codes) + static_cast<size_t>(e) * N * K / 2;
+    const size_t NB = cdiv(N, 128);
+    const uint8_t *atoms = (which == 1 ? c->w1_sf : c->w2_sf) + static_cast<size_t>(e) * NB * (K / 64) * 512;
+    LMOE_CUDA(cudaMemcpyAsync(codes, src, static_cast<size_t>(N) * K / 2, cudaMemcpyDeviceToDevice, s));
+    sf_atoms_to_rows_kernel<<<static_cast<unsigned>(cdiv(static_cast<int64_t>(N) * K / 16, 256)), 256, 0, s>>>(atoms, N, K, sf);
+    LMOE_LAUNCH();
+    LMOE_CUDA(cudaMemcpyAsync(s_dec, (which == 1 ? c->w1_sdec : c->w2_sdec) + e, 4, cudaMemcpyDeviceToHost, s));
+    LMOE_CUDA(cudaStreamSynchronize(s));
+    return LMOE_OK;
+}
+
+lmoe_status lmoe_check(lmoe_ctx *c, lmoe_stream stream) {
+    if (!c) return LMOE_EINVAL;
+    LMOE_CUDA(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+    return check_error_word(c);
+}
+
+}  // extern "C"

@@ -1,0 +1,69 @@
+"""Shared set-up for the GPU parity tests: one layer instance fed identically to the CUDA
+library (through its C ABI binding) and to the CPU oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import lmoe_synth
+import oracle
+
+E4M3 = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def rel_l2_rows(a, b):
+    a = np.asarray(a, np.float64).reshape(a.shape[0], -1)
+    b = np.asarray(b, np.float64).reshape(b.shape[0], -1)
+    num = np.linalg.norm(a - b, axis=1)
+    den = np.maximum(np.linalg.norm(b, axis=1), 1e-30)
+    return num / den
+
+
+def atoms_to_rows(atoms: np.ndarray, rows: int, K: int) -> np.ndarray:
+    """Tensor-core scale-atom layout [rows/128][K/64][512] -> row-major [rows][K/16]."""
+    a = atoms.reshape(rows // 128, K // 64, 32, 4, 4)          # [rb][kb][r0][r1][j]
+    a = a.transpose(0, 3, 2, 1, 4)                             # [rb][r1][r0][kb][j]
+    return a.reshape(rows, K // 16)
+
+
+class Case:
+    """A layer (dims, seed, routing skew) with its calibration, on the GPU and in the oracle."""
+
+    def __init__(self, dims: lmoe_synth.Dims, seed: int, zipf: float = 0.0, calib_T: int = 64,
+                 gen_device: str = "cpu"):
+        import nvfp4_latentmoe_fwd_02_b300 as lm
+        self.lm = lm
+        self.dims, self.seed, self.zipf = dims, seed, zipf
+        L = lmoe_synth.layer(dims, seed, gen_device, zipf)
+        self.L = L
+        self.dev = {n: getattr(L, n).cuda() for n in
+                    ("w_down", "w_up", "w_router", "b_router", "w1", "w2")}
+        host = {n: getattr(L, n).float().cpu().numpy() for n in
+                ("w_down", "w_up", "w_router", "b_router")}
+        self._w1, self._w2 = L.w1, L.w2
+        self.ol = oracle.OracleLayer(dims.d, dims.l, dims.E, dims.k, dims.ffn, host["w_down"],
+                                     host["w_up"], host["w_router"], host["b_router"],
+                                     self._expert_master)
+        xc = lmoe_synth.calibration_tokens(calib_T, dims.d, seed, gen_device).float().cpu().numpy()
+        self.amax_z, self.amax_h = self.ol.calibrate(xc)
+        self.moe = None
+
+    def _expert_master(self, e):
+        return (self._w1[e].float().cpu().numpy(), self._w2[e].float().cpu().numpy())
+
+    def gpu(self, debug=True):
+        if self.moe is None:
+            d = self.dims
+            D = self.dev
+            self.moe = self.lm.LatentMoE(d.d, d.l, d.E, d.k, d.ffn, D["w_down"], D["w_up"],
+                                         D["w_router"], D["b_router"], D["w1"], D["w2"],
+                                         self.amax_z, self.amax_h, debug=debug)
+        return self.moe
+
+    def tokens(self, T, seed_offset=0):
+        return lmoe_synth.tokens(T, self.dims.d, self.seed * 7919 + 13 + seed_offset, "cpu")
+
+    def close(self):
+        if self.moe is not None:
+            self.moe.close()
+            self.moe = None

@@ -1,0 +1,159 @@
+"""GPU parity of the LatentMoE layer (tiny dims) against the CPU oracle, through the C ABI.
+
+Layer: shengxinai.com Nemotron 3 blog, section 2.2 (project d -> l, route, latent experts,
+combine, project back); routing top-k of E (NVIDIA AI releases Nemotron 3 Ultra).
+Bit-exact: expert weight codes / scales / tensor scales, expert indices, per-expert counts,
+and the GPU's own z and h re-quantized by the oracle vs. the GPU's codes.  Float outputs:
+relative L2 per row <= 5e-3 for z and h, <= 2e-2 for c and y.
+"""
+import numpy as np
+import pytest
+import torch
+
+import lmoe_synth
+import oracle
+from lmoe_cases import Case, atoms_to_rows, rel_l2_rows
+
+pytestmark = pytest.mark.gpu
+
+TOL_INTER = 5e-3
+TOL_OUT = 2e-2
+
+
+@pytest.fixture(scope="module", params=[0.0, 1.1], ids=["uniform", "zipf1.1"])
+def tiny(request):
+    case = Case(lmoe_synth.TINY, seed=0 if request.param == 0.0 else 5, zipf=request.param)
+    yield case
+    case.close()
+
+
+def test_expert_weights_match_oracle(tiny):
+    moe = tiny.gpu()
+    d = tiny.dims
+    for which, (N, K) in ((1, (d.ffn, d.l)), (2, (d.l, d.ffn))):
+        codes = torch.empty((N, K // 2), dtype=torch.uint8, device="cuda")
+        sf = torch.empty((N, K // 16), dtype=torch.uint8, device="cuda")
+        for e in range(d.E):
+            sdec = tiny.lm.lmoe_get_expert_nvfp4(moe.ctx, which, e, codes, sf)
+            q = tiny.ol.quantized(e)
+            oc, os_, od = (q[0], q[1], q[2]) if which == 1 else (q[3], q[4], q[5])
+            assert sdec == od
+            assert np.array_equal(sf.cpu().numpy(), os_)
+            assert np.array_equal(codes.cpu().numpy(), oc)
+
+
+@pytest.mark.parametrize("T", [1, 7, 64, 65, 300])
+def test_route_matches_oracle(tiny, T):
+    moe = tiny.gpu()
+    x = tiny.tokens(T, seed_offset=T)
+    k, E = tiny.dims.k, tiny.dims.E
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    tiny.lm.lmoe_route(moe.ctx, x.cuda(), T, idx, w, counts)
+    torch.cuda.synchronize()
+    _, oidx, ow, ocounts = tiny.ol.route(x.float().numpy())
+    assert np.array_equal(idx.cpu().numpy(), oidx)
+    assert np.array_equal(counts.cpu().numpy(), ocounts)
+    assert np.allclose(w.cpu().numpy(), ow, rtol=2e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("T", [1, 5, 64, 129, 300])
+def test_forward_matches_oracle(tiny, T):
+    moe = tiny.gpu(debug=True)
+    d = tiny.dims
+    x = tiny.tokens(T, seed_offset=1000 + T)
+    y = moe.forward(x.cuda())
+    moe.check()
+    want = ("z", "zq_codes", "zq_sf", "h", "hq_codes", "hq_sf", "c", "y")
+    ref = tiny.ol.forward(x.float().numpy(), quant=True, want=want)
+
+    # routing: exact
+    idx = moe.stage("idx", T, torch.int32).view(T, d.k).cpu().numpy()
+    counts = moe.stage("counts", T, torch.int32).cpu().numpy()
+    assert np.array_equal(idx, ref["idx"])
+    assert np.array_equal(counts, ref["counts"])
+    w = moe.stage("w", T, torch.float32).view(T, d.k).cpu().numpy()
+    assert np.allclose(w, ref["w"], rtol=2e-6, atol=1e-7)
+
+    # z: float within tolerance; the GPU's codes are the oracle's quantizer on the GPU's z
+    z = moe.stage("z", T, torch.bfloat16).view(T, d.l).float().cpu().numpy()
+    assert rel_l2_rows(z, ref["z"]).max() <= TOL_INTER
+    zc = moe.stage("zq_codes", T).view(T, d.l // 2).cpu().numpy()
+    zs = moe.stage("zq_sf", T).view(T, d.l // 16).cpu().numpy()
+    oc, os_, _ = oracle.quantize_nvfp4(z, tiny.amax_z)
+    assert np.array_equal(zs, os_) and np.array_equal(zc, oc)
+
+    # permuted rows: a valid grouping of all T*k slots by expert
+    nrows = int(moe.stage("nrows", T, torch.int32).cpu()[0])
+    rows = moe.stage("rows", T, torch.int32).cpu().numpy()[:nrows]
+    slots = rows[rows >= 0]
+    assert np.array_equal(np.sort(slots), np.arange(T * d.k))
+    flat_idx = idx.ravel()
+    start = 0
+    for e in range(d.E):
+        n = int(counts[e])
+        seg = rows[start:start + n]
+        assert np.all(flat_idx[seg] == e)
+        assert np.all(rows[start + n:start + ((n + 127) // 128) * 128] == -1)
+        start += ((n + 127) // 128) * 128
+    assert start == nrows
+
+    # h per slot: float within tolerance; hq codes = oracle quantizer on the GPU's h
+    R = moe.stage("rows", T, torch.int32).numel()
+    h = moe.stage("h", T, torch.bfloat16).view(R, d.ffn)[:nrows].float().cpu().numpy()
+    hc = moe.stage("hq_codes", T).view(R, d.ffn // 2)[:nrows].cpu().numpy()
+    hs = atoms_to_rows(moe.stage("hq_sf", T).cpu().numpy()[: R * d.ffn // 16], R, d.ffn)[:nrows]
+    live = rows >= 0
+    s = rows[live]
+    ref_h = ref["h"].reshape(T * d.k, d.ffn)[s]
+    assert rel_l2_rows(h[live], ref_h).max() <= TOL_INTER
+    oc, os_, _ = oracle.quantize_nvfp4(h[live], tiny.amax_h)
+    assert np.array_equal(hs[live], os_)
+    assert np.array_equal(hc[live], oc)
+
+    # combine and output
+    c = moe.stage("c", T, torch.bfloat16).view(T, d.l).float().cpu().numpy()
+    assert rel_l2_rows(c, ref["c"]).max() <= TOL_OUT
+    assert rel_l2_rows(y.float().cpu().numpy(), ref["y"]).max() <= TOL_OUT
+
+
+def test_forward_host_matches_device(tiny):
+    moe = tiny.gpu()
+    T = 37
+    x = tiny.tokens(T, seed_offset=77)
+    y_dev = moe.forward(x.cuda()).cpu()
+    lm = tiny.lm
+    nb = lm.lmoe_host_workspace_size(moe.ctx, T)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    xh = x.pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    lm.lmoe_forward_host(moe.ctx, xh, T, yh, ws, nb)
+    # combine uses fp32 atomics; results agree to the last bf16 place almost everywhere
+    assert rel_l2_rows(yh.float().numpy(), y_dev.float().numpy()).max() <= 1e-2
+
+
+def test_routing_is_deterministic_across_calls(tiny):
+    moe = tiny.gpu()
+    T = 100
+    x = tiny.tokens(T, seed_offset=5).cuda()
+    moe.forward(x)
+    a = moe.stage("idx", T, torch.int32).clone()
+    moe.forward(x)
+    b = moe.stage("idx", T, torch.int32)
+    assert torch.equal(a, b)
+
+
+def test_invalid_arguments(tiny):
+    lm = tiny.lm
+    moe = tiny.gpu()
+    x = tiny.tokens(4).cuda()
+    y = torch.empty_like(x)
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(lm.LmoeError) as ei:
+        lm.lmoe_forward(moe.ctx, x, 4, y, ws, 16)
+    assert ei.value.status == lm.LMOE_ENOMEM
+    with pytest.raises(lm.LmoeError) as ei:
+        lm.lmoe_create(100, 64, 16, 4, 128, *[tiny.dev[n] for n in ("w_down", "w_up", "w_router", "b_router", "w1", "w2")], 1.0, 1.0)
+    assert ei.value.status == lm.LMOE_EINVAL
+    lm.lmoe_forward(moe.ctx, x, 0, y, ws, 16)   # T = 0 is a no-op

@@ -1,0 +1,99 @@
+"""GPU parity at the Ultra layer size (d = 8192, l = 2048, E = 512, top-22, ffn = 2048;
+NVIDIA AI releases Nemotron 3 Ultra, architecture paragraph; l = d/4 from the shengxinai.com
+Nemotron 3 blog, section 2.2), in the launch configuration the benchmark times.
+
+Decode (T = 8, uniform routing): every token against the oracle.  Prefill (T = 4096,
+Zipf(1.1) router bias): routing on a token sample plus the count invariants on all tokens,
+and full outputs on a token sample (tokens are independent under static scales).
+"""
+import numpy as np
+import pytest
+import torch
+
+import lmoe_synth
+import oracle
+from lmoe_cases import Case, rel_l2_rows
+
+pytestmark = pytest.mark.gpu
+
+TOL_INTER = 5e-3
+TOL_OUT = 2e-2
+
+
+@pytest.fixture(scope="module")
+def ultra_uniform():
+    case = Case(lmoe_synth.ULTRA, seed=1, zipf=0.0, calib_T=8, gen_device="cuda")
+    yield case
+    case.close()
+
+
+@pytest.fixture(scope="module")
+def ultra_zipf():
+    case = Case(lmoe_synth.ULTRA, seed=2, zipf=1.1, calib_T=8, gen_device="cuda")
+    yield case
+    case.close()
+
+
+def _check_tokens(case, T, x, y, sample):
+    d = case.dims
+    moe = case.moe
+    idx = moe.stage("idx", T, torch.int32).view(T, d.k).cpu().numpy()
+    counts = moe.stage("counts", T, torch.int32).cpu().numpy()
+    assert counts.sum() == T * d.k
+    assert np.array_equal(counts, np.bincount(idx.ravel(), minlength=d.E))
+    xs = x[sample].float().cpu().numpy()
+    ref = case.ol.forward(xs, quant=True, want=("z", "c", "y"))
+    assert np.array_equal(idx[sample], ref["idx"])
+    w = moe.stage("w", T, torch.float32).view(T, d.k).cpu().numpy()
+    assert np.allclose(w[sample], ref["w"], rtol=2e-6, atol=1e-7)
+    z = moe.stage("z", T, torch.bfloat16).view(T, d.l).float().cpu().numpy()[sample]
+    assert rel_l2_rows(z, ref["z"]).max() <= TOL_INTER
+    zc = moe.stage("zq_codes", T).view(T, d.l // 2).cpu().numpy()[sample]
+    zs = moe.stage("zq_sf", T).view(T, d.l // 16).cpu().numpy()[sample]
+    oc, os_, _ = oracle.quantize_nvfp4(z, case.amax_z)
+    assert np.array_equal(zs, os_) and np.array_equal(zc, oc)
+    c = moe.stage("c", T, torch.bfloat16).view(T, d.l).float().cpu().numpy()[sample]
+    assert rel_l2_rows(c, ref["c"]).max() <= TOL_OUT
+    assert rel_l2_rows(y[sample].float().cpu().numpy(), ref["y"]).max() <= TOL_OUT
+
+
+def test_ultra_expert_weights_sampled(ultra_uniform):
+    case = ultra_uniform
+    moe = case.gpu(debug=True)
+    d = case.dims
+    codes = torch.empty((d.ffn, d.l // 2), dtype=torch.uint8, device="cuda")
+    sf = torch.empty((d.ffn, d.l // 16), dtype=torch.uint8, device="cuda")
+    for e in (0, 137, 511):
+        for which in (1, 2):
+            sdec = case.lm.lmoe_get_expert_nvfp4(moe.ctx, which, e, codes, sf)
+            q = case.ol.quantized(e)
+            oc, os_, od = (q[0], q[1], q[2]) if which == 1 else (q[3], q[4], q[5])
+            assert sdec == od
+            assert np.array_equal(sf.cpu().numpy(), os_)
+            assert np.array_equal(codes.cpu().numpy(), oc)
+
+
+def test_ultra_decode_T8(ultra_uniform):
+    case = ultra_uniform
+    moe = case.gpu(debug=True)
+    T = 8
+    x = case.tokens(T).cuda()
+    y = moe.forward(x)
+    moe.check()
+    _check_tokens(case, T, x, y, np.arange(T))
+
+
+def test_ultra_prefill_T4096_zipf(ultra_zipf):
+    case = ultra_zipf
+    moe = case.gpu(debug=True)
+    T = 4096
+    x = case.tokens(T).cuda()
+    y = moe.forward(x)
+    moe.check()
+    counts = moe.stage("counts", T, torch.int32).cpu().numpy()
+    assert (counts == 0).sum() > 0 and counts.max() > 1000      # the skew the workload asks for
+    rng = np.random.default_rng(0)
+    sample = np.sort(rng.choice(T, 12, replace=False))
+    sample[0] = 0
+    sample[-1] = T - 1
+    _check_tokens(case, T, x, y, sample)
