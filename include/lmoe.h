@@ -147,6 +147,18 @@ lmoe_status lmoe_set_debug(lmoe_ctx *ctx, int on);
 lmoe_status lmoe_get_expert_nvfp4(const lmoe_ctx *ctx, int which, int e, uint8_t *codes,
                                   uint8_t *sf, float *s_dec, lmoe_stream stream);
 
+/* Number of kernels one lmoe_forward(ctx, ..., T, ...) launches (it depends on T only through
+ * the split-K plan of the two projections). */
+int lmoe_forward_kernel_count(const lmoe_ctx *ctx, int64_t T);
+
+/* Per-kernel timing of lmoe_forward.  When on, lmoe_forward records a CUDA event on its stream
+ * before its first kernel and after every kernel it launches (do not capture a forward into a
+ * CUDA graph while this is on).  lmoe_profile_read synchronizes on the last event and writes,
+ * for the last forward, each kernel's name (static strings) and duration in milliseconds, in
+ * launch order; it returns the number written (<= max), or -1 if nothing was recorded. */
+lmoe_status lmoe_set_profile(lmoe_ctx *ctx, int on);
+int lmoe_profile_read(lmoe_ctx *ctx, const char **names, float *ms, int max);
+
 /* Synchronize `stream` and report (and clear) the context's device error word. */
 lmoe_status lmoe_check(lmoe_ctx *ctx, lmoe_stream stream);
 

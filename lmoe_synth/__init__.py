@@ -125,3 +125,13 @@ def layer(dims: Dims, seed: int, device="cpu", zipf_s: float = 0.0) -> Layer:
 def calibration_tokens(T: int, d: int, seed: int, device="cpu") -> torch.Tensor:
     """The calibration batch: N(0,1) bf16 tokens drawn with seed + 1."""
     return tokens(T, d, seed + 1, device, tag="x_cal")
+
+
+# Named workloads.  "gen" is the device whose torch generator draws the inputs (Ultra-size
+# weights are drawn on the GPU, so their values are reproducible on the same GPU model).
+CONFIGS = {
+    "tiny": dict(dims=TINY, seed=0, zipf=0.0, T=64, calib_T=64, gen="cpu"),
+    "ultra_decode_T8": dict(dims=ULTRA, seed=1, zipf=0.0, T=8, calib_T=8, gen="cuda"),
+    "ultra_prefill_T4096_zipf1.1": dict(dims=ULTRA, seed=1, zipf=1.1, T=4096, calib_T=8,
+                                        gen="cuda"),
+}

@@ -66,6 +66,9 @@ def lib() -> C.CDLL:
         "lmoe_set_debug": (C.c_int, [vp, C.c_int]),
         "lmoe_get_expert_nvfp4": (C.c_int, [vp, C.c_int, C.c_int, vp, vp, C.POINTER(C.c_float), vp]),
         "lmoe_check": (C.c_int, [vp, vp]),
+        "lmoe_forward_kernel_count": (C.c_int, [vp, i64]),
+        "lmoe_set_profile": (C.c_int, [vp, C.c_int]),
+        "lmoe_profile_read": (C.c_int, [vp, C.POINTER(C.c_char_p), C.POINTER(C.c_float), C.c_int]),
         "lmoe_destroy": (None, [vp]),
     }
     for name, (res, args) in sig.items():
@@ -176,6 +179,24 @@ def lmoe_get_expert_nvfp4(ctx, which, e, codes, sf, stream=None) -> float:
     _check(lib().lmoe_get_expert_nvfp4(ctx, which, e, _ptr(codes), _ptr(sf), C.byref(sd),
                                        _stream(stream)), "lmoe_get_expert_nvfp4")
     return sd.value
+
+
+def lmoe_forward_kernel_count(ctx, T) -> int:
+    return lib().lmoe_forward_kernel_count(ctx, T)
+
+
+def lmoe_set_profile(ctx, on: bool):
+    _check(lib().lmoe_set_profile(ctx, 1 if on else 0), "lmoe_set_profile")
+
+
+def lmoe_profile_read(ctx, max_kernels: int = 32) -> list[tuple[str, float]]:
+    """[(kernel name, ms)] of the last forward run with profiling on."""
+    names = (C.c_char_p * max_kernels)()
+    ms = (C.c_float * max_kernels)()
+    n = lib().lmoe_profile_read(ctx, names, ms, max_kernels)
+    if n < 0:
+        raise LmoeError(LMOE_EINVAL, "lmoe_profile_read")
+    return [(names[i].decode(), float(ms[i])) for i in range(n)]
 
 
 def lmoe_check(ctx, stream=None):

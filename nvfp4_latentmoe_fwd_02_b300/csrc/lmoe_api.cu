@@ -93,6 +93,11 @@ struct lmoe_ctx {
     int debug;
     void *route_ws;
     size_t route_ws_bytes;
+    // per-kernel timing (lmoe_set_profile)
+    int profile;
+    int nprof;
+    cudaEvent_t ev[33];
+    const char *prof_name[32];
 };
 
 namespace {
@@ -193,6 +198,14 @@ int grid_for(int64_t tiles, int num_sms) {
     return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tiles, num_sms)));
 }
 
+// Record the end of the kernel just launched (profiling mode only).
+inline void prof_mark(lmoe_ctx *c, const char *name, cudaStream_t s) {
+    if (!c->profile || c->nprof >= 32) return;
+    c->prof_name[c->nprof] = name;
+    cudaEventRecord(c->ev[c->nprof + 1], s);
+    ++c->nprof;
+}
+
 lmoe_status check_error_word(lmoe_ctx *c) {
     unsigned v = 0;
     if (cudaMemcpy(&v, c->err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return LMOE_ECUDA;
@@ -203,7 +216,7 @@ lmoe_status check_error_word(lmoe_ctx *c) {
 }
 
 // The router on x: logits (chunk partials or tiled), top-k + softmax + counts.
-lmoe_status launch_router(const lmoe_ctx *c, const __nv_bfloat16 *x, int64_t T, bool partials,
+lmoe_status launch_router(lmoe_ctx *c, const __nv_bfloat16 *x, int64_t T, bool partials,
                           float *scratch, int32_t *idx, float *w, int32_t *counts,
                           cudaStream_t s) {
     const int C = c->d / kChunk;
@@ -216,10 +229,12 @@ lmoe_status launch_router(const lmoe_ctx *c, const __nv_bfloat16 *x, int64_t T, 
                                                   c->E, scratch);
     }
     LMOE_LAUNCH();
+    prof_mark(c, partials ? "router_partials" : "router_logits", s);
     router_topk_kernel<<<static_cast<unsigned>(cdiv(T, 8)), 256, 0, s>>>(
         scratch, partials ? 0 : 1, static_cast<int>(T), c->E, C, c->k,
         partials ? c->b_router : nullptr, idx, w, counts);
     LMOE_LAUNCH();
+    prof_mark(c, "router_topk", s);
     return LMOE_OK;
 }
 
@@ -394,6 +409,8 @@ void lmoe_destroy(lmoe_ctx *c) {
                     c->amax_bits, c->err, c->route_ws};
     for (void *p : ptrs)
         if (p) cudaFree(p);
+    for (cudaEvent_t e : c->ev)
+        if (e) cudaEventDestroy(e);
     delete c;
 }
 
@@ -492,6 +509,10 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     __nv_bfloat16 *cb = static_cast<__nv_bfloat16 *>(at(L.c));
     float *yacc = static_cast<float *>(at(L.yacc));
     const int d = c->d, l = c->l, E = c->E, k = c->k, F = c->ffn;
+    if (c->profile) {
+        c->nprof = 0;
+        cudaEventRecord(c->ev[0], s);
+    }
 
     // 0. zero the accumulators and the expert histogram
     {
@@ -503,6 +524,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         if (L.split_up) { z.p[3] = reinterpret_cast<uint4 *>(yacc); z.n16[3] = T * d * 4 / 16; }
         zero_kernel<<<c->num_sms * 4, 256, 0, s>>>(z);
         LMOE_LAUNCH();
+        prof_mark(c, "zero", s);
     }
     // 1. router
     {
@@ -513,6 +535,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     // 2. per-expert segments
     segments_kernel<<<1, 1024, 0, s>>>(counts, E, seg, mt, fill, row_slot, nrows);
     LMOE_LAUNCH();
+    prof_mark(c, "segments", s);
     // 3. down-projection z = x Wd^T, quantized to NVFP4
     {
         CUtensorMap tx;
@@ -526,10 +549,12 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         }
         LMOE_CUDA((launch_gemm<false, kStagesBF16>(tx, c->tm_wd, g,
                                                    grid_for(int64_t(g.m_tiles) * g.n_tiles * g.k_splits, c->num_sms), s)));
+        prof_mark(c, "down_proj", s);
         if (L.split_down) {
             const int grid = static_cast<int>(std::min<int64_t>(cdiv(T * l / 16, 256), c->num_sms * 8));
             z_finalize_kernel<<<grid, 256, 0, s>>>(zacc, T, l, c->qz, zq_codes, zq_sf, z_dbg);
             LMOE_LAUNCH();
+            prof_mark(c, "z_finalize", s);
         }
     }
     // 4. gather the quantized latent tokens into per-expert segments
@@ -538,6 +563,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         scatter_kernel<<<static_cast<unsigned>(cdiv(nslots, 8)), 256, 0, s>>>(
             idx, nslots, seg, fill, row_slot, k, l, zq_codes, zq_sf, a_codes, a_sf);
         LMOE_LAUNCH();
+        prof_mark(c, "scatter", s);
     }
     // 5. latent-up grouped GEMM + relu^2 + requantize
     {
@@ -553,6 +579,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         g.epi = EPI_H_QUANT; g.q = c->qh; g.q_codes = h_codes; g.q_sf = h_sf; g.dbg = h_dbg;
         g.alpha = c->alpha1; g.err = c->err;
         LMOE_CUDA((launch_gemm<true, kStagesF4>(ta, c->tm_w1, g, c->num_sms, s)));
+        prof_mark(c, "expert_up", s);
     }
     // 6. latent-down grouped GEMM, routing weight, combine into c_acc
     {
@@ -568,12 +595,14 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         g.epi = EPI_COMBINE; g.out = c_acc; g.ld_out = l;
         g.alpha = c->alpha2; g.row_slot = row_slot; g.route_w = rw; g.topk = k; g.err = c->err;
         LMOE_CUDA((launch_gemm<true, kStagesF4>(ta, c->tm_w2, g, c->num_sms, s)));
+        prof_mark(c, "expert_down", s);
     }
     // 7. c = bf16(c_acc)
     {
         const int grid = static_cast<int>(std::min<int64_t>(cdiv(T * l / 8, 256), c->num_sms * 8));
         f32_to_bf16_kernel<<<grid, 256, 0, s>>>(c_acc, T * l, cb);
         LMOE_LAUNCH();
+        prof_mark(c, "combine_cast", s);
     }
     // 8. up-projection y = c Wu^T
     {
@@ -585,10 +614,12 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         g.ld_out = d;
         LMOE_CUDA((launch_gemm<false, kStagesBF16>(tc, c->tm_wu, g,
                                                    grid_for(int64_t(g.m_tiles) * g.n_tiles * g.k_splits, c->num_sms), s)));
+        prof_mark(c, "up_proj", s);
         if (L.split_up) {
             const int grid = static_cast<int>(std::min<int64_t>(cdiv(T * d / 8, 256), c->num_sms * 8));
             f32_to_bf16_kernel<<<grid, 256, 0, s>>>(yacc, T * d, static_cast<__nv_bfloat16 *>(y));
             LMOE_LAUNCH();
+            prof_mark(c, "y_cast", s);
         }
     }
     return LMOE_OK;
@@ -630,6 +661,37 @@ lmoe_status lmoe_get_expert_nvfp4(const lmoe_ctx *c, int which, int e, uint8_t *
     LMOE_CUDA(cudaMemcpyAsync(s_dec, (which == 1 ? c->w1_sdec : c->w2_sdec) + e, 4, cudaMemcpyDeviceToHost, s));
     LMOE_CUDA(cudaStreamSynchronize(s));
     return LMOE_OK;
+}
+
+int lmoe_forward_kernel_count(const lmoe_ctx *c, int64_t T) {
+    if (!c || T <= 0) return 0;
+    const WsLayout L = layout(c, T);
+    // zero, router logits, top-k, segments, down-proj, scatter, expert-up, expert-down,
+    // combine cast, up-proj, plus one finalize per split projection
+    return 10 + (L.split_down ? 1 : 0) + (L.split_up ? 1 : 0);
+}
+
+lmoe_status lmoe_set_profile(lmoe_ctx *c, int on) {
+    if (!c) return LMOE_EINVAL;
+    if (on && !c->ev[0]) {
+        for (cudaEvent_t &e : c->ev) LMOE_CUDA(cudaEventCreate(&e));
+    }
+    c->profile = on ? 1 : 0;
+    c->nprof = 0;
+    return LMOE_OK;
+}
+
+int lmoe_profile_read(lmoe_ctx *c, const char **names, float *ms, int max) {
+    if (!c || !c->profile || c->nprof == 0 || max < 0) return -1;
+    if (cudaEventSynchronize(c->ev[c->nprof]) != cudaSuccess) return -1;
+    const int n = std::min(c->nprof, max);
+    for (int i = 0; i < n; ++i) {
+        float t = 0.0f;
+        cudaEventElapsedTime(&t, c->ev[i], c->ev[i + 1]);
+        if (names) names[i] = c->prof_name[i];
+        if (ms) ms[i] = t;
+    }
+    return n;
 }
 
 lmoe_status lmoe_check(lmoe_ctx *c, lmoe_stream stream) {
