@@ -27,7 +27,7 @@ namespace {
 
 constexpr int kStagesF4 = 5;
 constexpr int kStagesBF16 = 6;
-constexpr int kPartialsMaxT = 64;   // router: chunk-partials kernel up to this many tokens
+constexpr int kSmallRouterMaxT = 64;   // router: shared-memory chunk reduction up to this T
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -72,7 +72,7 @@ struct WsLayout {
     size_t idx, w, counts, seg, mt, fill, nrows, row_slot, router, zacc, zq_codes, zq_sf, z_dbg,
         a_codes, a_sf, h_codes, h_sf, h_dbg, c_acc, c, yacc, total;
     int64_t R;   // row capacity of the permuted buffers (multiple of 128)
-    bool partials, split_down, split_up;
+    bool small_router, split_down, split_up;
     int down_splits, up_splits;
 };
 
@@ -134,7 +134,7 @@ WsLayout layout(const lmoe_ctx *c, int64_t T) {
     const int64_t d = c->d, l = c->l, E = c->E, k = c->k, F = c->ffn;
     L.R = cdiv(T * k + E * 127, 128) * 128;
     if (L.R == 0) L.R = 128;
-    L.partials = T <= kPartialsMaxT;
+    L.small_router = T <= kSmallRouterMaxT;
     const int mt = static_cast<int>(cdiv(T, 128));
     L.down_splits = plan_splits(mt, static_cast<int>(cdiv(l, 128)), static_cast<int>(d / 64), c->num_sms);
     L.up_splits = plan_splits(mt, static_cast<int>(cdiv(d, 128)), static_cast<int>(l / 64), c->num_sms);
@@ -150,7 +150,7 @@ WsLayout layout(const lmoe_ctx *c, int64_t T) {
     L.fill = take(E * 4);
     L.nrows = take(4);
     L.row_slot = take(L.R * 4);
-    L.router = take(L.partials ? T * E * (d / kChunk) * 4 : T * E * 4);
+    L.router = take(T * E * 4);
     L.zacc = take(L.split_down ? T * l * 4 : 0);
     L.zq_codes = take(T * l / 2);
     L.zq_sf = take(T * l / 16);
@@ -215,27 +215,31 @@ lmoe_status check_error_word(lmoe_ctx *c) {
     return LMOE_OK;
 }
 
-// The router on x: logits (chunk partials or tiled), top-k + softmax + counts.
-lmoe_status launch_router(lmoe_ctx *c, const __nv_bfloat16 *x, int64_t T, bool partials,
-                          float *scratch, int32_t *idx, float *w, int32_t *counts,
-                          cudaStream_t s) {
-    const int C = c->d / kChunk;
-    if (partials) {
-        dim3 grid(static_cast<unsigned>(cdiv(C, 32)), static_cast<unsigned>(cdiv(c->E, 8)));
-        router_partials_kernel<<<grid, 256, 0, s>>>(x, c->w_router, static_cast<int>(T), c->d, c->E, scratch);
+// The router on x: logits (small-T or tiled kernel) into `logits` [T][E], then top-k,
+// softmax and counts.
+lmoe_status launch_router(lmoe_ctx *c, const __nv_bfloat16 *x, int64_t T, float *logits,
+                          int32_t *idx, float *w, int32_t *counts, cudaStream_t s) {
+    const bool small = T <= kSmallRouterMaxT && c->d / kChunk <= kSmallMaxC;
+    if (small) {
+        router_small_kernel<<<static_cast<unsigned>(cdiv(c->E, 2)), 256, 0, s>>>(
+            x, c->w_router, c->b_router, static_cast<int>(T), c->d, c->E, logits);
     } else {
         dim3 grid(static_cast<unsigned>(cdiv(T, kRT)), static_cast<unsigned>(cdiv(c->E, kRE)));
         router_logits_kernel<<<grid, 128, 0, s>>>(x, c->w_router, c->b_router, static_cast<int>(T), c->d,
-                                                  c->E, scratch);
+                                                  c->E, logits);
     }
     LMOE_LAUNCH();
-    prof_mark(c, partials ? "router_partials" : "router_logits", s);
+    prof_mark(c, small ? "router_small" : "router_logits", s);
     router_topk_kernel<<<static_cast<unsigned>(cdiv(T, 8)), 256, 0, s>>>(
-        scratch, partials ? 0 : 1, static_cast<int>(T), c->E, C, c->k,
-        partials ? c->b_router : nullptr, idx, w, counts);
+        logits, static_cast<int>(T), c->E, c->k, idx, w, counts);
     LMOE_LAUNCH();
     prof_mark(c, "router_topk", s);
     return LMOE_OK;
+}
+
+// Scratch bytes the router needs for T tokens (the fp32 logits).
+size_t route_scratch_bytes(const lmoe_ctx *c, int64_t T) {
+    return static_cast<size_t>(T) * c->E * 4;
 }
 
 }  // namespace
@@ -459,9 +463,7 @@ lmoe_status lmoe_route(lmoe_ctx *c, const void *x, int64_t T, int32_t *idx, floa
     if (T == 0) return LMOE_OK;
     if (!x || !idx || !w) return LMOE_EINVAL;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const bool partials = T <= kPartialsMaxT;
-    const size_t need = partials ? static_cast<size_t>(T) * c->E * (c->d / kChunk) * 4
-                                 : static_cast<size_t>(T) * c->E * 4;
+    const size_t need = route_scratch_bytes(c, T);
     if (need > c->route_ws_bytes) {
         if (c->route_ws) LMOE_CUDA(cudaFreeAsync(c->route_ws, s));
         c->route_ws = nullptr;
@@ -470,7 +472,7 @@ lmoe_status lmoe_route(lmoe_ctx *c, const void *x, int64_t T, int32_t *idx, floa
         c->route_ws_bytes = need;
     }
     if (counts) LMOE_CUDA(cudaMemsetAsync(counts, 0, c->E * 4, s));
-    return launch_router(c, static_cast<const __nv_bfloat16 *>(x), T, partials,
+    return launch_router(c, static_cast<const __nv_bfloat16 *>(x), T,
                          static_cast<float *>(c->route_ws), idx, w, counts, s);
 }
 
@@ -528,7 +530,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     }
     // 1. router
     {
-        lmoe_status st = launch_router(c, static_cast<const __nv_bfloat16 *>(x), T, L.partials,
+        lmoe_status st = launch_router(c, static_cast<const __nv_bfloat16 *>(x), T,
                                        static_cast<float *>(at(L.router)), idx, rw, counts, s);
         if (st != LMOE_OK) return st;
     }

@@ -6,8 +6,8 @@
 //   the d axis is cut into chunks of 64; p_c = fmaf chain over the chunk in ascending index
 //   starting from +0; logit = ((0 + p_0) + p_1) + ... in ascending c; then + bias.
 // Two kernels produce exactly these fp32 operations:
-//   router_partials_kernel   small T: one thread per (expert, chunk) computes p_c for all
-//                            tokens; the top-k kernel then adds the chunk partials in order;
+//   router_small_kernel      small T: one thread per (expert, chunk) computes p_c for a tile
+//                            of tokens; the partials are added in order from shared memory;
 //   router_logits_kernel     large T: register-tiled, each thread walks the chunks in order.
 // Selection: logit descending, lower expert index first on ties.  Weights: softmax (fp32,
 // expf) over the k selected logits.  Output slots are in ascending expert id.
@@ -18,55 +18,60 @@ namespace lmoe {
 
 constexpr int kChunk = 64;
 
-// P[t][e][c] = p_c(t, e).  Block: 8 warps = 8 experts; lane = chunk within a 32-chunk group.
-// grid = (ceil(C/32), ceil(E/8)).  Tokens are processed 4 at a time from shared memory.
-__global__ void __launch_bounds__(256) router_partials_kernel(
-    const __nv_bfloat16 *__restrict__ x, const float *__restrict__ Wr, int T, int d, int E,
-    float *__restrict__ P) {
-    constexpr int TT = 4;
-    __shared__ float xs[TT][32][kChunk + 1];
+// Small T: logits[t][e] with the chunk partials reduced through shared memory.  Block: two
+// experts x 128 threads; thread c computes the partial p_c (one 64-element fmaf chain) of its
+// chunk(s) for a tile of 8 tokens, then one thread per token adds the chunk partials of its
+// expert left to right and the bias.  grid = ceil(E / 2).
+constexpr int kSmallTT = 8;
+constexpr int kSmallMaxC = 256;   // d <= 16384
+__global__ void __launch_bounds__(256) router_small_kernel(
+    const __nv_bfloat16 *__restrict__ x, const float *__restrict__ Wr,
+    const float *__restrict__ bias, int T, int d, int E, float *__restrict__ logits) {
+    __shared__ float ps[2][kSmallTT][kSmallMaxC + 1];
+    const int grp = threadIdx.x >> 7, tc = threadIdx.x & 127;
+    const int e = blockIdx.x * 2 + grp;
     const int C = d / kChunk;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int c = blockIdx.x * 32 + lane;
-    const int e = blockIdx.y * 8 + warp;
-    const bool active = (c < C) && (e < E);
-    float w[kChunk];
-    if (active) {
-        const float4 *src = reinterpret_cast<const float4 *>(Wr + static_cast<int64_t>(e) * d + c * kChunk);
+    for (int t0 = 0; t0 < T; t0 += kSmallTT) {
+        const int nt = min(kSmallTT, T - t0);
+        if (e < E) {
+            for (int c = tc; c < C; c += 128) {
+                float w[kChunk];
+                const float4 *src = reinterpret_cast<const float4 *>(Wr + static_cast<int64_t>(e) * d + c * kChunk);
 #pragma unroll
-        for (int i = 0; i < kChunk / 4; ++i) {
-            float4 f = __ldg(src + i);
-            w[4 * i] = f.x; w[4 * i + 1] = f.y; w[4 * i + 2] = f.z; w[4 * i + 3] = f.w;
-        }
-    }
-    const int c_base = blockIdx.x * 32;
-    const int nc = min(32, C - c_base);
-    for (int t0 = 0; t0 < T; t0 += TT) {
-        const int nt = min(TT, T - t0);
-        __syncthreads();
-        // stage x[t0 .. t0+nt)[c_base*64 .. +nc*64) as fp32
-        for (int i = threadIdx.x; i < nt * nc * (kChunk / 8); i += blockDim.x) {
-            const int t = i / (nc * (kChunk / 8));
-            const int rem = i - t * (nc * (kChunk / 8));
-            const int cc = rem / (kChunk / 8), q = rem - cc * (kChunk / 8);
-            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(
-                x + static_cast<int64_t>(t0 + t) * d + (c_base + cc) * kChunk + q * 8));
-            const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+                for (int i = 0; i < kChunk / 4; ++i) {
+                    const float4 f = __ldg(src + i);
+                    w[4 * i] = f.x; w[4 * i + 1] = f.y; w[4 * i + 2] = f.z; w[4 * i + 3] = f.w;
+                }
+                float p[kSmallTT];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                xs[t][cc][q * 8 + 2 * j] = __uint_as_float(ww[j] << 16);
-                xs[t][cc][q * 8 + 2 * j + 1] = __uint_as_float(ww[j] & 0xFFFF0000u);
+                for (int t = 0; t < kSmallTT; ++t) p[t] = 0.0f;
+#pragma unroll
+                for (int q = 0; q < kChunk / 8; ++q) {
+#pragma unroll
+                    for (int t = 0; t < kSmallTT; ++t) {
+                        if (t < nt) {
+                            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(
+                                x + static_cast<int64_t>(t0 + t) * d + c * kChunk + q * 8));
+                            const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                p[t] = fmaf(__uint_as_float(ww[j] << 16), w[q * 8 + 2 * j], p[t]);
+                                p[t] = fmaf(__uint_as_float(ww[j] & 0xFFFF0000u), w[q * 8 + 2 * j + 1], p[t]);
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < kSmallTT; ++t) ps[grp][t][c] = p[t];
             }
         }
         __syncthreads();
-        if (active) {
-            for (int t = 0; t < nt; ++t) {
-                float p = 0.0f;
-#pragma unroll
-                for (int i = 0; i < kChunk; ++i) p = fmaf(xs[t][lane][i], w[i], p);
-                P[(static_cast<int64_t>(t0 + t) * E + e) * C + c] = p;
-            }
+        if (e < E && tc < nt) {
+            float acc = 0.0f;
+            for (int c = 0; c < C; ++c) acc = __fadd_rn(acc, ps[grp][tc][c]);
+            logits[static_cast<int64_t>(t0 + tc) * E + e] = __fadd_rn(acc, bias ? bias[e] : 0.0f);
         }
+        __syncthreads();
     }
 }
 
@@ -152,13 +157,12 @@ __global__ void __launch_bounds__(128) router_logits_kernel(
     }
 }
 
-// One warp per token: finish the logits (partials mode), select top-k, softmax, write
-// idx / w in ascending expert id, count tokens per expert.
-// mode 0: src = P[T][E][C] (chunk partials), bias added here; mode 1: src = logits[T][E].
+// One warp per token: select top-k from logits[T][E], softmax, write idx / w in ascending
+// expert id, count tokens per expert.
 constexpr int kMaxEPerLane = 32;   // E <= 1024
 __global__ void __launch_bounds__(256) router_topk_kernel(
-    const float *__restrict__ src, int mode, int T, int E, int C, int k,
-    const float *__restrict__ bias, int32_t *__restrict__ idx_out, float *__restrict__ w_out,
+    const float *__restrict__ logits, int T, int E, int k, int32_t *__restrict__ idx_out,
+    float *__restrict__ w_out,
     int32_t *__restrict__ counts) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -169,16 +173,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
     for (int j = 0; j < kMaxEPerLane; ++j) {
         v[j] = -INFINITY;
         const int e = lane + 32 * j;
-        if (j < npl && e < E) {
-            if (mode == 0) {
-                const float *pp = src + (static_cast<int64_t>(t) * E + e) * C;
-                float acc = 0.0f;
-                for (int c = 0; c < C; ++c) acc = __fadd_rn(acc, __ldg(pp + c));
-                v[j] = __fadd_rn(acc, bias ? bias[e] : 0.0f);
-            } else {
-                v[j] = src[static_cast<int64_t>(t) * E + e];
-            }
-        }
+        if (j < npl && e < E) v[j] = logits[static_cast<int64_t>(t) * E + e];
     }
     uint32_t taken = 0u;
     int my_idx = 0;
