@@ -100,6 +100,29 @@ lmoe_status lmoe_quantize_nvfp4(const void *src, lmoe_dtype dt, int64_t rows, in
 lmoe_status lmoe_route(lmoe_ctx *ctx, const void *x, int64_t T, int32_t *idx, float *w,
                        int32_t *counts, lmoe_stream stream);
 
+/* Allocation-free routing.  The paper has no counterpart: this is a deployment convenience.
+ * Some callers cannot allocate device memory at the moment they route: code running inside an
+ * allocator or memory-pool callback (where re-entering the allocator can deadlock), serving
+ * loops whose device memory is fixed at start-up, and hosts that embed the library without
+ * handing it any allocator.  lmoe_route may grow a context-owned scratch with cudaMallocAsync;
+ * lmoe_route_static never allocates or frees.  It has lmoe_route's arguments and results, but
+ * keeps the router's scratch (the T x E fp32 logits) in one fixed array of
+ * LMOE_ROUTE_STATIC_SCRATCH_BYTES compiled into liblmoe.so, which every GPU that loads the
+ * library holds until the process exits.
+ *   - T * E * 4 must not exceed LMOE_ROUTE_STATIC_SCRATCH_BYTES (T <= 8192 at E = 512);
+ *     larger T returns LMOE_EINVAL before anything is launched.
+ *   - The first call on a device looks up the array's device address (once per device, with
+ *     that device current; the context's device must be current).  Make that first call before
+ *     any CUDA stream capture.
+ *   - Every call on a device shares the one array, and it keeps the last call's contents.  The
+ *     logits are fully written before they are read, and `counts` is zeroed by the call, so no
+ *     earlier contents leak into a result; but two calls whose kernels overlap on the GPU (on
+ *     different streams, or from different contexts of one device) race on the array: order
+ *     such calls on one stream or with events. */
+#define LMOE_ROUTE_STATIC_SCRATCH_BYTES (16u << 20)
+lmoe_status lmoe_route_static(lmoe_ctx *ctx, const void *x, int64_t T, int32_t *idx, float *w,
+                              int32_t *counts, lmoe_stream stream);
+
 /* Bytes of device workspace lmoe_forward needs for T tokens (256-byte aligned pointer). */
 size_t lmoe_workspace_size(const lmoe_ctx *ctx, int64_t T);
 

@@ -58,6 +58,7 @@ def lib() -> C.CDLL:
         "lmoe_create": (C.c_int, [C.c_int] * 5 + [C.POINTER(_Weights), vp, C.POINTER(vp)]),
         "lmoe_quantize_nvfp4": (C.c_int, [vp, C.c_int, i64, i64, C.c_float, vp, vp, vp, vp]),
         "lmoe_route": (C.c_int, [vp, vp, i64, vp, vp, vp, vp]),
+        "lmoe_route_static": (C.c_int, [vp, vp, i64, vp, vp, vp, vp]),
         "lmoe_workspace_size": (sz, [vp, i64]),
         "lmoe_forward": (C.c_int, [vp, vp, i64, vp, vp, sz, vp]),
         "lmoe_host_workspace_size": (sz, [vp, i64]),
@@ -142,6 +143,13 @@ def lmoe_destroy(ctx: int):
 def lmoe_route(ctx, x, T, idx, w, counts=None, stream=None):
     _check(lib().lmoe_route(ctx, _ptr(x), T, _ptr(idx), _ptr(w), _ptr(counts), _stream(stream)),
            "lmoe_route")
+
+
+def lmoe_route_static(ctx, x, T, idx, w, counts=None, stream=None):
+    """lmoe_route without any device allocation (fixed scratch inside the library; see the
+    header for the size limit and the first-call and concurrency rules)."""
+    _check(lib().lmoe_route_static(ctx, _ptr(x), T, _ptr(idx), _ptr(w), _ptr(counts),
+                                   _stream(stream)), "lmoe_route_static")
 
 
 def lmoe_workspace_size(ctx, T) -> int:

@@ -242,6 +242,31 @@ size_t route_scratch_bytes(const lmoe_ctx *c, int64_t T) {
     return static_cast<size_t>(T) * c->E * 4;
 }
 
+// ---------------------------------------------------------------------------------------
+// Fixed router scratch for callers that cannot allocate (lmoe_route_static).  In host code
+// `g_route_static_scratch` names a host-side stand-in, not device memory: its device address
+// is looked up once per device with cudaGetSymbolAddress and that address is what the
+// kernels receive.
+// ---------------------------------------------------------------------------------------
+__device__ __align__(256) unsigned char g_route_static_scratch[LMOE_ROUTE_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void *g_static_ptr[kMaxDevices] = {};
+
+lmoe_status route_static_scratch(int dev, void **out) {
+    if (dev < 0 || dev >= kMaxDevices) return LMOE_EUNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_route_static_scratch);
+        if (e != cudaSuccess || !p) return e != cudaSuccess ? cuda_status(e) : LMOE_ECUDA;
+        g_static_ptr[dev] = p;
+    }
+    *out = g_static_ptr[dev];
+    return LMOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -416,6 +441,24 @@ void lmoe_destroy(lmoe_ctx *c) {
     for (cudaEvent_t e : c->ev)
         if (e) cudaEventDestroy(e);
     delete c;
+}
+
+lmoe_status lmoe_route_static(lmoe_ctx *c, const void *x, int64_t T, int32_t *idx, float *w,
+                              int32_t *counts, lmoe_stream stream) {
+    if (!c || T < 0) return LMOE_EINVAL;
+    if (T == 0) return LMOE_OK;
+    if (!x || !idx || !w) return LMOE_EINVAL;
+    if (route_scratch_bytes(c, T) > LMOE_ROUTE_STATIC_SCRATCH_BYTES) return LMOE_EINVAL;
+    int dev = -1;
+    LMOE_CUDA(cudaGetDevice(&dev));
+    if (dev != c->dev) return LMOE_EINVAL;
+    void *scratch = nullptr;
+    const lmoe_status st = route_static_scratch(dev, &scratch);
+    if (st != LMOE_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (counts) LMOE_CUDA(cudaMemsetAsync(counts, 0, c->E * 4, s));
+    return launch_router(c, static_cast<const __nv_bfloat16 *>(x), T, static_cast<float *>(scratch),
+                         idx, w, counts, s);
 }
 
 size_t lmoe_workspace_size(const lmoe_ctx *c, int64_t T) {
