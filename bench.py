@@ -178,6 +178,8 @@ def build_layers(names):
                            L.w_router, b, L.w1, L.w2, cal["amax_z"], cal["amax_h"])
         out[n] = moe
     torch.cuda.synchronize()
+    L.w1 = L.w2 = None            # the contexts hold the quantized experts; masters not kept
+    torch.cuda.empty_cache()
     return L, out
 
 
@@ -205,10 +207,14 @@ class Runner:
                 self.graphs.append(g)
         torch.cuda.synchronize()
         self.flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.flush_src = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+        self.flush_sink = torch.empty(1, dtype=torch.int64, device="cuda")
 
     def flush(self):
+        """Write 256 MB (evicts L2), then read another 256 MB (writes the dirty lines back)."""
         with torch.cuda.stream(self.stream):
             self.flush_buf.fill_(1)
+            self.flush_sink.copy_(self.flush_src.sum(dtype=torch.int64).view(1))
 
     def timed_steps(self, K, warmup):
         for i in range(warmup):
@@ -301,7 +307,8 @@ def cpu_baseline(T, L, cfg_name, budget_s=20.0):
     cal = calibration(cfg_name)
     ol = oracle.OracleLayer(dims.d, dims.l, dims.E, dims.k, dims.ffn, host["w_down"], host["w_up"],
                             host["w_router"], b.numpy(),
-                            lambda e: (L.w1[e].float().cpu().numpy(), L.w2[e].float().cpu().numpy()),
+                            lambda e: tuple(t.float().cpu().numpy()
+                                            for t in lmoe_synth.expert(dims, cfg["seed"], e, "cuda")),
                             cal["amax_z"], cal["amax_h"])
     x = lmoe_synth.tokens(T, dims.d, cfg["seed"] * 7919 + 101, "cuda").float().cpu().numpy()
     _, idx, _, _ = ol.route(x)
@@ -327,7 +334,9 @@ def run_reference(a, dist):
         return
     cfg = lmoe_synth.CONFIGS[HEADLINE]
     dims, T = cfg["dims"], cfg["T"]
-    L = lmoe_synth.layer(dims, cfg["seed"], "cuda", 0.0)
+    wd, wu = lmoe_synth.projections(dims, cfg["seed"], "cuda")
+    wr, b = lmoe_synth.router(dims, cfg["seed"], "cuda", 0.0)
+    L = lmoe_synth.Layer(dims, cfg["seed"], 0.0, wd, wu, wr, b, None, None)
     cb, ol, x = cpu_baseline(T, L, HEADLINE, budget_s=1.0)
     for _ in range(a.warmup):
         ol.forward(x, quant=True, want=("y",))
@@ -355,7 +364,7 @@ def workload_config(name):
                         f"ffn={d.ffn}, routing {'uniform' if c['zipf'] == 0 else 'Zipf(%g)' % c['zipf']}",
             "T": c["T"], "d": d.d, "l": d.l, "E": d.E, "k": d.k, "ffn": d.ffn,
             "routing": "uniform" if c["zipf"] == 0 else f"zipf{c['zipf']}",
-            "l2": "flushed before every step (256 MB write, outside the step's events)",
+            "l2": "flushed before every step (256 MB write + 256 MB read, outside the step's events)",
             "graph": "one CUDA graph replay per step"}
 
 

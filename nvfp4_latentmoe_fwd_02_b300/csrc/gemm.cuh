@@ -7,14 +7,17 @@
 //     UE4M3 scales, one per 16 K, E2M1 operands; blog section 3.1.1), grouped per expert.
 // D[m][n] = sum_k A[m][k] * B[n][k]: A = activations (rows = tokens), B = weights (rows = output
 // features); both K-major.  Tile 128 x 128, one SW128 row of 128 bytes per operand per stage
-// (64 bf16 or 256 e2m1 elements of K).
+// (64 bf16 or 256 e2m1 elements of K).  A is fetched in 32-row boxes, only as many as the tile
+// has valid rows (a decode tile of one token moves 4 KB of A per stage, not 16 KB); rows past
+// the loaded boxes hold stale data whose accumulator rows the epilogue never reads.
 //
-// Warp roles (192 threads, one CTA per SM):
+// Warp roles (320 threads, one CTA per SM):
 //   warp 0      TMA producer (one elected lane): operand tiles + scale atoms -> smem ring
 //   warp 1      TMEM allocator and MMA issuer (one lane): scale atoms smem -> TMEM with
 //               tcgen05.cp, tcgen05.mma into one of two 128-column accumulators
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads lane quadrant w % 4),
-//               fused output transform, global stores / reductions
+//   warps 2..9  epilogue: tcgen05.ld of the accumulator (warp w reads lane quadrant w % 4;
+//               two warps per quadrant, each taking half of the tile's columns), fused
+//               output transform, global stores / reductions
 // Barriers: full/empty per smem stage, tmem_full/tmem_empty per accumulator.  Every wait is
 // bounded (common.cuh); on a timeout the CTA records LMOE_ETIMEOUT, the roles leave their
 // loops, outstanding tensor-core work is drained with a bounded wait and TMEM is freed.
@@ -34,6 +37,8 @@ enum EpiMode : int {
 
 constexpr int kBM = 128, kBN = 128;
 constexpr int kTileBytes = kBM * 128;     // 16 KB per operand per stage
+constexpr int kABoxRows = 32;             // A is loaded in 32-row boxes: only the valid rows
+constexpr int kABoxBytes = kABoxRows * 128;
 constexpr int kSfStageBytes = 4 * 512;    // 4 scale atoms (4 x K64) per operand per stage
 
 struct GemmArgs {
@@ -64,23 +69,31 @@ struct Tile {
     int e, a_row0, rows, b_row0, n0, cols, kt0, kt1;
 };
 
-__device__ __forceinline__ Tile decode_tile(const GemmArgs &g, int t) {
+// Per-expert tables copied to shared memory at kernel start (grouped GEMMs): every role
+// decodes every tile, so the binary search must not walk global memory.
+struct SmemTables {
+    int32_t mt[1025];    // mt_start[0..E]
+    int32_t seg[1024];   // seg_start[e]
+    int32_t cnt[1024];   // counts[e]
+};
+
+__device__ __forceinline__ Tile decode_tile(const GemmArgs &g, const SmemTables *tb, int t) {
     Tile tl;
     if (g.grouped) {
         const int key = t / g.n_tiles;
         int lo = 0, hi = g.E - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (__ldg(g.mt_start + mid) <= key) lo = mid; else hi = mid - 1;
+            if (tb->mt[mid] <= key) lo = mid; else hi = mid - 1;
         }
         const int e = lo;
-        const int mt0 = __ldg(g.mt_start + e);
-        const int mt_e = __ldg(g.mt_start + e + 1) - mt0;
+        const int mt0 = tb->mt[e];
+        const int mt_e = tb->mt[e + 1] - mt0;
         const int local = t - mt0 * g.n_tiles;
         const int m = local % mt_e, n = local / mt_e;
         tl.e = e;
-        tl.a_row0 = __ldg(g.seg_start + e) + m * kBM;
-        tl.rows = min(kBM, __ldg(g.counts + e) - m * kBM);
+        tl.a_row0 = tb->seg[e] + m * kBM;
+        tl.rows = min(kBM, tb->cnt[e] - m * kBM);
         tl.n0 = n * kBN;
         tl.b_row0 = e * g.N + n * kBN;
         tl.cols = min(kBN, g.N - n * kBN);
@@ -121,9 +134,35 @@ __device__ __forceinline__ bool role_wait(uint64_t *bar, uint32_t parity, volati
 // ------------------------------------------------------------------------------------
 // epilogue: one thread owns one accumulator row; 32 columns per call
 // ------------------------------------------------------------------------------------
-__device__ __forceinline__ void epilogue_chunk(const GemmArgs &g, const Tile &tl, int row,
-                                               int c0, const uint32_t (&r)[32]) {
-    if (row >= tl.rows) return;
+// Per-tile, per-row scalars, loaded before the accumulator is ready so their latency hides
+// behind the tile's MMAs.
+struct EpiRow {
+    float alpha;     // per-expert tensor-scale product (grouped GEMMs)
+    float wslot;     // routing weight of the row's slot (combine)
+    int64_t orow;    // output row: the token (combine)
+    bool valid;
+};
+
+__device__ __forceinline__ EpiRow epilogue_row(const GemmArgs &g, const Tile &tl, int row) {
+    EpiRow er;
+    er.alpha = 1.0f; er.wslot = 0.0f; er.orow = 0;
+    er.valid = row < tl.rows;
+    if (g.epi == EPI_H_QUANT || g.epi == EPI_COMBINE) er.alpha = __ldg(g.alpha + tl.e);
+    if (g.epi == EPI_COMBINE && er.valid) {
+        const int slot = __ldg(g.row_slot + tl.a_row0 + row);
+        if (slot < 0) {
+            er.valid = false;
+        } else {
+            er.orow = slot / g.topk;
+            er.wslot = __ldg(g.route_w + slot);
+        }
+    }
+    return er;
+}
+
+__device__ __forceinline__ void epilogue_chunk(const GemmArgs &g, const Tile &tl, const EpiRow &er,
+                                               int row, int c0, const uint32_t (&r)[32]) {
+    if (!er.valid) return;
     const int64_t grow = static_cast<int64_t>(tl.a_row0) + row;   // global row of A / output
     const int col = tl.n0 + c0;                                    // output column
     float v[32];
@@ -147,7 +186,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs &g, const Tile &tl
     case EPI_Z_QUANT:
     case EPI_H_QUANT: {
         if (g.epi == EPI_H_QUANT) {
-            const float a = __ldg(g.alpha + tl.e);
+            const float a = er.alpha;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const float u = fmaxf(__fmul_rn(a, v[i]), 0.0f);
@@ -183,12 +222,9 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs &g, const Tile &tl
         break;
     }
     case EPI_COMBINE: {
-        const int slot = __ldg(g.row_slot + grow);
-        if (slot < 0) break;
-        const int64_t t = slot / g.topk;
-        const float ws = __ldg(g.route_w + slot);
-        const float a = __ldg(g.alpha + tl.e);
-        float *o = static_cast<float *>(g.out) + t * g.ld_out + col;
+        const float ws = er.wslot;
+        const float a = er.alpha;
+        float *o = static_cast<float *>(g.out) + er.orow * g.ld_out + col;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             red_add_v4_f32(o + 4 * i, __fmul_rn(ws, __fmul_rn(a, v[4 * i])),
@@ -201,20 +237,30 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs &g, const Tile &tl
     }
 }
 
-template <bool NVF4>
+// SMALLA (decode): every tile has at most 32 valid A rows, so each stage keeps only one
+// 4 KB A box; the MMA still reads 128 rows from the stage's A base, and rows 32..127 fall on
+// the following stages' boxes (or on the slack after the last one): they only feed
+// accumulator rows the epilogue never reads.  The smaller stage buys more stages, i.e. more
+// weight bytes in flight per SM.
+template <bool NVF4, bool SMALLA>
 constexpr int gemm_smem_bytes(int stages) {
-    return 1024 + stages * (2 * kTileBytes + (NVF4 ? 2 * kSfStageBytes : 0)) + 256;
+    return 1024 + stages * ((SMALLA ? kABoxBytes : kTileBytes) + kTileBytes + (NVF4 ? 2 * kSfStageBytes : 0)) +
+           (SMALLA ? kTileBytes - kABoxBytes : 0) + 256 + (NVF4 ? static_cast<int>(sizeof(SmemTables)) : 0);
 }
 
-template <bool NVF4, int STAGES>
-__global__ void __launch_bounds__(192, 1)
+constexpr int kEpiWarps = 8;
+constexpr int kGemmThreads = 32 * (2 + kEpiWarps);
+
+template <bool NVF4, bool SMALLA, int STAGES>
+__global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmArgs g) {
     extern __shared__ uint8_t smem_raw[];
+    constexpr int kAStride = SMALLA ? kABoxBytes : kTileBytes;
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sA = smem;
-    uint8_t *sB = sA + STAGES * kTileBytes;
+    uint8_t *sB = sA + STAGES * kAStride + (SMALLA ? kTileBytes - kABoxBytes : 0);
     uint8_t *sSFA = sB + STAGES * kTileBytes;
     uint8_t *sSFB = sSFA + (NVF4 ? STAGES * kSfStageBytes : 0);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sSFB + (NVF4 ? STAGES * kSfStageBytes : 0));
@@ -222,6 +268,7 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t *tfull = bars + 2 * STAGES, *tempty = tfull + 2, *drain = tempty + 2;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
+    SmemTables *tb = reinterpret_cast<SmemTables *>(bars + 256 / 8);
 
     constexpr uint32_t kAccCols = kBN;
     constexpr uint32_t kTmemCols = NVF4 ? 512 : 256;
@@ -231,19 +278,25 @@ __global__ void __launch_bounds__(192, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4); }
+        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], kEpiWarps); }
         mbar_init(drain, 1);
         *s_abort = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) { prefetch_tmap(&tmA); prefetch_tmap(&tmB); }
     if (warp == 1) { tmem_alloc(s_tmem, kTmemCols); tmem_relinquish(); }
+    if (NVF4 && g.grouped) {
+        for (int i = threadIdx.x; i <= g.E; i += blockDim.x) {
+            tb->mt[i] = __ldg(g.mt_start + i);
+            if (i < g.E) { tb->seg[i] = __ldg(g.seg_start + i); tb->cnt[i] = __ldg(g.counts + i); }
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
 
-    const int num_tiles = g.grouped ? __ldg(g.mt_start + g.E) * g.n_tiles
+    const int num_tiles = g.grouped ? tb->mt[g.E] * g.n_tiles
                                     : g.m_tiles * g.n_tiles * g.k_splits;
     const int K64 = g.K / 64;
 
@@ -254,14 +307,17 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t phase = 0;
             uint32_t issued = 0, issued_phase = 0;   // per stage: ever issued / phase of last issue
             for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x) {
-                const Tile tl = decode_tile(g, t);
+                const Tile tl = decode_tile(g, tb, t);
                 for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
                     if (!role_wait(&empty[stage], phase ^ 1, s_abort, g.err)) break;
                     const int nsteps = NVF4 ? min(4, K64 - 4 * kt) : 4;
-                    const uint32_t bytes = 2 * kTileBytes + (NVF4 ? 2 * nsteps * 512 : 0);
+                    const int nbox = SMALLA ? 1 : (tl.rows + kABoxRows - 1) / kABoxRows;
+                    const uint32_t bytes = nbox * kABoxBytes + kTileBytes + (NVF4 ? 2 * nsteps * 512 : 0);
                     mbar_arrive_expect_tx(&full[stage], bytes);
                     const int kx = NVF4 ? kt * 128 : kt * 64;
-                    tma_load_2d(sA + stage * kTileBytes, &tmA, &full[stage], kx, tl.a_row0);
+                    for (int j = 0; j < nbox; ++j)
+                        tma_load_2d(sA + stage * kAStride + j * kABoxBytes, &tmA, &full[stage], kx,
+                                    tl.a_row0 + j * kABoxRows);
                     tma_load_2d(sB + stage * kTileBytes, &tmB, &full[stage], kx, tl.b_row0);
                     if (NVF4) {
                         bulk_load(sSFA + stage * kSfStageBytes,
@@ -294,7 +350,7 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t phase = 0;
             int it = 0;
             for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x, ++it) {
-                const Tile tl = decode_tile(g, t);
+                const Tile tl = decode_tile(g, tb, t);
                 const int acc = it & 1;
                 const uint32_t aphase = (it >> 1) & 1;
                 if (!role_wait(&tempty[acc], aphase ^ 1, s_abort, g.err)) break;
@@ -304,7 +360,7 @@ __global__ void __launch_bounds__(192, 1)
                 for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
                     if (!role_wait(&full[stage], phase, s_abort, g.err)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a_base = smem_u32(sA + stage * kTileBytes);
+                    const uint32_t a_base = smem_u32(sA + stage * kAStride);
                     const uint32_t b_base = smem_u32(sB + stage * kTileBytes);
                     if constexpr (NVF4) {
                         const int nsteps = min(4, K64 - 4 * kt);
@@ -338,21 +394,29 @@ __global__ void __launch_bounds__(192, 1)
         // ---------------------------------------------------------------- epilogue
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
+        const int ch0 = ((warp - 2) / 4) * (kBN / 32 / 2);   // this warp's half of the columns
         int it = 0;
         for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x, ++it) {
-            const Tile tl = decode_tile(g, t);
+            const Tile tl = decode_tile(g, tb, t);
             const int acc = it & 1;
             const uint32_t aphase = (it >> 1) & 1;
+            const EpiRow er = epilogue_row(g, tl, row);
+            // A warp whose 32 rows are all past the tile's valid rows reads nothing; it still
+            // waits for the accumulator before releasing it, which keeps the release phases
+            // of all four warps in step.
+            const bool live = quad * 32 < tl.rows;
             if (!role_wait(&tfull[acc], aphase, s_abort, g.err)) break;
             tc_fence_after();
             const uint32_t taddr = tmem + acc * kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
+            if (live) {
 #pragma unroll 1
-            for (int ch = 0; ch < kBN / 32; ++ch) {
-                if (ch * 32 >= tl.cols) break;
-                uint32_t r[32];
-                tmem_ld32(taddr + ch * 32, r);
-                tmem_wait_ld();
-                epilogue_chunk(g, tl, row, ch * 32, r);
+                for (int ch = ch0; ch < ch0 + kBN / 32 / 2; ++ch) {
+                    if (ch * 32 >= tl.cols) break;
+                    uint32_t r[32];
+                    tmem_ld32(taddr + ch * 32, r);
+                    tmem_wait_ld();
+                    epilogue_chunk(g, tl, er, row, ch * 32, r);
+                }
             }
             tc_fence_before();
             __syncwarp();

@@ -14,7 +14,7 @@
 #include <mutex>
 #include <new>
 
-#include "../../include/lmoe.h"
+#include "lmoe.h"   // include/ (on the include path)
 #include "common.cuh"
 #include "gemm.cuh"
 #include "moe.cuh"
@@ -27,6 +27,9 @@ namespace {
 
 constexpr int kStagesF4 = 5;
 constexpr int kStagesBF16 = 6;
+constexpr int kStagesF4Small = 8;     // decode (T <= 32): one 4 KB A box per stage
+constexpr int kStagesBF16Small = 10;
+constexpr int kSmallAMaxT = 32;
 constexpr int kSmallRouterMaxT = 64;   // router: shared-memory chunk reduction up to this T
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -49,14 +52,14 @@ EncodeTiledFn encode_fn() {
 }
 
 // 2-D K-major operand: `inner` elements per row (contiguous), `rows` rows, row pitch in bytes.
-// Box: one 128-byte swizzle row by 128 rows.
+// Box: one 128-byte swizzle row by `box_rows` rows (128 for weights, 32 for activations).
 bool make_map(CUtensorMap *m, bool bf16, const void *ptr, uint64_t inner, uint64_t rows,
-              uint64_t pitch_bytes) {
+              uint64_t pitch_bytes, uint32_t box_rows = 128) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {inner, rows};
     cuuint64_t strides[1] = {pitch_bytes};
-    cuuint32_t box[2] = {bf16 ? 64u : 128u, 128u};
+    cuuint32_t box[2] = {bf16 ? 64u : 128u, box_rows};
     cuuint32_t es[2] = {1, 1};
     CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
                     const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -167,17 +170,30 @@ WsLayout layout(const lmoe_ctx *c, int64_t T) {
     return L;
 }
 
-template <bool NVF4, int STAGES>
+template <bool NVF4, bool SMALLA, int STAGES>
 cudaError_t set_smem_attr() {
-    return cudaFuncSetAttribute(gemm_kernel<NVF4, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                gemm_smem_bytes<NVF4>(STAGES));
+    static_assert(gemm_smem_bytes<NVF4, SMALLA>(STAGES) <= 232448, "shared memory budget");
+    return cudaFuncSetAttribute(gemm_kernel<NVF4, SMALLA, STAGES>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                gemm_smem_bytes<NVF4, SMALLA>(STAGES));
 }
 
-template <bool NVF4, int STAGES>
-cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int grid,
-                        cudaStream_t s) {
-    gemm_kernel<NVF4, STAGES><<<grid, 192, gemm_smem_bytes<NVF4>(STAGES), s>>>(ta, tb, g);
+template <bool NVF4, bool SMALLA, int STAGES>
+cudaError_t launch_gemm_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int grid,
+                            cudaStream_t s) {
+    gemm_kernel<NVF4, SMALLA, STAGES><<<grid, kGemmThreads, gemm_smem_bytes<NVF4, SMALLA>(STAGES), s>>>(ta, tb, g);
     return cudaGetLastError();
+}
+
+// small_a: every tile has at most 32 valid A rows (T <= 32).
+template <bool NVF4>
+cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int grid,
+                        bool small_a, cudaStream_t s) {
+    if (NVF4)
+        return small_a ? launch_gemm_cfg<true, true, kStagesF4Small>(ta, tb, g, grid, s)
+                       : launch_gemm_cfg<true, false, kStagesF4>(ta, tb, g, grid, s);
+    return small_a ? launch_gemm_cfg<false, true, kStagesBF16Small>(ta, tb, g, grid, s)
+                   : launch_gemm_cfg<false, false, kStagesBF16>(ta, tb, g, grid, s);
 }
 
 GemmArgs dense_args(int M, int N, int K, int splits, int epi, unsigned *err) {
@@ -218,23 +234,32 @@ lmoe_status check_error_word(lmoe_ctx *c) {
 // The router on x: logits (small-T or tiled kernel) into `logits` [T][E], then top-k,
 // softmax and counts.
 lmoe_status launch_router(lmoe_ctx *c, const __nv_bfloat16 *x, int64_t T, float *logits,
-                          int32_t *idx, float *w, int32_t *counts, cudaStream_t s) {
+                          int32_t *idx, float *w, int32_t *counts, const ZeroRanges &zr,
+                          cudaStream_t s) {
     const bool small = T <= kSmallRouterMaxT && c->d / kChunk <= kSmallMaxC;
     if (small) {
-        router_small_kernel<<<static_cast<unsigned>(cdiv(c->E, 2)), 256, 0, s>>>(
-            x, c->w_router, c->b_router, static_cast<int>(T), c->d, c->E, logits);
+        router_small_kernel<<<static_cast<unsigned>(cdiv(c->E, kSmallExperts)), 128 * kSmallExperts,
+                              router_small_smem(c->d), s>>>(x, c->w_router, c->b_router,
+                                                            static_cast<int>(T), c->d, c->E, logits, zr);
     } else {
         dim3 grid(static_cast<unsigned>(cdiv(T, kRT)), static_cast<unsigned>(cdiv(c->E, kRE)));
-        router_logits_kernel<<<grid, 128, 0, s>>>(x, c->w_router, c->b_router, static_cast<int>(T), c->d,
-                                                  c->E, logits);
+        router_logits_kernel<<<grid, 128, kRouterLogitsSmem, s>>>(x, c->w_router, c->b_router,
+                                                                  static_cast<int>(T), c->d, c->E, logits, zr);
     }
     LMOE_LAUNCH();
     prof_mark(c, small ? "router_small" : "router_logits", s);
-    router_topk_kernel<<<static_cast<unsigned>(cdiv(T, 8)), 256, 0, s>>>(
+    router_topk_kernel<<<static_cast<unsigned>(T), kTopkThreads, 0, s>>>(
         logits, static_cast<int>(T), c->E, c->k, idx, w, counts);
     LMOE_LAUNCH();
     prof_mark(c, "router_topk", s);
     return LMOE_OK;
+}
+
+ZeroRanges zero_counts(int32_t *counts, int E) {
+    ZeroRanges z;
+    std::memset(&z, 0, sizeof(z));
+    if (counts) { z.p[0] = reinterpret_cast<uint4 *>(counts); z.n16[0] = cdiv(E * 4, 16); }
+    return z;
 }
 
 // Scratch bytes the router needs for T tokens (the fp32 logits).
@@ -339,9 +364,16 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
         static std::once_flag once;
         static cudaError_t attr_err = cudaSuccess;
         std::call_once(once, [] {
-            cudaError_t a = set_smem_attr<true, kStagesF4>();
-            cudaError_t b = set_smem_attr<false, kStagesBF16>();
-            attr_err = a != cudaSuccess ? a : b;
+            cudaError_t a = set_smem_attr<true, false, kStagesF4>();
+            cudaError_t b = set_smem_attr<false, false, kStagesBF16>();
+            if (a == cudaSuccess) a = set_smem_attr<true, true, kStagesF4Small>();
+            if (b == cudaSuccess) b = set_smem_attr<false, true, kStagesBF16Small>();
+            cudaError_t r = cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 router_small_smem(kSmallMaxC * kChunk));
+            if (r == cudaSuccess)
+                r = cudaFuncSetAttribute(router_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kRouterLogitsSmem);
+            attr_err = a != cudaSuccess ? a : (b != cudaSuccess ? b : r);
         });
         if (attr_err != cudaSuccess) return cuda_status(attr_err);
     }
@@ -456,9 +488,9 @@ lmoe_status lmoe_route_static(lmoe_ctx *c, const void *x, int64_t T, int32_t *id
     const lmoe_status st = route_static_scratch(dev, &scratch);
     if (st != LMOE_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (counts) LMOE_CUDA(cudaMemsetAsync(counts, 0, c->E * 4, s));
+    if (counts && reinterpret_cast<uintptr_t>(counts) % 16) return LMOE_EINVAL;
     return launch_router(c, static_cast<const __nv_bfloat16 *>(x), T, static_cast<float *>(scratch),
-                         idx, w, counts, s);
+                         idx, w, counts, zero_counts(counts, c->E), s);
 }
 
 size_t lmoe_workspace_size(const lmoe_ctx *c, int64_t T) {
@@ -514,9 +546,9 @@ lmoe_status lmoe_route(lmoe_ctx *c, const void *x, int64_t T, int32_t *idx, floa
         LMOE_CUDA(cudaMallocAsync(&c->route_ws, need, s));
         c->route_ws_bytes = need;
     }
-    if (counts) LMOE_CUDA(cudaMemsetAsync(counts, 0, c->E * 4, s));
+    if (counts && reinterpret_cast<uintptr_t>(counts) % 16) return LMOE_EINVAL;
     return launch_router(c, static_cast<const __nv_bfloat16 *>(x), T,
-                         static_cast<float *>(c->route_ws), idx, w, counts, s);
+                         static_cast<float *>(c->route_ws), idx, w, counts, zero_counts(counts, c->E), s);
 }
 
 lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *ws, size_t ws_bytes,
@@ -554,12 +586,13 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     __nv_bfloat16 *cb = static_cast<__nv_bfloat16 *>(at(L.c));
     float *yacc = static_cast<float *>(at(L.yacc));
     const int d = c->d, l = c->l, E = c->E, k = c->k, F = c->ffn;
+    const bool small_a = T <= kSmallAMaxT;   // no GEMM tile then has more than 32 valid rows
     if (c->profile) {
         c->nprof = 0;
         cudaEventRecord(c->ev[0], s);
     }
 
-    // 0. zero the accumulators and the expert histogram
+    // 1. router (its first kernel also clears the histogram and the fp32 accumulators)
     {
         ZeroRanges z;
         std::memset(&z, 0, sizeof(z));
@@ -567,24 +600,18 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         z.p[1] = reinterpret_cast<uint4 *>(c_acc); z.n16[1] = T * l * 4 / 16;
         if (L.split_down) { z.p[2] = reinterpret_cast<uint4 *>(zacc); z.n16[2] = T * l * 4 / 16; }
         if (L.split_up) { z.p[3] = reinterpret_cast<uint4 *>(yacc); z.n16[3] = T * d * 4 / 16; }
-        zero_kernel<<<c->num_sms * 4, 256, 0, s>>>(z);
-        LMOE_LAUNCH();
-        prof_mark(c, "zero", s);
-    }
-    // 1. router
-    {
         lmoe_status st = launch_router(c, static_cast<const __nv_bfloat16 *>(x), T,
-                                       static_cast<float *>(at(L.router)), idx, rw, counts, s);
+                                       static_cast<float *>(at(L.router)), idx, rw, counts, z, s);
         if (st != LMOE_OK) return st;
     }
     // 2. per-expert segments
-    segments_kernel<<<1, 1024, 0, s>>>(counts, E, seg, mt, fill, row_slot, nrows);
+    segments_kernel<<<E, 128, 0, s>>>(counts, E, seg, mt, fill, row_slot, nrows);
     LMOE_LAUNCH();
     prof_mark(c, "segments", s);
     // 3. down-projection z = x Wd^T, quantized to NVFP4
     {
         CUtensorMap tx;
-        if (!make_map(&tx, true, x, d, T, static_cast<uint64_t>(d) * 2)) return LMOE_ECUDA;
+        if (!make_map(&tx, true, x, d, T, static_cast<uint64_t>(d) * 2, kABoxRows)) return LMOE_ECUDA;
         GemmArgs g = dense_args(static_cast<int>(T), l, d, L.down_splits,
                                 L.split_down ? EPI_RED_F32 : EPI_Z_QUANT, c->err);
         if (L.split_down) {
@@ -592,8 +619,8 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         } else {
             g.q = c->qz; g.q_codes = zq_codes; g.q_sf = zq_sf; g.dbg = z_dbg;
         }
-        LMOE_CUDA((launch_gemm<false, kStagesBF16>(tx, c->tm_wd, g,
-                                                   grid_for(int64_t(g.m_tiles) * g.n_tiles * g.k_splits, c->num_sms), s)));
+        LMOE_CUDA((launch_gemm<false>(tx, c->tm_wd, g,
+                                                   grid_for(int64_t(g.m_tiles) * g.n_tiles * g.k_splits, c->num_sms), small_a, s)));
         prof_mark(c, "down_proj", s);
         if (L.split_down) {
             const int grid = static_cast<int>(std::min<int64_t>(cdiv(T * l / 16, 256), c->num_sms * 8));
@@ -613,7 +640,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     // 5. latent-up grouped GEMM + relu^2 + requantize
     {
         CUtensorMap ta;
-        if (!make_map(&ta, false, a_codes, l / 2, L.R, l / 2)) return LMOE_ECUDA;
+        if (!make_map(&ta, false, a_codes, l / 2, L.R, l / 2, kABoxRows)) return LMOE_ECUDA;
         GemmArgs g;
         std::memset(&g, 0, sizeof(g));
         g.M = static_cast<int>(L.R); g.N = F; g.K = l;
@@ -623,13 +650,13 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         g.sfa = a_sf; g.sfb = c->w1_sf; g.NB = static_cast<int>(cdiv(F, 128));
         g.epi = EPI_H_QUANT; g.q = c->qh; g.q_codes = h_codes; g.q_sf = h_sf; g.dbg = h_dbg;
         g.alpha = c->alpha1; g.err = c->err;
-        LMOE_CUDA((launch_gemm<true, kStagesF4>(ta, c->tm_w1, g, c->num_sms, s)));
+        LMOE_CUDA((launch_gemm<true>(ta, c->tm_w1, g, c->num_sms, small_a, s)));
         prof_mark(c, "expert_up", s);
     }
     // 6. latent-down grouped GEMM, routing weight, combine into c_acc
     {
         CUtensorMap ta;
-        if (!make_map(&ta, false, h_codes, F / 2, L.R, F / 2)) return LMOE_ECUDA;
+        if (!make_map(&ta, false, h_codes, F / 2, L.R, F / 2, kABoxRows)) return LMOE_ECUDA;
         GemmArgs g;
         std::memset(&g, 0, sizeof(g));
         g.M = static_cast<int>(L.R); g.N = l; g.K = F;
@@ -639,7 +666,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         g.sfa = h_sf; g.sfb = c->w2_sf; g.NB = static_cast<int>(cdiv(l, 128));
         g.epi = EPI_COMBINE; g.out = c_acc; g.ld_out = l;
         g.alpha = c->alpha2; g.row_slot = row_slot; g.route_w = rw; g.topk = k; g.err = c->err;
-        LMOE_CUDA((launch_gemm<true, kStagesF4>(ta, c->tm_w2, g, c->num_sms, s)));
+        LMOE_CUDA((launch_gemm<true>(ta, c->tm_w2, g, c->num_sms, small_a, s)));
         prof_mark(c, "expert_down", s);
     }
     // 7. c = bf16(c_acc)
@@ -652,13 +679,13 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     // 8. up-projection y = c Wu^T
     {
         CUtensorMap tc;
-        if (!make_map(&tc, true, cb, l, T, static_cast<uint64_t>(l) * 2)) return LMOE_ECUDA;
+        if (!make_map(&tc, true, cb, l, T, static_cast<uint64_t>(l) * 2, kABoxRows)) return LMOE_ECUDA;
         GemmArgs g = dense_args(static_cast<int>(T), d, l, L.up_splits,
                                 L.split_up ? EPI_RED_F32 : EPI_STORE_BF16, c->err);
         g.out = L.split_up ? static_cast<void *>(yacc) : y;
         g.ld_out = d;
-        LMOE_CUDA((launch_gemm<false, kStagesBF16>(tc, c->tm_wu, g,
-                                                   grid_for(int64_t(g.m_tiles) * g.n_tiles * g.k_splits, c->num_sms), s)));
+        LMOE_CUDA((launch_gemm<false>(tc, c->tm_wu, g,
+                                                   grid_for(int64_t(g.m_tiles) * g.n_tiles * g.k_splits, c->num_sms), small_a, s)));
         prof_mark(c, "up_proj", s);
         if (L.split_up) {
             const int grid = static_cast<int>(std::min<int64_t>(cdiv(T * d / 8, 256), c->num_sms * 8));
@@ -711,9 +738,9 @@ lmoe_status lmoe_get_expert_nvfp4(const lmoe_ctx *c, int which, int e, uint8_t *
 int lmoe_forward_kernel_count(const lmoe_ctx *c, int64_t T) {
     if (!c || T <= 0) return 0;
     const WsLayout L = layout(c, T);
-    // zero, router logits, top-k, segments, down-proj, scatter, expert-up, expert-down,
-    // combine cast, up-proj, plus one finalize per split projection
-    return 10 + (L.split_down ? 1 : 0) + (L.split_up ? 1 : 0);
+    // router logits, top-k, segments, down-proj, scatter, expert-up, expert-down, combine
+    // cast, up-proj, plus one finalize per split projection
+    return 9 + (L.split_down ? 1 : 0) + (L.split_up ? 1 : 0);
 }
 
 lmoe_status lmoe_set_profile(lmoe_ctx *c, int on) {

@@ -12,52 +12,35 @@
 
 namespace lmoe {
 
-struct ZeroRanges {
-    uint4 *p[4];
-    int64_t n16[4];   // number of 16-byte words
-};
-__global__ void zero_kernel(ZeroRanges z) {
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int r = 0; r < 4; ++r) {
-        uint4 *p = z.p[r];
-        for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < z.n16[r]; i += stride)
-            p[i] = make_uint4(0, 0, 0, 0);
-    }
-}
-
-// One block of 1024 threads, E <= 1024.
-__global__ void __launch_bounds__(1024) segments_kernel(
+// One block per expert e: its segment start is the sum of the padded counts of experts < e
+// (a block reduction over the histogram); the block also marks the segment's padding rows.
+// Block E - 1 writes the totals.  grid = E, block = 128.
+__global__ void __launch_bounds__(128) segments_kernel(
     const int32_t *__restrict__ counts, int E, int32_t *__restrict__ seg_start,
     int32_t *__restrict__ mt_start, int32_t *__restrict__ fill, int32_t *__restrict__ row_slot,
     int32_t *__restrict__ nrows) {
-    __shared__ int32_t s_rows[1024], s_mt[1024];
-    const int e = threadIdx.x;
-    const int cnt = e < E ? counts[e] : 0;
-    const int padded = (cnt + 127) & ~127;
-    s_rows[e] = padded;
-    s_mt[e] = padded >> 7;
+    __shared__ int part[4];
+    const int e = blockIdx.x;
+    int sum = 0;
+    for (int i = threadIdx.x; i < e; i += blockDim.x) sum += (__ldg(counts + i) + 127) & ~127;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = sum;
     __syncthreads();
-    // Hillis-Steele inclusive scan
-    for (int o = 1; o < 1024; o <<= 1) {
-        int a = 0, b = 0;
-        if (e >= o) { a = s_rows[e - o]; b = s_mt[e - o]; }
-        __syncthreads();
-        s_rows[e] += a;
-        s_mt[e] += b;
-        __syncthreads();
-    }
-    const int start = s_rows[e] - padded;
-    if (e < E) {
+    const int start = part[0] + part[1] + part[2] + part[3];
+    const int cnt = __ldg(counts + e);
+    const int padded = (cnt + 127) & ~127;
+    if (threadIdx.x == 0) {
         seg_start[e] = start;
-        mt_start[e] = s_mt[e] - (padded >> 7);
+        mt_start[e] = start >> 7;
         fill[e] = 0;
-        for (int r = start + cnt; r < start + padded; ++r) row_slot[r] = -1;
+        if (e == E - 1) {
+            seg_start[E] = start + padded;
+            mt_start[E] = (start + padded) >> 7;
+            *nrows = start + padded;
+        }
     }
-    if (e == E - 1) {
-        seg_start[E] = s_rows[e];
-        mt_start[E] = s_mt[e];
-        *nrows = s_rows[e];
-    }
+    for (int r = start + cnt + threadIdx.x; r < start + padded; r += blockDim.x) row_slot[r] = -1;
 }
 
 // One warp per routing slot: claim a row of the expert's segment and copy the token's
