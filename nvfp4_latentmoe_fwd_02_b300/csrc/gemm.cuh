@@ -11,11 +11,15 @@
 // has valid rows (a decode tile of one token moves 4 KB of A per stage, not 16 KB); rows past
 // the loaded boxes hold stale data whose accumulator rows the epilogue never reads.
 //
-// Warp roles (320 threads, one CTA per SM):
+// Warp roles (384 threads, one CTA per SM):
 //   warp 0      TMA producer (one elected lane): operand tiles + scale atoms -> smem ring
-//   warp 1      TMEM allocator and MMA issuer (one lane): scale atoms smem -> TMEM with
-//               tcgen05.cp, tcgen05.mma into one of two 128-column accumulators
-//   warps 2..9  epilogue: tcgen05.ld of the accumulator (warp w reads lane quadrant w % 4;
+//   warp 1      TMEM allocator and MMA issuer (one lane): tcgen05.mma into one of two
+//               128-column accumulators
+//   warps 2, 3  scale-factor copiers (NVFP4 only, one lane each): the A and the B scale atoms
+//               of a stage, smem -> TMEM with tcgen05.cp, then a commit on the stage's
+//               "scales ready" barrier.  Issuing a tensor-core op costs a single thread tens of
+//               cycles, so copies and MMAs are issued from three threads in parallel.
+//   warps 4..11 epilogue: tcgen05.ld of the accumulator (warp w reads lane quadrant w % 4;
 //               two warps per quadrant, each taking half of the tile's columns), fused
 //               output transform, global stores / reductions
 // Barriers: full/empty per smem stage, tmem_full/tmem_empty per accumulator.  Every wait is
@@ -237,49 +241,72 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs &g, const Tile &tl
     }
 }
 
-// SMALLA (decode): every tile has at most 32 valid A rows, so each stage keeps only one
-// 4 KB A box; the MMA still reads 128 rows from the stage's A base, and rows 32..127 fall on
-// the following stages' boxes (or on the slack after the last one): they only feed
-// accumulator rows the epilogue never reads.  The smaller stage buys more stages, i.e. more
-// weight bytes in flight per SM.
-template <bool NVF4, bool SMALLA>
+// SMALLA (decode): every tile has at most 32 valid A rows, so each column block of a stage
+// keeps only one 4 KB A box; the MMA still reads 128 rows from the block's A base, and rows
+// 32..127 fall on the following boxes (or on the slack after the last one): they only feed
+// accumulator rows the epilogue never reads.  KB: 128-byte column blocks (256 e2m1 or 64 bf16
+// elements of K each) per pipeline stage; KB = 2 halves the per-stage barrier handshakes and
+// copies when each stage carries little MMA work (decode).
+template <bool NVF4, bool SMALLA, int KB>
+struct GemmCfg {
+    static constexpr int kACol = SMALLA ? kABoxBytes : kTileBytes;   // A bytes per column block
+    static constexpr int kAStage = KB * kACol;
+    static constexpr int kBStage = KB * kTileBytes;
+    static constexpr int kSfStage = NVF4 ? KB * kSfStageBytes : 0;   // per operand
+    static constexpr int kSlack = SMALLA ? kTileBytes - kABoxBytes : 0;
+    static constexpr int kElemsPerBlock = NVF4 ? 256 : 64;
+    static constexpr int kStepsPerBlock = 4;                          // MMA K steps per block
+    static constexpr int kSfCols = NVF4 ? 32 * KB : 0;                // TMEM columns per stage
+};
+
+template <bool NVF4, bool SMALLA, int KB>
 constexpr int gemm_smem_bytes(int stages) {
-    return 1024 + stages * ((SMALLA ? kABoxBytes : kTileBytes) + kTileBytes + (NVF4 ? 2 * kSfStageBytes : 0)) +
-           (SMALLA ? kTileBytes - kABoxBytes : 0) + 256 + (NVF4 ? static_cast<int>(sizeof(SmemTables)) : 0);
+    using C = GemmCfg<NVF4, SMALLA, KB>;
+    return 1024 + stages * (C::kAStage + C::kBStage + 2 * C::kSfStage) + C::kSlack + 256 +
+           (NVF4 ? static_cast<int>(sizeof(SmemTables)) : 0);
 }
 
 constexpr int kEpiWarps = 8;
-constexpr int kGemmThreads = 32 * (2 + kEpiWarps);
+constexpr int kEpiWarp0 = 4;
+constexpr int kGemmThreads = 32 * (kEpiWarp0 + kEpiWarps);
 
-template <bool NVF4, bool SMALLA, int STAGES>
+template <bool NVF4, bool SMALLA, int KB, int STAGES>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmArgs g) {
+    using C = GemmCfg<NVF4, SMALLA, KB>;
     extern __shared__ uint8_t smem_raw[];
-    constexpr int kAStride = SMALLA ? kABoxBytes : kTileBytes;
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sA = smem;
-    uint8_t *sB = sA + STAGES * kAStride + (SMALLA ? kTileBytes - kABoxBytes : 0);
-    uint8_t *sSFA = sB + STAGES * kTileBytes;
-    uint8_t *sSFB = sSFA + (NVF4 ? STAGES * kSfStageBytes : 0);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sSFB + (NVF4 ? STAGES * kSfStageBytes : 0));
-    uint64_t *full = bars, *empty = bars + STAGES;
-    uint64_t *tfull = bars + 2 * STAGES, *tempty = tfull + 2, *drain = tempty + 2;
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(drain + 1);
+    uint8_t *sB = sA + STAGES * C::kAStage + C::kSlack;
+    uint8_t *sSFA = sB + STAGES * C::kBStage;
+    uint8_t *sSFB = sSFA + STAGES * C::kSfStage;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sSFB + STAGES * C::kSfStage);
+    uint64_t *full = bars, *empty = bars + STAGES, *sfready = bars + 2 * STAGES;
+    uint64_t *tfull = bars + 3 * STAGES, *tempty = tfull + 2, *drain = tempty + 2;
+    uint64_t *cdrain = drain + 1;   // [2]: one per scale copier
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(cdrain + 2);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     SmemTables *tb = reinterpret_cast<SmemTables *>(bars + 256 / 8);
 
     constexpr uint32_t kAccCols = kBN;
     constexpr uint32_t kTmemCols = NVF4 ? 512 : 256;
     constexpr uint32_t kSfCol0 = 2 * kAccCols;
-    static_assert(!NVF4 || kSfCol0 + STAGES * 32 <= 512, "TMEM budget");
+    static_assert(!NVF4 || kSfCol0 + STAGES * C::kSfCols <= 512, "TMEM budget");
+    static_assert(3 * STAGES + 8 <= 32, "barrier area");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+            mbar_init(&sfready[s], 2);
+        }
         for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], kEpiWarps); }
         mbar_init(drain, 1);
+        mbar_init(&cdrain[0], 1);
+        mbar_init(&cdrain[1], 1);
         *s_abort = 0;
         fence_mbar_init();
     }
@@ -306,26 +333,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued = 0, issued_phase = 0;   // per stage: ever issued / phase of last issue
+            const uint32_t sA0 = smem_u32(sA), sB0 = smem_u32(sB);
+            const uint32_t sSFA0 = smem_u32(sSFA), sSFB0 = smem_u32(sSFB);
             for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x) {
                 const Tile tl = decode_tile(g, tb, t);
+                const int nbox = SMALLA ? 1 : (tl.rows + kABoxRows - 1) / kABoxRows;
+                const uint8_t *sfa_tile = NVF4 ? g.sfa + static_cast<size_t>(tl.a_row0 >> 7) * K64 * 512 : nullptr;
+                const uint8_t *sfb_tile = NVF4 ? g.sfb + (static_cast<size_t>(tl.e) * g.NB + (tl.n0 >> 7)) * K64 * 512 : nullptr;
                 for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
                     if (!role_wait(&empty[stage], phase ^ 1, s_abort, g.err)) break;
-                    const int nsteps = NVF4 ? min(4, K64 - 4 * kt) : 4;
-                    const int nbox = SMALLA ? 1 : (tl.rows + kABoxRows - 1) / kABoxRows;
-                    const uint32_t bytes = nbox * kABoxBytes + kTileBytes + (NVF4 ? 2 * nsteps * 512 : 0);
-                    mbar_arrive_expect_tx(&full[stage], bytes);
-                    const int kx = NVF4 ? kt * 128 : kt * 64;
-                    for (int j = 0; j < nbox; ++j)
-                        tma_load_2d(sA + stage * kAStride + j * kABoxBytes, &tmA, &full[stage], kx,
-                                    tl.a_row0 + j * kABoxRows);
-                    tma_load_2d(sB + stage * kTileBytes, &tmB, &full[stage], kx, tl.b_row0);
+                    const int kb0 = kt * KB;
+                    const int nsteps = NVF4 ? min(4 * KB, K64 - 4 * kb0) : 4 * KB;
+                    const uint32_t bytes = KB * (nbox * kABoxBytes + kTileBytes) + (NVF4 ? 2 * nsteps * 512 : 0);
+                    uint64_t *fb = &full[stage];
+                    mbar_arrive_expect_tx(fb, bytes);
+                    const uint32_t a_st = sA0 + stage * C::kAStage, b_st = sB0 + stage * C::kBStage;
+#pragma unroll
+                    for (int b = 0; b < KB; ++b) {
+                        const int kx = (kb0 + b) * (NVF4 ? 128 : 64);
+                        for (int j = 0; j < nbox; ++j)
+                            tma_load_2d_u32(a_st + b * C::kACol + j * kABoxBytes, &tmA, fb, kx, tl.a_row0 + j * kABoxRows);
+                        tma_load_2d_u32(b_st + b * kTileBytes, &tmB, fb, kx, tl.b_row0);
+                    }
                     if (NVF4) {
-                        bulk_load(sSFA + stage * kSfStageBytes,
-                                  g.sfa + (static_cast<size_t>(tl.a_row0 >> 7) * K64 + 4 * kt) * 512,
-                                  nsteps * 512, &full[stage]);
-                        bulk_load(sSFB + stage * kSfStageBytes,
-                                  g.sfb + ((static_cast<size_t>(tl.e) * g.NB + (tl.n0 >> 7)) * K64 + 4 * kt) * 512,
-                                  nsteps * 512, &full[stage]);
+                        bulk_load_u32(sSFA0 + stage * C::kSfStage, sfa_tile + kb0 * 2048, nsteps * 512, fb);
+                        bulk_load_u32(sSFB0 + stage * C::kSfStage, sfb_tile + kb0 * 2048, nsteps * 512, fb);
                     }
                     issued |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -346,6 +378,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = NVF4 ? idesc_nvf4(kBM, kBN) : idesc_bf16(kBM, kBN);
+            // descriptors of stage 0; a stage adds its byte offset >> 4 to the start address
+            const uint64_t adesc0 = sdesc_sw128(smem_u32(sA)), bdesc0 = sdesc_sw128(smem_u32(sB));
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
@@ -359,25 +393,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 bool ok = true;
                 for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
                     if (!role_wait(&full[stage], phase, s_abort, g.err)) { ok = false; break; }
+                    if (NVF4 && !role_wait(&sfready[stage], phase, s_abort, g.err)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a_base = smem_u32(sA + stage * kAStride);
-                    const uint32_t b_base = smem_u32(sB + stage * kTileBytes);
+                    const uint64_t ad = adesc0 + ((stage * C::kAStage) >> 4);
+                    const uint64_t bd = bdesc0 + ((stage * C::kBStage) >> 4);
+                    const uint32_t acc_flag0 = kt > tl.kt0 ? 1u : 0u;
                     if constexpr (NVF4) {
-                        const int nsteps = min(4, K64 - 4 * kt);
-                        const uint32_t sf_t = tmem + kSfCol0 + stage * 32;
-                        for (int kk = 0; kk < nsteps; ++kk) {
-                            tmem_cp_sf(sf_t + kk * 4, sdesc_sf(smem_u32(sSFA + stage * kSfStageBytes + kk * 512)));
-                            tmem_cp_sf(sf_t + 16 + kk * 4, sdesc_sf(smem_u32(sSFB + stage * kSfStageBytes + kk * 512)));
+                        const int nsteps = min(4 * KB, K64 - 4 * kt * KB);
+                        const uint32_t sf_t = tmem + kSfCol0 + stage * C::kSfCols;
+#pragma unroll
+                        for (int kk = 0; kk < 4 * KB; ++kk) {
+                            if (kk < nsteps)
+                                mma_nvf4(d_tmem, ad + (((kk >> 2) * C::kACol + (kk & 3) * 32) >> 4),
+                                         bd + (((kk >> 2) * kTileBytes + (kk & 3) * 32) >> 4), idesc,
+                                         sf_t + kk * 4, sf_t + 16 * KB + kk * 4, (acc_flag0 | kk) ? 1u : 0u);
                         }
-                        for (int kk = 0; kk < nsteps; ++kk)
-                            mma_nvf4(d_tmem, sdesc_sw128(a_base + kk * 32), sdesc_sw128(b_base + kk * 32),
-                                     idesc, sf_t + kk * 4, sf_t + 16 + kk * 4,
-                                     (kt > tl.kt0 || kk > 0) ? 1u : 0u);
                     } else {
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16(d_tmem, sdesc_sw128(a_base + kk * 32), sdesc_sw128(b_base + kk * 32),
-                                     idesc, (kt > tl.kt0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < 4 * KB; ++kk)
+                            mma_bf16(d_tmem, ad + (((kk >> 2) * C::kACol + (kk & 3) * 32) >> 4),
+                                     bd + (((kk >> 2) * kTileBytes + (kk & 3) * 32) >> 4), idesc,
+                                     (acc_flag0 | kk) ? 1u : 0u);
                     }
                     mma_commit(&empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -390,11 +426,41 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const long long t0 = clock64();
             while (!mbar_try_wait(drain, 0) && clock64() - t0 < kWaitLimitCycles) {}
         }
+    } else if (warp == 2 || warp == 3) {
+        // ---------------------------------------------------------------- scale copiers
+        if (NVF4 && lane == 0) {
+            const bool is_b = warp == 3;
+            const uint64_t sfdesc0 = sdesc_sf(smem_u32(is_b ? sSFB : sSFA));
+            const uint32_t col_off = is_b ? 16 * KB : 0;
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x) {
+                const Tile tl = decode_tile(g, tb, t);
+                bool ok = true;
+                for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
+                    if (!role_wait(&full[stage], phase, s_abort, g.err)) { ok = false; break; }
+                    tc_fence_after();
+                    const int nsteps = min(4 * KB, K64 - 4 * kt * KB);
+                    const uint32_t sf_t = tmem + kSfCol0 + stage * C::kSfCols + col_off;
+                    const uint64_t sfd = sfdesc0 + ((stage * C::kSfStage) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < 4 * KB; ++kk)
+                        if (kk < nsteps) tmem_cp_sf(sf_t + kk * 4, sfd + kk * (512 >> 4));
+                    mma_commit(&sfready[stage]);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+            }
+            // every copy this thread issued is complete before TMEM is released
+            mma_commit(&cdrain[is_b ? 1 : 0]);
+            const long long t0 = clock64();
+            while (!mbar_try_wait(&cdrain[is_b ? 1 : 0], 0) && clock64() - t0 < kWaitLimitCycles) {}
+        }
     } else {
         // ---------------------------------------------------------------- epilogue
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
-        const int ch0 = ((warp - 2) / 4) * (kBN / 32 / 2);   // this warp's half of the columns
+        const int ch0 = ((warp - kEpiWarp0) / 4) * (kBN / 32 / 2);   // this warp's half of the columns
         int it = 0;
         for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x, ++it) {
             const Tile tl = decode_tile(g, tb, t);

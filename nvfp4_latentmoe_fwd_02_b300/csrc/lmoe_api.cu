@@ -27,9 +27,10 @@ namespace {
 
 constexpr int kStagesF4 = 5;
 constexpr int kStagesBF16 = 6;
-constexpr int kStagesF4Small = 8;     // decode (T <= 32): one 4 KB A box per stage
-constexpr int kStagesBF16Small = 10;
+constexpr int kStagesF4Small = 4;     // decode (T <= 32): 4 KB A boxes, 2 column blocks per stage
+constexpr int kStagesBF16Small = 5;
 constexpr int kSmallAMaxT = 32;
+inline int kb_for(bool small_a) { return small_a ? 2 : 1; }   // column blocks per stage
 constexpr int kSmallRouterMaxT = 64;   // router: shared-memory chunk reduction up to this T
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -139,8 +140,9 @@ WsLayout layout(const lmoe_ctx *c, int64_t T) {
     if (L.R == 0) L.R = 128;
     L.small_router = T <= kSmallRouterMaxT;
     const int mt = static_cast<int>(cdiv(T, 128));
-    L.down_splits = plan_splits(mt, static_cast<int>(cdiv(l, 128)), static_cast<int>(d / 64), c->num_sms);
-    L.up_splits = plan_splits(mt, static_cast<int>(cdiv(d, 128)), static_cast<int>(l / 64), c->num_sms);
+    const int kb = kb_for(T <= kSmallAMaxT);
+    L.down_splits = plan_splits(mt, static_cast<int>(cdiv(l, 128)), static_cast<int>(cdiv(d / 64, kb)), c->num_sms);
+    L.up_splits = plan_splits(mt, static_cast<int>(cdiv(d, 128)), static_cast<int>(cdiv(l / 64, kb)), c->num_sms);
     L.split_down = L.down_splits > 1;
     L.split_up = L.up_splits > 1;
     size_t off = 0;
@@ -170,39 +172,41 @@ WsLayout layout(const lmoe_ctx *c, int64_t T) {
     return L;
 }
 
-template <bool NVF4, bool SMALLA, int STAGES>
+template <bool NVF4, bool SMALLA, int KB, int STAGES>
 cudaError_t set_smem_attr() {
-    static_assert(gemm_smem_bytes<NVF4, SMALLA>(STAGES) <= 232448, "shared memory budget");
-    return cudaFuncSetAttribute(gemm_kernel<NVF4, SMALLA, STAGES>,
+    static_assert(gemm_smem_bytes<NVF4, SMALLA, KB>(STAGES) <= 232448, "shared memory budget");
+    return cudaFuncSetAttribute(gemm_kernel<NVF4, SMALLA, KB, STAGES>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                gemm_smem_bytes<NVF4, SMALLA>(STAGES));
+                                gemm_smem_bytes<NVF4, SMALLA, KB>(STAGES));
 }
 
-template <bool NVF4, bool SMALLA, int STAGES>
+template <bool NVF4, bool SMALLA, int KB, int STAGES>
 cudaError_t launch_gemm_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int grid,
                             cudaStream_t s) {
-    gemm_kernel<NVF4, SMALLA, STAGES><<<grid, kGemmThreads, gemm_smem_bytes<NVF4, SMALLA>(STAGES), s>>>(ta, tb, g);
+    gemm_kernel<NVF4, SMALLA, KB, STAGES>
+        <<<grid, kGemmThreads, gemm_smem_bytes<NVF4, SMALLA, KB>(STAGES), s>>>(ta, tb, g);
     return cudaGetLastError();
 }
 
-// small_a: every tile has at most 32 valid A rows (T <= 32).
+// small_a: every tile has at most 32 valid A rows (T <= 32); such launches use two column
+// blocks per stage, and g.k_tiles must count stages of kb_for(true) blocks.
 template <bool NVF4>
 cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int grid,
                         bool small_a, cudaStream_t s) {
     if (NVF4)
-        return small_a ? launch_gemm_cfg<true, true, kStagesF4Small>(ta, tb, g, grid, s)
-                       : launch_gemm_cfg<true, false, kStagesF4>(ta, tb, g, grid, s);
-    return small_a ? launch_gemm_cfg<false, true, kStagesBF16Small>(ta, tb, g, grid, s)
-                   : launch_gemm_cfg<false, false, kStagesBF16>(ta, tb, g, grid, s);
+        return small_a ? launch_gemm_cfg<true, true, 2, kStagesF4Small>(ta, tb, g, grid, s)
+                       : launch_gemm_cfg<true, false, 1, kStagesF4>(ta, tb, g, grid, s);
+    return small_a ? launch_gemm_cfg<false, true, 2, kStagesBF16Small>(ta, tb, g, grid, s)
+                   : launch_gemm_cfg<false, false, 1, kStagesBF16>(ta, tb, g, grid, s);
 }
 
-GemmArgs dense_args(int M, int N, int K, int splits, int epi, unsigned *err) {
+GemmArgs dense_args(int M, int N, int K, int splits, int epi, unsigned *err, int kb) {
     GemmArgs g;
     std::memset(&g, 0, sizeof(g));
     g.M = M; g.N = N; g.K = K;
     g.m_tiles = static_cast<int>(cdiv(M, kBM));
     g.n_tiles = static_cast<int>(cdiv(N, kBN));
-    g.k_tiles = K / 64;
+    g.k_tiles = static_cast<int>(cdiv(K / 64, kb));
     g.kt_per_split = static_cast<int>(cdiv(g.k_tiles, splits));
     g.k_splits = static_cast<int>(cdiv(g.k_tiles, g.kt_per_split));
     g.epi = epi;
@@ -364,10 +368,10 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
         static std::once_flag once;
         static cudaError_t attr_err = cudaSuccess;
         std::call_once(once, [] {
-            cudaError_t a = set_smem_attr<true, false, kStagesF4>();
-            cudaError_t b = set_smem_attr<false, false, kStagesBF16>();
-            if (a == cudaSuccess) a = set_smem_attr<true, true, kStagesF4Small>();
-            if (b == cudaSuccess) b = set_smem_attr<false, true, kStagesBF16Small>();
+            cudaError_t a = set_smem_attr<true, false, 1, kStagesF4>();
+            cudaError_t b = set_smem_attr<false, false, 1, kStagesBF16>();
+            if (a == cudaSuccess) a = set_smem_attr<true, true, 2, kStagesF4Small>();
+            if (b == cudaSuccess) b = set_smem_attr<false, true, 2, kStagesBF16Small>();
             cudaError_t r = cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  router_small_smem(kSmallMaxC * kChunk));
             if (r == cudaSuccess)
@@ -613,7 +617,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         CUtensorMap tx;
         if (!make_map(&tx, true, x, d, T, static_cast<uint64_t>(d) * 2, kABoxRows)) return LMOE_ECUDA;
         GemmArgs g = dense_args(static_cast<int>(T), l, d, L.down_splits,
-                                L.split_down ? EPI_RED_F32 : EPI_Z_QUANT, c->err);
+                                L.split_down ? EPI_RED_F32 : EPI_Z_QUANT, c->err, kb_for(small_a));
         if (L.split_down) {
             g.out = zacc; g.ld_out = l;
         } else {
@@ -645,7 +649,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         std::memset(&g, 0, sizeof(g));
         g.M = static_cast<int>(L.R); g.N = F; g.K = l;
         g.n_tiles = static_cast<int>(cdiv(F, kBN));
-        g.k_tiles = static_cast<int>(cdiv(l, 256));
+        g.k_tiles = static_cast<int>(cdiv(l, 256 * kb_for(small_a)));
         g.grouped = 1; g.E = E; g.mt_start = mt; g.seg_start = seg; g.counts = counts;
         g.sfa = a_sf; g.sfb = c->w1_sf; g.NB = static_cast<int>(cdiv(F, 128));
         g.epi = EPI_H_QUANT; g.q = c->qh; g.q_codes = h_codes; g.q_sf = h_sf; g.dbg = h_dbg;
@@ -661,7 +665,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         std::memset(&g, 0, sizeof(g));
         g.M = static_cast<int>(L.R); g.N = l; g.K = F;
         g.n_tiles = static_cast<int>(cdiv(l, kBN));
-        g.k_tiles = static_cast<int>(cdiv(F, 256));
+        g.k_tiles = static_cast<int>(cdiv(F, 256 * kb_for(small_a)));
         g.grouped = 1; g.E = E; g.mt_start = mt; g.seg_start = seg; g.counts = counts;
         g.sfa = h_sf; g.sfb = c->w2_sf; g.NB = static_cast<int>(cdiv(l, 128));
         g.epi = EPI_COMBINE; g.out = c_acc; g.ld_out = l;
@@ -681,7 +685,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         CUtensorMap tc;
         if (!make_map(&tc, true, cb, l, T, static_cast<uint64_t>(l) * 2, kABoxRows)) return LMOE_ECUDA;
         GemmArgs g = dense_args(static_cast<int>(T), d, l, L.up_splits,
-                                L.split_up ? EPI_RED_F32 : EPI_STORE_BF16, c->err);
+                                L.split_up ? EPI_RED_F32 : EPI_STORE_BF16, c->err, kb_for(small_a));
         g.out = L.split_up ? static_cast<void *>(yacc) : y;
         g.ld_out = d;
         LMOE_CUDA((launch_gemm<false>(tc, c->tm_wu, g,
