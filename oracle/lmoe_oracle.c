@@ -217,17 +217,22 @@ double oracle_nvfp4_dot(const uint8_t *qa, const uint8_t *sfa,
 /* Router.  [NEWS] architecture paragraph: each MoE layer has 512 experts and activates   */
 /* the top 22 per token; [BLOG] 2.2 keeps the routing gate at width d.  The logit order   */
 /* is this project's canonical fp32 order (the pages are silent): the d axis is cut into */
-/* chunks of 64; inside a chunk an fmaf chain in ascending index starting from 0; chunk   */
-/* partials added left to right starting from 0; then the bias.  Selection: logit         */
-/* descending, lower expert index first on ties.  Weights: softmax over the k selected   */
-/* logits (fp64).                                                                        */
+/* chunks of 64; inside a chunk an fmaf chain in ascending index starting from 0; chunks  */
+/* are grouped 16 at a time (1024 elements); a group's chunk partials are added left to   */
+/* right starting from 0; the group sums are added left to right starting from 0; then    */
+/* the bias.  Selection: logit descending, lower expert index first on ties.  Weights:    */
+/* softmax over the k selected logits (fp64).                                             */
 /* ------------------------------------------------------------------------------------ */
 static float canonical_logit(const float *x, const float *w, int d) {
     float acc = 0.0f;
-    for (int c = 0; c < d; c += 64) {
-        float p = 0.0f;
-        for (int i = c; i < c + 64; ++i) p = fmaf(x[i], w[i], p);
-        acc = acc + p;
+    for (int g = 0; g < d; g += 16 * 64) {
+        float gs = 0.0f;
+        for (int c = g; c < g + 16 * 64 && c < d; c += 64) {
+            float p = 0.0f;
+            for (int i = c; i < c + 64; ++i) p = fmaf(x[i], w[i], p);
+            gs = gs + p;
+        }
+        acc = acc + gs;
     }
     return acc;
 }

@@ -52,7 +52,9 @@ void oracle_quantize_nvfp4(const float *src, int64_t R, int64_t K, float amax,
 double oracle_nvfp4_dot(const uint8_t *qa, const uint8_t *sfa,
                         const uint8_t *qb, const uint8_t *sfb, int64_t K);
 
-/* Router: canonical fp32 logits, top-k by (logit desc, index asc), softmax over the
+/* Router: canonical fp32 logits (64-element fmaf chunks; chunk partials summed left to right
+ * in groups of 16 chunks; group sums summed left to right; then the bias), top-k by
+ * (logit desc, index asc), softmax over the
  * k selected logits (fp64, rounded to float).  x: [T][d] values, Wr: [E][d], b: [E] or NULL.
  * idx/w: [T][k] in ascending expert id; logits [T][E] and counts [E] optional. */
 void oracle_router(const float *x, int64_t T, int d, const float *Wr, const float *b,

@@ -61,6 +61,21 @@ def test_k1_is_one_hot_and_all_equal_logits_pick_lowest_indices():
     assert np.allclose(w, 0.25)
 
 
+def test_canonical_two_level_order_worked_example():
+    # d = 2048: two groups of 16 chunks.  Chunk 0 gives p0 = 2^24 (group 0); chunks 16 and 17
+    # give 1 and -2^24 (group 1).  Group sums: G0 = 2^24, G1 = (0 + 1) + (-2^24) = 1 - 2^24
+    # (exact in fp32); logit = (0 + G0) + G1 = 1.  A flat left-to-right sum of the chunk
+    # partials would give ((2^24 + 1) -> 2^24) - 2^24 = 0.  Worked by hand from the order.
+    d = 2048
+    x = np.zeros((1, d), np.float32)
+    W = np.zeros((1, d), np.float32)
+    x[0, 0], W[0, 0] = 2.0 ** 12, 2.0 ** 12
+    x[0, 16 * 64], W[0, 16 * 64] = 1.0, 1.0
+    x[0, 17 * 64], W[0, 17 * 64] = -(2.0 ** 12), 2.0 ** 12
+    lg, _, _, _ = oracle.router(x, W, None, 1)
+    assert lg[0, 0] == 1.0
+
+
 def test_canonical_chunked_fp32_order_worked_example():
     # d = 192: three chunks of 64.  Chunk sums p0 = 2^24, p1 = 1, p2 = -2^24 (each exact).
     # Canonical order ((0 + p0) + p1) + p2 = (2^24 + 1 -> 2^24 in fp32) - 2^24 = 0, whereas
