@@ -48,6 +48,8 @@ def args_():
     p.add_argument("--no-prefill", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--prefill-steps", type=int, default=20)
+    p.add_argument("--only-prefill", action="store_true",
+                   help="profiling aid: build and run only the prefill workload, print its line")
     return p.parse_args()
 
 
@@ -55,17 +57,24 @@ def args_():
 # distributed plumbing (timing only; no data-path collective)
 # ----------------------------------------------------------------------------------------
 class Dist:
-    def __init__(self, n):
+    """One process per GPU (torchrun env).  Only timing is exchanged: a barrier around the
+    timed region and the max of the per-rank elapsed times.  backend "gloo" runs on CPU."""
+
+    def __init__(self, backend: str = "nccl"):
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
         self.rank = int(os.environ.get("RANK", "0"))
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
         self.pg = None
+        self.device = "cuda" if backend == "nccl" else "cpu"
         if self.world > 1:
             import torch.distributed as dist
-            torch.cuda.set_device(self.local)
-            dist.init_process_group("nccl", device_id=torch.device("cuda", self.local))
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+                dist.init_process_group("nccl", device_id=torch.device("cuda", self.local))
+            else:
+                dist.init_process_group("gloo")
             self.pg = dist
-        else:
+        elif backend == "nccl":
             torch.cuda.set_device(0)
 
     def barrier(self):
@@ -75,7 +84,7 @@ class Dist:
     def max(self, v: float) -> float:
         if not self.pg:
             return v
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        t = torch.tensor([v], dtype=torch.float64, device=self.device)
         self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
         return float(t.item())
 
@@ -382,13 +391,23 @@ def roofline_entry(prof, moe, T, pk):
 
 def main():
     a = args_()
-    dist = Dist(a.gpus)
+    dist = Dist("nccl")
     if a.impl == "reference":
         run_reference(a, dist)
         dist.close()
         return
     import nvfp4_latentmoe_fwd_02_b300 as lm
     pk = peaks()
+    if a.only_prefill:
+        L, moes = build_layers([PREFILL])
+        pc = lmoe_synth.CONFIGS[PREFILL]
+        pr = Runner(moes[PREFILL], pc["T"], pc["seed"], pool=2)
+        pms = pr.timed_steps(a.steps, max(3, a.warmup))
+        if dist.rank == 0:
+            print(json.dumps({"workload": PREFILL, "ms_per_step": sum(pms) / len(pms),
+                              "per_kernel_ms": dict(pr.profile(reps=2))}), flush=True)
+        dist.close()
+        return
     names = [HEADLINE] + ([] if a.no_prefill else [PREFILL])
     L, moes = build_layers(names)
     cfg = lmoe_synth.CONFIGS[HEADLINE]

@@ -69,7 +69,7 @@ typedef struct {
 /* Create a layer context: validates the dims, allocates the context buffers, quantizes every
  * expert matrix to NVFP4 (one FP32 tensor scale per expert per matrix, computed from its amax)
  * and lays the block scales out for the tensor cores; synchronizes `stream` once at the end.
- * Dims: d, l and ffn multiples of 64; 1 <= k <= 32; k <= E <= 1024.
+ * Dims: d, l and ffn multiples of 64; l <= 4096; 1 <= k <= 32; k <= E <= 1024; E % 4 == 0.
  * (The Ultra layer: d = 8192, l = 2048, E = 512, k = 22; ffn is not given by the pages.)
  * Errors: LMOE_EINVAL (dims / NULL pointers / amax <= 0), LMOE_ENOMEM, LMOE_ECUDA,
  * LMOE_EUNSUPPORTED (device is not compute capability 10.3). */
@@ -94,8 +94,9 @@ lmoe_status lmoe_quantize_nvfp4(const void *src, lmoe_dtype dt, int64_t rows, in
  *   idx     device int32 [T][k]  selected experts, ascending expert id per token
  *   w       device float [T][k]  softmax over the k selected logits, same order as idx
  *   counts  device int32 [E]     tokens per expert (may be NULL)
- * Logits are computed in the canonical fp32 order (64-element fma chunks, chunk partials added
- * left to right, then the bias), so idx and counts are exact.  Uses context-owned scratch
+ * Logits are computed in the canonical fp32 order (64-element fma chunks; chunk partials added
+ * left to right in groups of 16; group sums added left to right; then the bias), so idx and
+ * counts are exact.  Uses context-owned scratch
  * (grown with cudaMallocAsync on first use for a larger T).  T >= 0. */
 lmoe_status lmoe_route(lmoe_ctx *ctx, const void *x, int64_t T, int32_t *idx, float *w,
                        int32_t *counts, lmoe_stream stream);
@@ -106,16 +107,16 @@ lmoe_status lmoe_route(lmoe_ctx *ctx, const void *x, int64_t T, int32_t *idx, fl
  * loops whose device memory is fixed at start-up, and hosts that embed the library without
  * handing it any allocator.  lmoe_route may grow a context-owned scratch with cudaMallocAsync;
  * lmoe_route_static never allocates or frees.  It has lmoe_route's arguments and results, but
- * keeps the router's scratch (the T x E fp32 logits) in one fixed array of
- * LMOE_ROUTE_STATIC_SCRATCH_BYTES compiled into liblmoe.so, which every GPU that loads the
- * library holds until the process exits.
- *   - T * E * 4 must not exceed LMOE_ROUTE_STATIC_SCRATCH_BYTES (T <= 8192 at E = 512);
- *     larger T returns LMOE_EINVAL before anything is launched.
+ * keeps the router's scratch (fp32 group sums, T x ceil(d/1024) x E, when T <= 64; fp32
+ * logits, T x E, above) in one fixed array of LMOE_ROUTE_STATIC_SCRATCH_BYTES compiled into
+ * liblmoe.so, which every GPU that loads the library holds until the process exits.
+ *   - That scratch must fit in LMOE_ROUTE_STATIC_SCRATCH_BYTES (at d = 8192, E = 512: every
+ *     T <= 8192); a larger T returns LMOE_EINVAL before anything is launched.
  *   - The first call on a device looks up the array's device address (once per device, with
  *     that device current; the context's device must be current).  Make that first call before
  *     any CUDA stream capture.
  *   - Every call on a device shares the one array, and it keeps the last call's contents.  The
- *     logits are fully written before they are read, and `counts` is zeroed by the call, so no
+ *     scratch is fully written before it is read, and `counts` is zeroed by the call, so no
  *     earlier contents leak into a result; but two calls whose kernels overlap on the GPU (on
  *     different streams, or from different contexts of one device) race on the array: order
  *     such calls on one stream or with events. */
@@ -127,8 +128,11 @@ lmoe_status lmoe_route_static(lmoe_ctx *ctx, const void *x, int64_t T, int32_t *
 size_t lmoe_workspace_size(const lmoe_ctx *ctx, int64_t T);
 
 /* The layer forward: x device bf16 [T][d] -> y device bf16 [T][d].  No host synchronization
- * and no host read of device data; every launch is on `stream`, so the call can be captured
- * in a CUDA graph.  ws: device workspace of at least lmoe_workspace_size(ctx, T) bytes.
+ * and no host read of device data.  Work is launched on `stream` and, for small T, partly on a
+ * context-owned second stream that forks from `stream` and joins back into it with events, so
+ * the whole call is ordered after earlier work on `stream`, later work on `stream` is ordered
+ * after it, and it can be captured in a CUDA graph.
+ * ws: device workspace of at least lmoe_workspace_size(ctx, T) bytes.
  * Errors: LMOE_EINVAL (NULL / T < 0), LMOE_ENOMEM (ws_bytes too small), LMOE_ECUDA. */
 lmoe_status lmoe_forward(lmoe_ctx *ctx, const void *x, int64_t T, void *y, void *ws,
                          size_t ws_bytes, lmoe_stream stream);

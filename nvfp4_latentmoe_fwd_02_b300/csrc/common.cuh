@@ -221,6 +221,17 @@ __host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
 }
 
 // ------------------------------------------------------------------------------------
+// programmatic dependent launch: every kernel of the forward is launched so that its CTAs may
+// start while the previous kernel drains; pdl_wait() blocks until the previous grid has
+// completed and its writes are visible, so it comes before the first global access.
+// pdl_trigger() lets the next grid be scheduled (its CTAs then wait in their own pdl_wait()).
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ------------------------------------------------------------------------------------
 // numeric helpers
 // ------------------------------------------------------------------------------------
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {

@@ -66,6 +66,12 @@ struct GemmArgs {
     const int32_t *row_slot;     // [rows] routing slot of a permuted row (combine)
     const float *route_w;        // [T*k]
     int topk;
+    // z epilogue: copies of each token's zq row into its k expert-segment rows
+    const int32_t *idx;          // [T*k] selected experts
+    const int32_t *slot_off;     // [T*k] row of each slot inside its expert's segment
+    uint8_t *a_codes;            // [R][N/2]
+    uint8_t *a_sf;               // scale atoms [R/128][N/64][512]
+    int32_t *row_slot_out;       // [R]
     unsigned *err;
 };
 
@@ -219,10 +225,20 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs &g, const Tile &tl
         }
         *reinterpret_cast<uint4 *>(g.q_codes + grow * (g.N / 2) + col / 2) = make_uint4(w[0], w[1], w[2], w[3]);
         const uint16_t s2 = static_cast<uint16_t>(s[0] | (s[1] << 8));
-        if (g.epi == EPI_Z_QUANT)
+        if (g.epi == EPI_Z_QUANT) {
             *reinterpret_cast<uint16_t *>(g.q_sf + grow * (g.N / 16) + col / 16) = s2;
-        else
+            // the token's k expert-segment rows get the same codes and scales
+            for (int j = 0; j < g.topk; ++j) {
+                const int64_t slot = grow * g.topk + j;
+                const int row = __ldg(g.seg_start + __ldg(g.idx + slot)) + __ldg(g.slot_off + slot);
+                *reinterpret_cast<uint4 *>(g.a_codes + static_cast<int64_t>(row) * (g.N / 2) + col / 2) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint16_t *>(g.a_sf + sf_atom_offset(row, col / 16, g.N / 64)) = s2;
+                if (col == 0) g.row_slot_out[row] = static_cast<int32_t>(slot);
+            }
+        } else {
             *reinterpret_cast<uint16_t *>(g.q_sf + sf_atom_offset(grow, col / 16, g.N / 64)) = s2;
+        }
         break;
     }
     case EPI_COMBINE: {
@@ -312,6 +328,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     if (warp == 0 && lane == 0) { prefetch_tmap(&tmA); prefetch_tmap(&tmB); }
     if (warp == 1) { tmem_alloc(s_tmem, kTmemCols); tmem_relinquish(); }
+    pdl_wait();      // the previous kernel's outputs (tables, activations) are complete
+    pdl_trigger();
     if (NVF4 && g.grouped) {
         for (int i = threadIdx.x; i <= g.E; i += blockDim.x) {
             tb->mt[i] = __ldg(g.mt_start + i);

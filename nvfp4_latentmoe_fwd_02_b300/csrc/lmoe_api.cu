@@ -13,6 +13,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <utility>
 
 #include "lmoe.h"   // include/ (on the include path)
 #include "common.cuh"
@@ -31,7 +32,6 @@ constexpr int kStagesF4Small = 4;     // decode (T <= 32): 4 KB A boxes, 2 colum
 constexpr int kStagesBF16Small = 5;
 constexpr int kSmallAMaxT = 32;
 inline int kb_for(bool small_a) { return small_a ? 2 : 1; }   // column blocks per stage
-constexpr int kSmallRouterMaxT = 64;   // router: shared-memory chunk reduction up to this T
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -70,10 +70,29 @@ bool make_map(CUtensorMap *m, bool bf16, const void *ptr, uint64_t inner, uint64
 }
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Launch with programmatic stream serialization: the kernel's CTAs may be scheduled while the
+// previous kernel on the stream drains; each kernel of this library calls pdl_wait() before
+// its first global access (see common.cuh), so results are the same as a plain launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct WsLayout {
-    size_t idx, w, counts, seg, mt, fill, nrows, row_slot, router, zacc, zq_codes, zq_sf, z_dbg,
+    size_t idx, w, counts, seg, mt, slot_off, nrows, row_slot, router, zacc, zq_codes, zq_sf, z_dbg,
         a_codes, a_sf, h_codes, h_sf, h_dbg, c_acc, c, yacc, total;
     int64_t R;   // row capacity of the permuted buffers (multiple of 128)
     bool small_router, split_down, split_up;
@@ -86,7 +105,7 @@ struct lmoe_ctx {
     int d, l, E, k, ffn;
     int dev, num_sms;
     __nv_bfloat16 *w_down, *w_up;
-    float *w_router, *b_router;
+    float *w_router, *b_router;   // w_router transposed: [d][E]
     uint8_t *w1_codes, *w1_sf, *w2_codes, *w2_sf;
     float *w1_sdec, *w2_sdec, *alpha1, *alpha2;
     unsigned *amax_bits;   // [2E]
@@ -97,6 +116,9 @@ struct lmoe_ctx {
     int debug;
     void *route_ws;
     size_t route_ws_bytes;
+    // second stream: the split-K down-projection runs beside the router (fork / join events)
+    cudaStream_t aux;
+    cudaEvent_t ev_fork, ev_join;
     // per-kernel timing (lmoe_set_profile)
     int profile;
     int nprof;
@@ -138,7 +160,7 @@ WsLayout layout(const lmoe_ctx *c, int64_t T) {
     const int64_t d = c->d, l = c->l, E = c->E, k = c->k, F = c->ffn;
     L.R = cdiv(T * k + E * 127, 128) * 128;
     if (L.R == 0) L.R = 128;
-    L.small_router = T <= kSmallRouterMaxT;
+    L.small_router = T <= kSmallMaxT;
     const int mt = static_cast<int>(cdiv(T, 128));
     const int kb = kb_for(T <= kSmallAMaxT);
     L.down_splits = plan_splits(mt, static_cast<int>(cdiv(l, 128)), static_cast<int>(cdiv(d / 64, kb)), c->num_sms);
@@ -152,10 +174,10 @@ WsLayout layout(const lmoe_ctx *c, int64_t T) {
     L.counts = take(E * 4);
     L.seg = take((E + 1) * 4);
     L.mt = take((E + 1) * 4);
-    L.fill = take(E * 4);
+    L.slot_off = take(T * k * 4);
     L.nrows = take(4);
     L.row_slot = take(L.R * 4);
-    L.router = take(T * E * 4);
+    L.router = take(T <= kSmallMaxT ? T * cdiv(d / kChunk, kGroupChunks) * E * 4 : T * E * 4);
     L.zacc = take(L.split_down ? T * l * 4 : 0);
     L.zq_codes = take(T * l / 2);
     L.zq_sf = take(T * l / 16);
@@ -183,9 +205,8 @@ cudaError_t set_smem_attr() {
 template <bool NVF4, bool SMALLA, int KB, int STAGES>
 cudaError_t launch_gemm_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int grid,
                             cudaStream_t s) {
-    gemm_kernel<NVF4, SMALLA, KB, STAGES>
-        <<<grid, kGemmThreads, gemm_smem_bytes<NVF4, SMALLA, KB>(STAGES), s>>>(ta, tb, g);
-    return cudaGetLastError();
+    return launch_pdl(gemm_kernel<NVF4, SMALLA, KB, STAGES>, dim3(grid), dim3(kGemmThreads),
+                      gemm_smem_bytes<NVF4, SMALLA, KB>(STAGES), s, ta, tb, g);
 }
 
 // small_a: every tile has at most 32 valid A rows (T <= 32); such launches use two column
@@ -235,26 +256,30 @@ lmoe_status check_error_word(lmoe_ctx *c) {
     return LMOE_OK;
 }
 
-// The router on x: logits (small-T or tiled kernel) into `logits` [T][E], then top-k,
+// The router on x: chunk partials (small T) or logits (large T) into `scratch`, then top-k,
 // softmax and counts.
-lmoe_status launch_router(lmoe_ctx *c, const __nv_bfloat16 *x, int64_t T, float *logits,
-                          int32_t *idx, float *w, int32_t *counts, const ZeroRanges &zr,
-                          cudaStream_t s) {
-    const bool small = T <= kSmallRouterMaxT && c->d / kChunk <= kSmallMaxC;
+lmoe_status launch_router(lmoe_ctx *c, const __nv_bfloat16 *x, int64_t T, float *scratch,
+                          int32_t *idx, float *w, int32_t *counts, int32_t *slot_off,
+                          const ZeroRanges &zr, cudaStream_t s) {
+    const bool small = T <= kSmallMaxT;
+    const int C = c->d / kChunk;
+    const int NG = static_cast<int>(cdiv(C, kGroupChunks));
     if (small) {
-        router_small_kernel<<<static_cast<unsigned>(cdiv(c->E, kSmallExperts)), 128 * kSmallExperts,
-                              router_small_smem(c->d), s>>>(x, c->w_router, c->b_router,
-                                                            static_cast<int>(T), c->d, c->E, logits, zr);
+        LMOE_CUDA(launch_pdl(router_small_kernel,
+                             dim3(static_cast<unsigned>(cdiv(c->E, kSmallEG)), static_cast<unsigned>(cdiv(C, kSmallCG))),
+                             dim3(kSmallEG * kSmallCG), kRouterSmallSmem, s, x,
+                             static_cast<const float *>(c->w_router), static_cast<int>(T), c->d, c->E, scratch, zr));
     } else {
         dim3 grid(static_cast<unsigned>(cdiv(T, kRT)), static_cast<unsigned>(cdiv(c->E, kRE)));
-        router_logits_kernel<<<grid, 128, kRouterLogitsSmem, s>>>(x, c->w_router, c->b_router,
-                                                                  static_cast<int>(T), c->d, c->E, logits, zr);
+        LMOE_CUDA(launch_pdl(router_logits_kernel, grid, dim3(128), kRouterLogitsSmem, s, x,
+                             static_cast<const float *>(c->w_router), static_cast<const float *>(c->b_router),
+                             static_cast<int>(T), c->d, c->E, scratch, zr));
     }
-    LMOE_LAUNCH();
     prof_mark(c, small ? "router_small" : "router_logits", s);
-    router_topk_kernel<<<static_cast<unsigned>(T), kTopkThreads, 0, s>>>(
-        logits, static_cast<int>(T), c->E, c->k, idx, w, counts);
-    LMOE_LAUNCH();
+    LMOE_CUDA(launch_pdl(router_topk_kernel, dim3(static_cast<unsigned>(T)), dim3(kTopkThreads), 0, s,
+                         static_cast<const float *>(scratch), small ? NG : 0,
+                         static_cast<const float *>(small ? c->b_router : nullptr), static_cast<int>(T), c->E,
+                         c->k, idx, w, counts, slot_off));
     prof_mark(c, "router_topk", s);
     return LMOE_OK;
 }
@@ -266,9 +291,10 @@ ZeroRanges zero_counts(int32_t *counts, int E) {
     return z;
 }
 
-// Scratch bytes the router needs for T tokens (the fp32 logits).
+// Scratch bytes the router needs for T tokens: fp32 group sums (T <= 64) or logits.
 size_t route_scratch_bytes(const lmoe_ctx *c, int64_t T) {
-    return static_cast<size_t>(T) * c->E * 4;
+    return T <= kSmallMaxT ? static_cast<size_t>(T) * cdiv(c->d / kChunk, kGroupChunks) * c->E * 4
+                           : static_cast<size_t>(T) * c->E * 4;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -356,7 +382,8 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
     *out = nullptr;
     if (!w || !w->w_down || !w->w_up || !w->w_router || !w->w1 || !w->w2) return LMOE_EINVAL;
     if (d <= 0 || l <= 0 || ffn <= 0 || d % 64 || l % 64 || ffn % 64) return LMOE_EINVAL;
-    if (k < 1 || k > 32 || E < k || E > 1024) return LMOE_EINVAL;
+    if (l > 4096) return LMOE_EINVAL;
+    if (k < 1 || k > 32 || E < k || E > 1024 || E % 4) return LMOE_EINVAL;
     if (!(w->amax_z > 0.0f) || !(w->amax_h > 0.0f)) return LMOE_EINVAL;
     int dev = 0;
     LMOE_CUDA(cudaGetDevice(&dev));
@@ -372,11 +399,11 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
             cudaError_t b = set_smem_attr<false, false, 1, kStagesBF16>();
             if (a == cudaSuccess) a = set_smem_attr<true, true, 2, kStagesF4Small>();
             if (b == cudaSuccess) b = set_smem_attr<false, true, 2, kStagesBF16Small>();
-            cudaError_t r = cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 router_small_smem(kSmallMaxC * kChunk));
+            cudaError_t r = cudaFuncSetAttribute(router_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kRouterLogitsSmem);
             if (r == cudaSuccess)
-                r = cudaFuncSetAttribute(router_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kRouterLogitsSmem);
+                r = cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kRouterSmallSmem);
             attr_err = a != cudaSuccess ? a : (b != cudaSuccess ? b : r);
         });
         if (attr_err != cudaSuccess) return cuda_status(attr_err);
@@ -415,10 +442,15 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
     CREATE_CUDA(cudaMalloc(&c->alpha2, E * 4));
     CREATE_CUDA(cudaMalloc(&c->amax_bits, 2 * E * 4));
     CREATE_CUDA(cudaMalloc(&c->err, sizeof(unsigned)));
+    CREATE_CUDA(cudaStreamCreateWithFlags(&c->aux, cudaStreamNonBlocking));
+    CREATE_CUDA(cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming));
+    CREATE_CUDA(cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming));
     CREATE_CUDA(cudaMemsetAsync(c->err, 0, sizeof(unsigned), s));
     CREATE_CUDA(cudaMemcpyAsync(c->w_down, w->w_down, static_cast<size_t>(l) * d * 2, cudaMemcpyDeviceToDevice, s));
     CREATE_CUDA(cudaMemcpyAsync(c->w_up, w->w_up, static_cast<size_t>(d) * l * 2, cudaMemcpyDeviceToDevice, s));
-    CREATE_CUDA(cudaMemcpyAsync(c->w_router, w->w_router, static_cast<size_t>(E) * d * 4, cudaMemcpyDeviceToDevice, s));
+    transpose_f32_kernel<<<dim3(static_cast<unsigned>(cdiv(d, 32)), static_cast<unsigned>(cdiv(E, 32))),
+                           dim3(32, 8), 0, s>>>(w->w_router, E, d, c->w_router);
+    CREATE_CUDA(cudaGetLastError());
     if (w->b_router)
         CREATE_CUDA(cudaMemcpyAsync(c->b_router, w->b_router, E * 4, cudaMemcpyDeviceToDevice, s));
     else
@@ -476,6 +508,9 @@ void lmoe_destroy(lmoe_ctx *c) {
         if (p) cudaFree(p);
     for (cudaEvent_t e : c->ev)
         if (e) cudaEventDestroy(e);
+    if (c->ev_fork) cudaEventDestroy(c->ev_fork);
+    if (c->ev_join) cudaEventDestroy(c->ev_join);
+    if (c->aux) cudaStreamDestroy(c->aux);
     delete c;
 }
 
@@ -494,7 +529,7 @@ lmoe_status lmoe_route_static(lmoe_ctx *c, const void *x, int64_t T, int32_t *id
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (counts && reinterpret_cast<uintptr_t>(counts) % 16) return LMOE_EINVAL;
     return launch_router(c, static_cast<const __nv_bfloat16 *>(x), T, static_cast<float *>(scratch),
-                         idx, w, counts, zero_counts(counts, c->E), s);
+                         idx, w, counts, nullptr, zero_counts(counts, c->E), s);
 }
 
 size_t lmoe_workspace_size(const lmoe_ctx *c, int64_t T) {
@@ -552,7 +587,8 @@ lmoe_status lmoe_route(lmoe_ctx *c, const void *x, int64_t T, int32_t *idx, floa
     }
     if (counts && reinterpret_cast<uintptr_t>(counts) % 16) return LMOE_EINVAL;
     return launch_router(c, static_cast<const __nv_bfloat16 *>(x), T,
-                         static_cast<float *>(c->route_ws), idx, w, counts, zero_counts(counts, c->E), s);
+                         static_cast<float *>(c->route_ws), idx, w, counts, nullptr,
+                         zero_counts(counts, c->E), s);
 }
 
 lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *ws, size_t ws_bytes,
@@ -574,7 +610,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     int32_t *counts = static_cast<int32_t *>(at(L.counts));
     int32_t *seg = static_cast<int32_t *>(at(L.seg));
     int32_t *mt = static_cast<int32_t *>(at(L.mt));
-    int32_t *fill = static_cast<int32_t *>(at(L.fill));
+    int32_t *slot_off = static_cast<int32_t *>(at(L.slot_off));
     int32_t *nrows = static_cast<int32_t *>(at(L.nrows));
     int32_t *row_slot = static_cast<int32_t *>(at(L.row_slot));
     float *zacc = static_cast<float *>(at(L.zacc));
@@ -596,24 +632,10 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         cudaEventRecord(c->ev[0], s);
     }
 
-    // 1. router (its first kernel also clears the histogram and the fp32 accumulators)
-    {
-        ZeroRanges z;
-        std::memset(&z, 0, sizeof(z));
-        z.p[0] = reinterpret_cast<uint4 *>(counts); z.n16[0] = cdiv(E * 4, 16);
-        z.p[1] = reinterpret_cast<uint4 *>(c_acc); z.n16[1] = T * l * 4 / 16;
-        if (L.split_down) { z.p[2] = reinterpret_cast<uint4 *>(zacc); z.n16[2] = T * l * 4 / 16; }
-        if (L.split_up) { z.p[3] = reinterpret_cast<uint4 *>(yacc); z.n16[3] = T * d * 4 / 16; }
-        lmoe_status st = launch_router(c, static_cast<const __nv_bfloat16 *>(x), T,
-                                       static_cast<float *>(at(L.router)), idx, rw, counts, z, s);
-        if (st != LMOE_OK) return st;
-    }
-    // 2. per-expert segments
-    segments_kernel<<<E, 128, 0, s>>>(counts, E, seg, mt, fill, row_slot, nrows);
-    LMOE_LAUNCH();
-    prof_mark(c, "segments", s);
-    // 3. down-projection z = x Wd^T, quantized to NVFP4
-    {
+    // The split-K down-projection does not depend on routing: it runs on the context's second
+    // stream, beside the router, and joins before its finalize (which needs the segments).
+    const bool fork = L.split_down && !c->profile;
+    auto down_proj = [&](cudaStream_t ds) -> lmoe_status {
         CUtensorMap tx;
         if (!make_map(&tx, true, x, d, T, static_cast<uint64_t>(d) * 2, kABoxRows)) return LMOE_ECUDA;
         GemmArgs g = dense_args(static_cast<int>(T), l, d, L.down_splits,
@@ -622,24 +644,60 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
             g.out = zacc; g.ld_out = l;
         } else {
             g.q = c->qz; g.q_codes = zq_codes; g.q_sf = zq_sf; g.dbg = z_dbg;
+            g.topk = k; g.idx = idx; g.slot_off = slot_off; g.seg_start = seg;
+            g.a_codes = a_codes; g.a_sf = a_sf; g.row_slot_out = row_slot;
         }
         LMOE_CUDA((launch_gemm<false>(tx, c->tm_wd, g,
-                                                   grid_for(int64_t(g.m_tiles) * g.n_tiles * g.k_splits, c->num_sms), small_a, s)));
-        prof_mark(c, "down_proj", s);
+                                      grid_for(int64_t(g.m_tiles) * g.n_tiles * g.k_splits, c->num_sms), small_a, ds)));
+        prof_mark(c, "down_proj", ds);
+        return LMOE_OK;
+    };
+    if (fork) {
+        LMOE_CUDA(cudaEventRecord(c->ev_fork, s));
+        LMOE_CUDA(cudaStreamWaitEvent(c->aux, c->ev_fork, 0));
+        ZeroRanges zz;
+        std::memset(&zz, 0, sizeof(zz));
+        zz.p[0] = reinterpret_cast<uint4 *>(zacc); zz.n16[0] = T * l * 4 / 16;
+        LMOE_CUDA(launch_pdl(zero_kernel, dim3(c->num_sms), dim3(256), 0, c->aux, zz));
+        lmoe_status st = down_proj(c->aux);
+        if (st != LMOE_OK) return st;
+        LMOE_CUDA(cudaEventRecord(c->ev_join, c->aux));
+    }
+
+    // 1. router (its first kernel also clears the histogram and the fp32 accumulators)
+    {
+        ZeroRanges z;
+        std::memset(&z, 0, sizeof(z));
+        z.p[0] = reinterpret_cast<uint4 *>(counts); z.n16[0] = cdiv(E * 4, 16);
+        z.p[1] = reinterpret_cast<uint4 *>(c_acc); z.n16[1] = T * l * 4 / 16;
+        if (L.split_down && !fork) { z.p[2] = reinterpret_cast<uint4 *>(zacc); z.n16[2] = T * l * 4 / 16; }
+        if (L.split_up) { z.p[3] = reinterpret_cast<uint4 *>(yacc); z.n16[3] = T * d * 4 / 16; }
+        lmoe_status st = launch_router(c, static_cast<const __nv_bfloat16 *>(x), T,
+                                       static_cast<float *>(at(L.router)), idx, rw, counts, slot_off, z, s);
+        if (st != LMOE_OK) return st;
+    }
+    // 2. per-expert segments
+    LMOE_CUDA(launch_pdl(segments_kernel, dim3(E), dim3(128), 0, s, static_cast<const int32_t *>(counts), E,
+                         seg, mt, row_slot, nrows));
+    prof_mark(c, "segments", s);
+    // 3. down-projection z = x Wd^T, quantized to NVFP4
+    {
+        if (fork) {
+            LMOE_CUDA(cudaStreamWaitEvent(s, c->ev_join, 0));
+        } else {
+            lmoe_status st = down_proj(s);
+            if (st != LMOE_OK) return st;
+        }
         if (L.split_down) {
-            const int grid = static_cast<int>(std::min<int64_t>(cdiv(T * l / 16, 256), c->num_sms * 8));
-            z_finalize_kernel<<<grid, 256, 0, s>>>(zacc, T, l, c->qz, zq_codes, zq_sf, z_dbg);
-            LMOE_LAUNCH();
+            // whole tokens per block: 256 threads cover 256 / (l/16) tokens (l <= 4096, k * tokens <= 256)
+            const int nb = l / 16;
+            const int tpb = std::max(1, std::min(256 / nb, 256 / k));
+            LMOE_CUDA(launch_pdl(z_finalize_kernel, dim3(static_cast<unsigned>(cdiv(T, tpb))), dim3(tpb * nb), 0, s,
+                                 static_cast<const float *>(zacc), T, l, c->qz, zq_codes, zq_sf, z_dbg,
+                                 static_cast<const int32_t *>(idx), static_cast<const int32_t *>(slot_off),
+                                 static_cast<const int32_t *>(seg), k, row_slot, a_codes, a_sf));
             prof_mark(c, "z_finalize", s);
         }
-    }
-    // 4. gather the quantized latent tokens into per-expert segments
-    {
-        const int64_t nslots = T * k;
-        scatter_kernel<<<static_cast<unsigned>(cdiv(nslots, 8)), 256, 0, s>>>(
-            idx, nslots, seg, fill, row_slot, k, l, zq_codes, zq_sf, a_codes, a_sf);
-        LMOE_LAUNCH();
-        prof_mark(c, "scatter", s);
     }
     // 5. latent-up grouped GEMM + relu^2 + requantize
     {
@@ -676,8 +734,8 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     // 7. c = bf16(c_acc)
     {
         const int grid = static_cast<int>(std::min<int64_t>(cdiv(T * l / 8, 256), c->num_sms * 8));
-        f32_to_bf16_kernel<<<grid, 256, 0, s>>>(c_acc, T * l, cb);
-        LMOE_LAUNCH();
+        LMOE_CUDA(launch_pdl(f32_to_bf16_kernel, dim3(grid), dim3(256), 0, s, static_cast<const float *>(c_acc),
+                             T * l, cb));
         prof_mark(c, "combine_cast", s);
     }
     // 8. up-projection y = c Wu^T
@@ -693,8 +751,8 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         prof_mark(c, "up_proj", s);
         if (L.split_up) {
             const int grid = static_cast<int>(std::min<int64_t>(cdiv(T * d / 8, 256), c->num_sms * 8));
-            f32_to_bf16_kernel<<<grid, 256, 0, s>>>(yacc, T * d, static_cast<__nv_bfloat16 *>(y));
-            LMOE_LAUNCH();
+            LMOE_CUDA(launch_pdl(f32_to_bf16_kernel, dim3(grid), dim3(256), 0, s, static_cast<const float *>(yacc),
+                                 T * d, static_cast<__nv_bfloat16 *>(y)));
             prof_mark(c, "y_cast", s);
         }
     }
@@ -742,9 +800,10 @@ lmoe_status lmoe_get_expert_nvfp4(const lmoe_ctx *c, int which, int e, uint8_t *
 int lmoe_forward_kernel_count(const lmoe_ctx *c, int64_t T) {
     if (!c || T <= 0) return 0;
     const WsLayout L = layout(c, T);
-    // router logits, top-k, segments, down-proj, scatter, expert-up, expert-down, combine
-    // cast, up-proj, plus one finalize per split projection
-    return 9 + (L.split_down ? 1 : 0) + (L.split_up ? 1 : 0);
+    // router logits, top-k, segments, down-proj, expert-up, expert-down, combine cast,
+    // up-proj, plus one finalize per split projection (and, for a split down-projection run
+    // beside the router, the clearing of its accumulator)
+    return 8 + (L.split_down ? 2 : 0) + (L.split_up ? 1 : 0);
 }
 
 lmoe_status lmoe_set_profile(lmoe_ctx *c, int on) {

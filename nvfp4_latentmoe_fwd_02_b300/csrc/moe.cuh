@@ -5,7 +5,8 @@
 // buffers; each segment is padded to a multiple of 128 rows (one tensor-core M tile) so that
 // every tile's block scales sit in whole 128-row scale atoms.  row_slot[row] is the routing
 // slot (token * k + j) of a row, -1 for padding.  mt_start[e] is the prefix sum of M tiles.
-// Rows inside a segment are in atomic-arrival order (the grouping, not the order, is fixed).
+// A slot's row inside its segment is the histogram's old value when the top-k kernel counted
+// it (atomic-arrival order: the grouping, not the order inside a segment, is fixed).
 #pragma once
 #include "common.cuh"
 #include "nvfp4.cuh"
@@ -17,10 +18,11 @@ namespace lmoe {
 // Block E - 1 writes the totals.  grid = E, block = 128.
 __global__ void __launch_bounds__(128) segments_kernel(
     const int32_t *__restrict__ counts, int E, int32_t *__restrict__ seg_start,
-    int32_t *__restrict__ mt_start, int32_t *__restrict__ fill, int32_t *__restrict__ row_slot,
-    int32_t *__restrict__ nrows) {
+    int32_t *__restrict__ mt_start, int32_t *__restrict__ row_slot, int32_t *__restrict__ nrows) {
     __shared__ int part[4];
     const int e = blockIdx.x;
+    pdl_wait();
+    pdl_trigger();
     int sum = 0;
     for (int i = threadIdx.x; i < e; i += blockDim.x) sum += (__ldg(counts + i) + 127) & ~127;
 #pragma unroll
@@ -33,7 +35,6 @@ __global__ void __launch_bounds__(128) segments_kernel(
     if (threadIdx.x == 0) {
         seg_start[e] = start;
         mt_start[e] = start >> 7;
-        fill[e] = 0;
         if (e == E - 1) {
             seg_start[E] = start + padded;
             mt_start[E] = (start + padded) >> 7;
@@ -43,63 +44,84 @@ __global__ void __launch_bounds__(128) segments_kernel(
     for (int r = start + cnt + threadIdx.x; r < start + padded; r += blockDim.x) row_slot[r] = -1;
 }
 
-// One warp per routing slot: claim a row of the expert's segment and copy the token's
-// quantized latent vector (codes and scales) into it.  l: latent width.
-__global__ void __launch_bounds__(256) scatter_kernel(
-    const int32_t *__restrict__ idx, int64_t nslots, const int32_t *__restrict__ seg_start,
-    int32_t *__restrict__ fill, int32_t *__restrict__ row_slot, int k, int l,
-    const uint8_t *__restrict__ zq_codes, const uint8_t *__restrict__ zq_sf,
-    uint8_t *__restrict__ a_codes, uint8_t *__restrict__ a_sf) {
-    const int lane = threadIdx.x & 31;
-    const int64_t s = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (s >= nslots) return;
-    int pos = 0;
-    if (lane == 0) {
-        const int e = idx[s];
-        pos = seg_start[e] + atomicAdd(fill + e, 1);
-        row_slot[pos] = static_cast<int32_t>(s);
-    }
-    pos = __shfl_sync(0xffffffffu, pos, 0);
-    const int64_t t = s / k;
-    const int row_bytes = l / 2;
-    const uint4 *src = reinterpret_cast<const uint4 *>(zq_codes + t * row_bytes);
-    uint4 *dst = reinterpret_cast<uint4 *>(a_codes + static_cast<int64_t>(pos) * row_bytes);
-    for (int i = lane; i < row_bytes / 16; i += 32) dst[i] = __ldg(src + i);
-    const int K64 = l / 64;
-    const uint32_t *ssrc = reinterpret_cast<const uint32_t *>(zq_sf + t * (l / 16));
-    for (int kb = lane; kb < K64; kb += 32)
-        *reinterpret_cast<uint32_t *>(a_sf + sf_atom_offset(pos, 4 * kb, K64)) = __ldg(ssrc + kb);
+// Where the k copies of token t's quantized latent vector go: segment row of each slot.
+__device__ __forceinline__ int slot_row(const int32_t *idx, const int32_t *slot_off,
+                                        const int32_t *seg_start, int64_t slot) {
+    return __ldg(seg_start + __ldg(idx + slot)) + __ldg(slot_off + slot);
 }
 
-// zacc [T][l] fp32 -> z = bf16(zacc) -> zq (row-major codes and scales); z kept if z_out.
-__global__ void z_finalize_kernel(const float *__restrict__ zacc, int64_t T, int l, QScale q,
-                                  uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,
-                                  __nv_bfloat16 *__restrict__ z_out) {
-    const int64_t total = T * (l / 16);
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        float x[16];
-        load16<float>(zacc + i * 16, x);
+// Split-K finalize of the down-projection, one thread per (token, 16-block): z = bf16(zacc),
+// zq = NVFP4(z) into the row-major buffers and into the token's k segment rows (codes and
+// scale atoms); row_slot records the slot of each written row.  A block covers whole tokens
+// (blockDim / (l/16) of them); their k segment rows are looked up once into shared memory.
+__global__ void __launch_bounds__(256) z_finalize_kernel(
+    const float *__restrict__ zacc, int64_t T, int l, QScale q, uint8_t *__restrict__ codes,
+    uint8_t *__restrict__ sf, __nv_bfloat16 *__restrict__ z_out, const int32_t *__restrict__ idx,
+    const int32_t *__restrict__ slot_off, const int32_t *__restrict__ seg_start, int k,
+    int32_t *__restrict__ row_slot, uint8_t *__restrict__ a_codes, uint8_t *__restrict__ a_sf) {
+    __shared__ int rows_s[256];   // [tokens per block][k]
+    pdl_wait();
+    pdl_trigger();
+    const int nb = l / 16, K64 = l / 64;
+    const int tpb = blockDim.x / nb;                   // tokens per block (>= 1)
+    const int64_t t_first = static_cast<int64_t>(blockIdx.x) * tpb;
+    for (int i = threadIdx.x; i < tpb * k; i += blockDim.x) {
+        const int64_t slot = t_first * k + i;
+        if (t_first + i / k < T) {
+            const int row = slot_row(idx, slot_off, seg_start, slot);
+            rows_s[i] = row;
+            row_slot[row] = static_cast<int32_t>(slot);
+        }
+    }
+    __syncthreads();
+    const int tl = threadIdx.x / nb, b = threadIdx.x - tl * nb;
+    const int64_t t = t_first + tl;
+    if (tl >= tpb || t >= T) return;
+    const int64_t i = t * nb + b;
+    float x[16];
+    load16<float>(zacc + i * 16, x);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) x[j] = bf16_bits_to_f32(f32_to_bf16_bits(x[j]));
+    if (z_out) {
         uint32_t zb[8];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) x[j] = bf16_bits_to_f32(f32_to_bf16_bits(x[j]));
-#pragma unroll
         for (int j = 0; j < 8; ++j) zb[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
-        if (z_out) {
-            uint4 *zo = reinterpret_cast<uint4 *>(z_out + i * 16);
-            zo[0] = make_uint4(zb[0], zb[1], zb[2], zb[3]);
-            zo[1] = make_uint4(zb[4], zb[5], zb[6], zb[7]);
-        }
-        uint32_t lo, hi;
-        const uint32_t s = quant_block16(x, q, lo, hi);
-        reinterpret_cast<uint2 *>(codes)[i] = make_uint2(lo, hi);
-        sf[i] = static_cast<uint8_t>(s);
+        uint4 *zo = reinterpret_cast<uint4 *>(z_out + i * 16);
+        zo[0] = make_uint4(zb[0], zb[1], zb[2], zb[3]);
+        zo[1] = make_uint4(zb[4], zb[5], zb[6], zb[7]);
+    }
+    uint32_t lo, hi;
+    const uint32_t s = quant_block16(x, q, lo, hi);
+    reinterpret_cast<uint2 *>(codes)[i] = make_uint2(lo, hi);
+    sf[i] = static_cast<uint8_t>(s);
+    for (int j = 0; j < k; ++j) {
+        const int row = rows_s[tl * k + j];
+        reinterpret_cast<uint2 *>(a_codes + static_cast<int64_t>(row) * (l / 2))[b] = make_uint2(lo, hi);
+        a_sf[sf_atom_offset(row, b, K64)] = static_cast<uint8_t>(s);
+    }
+}
+
+// out[c][r] = in[r][c] for an [R][Cn] fp32 matrix (router weights, once at create).
+__global__ void transpose_f32_kernel(const float *__restrict__ in, int64_t R, int64_t Cn,
+                                     float *__restrict__ out) {
+    __shared__ float tile[32][33];
+    const int64_t c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+    for (int j = threadIdx.y; j < 32; j += blockDim.y) {
+        const int64_t r = r0 + j, c = c0 + threadIdx.x;
+        if (r < R && c < Cn) tile[j][threadIdx.x] = in[r * Cn + c];
+    }
+    __syncthreads();
+    for (int j = threadIdx.y; j < 32; j += blockDim.y) {
+        const int64_t c = c0 + j, r = r0 + threadIdx.x;
+        if (r < R && c < Cn) out[c * R + r] = tile[threadIdx.x][j];
     }
 }
 
 // acc [n] fp32 -> out [n] bf16 (n % 8 == 0).
 __global__ void f32_to_bf16_kernel(const float *__restrict__ acc, int64_t n,
                                    __nv_bfloat16 *__restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n / 8;
          i += (int64_t)gridDim.x * blockDim.x) {
         const float4 a = __ldg(reinterpret_cast<const float4 *>(acc) + 2 * i);

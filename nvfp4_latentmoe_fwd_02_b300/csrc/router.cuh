@@ -4,11 +4,15 @@
 // per token; shengxinai.com Nemotron 3 blog, section 2.2: the routing gate stays at width d).
 // Logit order (the library's canonical fp32 order, so expert indices are exact):
 //   the d axis is cut into chunks of 64; p_c = fmaf chain over the chunk in ascending index
-//   starting from +0; logit = ((0 + p_0) + p_1) + ... in ascending c; then + bias.
-// Two kernels produce exactly these fp32 operations:
-//   router_small_kernel      small T: one thread per (expert, chunk) computes p_c for a tile
-//                            of tokens; the partials are added in order from shared memory;
-//   router_logits_kernel     large T: register-tiled, each thread walks the chunks in order.
+//   starting from +0; chunks form groups of 16; a group sum is ((0 + p_c0) + p_c0+1) + ...
+//   over its chunks; logit = ((0 + G_0) + G_1) + ... over the groups; then + bias.
+// The router weights are kept transposed, Wt[d][E], so that consecutive experts are
+// consecutive in memory (coalesced loads for threads that own one expert each).
+// Two paths produce exactly these fp32 operations:
+//   small T  router_small_kernel computes the group sums G_g(t, e) into G[t][g][e] (a block
+//            owns one group of 16 chunks); the top-k kernel adds them in ascending g and the
+//            bias;
+//   large T  router_logits_kernel: register-tiled, each thread walks the chunks in order.
 // Selection: logit descending, lower expert index first on ties.  Weights: softmax (fp32,
 // expf) over the k selected logits.  Output slots are in ascending expert id.
 #pragma once
@@ -32,104 +36,79 @@ __device__ __forceinline__ void zero_ranges(const ZeroRanges &z) {
     for (int r = 0; r < 4; ++r)
         for (int64_t i = tid; i < z.n16[r]; i += nthreads) z.p[r][i] = make_uint4(0, 0, 0, 0);
 }
-
-// Small T: logits[t][e] with the chunk partials reduced through shared memory.  Block: four
-// experts x 128 threads; the block stages a tile of 8 tokens of x in shared memory (bf16, chunk
-// rows padded by 16 bytes against bank conflicts); thread c computes the partial p_c (one
-// 64-element fmaf chain) of chunk c for the tile; then one thread per (expert, token) adds the
-// chunk partials left to right and the bias.  d <= 8192 (one chunk per thread);
-// grid = ceil(E / 4); dynamic smem router_small_smem(d).
-constexpr int kSmallTT = 8;
-constexpr int kSmallMaxC = 128;
-constexpr int kSmallExperts = 4;
-constexpr int kXRow = kChunk + 8;   // bf16 elements per staged chunk row (16-byte pad)
-__host__ __device__ constexpr int router_small_smem(int d) {
-    return kSmallTT * (d / kChunk) * kXRow * 2 + kSmallExperts * kSmallTT * (kSmallMaxC + 4) * 4;
+__global__ void zero_kernel(ZeroRanges z) {
+    pdl_wait();
+    pdl_trigger();
+    zero_ranges(z);
 }
-__global__ void __launch_bounds__(512) router_small_kernel(
-    const __nv_bfloat16 *__restrict__ x, const float *__restrict__ Wr,
-    const float *__restrict__ bias, int T, int d, int E, float *__restrict__ logits, ZeroRanges zr) {
-    zero_ranges(zr);
-    extern __shared__ __align__(16) uint8_t rs_smem[];
+
+// Small T: group sums G[t][g][e].  Block: 32 experts (lanes) x the 16 chunks of group g
+// (warps); thread (e, c) loads its 64 weights once (one coalesced 128-byte load per element
+// across the warp) and runs one fmaf chain per token; the block then adds its 16 chunk
+// partials in order per (token, expert) from shared memory.  Tokens are staged 16 at a time
+// in shared memory as fp32 (all lanes of a warp read the same element: a broadcast).
+// grid = (ceil(E / 32), ceil(C / 16)); T <= 64.
+constexpr int kSmallMaxT = 64;
+constexpr int kSmallEG = 32, kSmallCG = 16, kSmallTG = 16;
+constexpr int kGroupChunks = 16;
+constexpr int kRouterSmallSmem = kSmallTG * kSmallCG * kChunk * 4 + kSmallTG * kSmallCG * kSmallEG * 4;
+__global__ void __launch_bounds__(kSmallEG * kSmallCG) router_small_kernel(
+    const __nv_bfloat16 *__restrict__ x, const float *__restrict__ Wt, int T, int d, int E,
+    float *__restrict__ G, ZeroRanges zr) {
+    extern __shared__ __align__(16) float xs[];        // [kSmallTG][kSmallCG][64], then ps
+    float *ps = xs + kSmallTG * kSmallCG * kChunk;      // [kSmallTG][kSmallCG][32]
     const int C = d / kChunk;
-    uint16_t *xs = reinterpret_cast<uint16_t *>(rs_smem);                                  // [TT][C][kXRow]
-    float *ps = reinterpret_cast<float *>(rs_smem + kSmallTT * C * kXRow * 2);             // [4][TT][kSmallMaxC + 4]
-    const int grp = threadIdx.x >> 7, c = threadIdx.x & 127;
-    const int e = blockIdx.x * kSmallExperts + grp;
+    const int ng = (C + kGroupChunks - 1) / kGroupChunks;
+    const int lane = threadIdx.x & 31, cl = threadIdx.x >> 5;
+    const int e = blockIdx.x * kSmallEG + lane;
+    const int c0 = blockIdx.y * kSmallCG;
+    const int c = c0 + cl;
     const bool active = e < E && c < C;
+    pdl_wait();
+    pdl_trigger();
+    zero_ranges(zr);
     float w[kChunk];
     if (active) {
-        const float4 *src = reinterpret_cast<const float4 *>(Wr + static_cast<int64_t>(e) * d + c * kChunk);
 #pragma unroll
-        for (int i = 0; i < kChunk / 4; ++i) {
-            const float4 f = __ldg(src + i);
-            w[4 * i] = f.x; w[4 * i + 1] = f.y; w[4 * i + 2] = f.z; w[4 * i + 3] = f.w;
-        }
+        for (int i = 0; i < kChunk; ++i) w[i] = __ldg(Wt + static_cast<int64_t>(c * kChunk + i) * E + e);
     }
-    for (int t0 = 0; t0 < T; t0 += kSmallTT) {
-        const int nt = min(kSmallTT, T - t0);
+    const int ncg = min(kSmallCG, C - c0);
+    const int per_tok = ncg * (kChunk / 8);            // uint4 per token
+    for (int t0 = 0; t0 < T; t0 += kSmallTG) {
+        const int nt = min(kSmallTG, T - t0);
         __syncthreads();
-        {
-            // loads in flight in groups of 8 before their stores (at most 16 per thread)
-            const int total = nt * C * (kChunk / 8);
-#pragma unroll
-            for (int g0 = 0; g0 < 16; g0 += 8) {
-                uint4 buf[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int i = threadIdx.x + (g0 + j) * 512;
-                    if (i < total) {
-                        const int t = i / (C * (kChunk / 8));
-                        const int r = i - t * (C * (kChunk / 8));
-                        buf[j] = __ldg(reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(t0 + t) * d + r * 8));
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int i = threadIdx.x + (g0 + j) * 512;
-                    if (i < total) {
-                        const int t = i / (C * (kChunk / 8));
-                        const int r = i - t * (C * (kChunk / 8));
-                        const int cc = r >> 3, q = r & 7;
-                        *reinterpret_cast<uint4 *>(xs + (t * C + cc) * kXRow + q * 8) = buf[j];
-                    }
-                }
-            }
+        for (int i = threadIdx.x; i < nt * per_tok; i += blockDim.x) {
+            const int t = i / per_tok, r = i - t * per_tok;
+            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(t0 + t) * d + c0 * kChunk) + r);
+            float4 *dst = reinterpret_cast<float4 *>(xs + (t * kSmallCG) * kChunk + r * 8);
+            dst[0] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                                 __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+            dst[1] = make_float4(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xFFFF0000u),
+                                 __uint_as_float(u.w << 16), __uint_as_float(u.w & 0xFFFF0000u));
         }
         __syncthreads();
         if (active) {
-            float p[kSmallTT];
+            for (int t = 0; t < nt; ++t) {
+                const float4 *xr = reinterpret_cast<const float4 *>(xs + (t * kSmallCG + cl) * kChunk);
+                float p = 0.0f;
 #pragma unroll
-            for (int t = 0; t < kSmallTT; ++t) p[t] = 0.0f;
-#pragma unroll
-            for (int q = 0; q < kChunk / 8; ++q) {
-#pragma unroll
-                for (int t = 0; t < kSmallTT; ++t) {
-                    const uint4 u = *reinterpret_cast<const uint4 *>(xs + (t * C + c) * kXRow + q * 8);
-                    const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        p[t] = fmaf(__uint_as_float(ww[j] << 16), w[q * 8 + 2 * j], p[t]);
-                        p[t] = fmaf(__uint_as_float(ww[j] & 0xFFFF0000u), w[q * 8 + 2 * j + 1], p[t]);
-                    }
+                for (int i4 = 0; i4 < kChunk / 4; ++i4) {
+                    const float4 v = xr[i4];
+                    p = fmaf(v.x, w[4 * i4], p);
+                    p = fmaf(v.y, w[4 * i4 + 1], p);
+                    p = fmaf(v.z, w[4 * i4 + 2], p);
+                    p = fmaf(v.w, w[4 * i4 + 3], p);
                 }
+                ps[(t * kSmallCG + cl) * kSmallEG + lane] = p;
             }
-#pragma unroll
-            for (int t = 0; t < kSmallTT; ++t) ps[(grp * kSmallTT + t) * (kSmallMaxC + 4) + c] = p[t];
         }
         __syncthreads();
-        if (e < E && c < nt) {
-            const float4 *pp = reinterpret_cast<const float4 *>(ps + (grp * kSmallTT + c) * (kSmallMaxC + 4));
-            float acc = 0.0f;
-            for (int c4 = 0; c4 < C / 4; ++c4) {
-                const float4 v = pp[c4];
-                acc = __fadd_rn(acc, v.x);
-                acc = __fadd_rn(acc, v.y);
-                acc = __fadd_rn(acc, v.z);
-                acc = __fadd_rn(acc, v.w);
-            }
-            for (int cc = (C / 4) * 4; cc < C; ++cc) acc = __fadd_rn(acc, ps[(grp * kSmallTT + c) * (kSmallMaxC + 4) + cc]);
-            logits[static_cast<int64_t>(t0 + c) * E + e] = __fadd_rn(acc, bias ? bias[e] : 0.0f);
+        // thread (t, e): the group sum of its 16 chunk partials, in order
+        const int tt = threadIdx.x >> 5;
+        if (tt < nt && e < E) {
+            float gs = 0.0f;
+            for (int q = 0; q < ncg; ++q) gs = __fadd_rn(gs, ps[(tt * kSmallCG + q) * kSmallEG + lane]);
+            G[(static_cast<int64_t>(t0 + tt) * ng + blockIdx.y) * E + e] = gs;
         }
     }
 }
@@ -142,7 +121,7 @@ __global__ void __launch_bounds__(512) router_small_kernel(
 // fp32 fmas, so every (t, e) chain is exactly the scalar canonical one.  Dynamic smem.
 constexpr int kRT = 128, kRE = 64, kHalf = 32;
 constexpr int kXsStride = kRT + 4, kWsStride = kRE + 4;
-constexpr int kRouterLogitsSmem = 2 * kHalf * (kXsStride + kWsStride) * 4;
+constexpr int kRouterLogitsSmem = 2 * kHalf * (kXsStride + kWsStride) * 4 + 128 * 64 * 4;
 
 __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
     uint64_t r;
@@ -159,12 +138,15 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
 }
 
 __global__ void __launch_bounds__(128) router_logits_kernel(
-    const __nv_bfloat16 *__restrict__ x, const float *__restrict__ Wr,
+    const __nv_bfloat16 *__restrict__ x, const float *__restrict__ Wt,
     const float *__restrict__ bias, int T, int d, int E, float *__restrict__ logits, ZeroRanges zr) {
+    pdl_wait();
+    pdl_trigger();
     zero_ranges(zr);
     extern __shared__ __align__(16) float rl_smem[];
     float *xs = rl_smem;                              // [2][kHalf][kXsStride]
     float *ws = rl_smem + 2 * kHalf * kXsStride;      // [2][kHalf][kWsStride]
+    float4 *gsum = reinterpret_cast<float4 *>(ws + 2 * kHalf * kWsStride) + threadIdx.x;   // [16][128] float4: this thread's group sums
     const int tid = threadIdx.x;
     const int ty = tid >> 3, tx = tid & 7;
     const int t_base = blockIdx.x * kRT, e_base = blockIdx.y * kRE;
@@ -174,6 +156,8 @@ __global__ void __launch_bounds__(128) router_logits_kernel(
     for (int a = 0; a < 8; ++a)
 #pragma unroll
         for (int b = 0; b < 8; ++b) acc[a][b] = 0.0f;
+#pragma unroll
+    for (int m = 0; m < 16; ++m) gsum[m * 128] = make_float4(0.f, 0.f, 0.f, 0.f);
     uint4 xr[4];
     float4 wr[4];
     auto load = [&](int h) {
@@ -183,9 +167,9 @@ __global__ void __launch_bounds__(128) router_logits_kernel(
             const int t = i >> 2, q = i & 3;
             xr[j] = t_base + t < T ? __ldg(reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(t_base + t) * d + h * kHalf + q * 8))
                                    : make_uint4(0, 0, 0, 0);
-            const int e = i >> 3, qw = i & 7;       // W: 64 experts x 8 float4
-            wr[j] = e_base + e < E ? __ldg(reinterpret_cast<const float4 *>(Wr + static_cast<int64_t>(e_base + e) * d + h * kHalf + qw * 4))
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int r = i >> 4, qe = i & 15;      // Wt: 32 rows x 16 float4 of 4 experts
+            wr[j] = e_base + qe * 4 < E ? __ldg(reinterpret_cast<const float4 *>(Wt + static_cast<int64_t>(h * kHalf + r) * E + e_base + qe * 4))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     };
     auto store = [&](int buf) {
@@ -201,11 +185,8 @@ __global__ void __launch_bounds__(128) router_logits_kernel(
                 X[(q * 8 + 2 * m) * kXsStride + t] = __uint_as_float(ww[m] << 16);
                 X[(q * 8 + 2 * m + 1) * kXsStride + t] = __uint_as_float(ww[m] & 0xFFFF0000u);
             }
-            const int e = i >> 3, qw = i & 7;
-            W[(qw * 4) * kWsStride + e] = wr[j].x;
-            W[(qw * 4 + 1) * kWsStride + e] = wr[j].y;
-            W[(qw * 4 + 2) * kWsStride + e] = wr[j].z;
-            W[(qw * 4 + 3) * kWsStride + e] = wr[j].w;
+            const int r = i >> 4, qe = i & 15;
+            *reinterpret_cast<float4 *>(W + r * kWsStride + qe * 4) = wr[j];
         }
     };
     const int H = d / kHalf;
@@ -239,15 +220,28 @@ __global__ void __launch_bounds__(128) router_logits_kernel(
             }
         }
         if (h & 1) {
+            // chunk done: add it to the group sum; at a group's end add that to acc
+            const int chunk = h >> 1;
+            const bool group_end = ((chunk + 1) % kGroupChunks == 0) || (h + 1 == H);
 #pragma unroll
-            for (int a = 0; a < 8; ++a)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float lo, hi;
-                    unpack2(p[a][q], lo, hi);
-                    acc[a][2 * q] = __fadd_rn(acc[a][2 * q], lo);
-                    acc[a][2 * q + 1] = __fadd_rn(acc[a][2 * q + 1], hi);
+            for (int a = 0; a < 8; ++a) {
+                float4 g0 = gsum[(2 * a) * 128], g1 = gsum[(2 * a + 1) * 128];
+                float lo, hi;
+                unpack2(p[a][0], lo, hi); g0.x = __fadd_rn(g0.x, lo); g0.y = __fadd_rn(g0.y, hi);
+                unpack2(p[a][1], lo, hi); g0.z = __fadd_rn(g0.z, lo); g0.w = __fadd_rn(g0.w, hi);
+                unpack2(p[a][2], lo, hi); g1.x = __fadd_rn(g1.x, lo); g1.y = __fadd_rn(g1.y, hi);
+                unpack2(p[a][3], lo, hi); g1.z = __fadd_rn(g1.z, lo); g1.w = __fadd_rn(g1.w, hi);
+                if (group_end) {
+                    acc[a][0] = __fadd_rn(acc[a][0], g0.x); acc[a][1] = __fadd_rn(acc[a][1], g0.y);
+                    acc[a][2] = __fadd_rn(acc[a][2], g0.z); acc[a][3] = __fadd_rn(acc[a][3], g0.w);
+                    acc[a][4] = __fadd_rn(acc[a][4], g1.x); acc[a][5] = __fadd_rn(acc[a][5], g1.y);
+                    acc[a][6] = __fadd_rn(acc[a][6], g1.z); acc[a][7] = __fadd_rn(acc[a][7], g1.w);
+                    g0 = make_float4(0.f, 0.f, 0.f, 0.f);
+                    g1 = g0;
                 }
+                gsum[(2 * a) * 128] = g0;
+                gsum[(2 * a + 1) * 128] = g1;
+            }
         }
         if (h + 1 < H) store(buf ^ 1);
         __syncthreads();
@@ -266,23 +260,56 @@ __global__ void __launch_bounds__(128) router_logits_kernel(
 
 // One block of 128 threads per token: select the top-k from logits[T][E] (each thread holds
 // E/128 logits; every round is a block-wide argmax by (logit desc, index asc)), softmax over
-// the selected logits, write idx / w in ascending expert id, count tokens per expert.
-constexpr int kTopkThreads = 128;
-constexpr int kMaxEPerThread = 8;   // E <= 1024
+// the selected logits, write idx / w in ascending expert id, count tokens per expert and
+// record each slot's offset inside its expert's segment.
+constexpr int kTopkThreads = 256;
+constexpr int kMaxEPerThread = 4;   // E <= 1024
+// src: logits[T][E] (C == 0) or group sums G[T][C][E] (C > 0 groups: summed here in
+// ascending group order, then the bias).
 __global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(
-    const float *__restrict__ logits, int T, int E, int k, int32_t *__restrict__ idx_out,
-    float *__restrict__ w_out, int32_t *__restrict__ counts) {
+    const float *__restrict__ src, int C, const float *__restrict__ bias, int T, int E, int k,
+    int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts,
+    int32_t *__restrict__ slot_off) {
     __shared__ float cand_v[2][kTopkThreads / 32];
     __shared__ int cand_i[2][kTopkThreads / 32];
     __shared__ float sel_v[32];
     __shared__ int sel_i[32];
     const int t = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_wait();
+    pdl_trigger();
     float v[kMaxEPerThread];
+    if (C == 0) {
 #pragma unroll
-    for (int j = 0; j < kMaxEPerThread; ++j) {
-        const int e = tid + kTopkThreads * j;
-        v[j] = e < E ? __ldg(logits + static_cast<int64_t>(t) * E + e) : -INFINITY;
+        for (int j = 0; j < kMaxEPerThread; ++j) {
+            const int e = tid + kTopkThreads * j;
+            v[j] = e < E ? __ldg(src + static_cast<int64_t>(t) * E + e) : -INFINITY;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < kMaxEPerThread; ++j) v[j] = 0.0f;
+        const float *pt = src + static_cast<int64_t>(t) * C * E;
+        constexpr int U = 8;                 // chunks loaded ahead of their (in-order) adds
+        for (int c0 = 0; c0 < C; c0 += U) {
+            float buf[U][kMaxEPerThread];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int j = 0; j < kMaxEPerThread; ++j) {
+                    const int e = tid + kTopkThreads * j;
+                    buf[u][j] = (c0 + u < C && e < E) ? __ldg(pt + static_cast<int64_t>(c0 + u) * E + e) : 0.0f;
+                }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int j = 0; j < kMaxEPerThread; ++j)
+                    if (c0 + u < C) v[j] = __fadd_rn(v[j], buf[u][j]);
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxEPerThread; ++j) {
+            const int e = tid + kTopkThreads * j;
+            v[j] = e < E ? __fadd_rn(v[j], bias ? bias[e] : 0.0f) : -INFINITY;
+        }
     }
     uint32_t taken = 0u;
     for (int r = 0; r < k; ++r) {
@@ -328,7 +355,11 @@ __global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(
     if (lane < k) {
         idx_out[static_cast<int64_t>(t) * k + rank] = my_idx;
         w_out[static_cast<int64_t>(t) * k + rank] = __fdiv_rn(ex, ssum);
-        if (counts) atomicAdd(counts + my_idx, 1);
+        if (counts) {
+            // the histogram's old value is this slot's row inside its expert's segment
+            const int off = atomicAdd(counts + my_idx, 1);
+            if (slot_off) slot_off[static_cast<int64_t>(t) * k + rank] = off;
+        }
     }
 }
 
