@@ -258,91 +258,130 @@ __global__ void __launch_bounds__(128) router_logits_kernel(
     }
 }
 
-// One block of 128 threads per token: select the top-k from logits[T][E] (each thread holds
-// E/128 logits; every round is a block-wide argmax by (logit desc, index asc)), softmax over
-// the selected logits, write idx / w in ascending expert id, count tokens per expert and
-// record each slot's offset inside its expert's segment.
+// Top-k by sorting.  A selection key packs (logit, expert) into 64 bits so that a larger key
+// means a higher logit, then a lower expert index (-0 is folded onto +0 first): the k largest
+// keys are exactly the top-k under (logit desc, index asc), and all keys are distinct.
+__device__ __forceinline__ uint64_t topk_key(float v, int e) {
+    if (v == 0.0f) v = 0.0f;
+    uint32_t u = __float_as_uint(v);
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);        // order-preserving on floats
+    return (static_cast<uint64_t>(u) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(e));
+}
+__device__ __forceinline__ float key_value(uint64_t k) {
+    uint32_t u = static_cast<uint32_t>(k >> 32);
+    u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+    return __uint_as_float(u);
+}
+__device__ __forceinline__ int key_index(uint64_t k) {
+    return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k));
+}
+__device__ __forceinline__ uint64_t shfl_xor64(uint64_t v, int m) {
+    const uint32_t lo = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(v), m);
+    const uint32_t hi = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(v >> 32), m);
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// Descending bitonic sort of the warp's 128 keys, 4 per lane; key r of lane L sits at position
+// 4L + r.
+__device__ __forceinline__ void warp_sort128_desc(uint64_t (&a)[4], int lane) {
+#pragma unroll
+    for (int k = 2; k <= 128; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j >= 1; j >>= 1) {
+            if (j >= 4) {
+                const int m = j >> 2;                      // partner lane distance
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int i = 4 * lane + r;
+                    const uint64_t o = shfl_xor64(a[r], m);
+                    const bool lower = (i & j) == 0;       // i < partner
+                    const bool desc = (i & k) == 0;        // this run sorts descending
+                    const bool keep_max = (lower == desc);
+                    a[r] = keep_max ? (a[r] > o ? a[r] : o) : (a[r] < o ? a[r] : o);
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int pr = r ^ j;
+                    if (pr > r) {
+                        const int i = 4 * lane + r;
+                        const bool desc = (i & k) == 0;
+                        const uint64_t x = a[r], y = a[pr];
+                        const bool swap = desc ? (x < y) : (x > y);
+                        a[r] = swap ? y : x;
+                        a[pr] = swap ? x : y;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Two descending 32-lists (lane i holds element i of each): the top 32 of their union,
+// descending, lane i holding element i.
+__device__ __forceinline__ uint64_t merge_top32(uint64_t a_i, uint64_t b_rev_i, int lane) {
+    uint64_t c = a_i > b_rev_i ? a_i : b_rev_i;             // bitonic, holds the top 32
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+        const uint64_t o = shfl_xor64(c, m);
+        const bool lower = (lane & m) == 0;
+        c = lower ? (c > o ? c : o) : (c < o ? c : o);
+    }
+    return c;
+}
+
+// One block of 256 threads (8 warps) per token: each warp sorts 128 selection keys (E <= 1024),
+// the per-warp top-32 lists are merged pairwise (8 -> 4 -> 2 -> 1) through shared memory,
+// then warp 0 holds the top-k: softmax over their logits, write idx / w in ascending expert
+// id, count tokens per expert and record each slot's offset inside its expert's segment.
 constexpr int kTopkThreads = 256;
-constexpr int kMaxEPerThread = 4;   // E <= 1024
 // src: logits[T][E] (C == 0) or group sums G[T][C][E] (C > 0 groups: summed here in
 // ascending group order, then the bias).
 __global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(
     const float *__restrict__ src, int C, const float *__restrict__ bias, int T, int E, int k,
     int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts,
     int32_t *__restrict__ slot_off) {
-    __shared__ float cand_v[2][kTopkThreads / 32];
-    __shared__ int cand_i[2][kTopkThreads / 32];
-    __shared__ float sel_v[32];
-    __shared__ int sel_i[32];
+    __shared__ uint64_t lists[8][32];
     const int t = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_wait();
     pdl_trigger();
-    float v[kMaxEPerThread];
-    if (C == 0) {
+    uint64_t key[4];
 #pragma unroll
-        for (int j = 0; j < kMaxEPerThread; ++j) {
-            const int e = tid + kTopkThreads * j;
-            v[j] = e < E ? __ldg(src + static_cast<int64_t>(t) * E + e) : -INFINITY;
+    for (int r = 0; r < 4; ++r) {
+        const int e = warp * 128 + 4 * lane + r;
+        float v = 0.0f;
+        if (e < E) {
+            if (C == 0) {
+                v = __ldg(src + static_cast<int64_t>(t) * E + e);
+            } else {
+                const float *pt = src + static_cast<int64_t>(t) * C * E + e;
+                float acc = 0.0f;
+                for (int g = 0; g < C; ++g) acc = __fadd_rn(acc, __ldg(pt + static_cast<int64_t>(g) * E));
+                v = __fadd_rn(acc, bias ? bias[e] : 0.0f);
+            }
         }
-    } else {
-#pragma unroll
-        for (int j = 0; j < kMaxEPerThread; ++j) v[j] = 0.0f;
-        const float *pt = src + static_cast<int64_t>(t) * C * E;
-        constexpr int U = 8;                 // chunks loaded ahead of their (in-order) adds
-        for (int c0 = 0; c0 < C; c0 += U) {
-            float buf[U][kMaxEPerThread];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-#pragma unroll
-                for (int j = 0; j < kMaxEPerThread; ++j) {
-                    const int e = tid + kTopkThreads * j;
-                    buf[u][j] = (c0 + u < C && e < E) ? __ldg(pt + static_cast<int64_t>(c0 + u) * E + e) : 0.0f;
-                }
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-#pragma unroll
-                for (int j = 0; j < kMaxEPerThread; ++j)
-                    if (c0 + u < C) v[j] = __fadd_rn(v[j], buf[u][j]);
-        }
-#pragma unroll
-        for (int j = 0; j < kMaxEPerThread; ++j) {
-            const int e = tid + kTopkThreads * j;
-            v[j] = e < E ? __fadd_rn(v[j], bias ? bias[e] : 0.0f) : -INFINITY;
-        }
+        key[r] = e < E ? topk_key(v, e) : 0ull;             // padding sorts last
     }
-    uint32_t taken = 0u;
-    for (int r = 0; r < k; ++r) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
+    warp_sort128_desc(key, lane);
+    // positions 0..31 (lanes 0..7) -> list of this warp
+    if (lane < 8) {
 #pragma unroll
-        for (int j = 0; j < kMaxEPerThread; ++j) {
-            const int e = tid + kTopkThreads * j;
-            if (e < E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < bi))) { bv = v[j]; bi = e; }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-        }
-        if (lane == 0) { cand_v[r & 1][warp] = bv; cand_i[r & 1][warp] = bi; }
-        __syncthreads();
-        bv = cand_v[r & 1][0];
-        bi = cand_i[r & 1][0];
-#pragma unroll
-        for (int q = 1; q < kTopkThreads / 32; ++q) {
-            const float ov = cand_v[r & 1][q];
-            const int oi = cand_i[r & 1][q];
-            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-        }
-        if (bi % kTopkThreads == tid) taken |= 1u << (bi / kTopkThreads);
-        if (tid == 0) { sel_v[r] = bv; sel_i[r] = bi; }
+        for (int r = 0; r < 4; ++r) lists[warp][4 * lane + r] = key[r];
     }
     __syncthreads();
+#pragma unroll
+    for (int n = 8; n > 1; n >>= 1) {
+        uint64_t res = 0;
+        if (warp < n / 2) res = merge_top32(lists[2 * warp][lane], lists[2 * warp + 1][31 - lane], lane);
+        __syncthreads();
+        if (warp < n / 2) lists[warp][lane] = res;
+        __syncthreads();
+    }
     if (warp != 0) return;
-    const int my_idx = lane < k ? sel_i[lane] : 0x7fffffff;
-    const float my_val = lane < k ? sel_v[lane] : -INFINITY;
+    const uint64_t best = lists[0][lane];
+    const int my_idx = lane < k ? key_index(best) : 0x7fffffff;
+    const float my_val = lane < k ? key_value(best) : -INFINITY;
     int rank = 0;
     for (int r = 0; r < k; ++r) rank += (__shfl_sync(0xffffffffu, my_idx, r) < my_idx) ? 1 : 0;
     float m = my_val;
