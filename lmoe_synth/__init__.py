@@ -13,6 +13,8 @@ config seed and a fixed tag, so any one expert can be regenerated alone):
                             permutation (so expert popularity follows a Zipf(s) law)
   w1[e]     [ffn][l]        ~ N(0, 1/l)          rounded to bf16    (u = zq w1_e^T)
   w2[e]     [l][ffn]        ~ N(0, 1/ffn)        rounded to bf16    (o = hq w2_e^T)
+  ws1       [shared_ffn][d] ~ N(0, 1/d)          rounded to bf16    (shared expert, optional)
+  ws2       [d][shared_ffn] ~ N(0, 1/shared_ffn) rounded to bf16
   x_cal     [T_cal][d]      ~ N(0, 1) bf16, seed + 1: the calibration batch
 """
 from __future__ import annotations
@@ -30,13 +32,16 @@ class Dims:
     E: int
     k: int
     ffn: int
+    shared_ffn: int = 0      # 0: no shared expert
 
 
 TINY = Dims(d=256, l=64, E=16, k=4, ffn=128)
 ULTRA = Dims(d=8192, l=2048, E=512, k=22, ffn=2048)
+TINY_SHARED = Dims(d=256, l=64, E=16, k=4, ffn=128, shared_ffn=320)
+ULTRA_SHARED = Dims(d=8192, l=2048, E=512, k=22, ffn=2048, shared_ffn=8192)
 
 _TAG = {"x": 1, "w_down": 2, "w_up": 3, "w_router": 4, "perm": 5, "w1": 1000, "w2": 2000000,
-        "x_cal": 7}
+        "x_cal": 7, "ws1": 8, "ws2": 9}
 
 
 def _gen(device, seed: int, tag: int) -> torch.Generator:
@@ -101,6 +106,17 @@ def experts(dims: Dims, seed: int, device="cpu"):
     return w1, w2
 
 
+def shared_expert(dims: Dims, seed: int, device="cpu"):
+    """(ws1 [shared_ffn][d], ws2 [d][shared_ffn]) bf16, or (None, None) without one."""
+    if not dims.shared_ffn:
+        return None, None
+    ws1 = _normal((dims.shared_ffn, dims.d), 1.0 / math.sqrt(dims.d), device, seed, _TAG["ws1"],
+                  torch.bfloat16)
+    ws2 = _normal((dims.d, dims.shared_ffn), 1.0 / math.sqrt(dims.shared_ffn), device, seed,
+                  _TAG["ws2"], torch.bfloat16)
+    return ws1, ws2
+
+
 @dataclasses.dataclass
 class Layer:
     """All inputs of one layer instance (tensors on `device`)."""
@@ -113,13 +129,16 @@ class Layer:
     b_router: torch.Tensor
     w1: torch.Tensor
     w2: torch.Tensor
+    ws1: torch.Tensor = None
+    ws2: torch.Tensor = None
 
 
 def layer(dims: Dims, seed: int, device="cpu", zipf_s: float = 0.0) -> Layer:
     wd, wu = projections(dims, seed, device)
     wr, b = router(dims, seed, device, zipf_s)
     w1, w2 = experts(dims, seed, device)
-    return Layer(dims, seed, zipf_s, wd, wu, wr, b, w1, w2)
+    ws1, ws2 = shared_expert(dims, seed, device)
+    return Layer(dims, seed, zipf_s, wd, wu, wr, b, w1, w2, ws1, ws2)
 
 
 def calibration_tokens(T: int, d: int, seed: int, device="cpu") -> torch.Tensor:
@@ -134,4 +153,8 @@ CONFIGS = {
     "ultra_decode_T8": dict(dims=ULTRA, seed=1, zipf=0.0, T=8, calib_T=8, gen="cuda"),
     "ultra_prefill_T4096_zipf1.1": dict(dims=ULTRA, seed=1, zipf=1.1, T=4096, calib_T=8,
                                         gen="cuda"),
+    # with the FP8 shared expert at width d
+    "tiny_shared": dict(dims=TINY_SHARED, seed=0, zipf=0.0, T=64, calib_T=64, gen="cpu"),
+    "ultra_long_T32768_shared": dict(dims=ULTRA_SHARED, seed=1, zipf=0.0, T=32768, calib_T=8,
+                                     gen="cuda"),
 }

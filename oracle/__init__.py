@@ -46,13 +46,18 @@ class _Layer(C.Structure):
         ("w2_codes", C.c_void_p), ("w2_sf", C.c_void_p), ("w2_sdec", C.c_void_p),
         ("w1", C.c_void_p), ("w2", C.c_void_p),
         ("amax_z", C.c_float), ("amax_h", C.c_float),
+        ("shared_ffn", C.c_int),
+        ("ws1_codes", C.c_void_p), ("ws1_sdec", C.c_float),
+        ("ws2_codes", C.c_void_p), ("ws2_sdec", C.c_float),
+        ("ws1", C.c_void_p), ("ws2", C.c_void_p),
+        ("amax_xs", C.c_float), ("amax_hs", C.c_float),
     ]
 
 
 class _Out(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in (
         "z", "zq_codes", "zq_sf", "logits", "idx", "w", "counts", "h", "hq_codes", "hq_sf",
-        "c64", "c", "y64", "y")]
+        "c64", "c", "y64", "y", "xs_q", "hs", "hs_q", "s")]
 
 
 def lib():
@@ -79,6 +84,19 @@ def lib():
                                                 C.c_void_p, C.c_void_p, C.c_void_p, C.c_int]
             L.oracle_nvfp4_dot.restype = C.c_double
             L.oracle_nvfp4_dot.argtypes = [C.c_void_p] * 4 + [C.c_int64]
+            L.oracle_quantize_fp8.restype = None
+            L.oracle_quantize_fp8.argtypes = [C.c_void_p, C.c_int64, C.c_float, C.c_void_p,
+                                              C.c_void_p, C.c_int]
+            L.oracle_fp8_dot.restype = C.c_double
+            L.oracle_fp8_dot.argtypes = [C.c_void_p, C.c_void_p, C.c_int64]
+            L.oracle_shared_forward.restype = C.c_int
+            L.oracle_shared_forward.argtypes = [C.POINTER(_Layer), C.c_void_p, C.c_int64, C.c_int,
+                                                C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                                C.c_int]
+            L.oracle_calibrate_shared.restype = C.c_int
+            L.oracle_calibrate_shared.argtypes = [C.POINTER(_Layer), C.c_void_p, C.c_int64,
+                                                  C.POINTER(C.c_float), C.POINTER(C.c_float),
+                                                  C.c_int]
             L.oracle_router.restype = None
             L.oracle_router.argtypes = [C.c_void_p, C.c_int64, C.c_int, C.c_void_p, C.c_void_p,
                                         C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p,
@@ -151,6 +169,24 @@ def nvfp4_dot(qa, sfa, qb, sfb) -> float:
 
 
 # --------------------------------------------------------------------------------------
+# FP8 E4M3, one per-tensor scale
+# --------------------------------------------------------------------------------------
+def quantize_fp8(x, amax: float = -1.0, nthreads: int = 0):
+    """x: any shape -> (codes uint8 of that shape, s_dec float)."""
+    x = _f32(x)
+    codes = np.empty(x.shape, np.uint8)
+    sdec = np.zeros(1, np.float32)
+    lib().oracle_quantize_fp8(_p(x), x.size, float(amax), _p(codes), _p(sdec), nthreads)
+    return codes, float(sdec[0])
+
+
+def fp8_dot(a, b) -> float:
+    a, b = (np.ascontiguousarray(v, np.uint8) for v in (a, b))
+    assert a.size == b.size
+    return lib().oracle_fp8_dot(_p(a), _p(b), a.size)
+
+
+# --------------------------------------------------------------------------------------
 # router
 # --------------------------------------------------------------------------------------
 def router(x, w_router, b_router, k: int, nthreads: int = 0):
@@ -182,7 +218,7 @@ class OracleLayer:
     """
 
     def __init__(self, d, l, E, k, ffn, w_down, w_up, w_router, b_router, expert_fn,
-                 amax_z=0.0, amax_h=0.0, nthreads=0):
+                 amax_z=0.0, amax_h=0.0, nthreads=0, shared=None, amax_xs=0.0, amax_hs=0.0):
         self.d, self.l, self.E, self.k, self.ffn = d, l, E, k, ffn
         self.w_down = _f32(w_down)
         self.w_up = _f32(w_up)
@@ -191,6 +227,11 @@ class OracleLayer:
         self.expert_fn = expert_fn
         self.amax_z, self.amax_h = float(amax_z), float(amax_h)
         self.nthreads = nthreads
+        # optional shared expert: (ws1 [shared_ffn][d], ws2 [d][shared_ffn]) bf16 values
+        self.shared = None if shared is None else (_f32(shared[0]), _f32(shared[1]))
+        self.shared_ffn = 0 if shared is None else self.shared[0].shape[0]
+        self.amax_xs, self.amax_hs = float(amax_xs), float(amax_hs)
+        self._sq = None    # (ws1 codes, ws1 s_dec, ws2 codes, ws2 s_dec)
         self._q = {}       # e -> (c1, s1, d1, c2, s2, d2)
         self._m = {}       # e -> (w1, w2) float32 masters
         self._arrays = {}
@@ -210,6 +251,14 @@ class OracleLayer:
             c2, s2, d2 = quantize_nvfp4(w2, -1.0, self.nthreads)
             self._q[e] = (c1, s1, d1, c2, s2, d2)
         return self._q[e]
+
+    def quantized_shared(self):
+        """Oracle-quantized shared expert: (ws1 codes, ws1 s_dec, ws2 codes, ws2 s_dec)."""
+        if self._sq is None and self.shared is not None:
+            c1, d1 = quantize_fp8(self.shared[0], -1.0, self.nthreads)
+            c2, d2 = quantize_fp8(self.shared[1], -1.0, self.nthreads)
+            self._sq = (c1, d1, c2, d2)
+        return self._sq
 
     def route(self, x):
         return router(x, self.w_router, self.b_router, self.k, self.nthreads)
@@ -231,12 +280,19 @@ class OracleLayer:
                 w1, w2 = self.master(e)
                 m1[e], m2[e] = _p(w1), _p(w2)
                 keep.append((w1, w2))
+        sq = self.quantized_shared() if (quant and self.shared is not None) else None
+        sm = self.shared if (not quant and self.shared is not None) else None
         st = _Layer(self.d, self.l, self.E, self.k, self.ffn,
                     _p(self.w_down), _p(self.w_up), _p(self.w_router), _p(self.b_router),
                     C.cast(c1, C.c_void_p), C.cast(s1, C.c_void_p), _p(d1),
                     C.cast(c2, C.c_void_p), C.cast(s2, C.c_void_p), _p(d2),
                     C.cast(m1, C.c_void_p), C.cast(m2, C.c_void_p),
-                    self.amax_z, self.amax_h)
+                    self.amax_z, self.amax_h, self.shared_ffn,
+                    _p(sq[0]) if sq else None, sq[1] if sq else 1.0,
+                    _p(sq[2]) if sq else None, sq[3] if sq else 1.0,
+                    _p(sm[0]) if sm else None, _p(sm[1]) if sm else None,
+                    self.amax_xs, self.amax_hs)
+        keep += [sq, sm]
         keep += [c1, s1, c2, s2, m1, m2, d1, d2]
         return st, keep
 
@@ -244,7 +300,8 @@ class OracleLayer:
         """Run the layer on the token rows x [T][d]; returns a dict of requested outputs.
 
         Available: z, zq_codes, zq_sf, logits, idx, w, counts, h, hq_codes, hq_sf, c64, c,
-        y64, y.  idx / w / counts are always returned."""
+        y64, y, and with a shared expert xs_q, hs, hs_q, s.  idx / w / counts are always
+        returned."""
         x = _f32(x)
         T = x.shape[0]
         d, l, E, k, F = self.d, self.l, self.E, self.k, self.ffn
@@ -257,6 +314,8 @@ class OracleLayer:
             "h": ((T, k, F), np.float32), "hq_codes": ((T, k, F // 2), np.uint8),
             "hq_sf": ((T, k, F // 16), np.uint8), "c64": ((T, l), np.float64),
             "c": ((T, l), np.float32), "y64": ((T, d), np.float64), "y": ((T, d), np.float32),
+            "xs_q": ((T, d), np.uint8), "hs": ((T, max(self.shared_ffn, 1)), np.float32),
+            "hs_q": ((T, max(self.shared_ffn, 1)), np.uint8), "s": ((T, d), np.float32),
         }
         names = set(want) | {"idx", "w", "counts"}
         res = {n: np.zeros(*shapes[n]) for n in names}
@@ -268,6 +327,35 @@ class OracleLayer:
             raise RuntimeError("oracle_layer_forward: missing expert weights")
         del keep
         return res
+
+    def shared_forward(self, x, quant=True):
+        """The shared expert alone on x [T][d]: dict xs_q, hs, hs_q, s (codes only if quant)."""
+        assert self.shared is not None
+        x = _f32(x)
+        T, F = x.shape[0], self.shared_ffn
+        res = {"xs_q": np.zeros((T, self.d), np.uint8), "hs": np.zeros((T, F), np.float32),
+               "hs_q": np.zeros((T, F), np.uint8), "s": np.zeros((T, self.d), np.float32)}
+        st, keep = self._struct([], quant)
+        rc = lib().oracle_shared_forward(C.byref(st), _p(x), T, 1 if quant else 0,
+                                         _p(res["xs_q"]), _p(res["hs"]), _p(res["hs_q"]),
+                                         _p(res["s"]), self.nthreads)
+        if rc != 0:
+            raise RuntimeError("oracle_shared_forward: no shared expert weights")
+        del keep
+        return res
+
+    def calibrate_shared(self, x_cal):
+        """Static amax of the shared expert's x and h; stores and returns them."""
+        x = _f32(x_cal)
+        st, keep = self._struct([], True)
+        ax, ah = C.c_float(0), C.c_float(0)
+        rc = lib().oracle_calibrate_shared(C.byref(st), _p(x), x.shape[0], C.byref(ax),
+                                           C.byref(ah), self.nthreads)
+        if rc != 0:
+            raise RuntimeError("oracle_calibrate_shared: no shared expert weights")
+        del keep
+        self.amax_xs, self.amax_hs = float(ax.value), float(ah.value)
+        return self.amax_xs, self.amax_hs
 
     def calibrate(self, x_cal):
         """Static activation amax (z, h) from a calibration batch; stores and returns them."""

@@ -123,9 +123,13 @@ double oracle_round_bf16(double v) {
 /* decode tables filled from the closed forms above */
 static double g_e4m3[256];
 static int g_e2m1x2[16];           /* 2 * value: an integer in {0, 1, 2, 3, 4, 6, 8, 12} */
+static int64_t g_e4m3x512[256];    /* 512 * value: an integer (E4M3 values are multiples of 2^-9) */
 static pthread_once_t g_once = PTHREAD_ONCE_INIT;
 static void init_tables(void) {
-    for (int c = 0; c < 256; ++c) g_e4m3[c] = oracle_e4m3_value((uint8_t)c);
+    for (int c = 0; c < 256; ++c) {
+        g_e4m3[c] = oracle_e4m3_value((uint8_t)c);
+        g_e4m3x512[c] = isnan(g_e4m3[c]) ? 0 : (int64_t)(g_e4m3[c] * 512.0);
+    }
     for (int c = 0; c < 16; ++c) g_e2m1x2[c] = (int)(2.0 * oracle_e2m1_value((uint8_t)c));
 }
 
@@ -214,6 +218,46 @@ double oracle_nvfp4_dot(const uint8_t *qa, const uint8_t *sfa,
 }
 
 /* ------------------------------------------------------------------------------------ */
+/* FP8 E4M3 with one per-tensor scale ([NEWS] quantization paragraph: the shared expert is */
+/* FP8).  The scale arithmetic is this project's reading, in IEEE fp32: s_enc = 448/amax,  */
+/* s_dec = amax/448, code = e4m3_satfinite(x * s_enc); amax == 0 -> codes 0, s_dec = 1.    */
+/* ------------------------------------------------------------------------------------ */
+typedef struct { const float *src; float s_enc; uint8_t *codes; } fp8_job;
+static void fp8_rows(int64_t b, int64_t e, void *arg) {
+    fp8_job *j = (fp8_job *)arg;
+    for (int64_t i = b; i < e; ++i) j->codes[i] = oracle_f32_to_e4m3(j->src[i] * j->s_enc);
+}
+
+void oracle_quantize_fp8(const float *src, int64_t n, float amax, uint8_t *codes,
+                         float *s_dec_out, int nthreads) {
+    pthread_once(&g_once, init_tables);
+    if (amax < 0.0f) {
+        amax = 0.0f;
+        for (int64_t i = 0; i < n; ++i) {
+            float a = fabsf(src[i]);
+            if (a > amax) amax = a;
+        }
+    }
+    if (amax == 0.0f) {
+        memset(codes, 0, (size_t)n);
+        if (s_dec_out) *s_dec_out = 1.0f;
+        return;
+    }
+    fp8_job j = {src, 448.0f / amax, codes};
+    parallel_for(n, nthreads, fp8_rows, &j);
+    if (s_dec_out) *s_dec_out = amax / 448.0f;
+}
+
+/* Exact E4M3 dot: with every value scaled by 512 the products are integers below 2^36, so */
+/* an int64 sum is exact; the result counts units of 2^-18.                                */
+double oracle_fp8_dot(const uint8_t *a, const uint8_t *b, int64_t K) {
+    pthread_once(&g_once, init_tables);
+    int64_t acc = 0;
+    for (int64_t i = 0; i < K; ++i) acc += g_e4m3x512[a[i]] * g_e4m3x512[b[i]];
+    return ldexp((double)acc, -18);
+}
+
+/* ------------------------------------------------------------------------------------ */
 /* Router.  [NEWS] architecture paragraph: each MoE layer has 512 experts and activates   */
 /* the top 22 per token; [BLOG] 2.2 keeps the routing gate at width d.  The logit order   */
 /* is this project's canonical fp32 order (the pages are silent): the d axis is cut into */
@@ -295,6 +339,115 @@ void oracle_router(const float *x, int64_t T, int d, const float *Wr, const floa
 }
 
 /* ------------------------------------------------------------------------------------ */
+/* The shared expert of one token: it runs at the full width d ([BLOG] 2.2, closing       */
+/* remark: the shared expert is not moved into the latent space) in FP8 ([NEWS]            */
+/* quantization paragraph), with the routed experts' squared ReLU (the pages name no other */
+/* activation for it):                                                                    */
+/*   xq = q8(x; amax_xs)                                                                  */
+/*   h  = bf16( max(s_x s_w1 (xq . Ws1q_f), 0)^2 )       (exact E4M3 dots, fp64 scaling)  */
+/*   hq = q8(h; amax_hs)                                                                  */
+/*   s  = bf16( s_h s_w2 (hq . Ws2q_j) )                                                  */
+/* Unquantized mode: the same steps in fp64 on the masters with no quantization and no    */
+/* rounding.  s64 receives s; hmax (optional) the largest h.                              */
+/* ------------------------------------------------------------------------------------ */
+static void shared_token(const oracle_layer *L, const float *xt, int quant, float amax_xs,
+                         float amax_hs, uint8_t *xq, float *hf, uint8_t *hq, double *h64,
+                         double *s64, float *hmax) {
+    const int d = L->d, F = L->shared_ffn;
+    float mh = 0.0f;
+    if (quant) {
+        float sdx, sdh;
+        oracle_quantize_fp8(xt, d, amax_xs, xq, &sdx, 1);
+        double a1 = (double)sdx * (double)L->ws1_sdec;
+        for (int f = 0; f < F; ++f) {
+            double u = a1 * oracle_fp8_dot(xq, L->ws1_codes + (int64_t)f * d, d);
+            double r = u > 0.0 ? u : 0.0;
+            hf[f] = (float)oracle_round_bf16(r * r);
+            if (hf[f] > mh) mh = hf[f];
+        }
+        oracle_quantize_fp8(hf, F, amax_hs, hq, &sdh, 1);
+        double a2 = (double)sdh * (double)L->ws2_sdec;
+        for (int j = 0; j < d; ++j)
+            s64[j] = oracle_round_bf16(a2 * oracle_fp8_dot(hq, L->ws2_codes + (int64_t)j * F, F));
+    } else {
+        for (int f = 0; f < F; ++f) {
+            const float *wr = L->ws1 + (int64_t)f * d;
+            double u = 0.0;
+            for (int i = 0; i < d; ++i) u += (double)xt[i] * (double)wr[i];
+            double r = u > 0.0 ? u : 0.0;
+            h64[f] = r * r;
+            hf[f] = (float)h64[f];
+            if (hf[f] > mh) mh = hf[f];
+        }
+        for (int j = 0; j < d; ++j) {
+            const float *wr = L->ws2 + (int64_t)j * F;
+            double o = 0.0;
+            for (int f = 0; f < F; ++f) o += h64[f] * (double)wr[f];
+            s64[j] = o;
+        }
+    }
+    if (hmax) *hmax = mh;
+}
+
+static int shared_ready(const oracle_layer *L, int quant) {
+    return quant ? (L->ws1_codes && L->ws2_codes) : (L->ws1 && L->ws2);
+}
+
+typedef struct {
+    const oracle_layer *L; const float *x; int quant;
+    uint8_t *xs_q; float *hs; uint8_t *hs_q; float *s; float *hmax_seen; float amax_hs;
+} shared_job;
+
+static void shared_rows(int64_t tb, int64_t te, void *arg) {
+    shared_job *J = (shared_job *)arg;
+    const oracle_layer *L = J->L;
+    const int d = L->d, F = L->shared_ffn;
+    uint8_t *xq = (uint8_t *)malloc((size_t)d), *hq = (uint8_t *)malloc((size_t)F);
+    float *hf = (float *)malloc(sizeof(float) * F);
+    double *h64 = (double *)malloc(sizeof(double) * F), *s64 = (double *)malloc(sizeof(double) * d);
+    for (int64_t t = tb; t < te; ++t) {
+        float mh;
+        shared_token(L, J->x + t * d, J->quant, L->amax_xs, J->amax_hs, xq, hf, hq, h64, s64, &mh);
+        if (J->hmax_seen) J->hmax_seen[t] = mh;
+        if (J->xs_q) memcpy(J->xs_q + t * d, xq, (size_t)d);
+        if (J->hs) memcpy(J->hs + t * F, hf, sizeof(float) * F);
+        if (J->hs_q) memcpy(J->hs_q + t * F, hq, (size_t)F);
+        if (J->s) for (int j = 0; j < d; ++j) J->s[t * d + j] = (float)s64[j];
+    }
+    free(xq); free(hq); free(hf); free(h64); free(s64);
+}
+
+int oracle_shared_forward(const oracle_layer *L, const float *x, int64_t T, int quant,
+                          uint8_t *xs_q, float *hs, uint8_t *hs_q, float *s, int nthreads) {
+    pthread_once(&g_once, init_tables);
+    if (L->shared_ffn <= 0 || !shared_ready(L, quant)) return -1;
+    shared_job J = {L, x, quant, quant ? xs_q : NULL, hs, quant ? hs_q : NULL, s, NULL, L->amax_hs};
+    parallel_for(T, nthreads, shared_rows, &J);
+    return 0;
+}
+
+int oracle_calibrate_shared(const oracle_layer *L, const float *x, int64_t T,
+                            float *amax_xs, float *amax_hs, int nthreads) {
+    pthread_once(&g_once, init_tables);
+    if (L->shared_ffn <= 0 || !shared_ready(L, 1)) return -1;
+    float mx = 0.0f;
+    for (int64_t i = 0; i < T * L->d; ++i) {
+        float a = fabsf(x[i]);
+        if (a > mx) mx = a;
+    }
+    oracle_layer Lc = *L;
+    Lc.amax_xs = mx;
+    float *seen = (float *)calloc((size_t)(T > 0 ? T : 1), sizeof(float));
+    shared_job J = {&Lc, x, 1, NULL, NULL, NULL, NULL, seen, 1.0f};
+    parallel_for(T, nthreads, shared_rows, &J);
+    float mh = 0.0f;
+    for (int64_t t = 0; t < T; ++t) if (seen[t] > mh) mh = seen[t];
+    free(seen);
+    *amax_xs = mx; *amax_hs = mh;
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------------ */
 /* The layer ([BLOG] 2.2, steps 1-3; [SUPER] "潜在MoE"):                                  */
 /*   z  = bf16( x Wd^T )                      down-projection d -> l, BF16 ([BLOG] 3.1.3) */
 /*   zq = NVFP4(z) with the static amax_z                                                */
@@ -305,6 +458,7 @@ void oracle_router(const float *x, int64_t T, int d, const float *Wr, const floa
 /*                           o = s_h s_w2e (hq . W2q_e)                                   */
 /*   c  = bf16( sum_j w_j o_j )               routing-weighted combine in l space        */
 /*   y  = bf16( c Wu^T )                      up-projection l -> d, BF16                 */
+/*        (+ s, the shared expert above, before the rounding, when the layer has one)    */
 /* In unquantized mode (quant = 0) the same steps run in fp64 on the master weights with  */
 /* no quantization and no rounding.                                                      */
 /* ------------------------------------------------------------------------------------ */
@@ -332,6 +486,12 @@ static void layer_rows(int64_t tb, int64_t te, void *arg) {
     uint8_t *hc = (uint8_t *)malloc((size_t)F / 2), *hs = (uint8_t *)malloc((size_t)F / 16);
     double *c64 = (double *)malloc(sizeof(double) * l);
     double *cin = (double *)malloc(sizeof(double) * l);
+    const int FS = L->shared_ffn > 0 ? L->shared_ffn : 1;
+    const int has_shared = L->shared_ffn > 0;
+    if (has_shared && !shared_ready(L, J->quant)) J->error = 1;
+    uint8_t *sxq = (uint8_t *)malloc((size_t)d), *shq = (uint8_t *)malloc((size_t)FS);
+    float *shf = (float *)malloc(sizeof(float) * FS);
+    double *sh64 = (double *)malloc(sizeof(double) * FS), *ss64 = (double *)malloc(sizeof(double) * d);
 
     for (int64_t t = tb; t < te; ++t) {
         const float *xt = J->x + t * d;
@@ -412,17 +572,29 @@ static void layer_rows(int64_t tb, int64_t te, void *arg) {
             cin[j] = J->quant ? oracle_round_bf16(c64[j]) : c64[j];
             if (O->c) O->c[t * l + j] = (float)cin[j];
         }
-        /* step 3: up-projection */
+        /* shared expert (at width d, on x) */
+        if (has_shared && shared_ready(L, J->quant)) {
+            shared_token(L, xt, J->quant, L->amax_xs, L->amax_hs, sxq, shf, shq, sh64, ss64, NULL);
+            if (O->xs_q && J->quant) memcpy(O->xs_q + t * d, sxq, (size_t)d);
+            if (O->hs) memcpy(O->hs + t * L->shared_ffn, shf, sizeof(float) * L->shared_ffn);
+            if (O->hs_q && J->quant) memcpy(O->hs_q + t * L->shared_ffn, shq, (size_t)L->shared_ffn);
+            if (O->s) for (int j = 0; j < d; ++j) O->s[t * d + j] = (float)ss64[j];
+        } else {
+            for (int j = 0; j < d; ++j) ss64[j] = 0.0;
+        }
+        /* step 3: up-projection (plus the shared expert's output) */
         for (int j = 0; j < d; ++j) {
             const float *wr = L->w_up + (int64_t)j * l;
             double s = 0.0;
             for (int i = 0; i < l; ++i) s += cin[i] * (double)wr[i];
+            s += ss64[j];
             if (O->y64) O->y64[t * d + j] = s;
             if (O->y) O->y[t * d + j] = (float)(J->quant ? oracle_round_bf16(s) : s);
         }
     }
     free(z64); free(zf); free(zc); free(zs); free(lg); free(idx); free(w64); free(wf);
     free(u64); free(hf); free(hc); free(hs); free(c64); free(cin);
+    free(sxq); free(shq); free(shf); free(sh64); free(ss64);
 }
 
 int oracle_layer_forward(const oracle_layer *L, const float *x, int64_t T, int quant,
@@ -469,9 +641,11 @@ int oracle_calibrate(const oracle_layer *L, const float *x, int64_t T,
     float *seen_h = (float *)calloc((size_t)T, sizeof(float));
     oracle_out none;
     memset(&none, 0, sizeof(none));
+    oracle_layer Lc = *L;
+    Lc.shared_ffn = 0;          /* the shared expert does not feed z or h */
     layer_job J;
     memset(&J, 0, sizeof(J));
-    J.L = L; J.x = x; J.quant = 1; J.out = &none;
+    J.L = &Lc; J.x = x; J.quant = 1; J.out = &none;
     J.amax_z = mz; J.amax_h = 1.0f; J.amax_h_seen = seen_h;
     parallel_for(T, nthreads, layer_rows, &J);
     float mh = 0.0f;

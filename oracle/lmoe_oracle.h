@@ -40,6 +40,17 @@ double  oracle_round_bf16(double v);           /* round-to-nearest-even to bfloa
 void    oracle_f32_to_e2m1_array(const float *v, int64_t n, uint8_t *out, int nthreads);
 void    oracle_f32_to_e4m3_array(const float *v, int64_t n, uint8_t *out, int nthreads);
 
+/* FP8 E4M3 with one FP32 per-tensor scale (the shared expert: [NEWS] quantization paragraph,
+ * NVFP4 routed experts mixed with an FP8 shared expert).  s_enc = 448/amax, s_dec = amax/448 (fp32); code = e4m3_satfinite(x * s_enc).
+ * amax < 0: computed from src; amax == 0: all codes 0 and s_dec = 1.  n elements. */
+void oracle_quantize_fp8(const float *src, int64_t n, float amax, uint8_t *codes,
+                         float *s_dec, int nthreads);
+
+/* Exact E4M3 x E4M3 dot product over K elements (tensor scales NOT applied): every E4M3
+ * value is an integer multiple of 2^-9, so the sum is an exact integer count of 2^-18;
+ * it is returned as a double (exact for K <= 2^17). */
+double oracle_fp8_dot(const uint8_t *a, const uint8_t *b, int64_t K);
+
 /* NVFP4 quantization of a row-major [R][K] fp32 array along K (16-element blocks).
  * amax < 0: the tensor amax is computed from src.  codes: [R][K/2] (even element in
  * the low nibble), sf: [R][K/16] E4M3 bytes, *s_dec: the FP32 tensor (decode) scale.
@@ -79,6 +90,18 @@ typedef struct {
     const float *const *w1;         /* [E] -> [ffn][l]     */
     const float *const *w2;         /* [E] -> [l][ffn]     */
     float amax_z, amax_h;           /* static activation amax (calibration)          */
+    /* optional shared expert, kept at the width d ([BLOG] 2.2, closing remark) and in FP8
+     * ([NEWS] quantization paragraph), E4M3 with per-tensor scales:
+     *   s = bf16( s_h s_w2 (q8(h) . Ws2q) ),  h = bf16( max(s_x s_w1 (q8(x) . Ws1q), 0)^2 )
+     * and y = bf16( c Wu^T + s ).  shared_ffn == 0: no shared expert.                   */
+    int shared_ffn;
+    const uint8_t *ws1_codes;       /* [shared_ffn][d]  E4M3 (quant mode)             */
+    float ws1_sdec;
+    const uint8_t *ws2_codes;       /* [d][shared_ffn]  E4M3 (quant mode)             */
+    float ws2_sdec;
+    const float *ws1;               /* [shared_ffn][d]  bf16 values (unquant mode)    */
+    const float *ws2;               /* [d][shared_ffn]  bf16 values (unquant mode)    */
+    float amax_xs, amax_hs;         /* static amax of x and of the shared h           */
 } oracle_layer;
 
 typedef struct {               /* every pointer optional (NULL = not wanted)          */
@@ -96,6 +119,10 @@ typedef struct {               /* every pointer optional (NULL = not wanted)    
     float   *c;        /* [T][l]            bf16 values              */
     double  *y64;      /* [T][d]            before the final rounding */
     float   *y;        /* [T][d]            bf16 values              */
+    uint8_t *xs_q;     /* [T][d]            shared expert: E4M3 codes of x */
+    float   *hs;       /* [T][shared_ffn]   shared expert: h (bf16 values)  */
+    uint8_t *hs_q;     /* [T][shared_ffn]   shared expert: E4M3 codes of h */
+    float   *s;        /* [T][d]            shared expert output (bf16 values) */
 } oracle_out;
 
 /* quant = 1: the NVFP4 layer.  quant = 0: the same layer in plain fp64 with the master
@@ -104,9 +131,17 @@ typedef struct {               /* every pointer optional (NULL = not wanted)    
 int oracle_layer_forward(const oracle_layer *L, const float *x, int64_t T, int quant,
                          oracle_out *out, int nthreads);
 
+/* The shared expert alone on token rows x [T][d] (outputs as in oracle_out; each optional).
+ * quant = 0: fp64 with the master weights, no quantization and no rounding. */
+int oracle_shared_forward(const oracle_layer *L, const float *x, int64_t T, int quant,
+                          uint8_t *xs_q, float *hs, uint8_t *hs_q, float *s, int nthreads);
+
 /* Static activation calibration ([HEIDI]): amax of z and of h over a calibration batch. */
 int oracle_calibrate(const oracle_layer *L, const float *x, int64_t T,
                      float *amax_z, float *amax_h, int nthreads);
+/* The shared expert's static amax: of x, then of h with x quantized by that amax. */
+int oracle_calibrate_shared(const oracle_layer *L, const float *x, int64_t T,
+                            float *amax_xs, float *amax_hs, int nthreads);
 
 #ifdef __cplusplus
 }
