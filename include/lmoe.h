@@ -8,7 +8,11 @@
  *     per selected expert, in latent space:   u = zq W1q_e^T, h = bf16(relu(u)^2), o = hq W2q_e^T
  *                                             (NVFP4 weights and activations)
  *     c  = bf16(sum_j w_j o_j)                routing-weighted combine
- *     y  = bf16(c Wu^T)                       up-projection l -> d, BF16
+ *     y  = bf16(c Wu^T [+ s])                 up-projection l -> d, BF16
+ * and, optionally, a shared expert on x at the full width d (same blog, section 2.2, closing
+ * remark) in FP8 E4M3 with per-tensor scales (NVIDIA AI releases Nemotron 3 Ultra,
+ * quantization paragraph: FP8 shared expert):
+ *     s  = bf16(s_h s_w2 (q8(h) Ws2q^T)),  h = bf16(relu(s_x s_w1 (q8(x) Ws1q^T))^2)
  * NVFP4 (same blog, section 3.1.1): E2M1 elements, one E4M3 scale per 16 contiguous
  * contraction-axis elements, one FP32 tensor scale.
  *
@@ -64,12 +68,20 @@ typedef struct {
     const void  *w2;        /* bf16 [E][l][ffn]   latent-down expert masters, quantized at create */
     float amax_z;           /* static amax of z (calibration); > 0                           */
     float amax_h;           /* static amax of h (calibration); > 0                           */
+    /* Optional shared expert (ws1 == NULL: none).  Quantized to FP8 E4M3 at create, one FP32
+     * tensor scale per matrix from its amax (s_dec = amax / 448).                            */
+    const void  *ws1;       /* bf16 [shared_ffn][d]  h = relu(x ws1^T)^2                        */
+    const void  *ws2;       /* bf16 [d][shared_ffn]  s = h ws2^T                                */
+    int shared_ffn;         /* multiple of 64 when ws1 != NULL                                */
+    float amax_xs;          /* static amax of x for its FP8 quantization (calibration); > 0    */
+    float amax_hs;          /* static amax of the shared h (calibration); > 0                 */
 } lmoe_weights;
 
 /* Create a layer context: validates the dims, allocates the context buffers, quantizes every
  * expert matrix to NVFP4 (one FP32 tensor scale per expert per matrix, computed from its amax)
  * and lays the block scales out for the tensor cores; synchronizes `stream` once at the end.
- * Dims: d, l and ffn multiples of 64; l <= 4096; 1 <= k <= 32; k <= E <= 1024; E % 4 == 0.
+ * Dims: d, l and ffn multiples of 64; l <= 4096; 1 <= k <= 32; k <= E <= 1024; E % 4 == 0;
+ * with a shared expert, shared_ffn a multiple of 64 and amax_xs, amax_hs > 0.
  * (The Ultra layer: d = 8192, l = 2048, E = 512, k = 22; ffn is not given by the pages.)
  * Errors: LMOE_EINVAL (dims / NULL pointers / amax <= 0), LMOE_ENOMEM, LMOE_ECUDA,
  * LMOE_EUNSUPPORTED (device is not compute capability 10.3). */
@@ -88,6 +100,16 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
 lmoe_status lmoe_quantize_nvfp4(const void *src, lmoe_dtype dt, int64_t rows, int64_t K,
                                 float amax, uint8_t *codes, uint8_t *sf, float *tensor_scale,
                                 lmoe_stream stream);
+
+/* FP8 E4M3 quantization with one FP32 per-tensor scale (the shared expert's format):
+ *   src          device, bf16 or fp32 per `dt`, n elements (n % 16 == 0, n >= 0; 0 is a no-op)
+ *   amax         tensor amax; < 0: computed on the device from src
+ *   codes        device uint8 [n]
+ *   tensor_scale device float [1]   the FP32 decode scale amax/448 (1 if amax == 0)
+ * Arithmetic (fp32, round-to-nearest-even): s_enc = 448/amax; code = e4m3_satfinite(x * s_enc);
+ * every code is 0 when amax == 0. */
+lmoe_status lmoe_quantize_fp8(const void *src, lmoe_dtype dt, int64_t n, float amax,
+                              uint8_t *codes, float *tensor_scale, lmoe_stream stream);
 
 /* Routing alone (top-k of E per token, NVIDIA AI releases Nemotron 3 Ultra, architecture):
  *   x       device bf16 [T][d]
@@ -159,7 +181,11 @@ typedef enum {
     LMOE_STAGE_H = 8,        /* bf16  [R][ffn]    debug mode only, permuted rows        */
     LMOE_STAGE_HQ_CODES = 9, /* uint8 [R][ffn/2]  permuted rows                         */
     LMOE_STAGE_HQ_SF = 10,   /* uint8 [R/128][ffn/64][512] tensor-core scale atoms      */
-    LMOE_STAGE_NROWS = 11    /* int32 [1]         R actually used                       */
+    LMOE_STAGE_NROWS = 11,   /* int32 [1]         R actually used                       */
+    LMOE_STAGE_XS_Q = 12,    /* uint8 [T][d]      shared expert: E4M3 codes of x        */
+    LMOE_STAGE_HS = 13,      /* bf16  [T][shared_ffn] shared expert h, debug mode only   */
+    LMOE_STAGE_HS_Q = 14,    /* uint8 [T][shared_ffn] shared expert: E4M3 codes of h     */
+    LMOE_STAGE_S = 15        /* bf16  [T][d]      shared expert output s                */
 } lmoe_stage;
 lmoe_status lmoe_workspace_range(const lmoe_ctx *ctx, int64_t T, int stage, size_t *offset,
                                  size_t *bytes);
@@ -174,8 +200,14 @@ lmoe_status lmoe_set_debug(lmoe_ctx *ctx, int on);
 lmoe_status lmoe_get_expert_nvfp4(const lmoe_ctx *ctx, int which, int e, uint8_t *codes,
                                   uint8_t *sf, float *s_dec, lmoe_stream stream);
 
+/* Copy the shared expert's quantized matrix (which = 1: Ws1 [shared_ffn][d], which = 2: Ws2
+ * [d][shared_ffn]) out of the context: codes device uint8, *s_dec (host) its FP32 tensor
+ * scale.  LMOE_EINVAL if the context has no shared expert.  Synchronizes `stream`. */
+lmoe_status lmoe_get_shared_fp8(const lmoe_ctx *ctx, int which, uint8_t *codes, float *s_dec,
+                                lmoe_stream stream);
+
 /* Number of kernels one lmoe_forward(ctx, ..., T, ...) launches (it depends on T only through
- * the split-K plan of the two projections). */
+ * the split-K plan of the two projections; a shared expert adds three). */
 int lmoe_forward_kernel_count(const lmoe_ctx *ctx, int64_t T);
 
 /* Per-kernel timing of lmoe_forward.  When on, lmoe_forward records a CUDA event on its stream

@@ -22,7 +22,7 @@ LMOE_OK, LMOE_EINVAL, LMOE_ENOMEM, LMOE_ECUDA, LMOE_EUNSUPPORTED, LMOE_ETIMEOUT,
 LMOE_BF16, LMOE_FP32 = 0, 1
 STAGES = {
     "idx": 0, "w": 1, "counts": 2, "zq_codes": 3, "zq_sf": 4, "c": 5, "z": 6, "rows": 7, "h": 8,
-    "hq_codes": 9, "hq_sf": 10, "nrows": 11,
+    "hq_codes": 9, "hq_sf": 10, "nrows": 11, "xs_q": 12, "hs": 13, "hs_q": 14, "s": 15,
 }
 
 
@@ -35,7 +35,9 @@ class LmoeError(RuntimeError):
 class _Weights(C.Structure):
     _fields_ = [("w_down", C.c_void_p), ("w_up", C.c_void_p), ("w_router", C.c_void_p),
                 ("b_router", C.c_void_p), ("w1", C.c_void_p), ("w2", C.c_void_p),
-                ("amax_z", C.c_float), ("amax_h", C.c_float)]
+                ("amax_z", C.c_float), ("amax_h", C.c_float),
+                ("ws1", C.c_void_p), ("ws2", C.c_void_p), ("shared_ffn", C.c_int),
+                ("amax_xs", C.c_float), ("amax_hs", C.c_float)]
 
 
 _lib = None
@@ -57,6 +59,8 @@ def lib() -> C.CDLL:
         "lmoe_status_string": (C.c_char_p, [C.c_int]),
         "lmoe_create": (C.c_int, [C.c_int] * 5 + [C.POINTER(_Weights), vp, C.POINTER(vp)]),
         "lmoe_quantize_nvfp4": (C.c_int, [vp, C.c_int, i64, i64, C.c_float, vp, vp, vp, vp]),
+        "lmoe_quantize_fp8": (C.c_int, [vp, C.c_int, i64, C.c_float, vp, vp, vp]),
+        "lmoe_get_shared_fp8": (C.c_int, [vp, C.c_int, vp, C.POINTER(C.c_float), vp]),
         "lmoe_route": (C.c_int, [vp, vp, i64, vp, vp, vp, vp]),
         "lmoe_route_static": (C.c_int, [vp, vp, i64, vp, vp, vp, vp]),
         "lmoe_workspace_size": (sz, [vp, i64]),
@@ -123,14 +127,28 @@ def lmoe_quantize_nvfp4(src: torch.Tensor, amax: float = -1.0, codes=None, sf=No
     return codes, sf, tensor_scale
 
 
+def lmoe_quantize_fp8(src: torch.Tensor, amax: float = -1.0, codes=None, tensor_scale=None,
+                      stream=None):
+    """FP8 E4M3 per-tensor quantization of a bf16/fp32 device tensor -> (codes, tensor_scale)."""
+    assert src.is_cuda and src.is_contiguous()
+    dt = {torch.bfloat16: LMOE_BF16, torch.float32: LMOE_FP32}[src.dtype]
+    codes = codes if codes is not None else torch.empty(src.shape, dtype=torch.uint8, device=src.device)
+    tensor_scale = tensor_scale if tensor_scale is not None else torch.empty(1, dtype=torch.float32, device=src.device)
+    _check(lib().lmoe_quantize_fp8(_ptr(src), dt, src.numel(), float(amax), _ptr(codes),
+                                   _ptr(tensor_scale), _stream(stream)), "lmoe_quantize_fp8")
+    return codes, tensor_scale
+
+
 def lmoe_create(d, l, E, k, ffn, w_down, w_up, w_router, b_router, w1, w2, amax_z, amax_h,
-                stream=None) -> int:
+                stream=None, ws1=None, ws2=None, amax_xs=0.0, amax_hs=0.0) -> int:
     """Create a context from device tensors: w_down bf16 [l][d], w_up bf16 [d][l], w_router fp32
-    [E][d], b_router fp32 [E] or None, w1 bf16 [E][ffn][l], w2 bf16 [E][l][ffn]."""
-    for t in (w_down, w_up, w_router, w1, w2):
+    [E][d], b_router fp32 [E] or None, w1 bf16 [E][ffn][l], w2 bf16 [E][l][ffn]; optional
+    shared expert ws1 bf16 [shared_ffn][d], ws2 bf16 [d][shared_ffn]."""
+    for t in (w_down, w_up, w_router, w1, w2) + ((ws1, ws2) if ws1 is not None else ()):
         assert t.is_cuda and t.is_contiguous()
     ws = _Weights(_ptr(w_down), _ptr(w_up), _ptr(w_router), _ptr(b_router), _ptr(w1), _ptr(w2),
-                  float(amax_z), float(amax_h))
+                  float(amax_z), float(amax_h), _ptr(ws1), _ptr(ws2),
+                  0 if ws1 is None else ws1.shape[0], float(amax_xs), float(amax_hs))
     out = C.c_void_p()
     _check(lib().lmoe_create(d, l, E, k, ffn, C.byref(ws), _stream(stream), C.byref(out)), "lmoe_create")
     return out.value
@@ -189,6 +207,13 @@ def lmoe_get_expert_nvfp4(ctx, which, e, codes, sf, stream=None) -> float:
     return sd.value
 
 
+def lmoe_get_shared_fp8(ctx, which, codes, stream=None) -> float:
+    sd = C.c_float()
+    _check(lib().lmoe_get_shared_fp8(ctx, which, _ptr(codes), C.byref(sd), _stream(stream)),
+           "lmoe_get_shared_fp8")
+    return sd.value
+
+
 def lmoe_forward_kernel_count(ctx, T) -> int:
     return lib().lmoe_forward_kernel_count(ctx, T)
 
@@ -215,10 +240,11 @@ class LatentMoE:
     """Owns one context and a workspace; forward(x) -> y.  Marshalling only."""
 
     def __init__(self, d, l, E, k, ffn, w_down, w_up, w_router, b_router, w1, w2, amax_z, amax_h,
-                 debug=False, stream=None):
+                 debug=False, stream=None, ws1=None, ws2=None, amax_xs=0.0, amax_hs=0.0):
         self.d, self.l, self.E, self.k, self.ffn = d, l, E, k, ffn
+        self.shared_ffn = 0 if ws1 is None else ws1.shape[0]
         self.ctx = lmoe_create(d, l, E, k, ffn, w_down, w_up, w_router, b_router, w1, w2,
-                               amax_z, amax_h, stream)
+                               amax_z, amax_h, stream, ws1, ws2, amax_xs, amax_hs)
         if debug:
             lmoe_set_debug(self.ctx, True)
         self.ws = None

@@ -4,10 +4,12 @@
 //   * the BF16 latent projections d -> l and l -> d (kind::f16, fp32 accumulate) -- the
 //     projections stay in BF16 (shengxinai.com Nemotron 3 blog, section 3.1.3 table), and
 //   * the NVFP4 expert GEMMs latent-up and latent-down (kind::mxf4nvf4.block_scale with
-//     UE4M3 scales, one per 16 K, E2M1 operands; blog section 3.1.1), grouped per expert.
+//     UE4M3 scales, one per 16 K, E2M1 operands; blog section 3.1.1), grouped per expert, and
+//   * the FP8 E4M3 shared-expert GEMMs (kind::f8f6f4, per-tensor scales applied in the
+//     epilogue; NVIDIA AI releases Nemotron 3 Ultra, quantization paragraph).
 // D[m][n] = sum_k A[m][k] * B[n][k]: A = activations (rows = tokens), B = weights (rows = output
 // features); both K-major.  Tile 128 x 128, one SW128 row of 128 bytes per operand per stage
-// (64 bf16 or 256 e2m1 elements of K).  A is fetched in 32-row boxes, only as many as the tile
+// (64 bf16, 128 e4m3 or 256 e2m1 elements of K).  A is fetched in 32-row boxes, only as many as the tile
 // has valid rows (a decode tile of one token moves 4 KB of A per stage, not 16 KB); rows past
 // the loaded boxes hold stale data whose accumulator rows the epilogue never reads.
 //
@@ -28,15 +30,21 @@
 #pragma once
 #include "common.cuh"
 #include "nvfp4.cuh"
+#include "fp8.cuh"
 
 namespace lmoe {
 
+// Operand kinds (template argument KIND).
+constexpr int kKindBf16 = 0, kKindNvf4 = 1, kKindFp8 = 2;
+
 enum EpiMode : int {
-    EPI_STORE_BF16 = 0,   // out bf16 [M][ld] = acc
+    EPI_STORE_BF16 = 0,   // out bf16 [M][ld] = acc (+ addend bf16 [M][ld], if given)
     EPI_RED_F32 = 1,      // out fp32 [M][ld] += acc (split-K partial)
     EPI_Z_QUANT = 2,      // z = bf16(acc); zq = NVFP4(z) row-major; dbg = z
     EPI_H_QUANT = 3,      // h = bf16(relu(alpha_e acc)^2); hq = NVFP4(h) (scale atoms); dbg = h
-    EPI_COMBINE = 4       // c_acc[token] += w_slot * alpha_e * acc
+    EPI_COMBINE = 4,      // c_acc[token] += w_slot * alpha_e * acc
+    EPI_FP8_SQRELU = 5,   // h = bf16(relu(alpha_s acc)^2); q_codes [M][N] = e4m3(h * s_enc8); dbg = h
+    EPI_STORE_SCALED = 6  // out bf16 [M][ld] = alpha_s * acc
 };
 
 constexpr int kBM = 128, kBN = 128;
@@ -72,6 +80,10 @@ struct GemmArgs {
     uint8_t *a_codes;            // [R][N/2]
     uint8_t *a_sf;               // scale atoms [R/128][N/64][512]
     int32_t *row_slot_out;       // [R]
+    // shared expert (FP8): per-tensor scale product and the h encode scale; up-projection addend
+    float alpha_s;
+    float s_enc8;
+    const __nv_bfloat16 *addend; // EPI_STORE_BF16: bf16 [M][ld_out] added before the rounding
     unsigned *err;
 };
 
@@ -179,12 +191,57 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs &g, const Tile &tl
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
     switch (g.epi) {
-    case EPI_STORE_BF16: {
+    case EPI_STORE_BF16:
+    case EPI_STORE_SCALED: {
+        if (g.epi == EPI_STORE_SCALED) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(g.alpha_s, v[i]);
+        } else if (g.addend) {
+            const uint4 *a = reinterpret_cast<const uint4 *>(g.addend + grow * g.ld_out + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 u = __ldg(a + i);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    v[8 * i + 2 * j] = __fadd_rn(v[8 * i + 2 * j], __uint_as_float(w[j] << 16));
+                    v[8 * i + 2 * j + 1] = __fadd_rn(v[8 * i + 2 * j + 1], __uint_as_float(w[j] & 0xFFFF0000u));
+                }
+            }
+        }
         uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(g.out) + grow * g.ld_out + col);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             o[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
                               pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+        break;
+    }
+    case EPI_FP8_SQRELU: {
+        const float a = g.alpha_s;
+        uint32_t hb[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float u0 = fmaxf(__fmul_rn(a, v[2 * i]), 0.0f);
+            const float u1 = fmaxf(__fmul_rn(a, v[2 * i + 1]), 0.0f);
+            hb[i] = pack_bf16x2(__fmul_rn(u0, u0), __fmul_rn(u1, u1));
+            v[2 * i] = __fmul_rn(__uint_as_float(hb[i] << 16), g.s_enc8);
+            v[2 * i + 1] = __fmul_rn(__uint_as_float(hb[i] & 0xFFFF0000u), g.s_enc8);
+        }
+        if (g.dbg) {
+            uint4 *o = reinterpret_cast<uint4 *>(g.dbg + grow * g.N + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[i] = make_uint4(hb[4 * i], hb[4 * i + 1], hb[4 * i + 2], hb[4 * i + 3]);
+        }
+        uint4 *q = reinterpret_cast<uint4 *>(g.q_codes + grow * g.N + col);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                w[i] = f32x2_to_e4m3x2(v[16 * b + 4 * i], v[16 * b + 4 * i + 1]) |
+                       (f32x2_to_e4m3x2(v[16 * b + 4 * i + 2], v[16 * b + 4 * i + 3]) << 16);
+            q[b] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
         break;
     }
     case EPI_RED_F32: {
@@ -257,40 +314,43 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs &g, const Tile &tl
     }
 }
 
-// SMALLA (decode): every tile has at most 32 valid A rows, so each column block of a stage
+// KIND: kKindBf16, kKindNvf4 or kKindFp8.  SMALLA (decode): every tile has at most 32 valid A rows, so each column block of a stage
 // keeps only one 4 KB A box; the MMA still reads 128 rows from the block's A base, and rows
 // 32..127 fall on the following boxes (or on the slack after the last one): they only feed
 // accumulator rows the epilogue never reads.  KB: 128-byte column blocks (256 e2m1 or 64 bf16
-// elements of K each) per pipeline stage; KB = 2 halves the per-stage barrier handshakes and
+// elements of K each; 128 e4m3) per pipeline stage; KB = 2 halves the per-stage barrier handshakes and
 // copies when each stage carries little MMA work (decode).
-template <bool NVF4, bool SMALLA, int KB>
+template <int KIND, bool SMALLA, int KB>
 struct GemmCfg {
+    static constexpr bool NVF4 = KIND == kKindNvf4;
     static constexpr int kACol = SMALLA ? kABoxBytes : kTileBytes;   // A bytes per column block
     static constexpr int kAStage = KB * kACol;
     static constexpr int kBStage = KB * kTileBytes;
     static constexpr int kSfStage = NVF4 ? KB * kSfStageBytes : 0;   // per operand
     static constexpr int kSlack = SMALLA ? kTileBytes - kABoxBytes : 0;
-    static constexpr int kElemsPerBlock = NVF4 ? 256 : 64;
+    static constexpr int kElemsPerBlock = NVF4 ? 256 : (KIND == kKindFp8 ? 128 : 64);
+    static constexpr int kTmaXPerBlock = KIND == kKindBf16 ? 64 : 128;  // tensor-map x units per block
     static constexpr int kStepsPerBlock = 4;                          // MMA K steps per block
     static constexpr int kSfCols = NVF4 ? 32 * KB : 0;                // TMEM columns per stage
 };
 
-template <bool NVF4, bool SMALLA, int KB>
+template <int KIND, bool SMALLA, int KB>
 constexpr int gemm_smem_bytes(int stages) {
-    using C = GemmCfg<NVF4, SMALLA, KB>;
+    using C = GemmCfg<KIND, SMALLA, KB>;
     return 1024 + stages * (C::kAStage + C::kBStage + 2 * C::kSfStage) + C::kSlack + 256 +
-           (NVF4 ? static_cast<int>(sizeof(SmemTables)) : 0);
+           (C::NVF4 ? static_cast<int>(sizeof(SmemTables)) : 0);
 }
 
 constexpr int kEpiWarps = 8;
 constexpr int kEpiWarp0 = 4;
 constexpr int kGemmThreads = 32 * (kEpiWarp0 + kEpiWarps);
 
-template <bool NVF4, bool SMALLA, int KB, int STAGES>
+template <int KIND, bool SMALLA, int KB, int STAGES>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmArgs g) {
-    using C = GemmCfg<NVF4, SMALLA, KB>;
+    using C = GemmCfg<KIND, SMALLA, KB>;
+    constexpr bool NVF4 = C::NVF4;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -368,7 +428,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const uint32_t a_st = sA0 + stage * C::kAStage, b_st = sB0 + stage * C::kBStage;
 #pragma unroll
                     for (int b = 0; b < KB; ++b) {
-                        const int kx = (kb0 + b) * (NVF4 ? 128 : 64);
+                        const int kx = (kb0 + b) * C::kTmaXPerBlock;
                         for (int j = 0; j < nbox; ++j)
                             tma_load_2d_u32(a_st + b * C::kACol + j * kABoxBytes, &tmA, fb, kx, tl.a_row0 + j * kABoxRows);
                         tma_load_2d_u32(b_st + b * kTileBytes, &tmB, fb, kx, tl.b_row0);
@@ -395,7 +455,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = NVF4 ? idesc_nvf4(kBM, kBN) : idesc_bf16(kBM, kBN);
+            const uint32_t idesc = NVF4 ? idesc_nvf4(kBM, kBN)
+                                        : (KIND == kKindFp8 ? idesc_f8(kBM, kBN) : idesc_bf16(kBM, kBN));
             // descriptors of stage 0; a stage adds its byte offset >> 4 to the start address
             const uint64_t adesc0 = sdesc_sw128(smem_u32(sA)), bdesc0 = sdesc_sw128(smem_u32(sB));
             int stage = 0;
@@ -426,6 +487,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                          bd + (((kk >> 2) * kTileBytes + (kk & 3) * 32) >> 4), idesc,
                                          sf_t + kk * 4, sf_t + 16 * KB + kk * 4, (acc_flag0 | kk) ? 1u : 0u);
                         }
+                    } else if constexpr (KIND == kKindFp8) {
+#pragma unroll
+                        for (int kk = 0; kk < 4 * KB; ++kk)
+                            mma_f8(d_tmem, ad + (((kk >> 2) * C::kACol + (kk & 3) * 32) >> 4),
+                                   bd + (((kk >> 2) * kTileBytes + (kk & 3) * 32) >> 4), idesc,
+                                   (acc_flag0 | kk) ? 1u : 0u);
                     } else {
 #pragma unroll
                         for (int kk = 0; kk < 4 * KB; ++kk)

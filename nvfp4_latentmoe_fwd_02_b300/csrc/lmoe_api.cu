@@ -1,7 +1,8 @@
 // lmoe_api.cu -- host side of liblmoe.so: the C ABI declared in include/lmoe.h.
 //
 // The LatentMoE expert layer forward (shengxinai.com Nemotron 3 blog, section 2.2, steps 1-3):
-// down-projection d -> l, routing on x, NVFP4 latent experts, weighted combine, up-projection.
+// down-projection d -> l, routing on x, NVFP4 latent experts, weighted combine, up-projection,
+// plus the optional FP8 shared expert at width d whose output joins the up-projection.
 // The host code validates arguments, lays out the workspace, encodes TMA descriptors and
 // launches the kernels of this directory on the caller's stream; it never synchronizes or
 // reads device memory inside lmoe_forward.
@@ -17,6 +18,7 @@
 
 #include "lmoe.h"   // include/ (on the include path)
 #include "common.cuh"
+#include "fp8.cuh"
 #include "gemm.cuh"
 #include "moe.cuh"
 #include "nvfp4.cuh"
@@ -30,6 +32,8 @@ constexpr int kStagesF4 = 5;
 constexpr int kStagesBF16 = 6;
 constexpr int kStagesF4Small = 4;     // decode (T <= 32): 4 KB A boxes, 2 column blocks per stage
 constexpr int kStagesBF16Small = 5;
+constexpr int kStagesF8 = 6;          // FP8 stages have the BF16 byte layout
+constexpr int kStagesF8Small = 5;
 constexpr int kSmallAMaxT = 32;
 inline int kb_for(bool small_a) { return small_a ? 2 : 1; }   // column blocks per stage
 
@@ -93,7 +97,7 @@ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct WsLayout {
     size_t idx, w, counts, seg, mt, slot_off, nrows, row_slot, router, zacc, zq_codes, zq_sf, z_dbg,
-        a_codes, a_sf, h_codes, h_sf, h_dbg, c_acc, c, yacc, total;
+        a_codes, a_sf, h_codes, h_sf, h_dbg, c_acc, c, yacc, xs_q, hs_q, hs_dbg, s_out, total;
     int64_t R;   // row capacity of the permuted buffers (multiple of 128)
     bool small_router, split_down, split_up;
     int down_splits, up_splits;
@@ -112,6 +116,12 @@ struct lmoe_ctx {
     float amax_z, amax_h;
     QScale qz, qh;
     CUtensorMap tm_wd, tm_wu, tm_w1, tm_w2;
+    // shared expert (FP8 E4M3, per-tensor scales); shared_ffn == 0: none
+    int shared_ffn;
+    uint8_t *ws1_codes, *ws2_codes;
+    float ws1_sdec, ws2_sdec, amax_xs, amax_hs;
+    float alpha_s1, alpha_s2, s_enc_hs;
+    CUtensorMap tm_ws1, tm_ws2;
     unsigned *err;
     int debug;
     void *route_ws;
@@ -190,44 +200,53 @@ WsLayout layout(const lmoe_ctx *c, int64_t T) {
     L.c_acc = take(T * l * 4);
     L.c = take(T * l * 2);
     L.yacc = take(L.split_up ? T * d * 4 : 0);
+    const int64_t FS = c->shared_ffn;
+    L.xs_q = take(FS ? T * d : 0);
+    L.hs_q = take(T * FS);
+    L.hs_dbg = take(c->debug ? T * FS * 2 : 0);
+    L.s_out = take(FS ? T * d * 2 : 0);
     L.total = off;
     return L;
 }
 
-template <bool NVF4, bool SMALLA, int KB, int STAGES>
+template <int KIND, bool SMALLA, int KB, int STAGES>
 cudaError_t set_smem_attr() {
-    static_assert(gemm_smem_bytes<NVF4, SMALLA, KB>(STAGES) <= 232448, "shared memory budget");
-    return cudaFuncSetAttribute(gemm_kernel<NVF4, SMALLA, KB, STAGES>,
+    static_assert(gemm_smem_bytes<KIND, SMALLA, KB>(STAGES) <= 232448, "shared memory budget");
+    return cudaFuncSetAttribute(gemm_kernel<KIND, SMALLA, KB, STAGES>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                gemm_smem_bytes<NVF4, SMALLA, KB>(STAGES));
+                                gemm_smem_bytes<KIND, SMALLA, KB>(STAGES));
 }
 
-template <bool NVF4, bool SMALLA, int KB, int STAGES>
+template <int KIND, bool SMALLA, int KB, int STAGES>
 cudaError_t launch_gemm_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int grid,
                             cudaStream_t s) {
-    return launch_pdl(gemm_kernel<NVF4, SMALLA, KB, STAGES>, dim3(grid), dim3(kGemmThreads),
-                      gemm_smem_bytes<NVF4, SMALLA, KB>(STAGES), s, ta, tb, g);
+    return launch_pdl(gemm_kernel<KIND, SMALLA, KB, STAGES>, dim3(grid), dim3(kGemmThreads),
+                      gemm_smem_bytes<KIND, SMALLA, KB>(STAGES), s, ta, tb, g);
 }
 
 // small_a: every tile has at most 32 valid A rows (T <= 32); such launches use two column
 // blocks per stage, and g.k_tiles must count stages of kb_for(true) blocks.
-template <bool NVF4>
+template <int KIND>
 cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int grid,
                         bool small_a, cudaStream_t s) {
-    if (NVF4)
-        return small_a ? launch_gemm_cfg<true, true, 2, kStagesF4Small>(ta, tb, g, grid, s)
-                       : launch_gemm_cfg<true, false, 1, kStagesF4>(ta, tb, g, grid, s);
-    return small_a ? launch_gemm_cfg<false, true, 2, kStagesBF16Small>(ta, tb, g, grid, s)
-                   : launch_gemm_cfg<false, false, 1, kStagesBF16>(ta, tb, g, grid, s);
+    if (KIND == kKindNvf4)
+        return small_a ? launch_gemm_cfg<kKindNvf4, true, 2, kStagesF4Small>(ta, tb, g, grid, s)
+                       : launch_gemm_cfg<kKindNvf4, false, 1, kStagesF4>(ta, tb, g, grid, s);
+    if (KIND == kKindFp8)
+        return small_a ? launch_gemm_cfg<kKindFp8, true, 2, kStagesF8Small>(ta, tb, g, grid, s)
+                       : launch_gemm_cfg<kKindFp8, false, 1, kStagesF8>(ta, tb, g, grid, s);
+    return small_a ? launch_gemm_cfg<kKindBf16, true, 2, kStagesBF16Small>(ta, tb, g, grid, s)
+                   : launch_gemm_cfg<kKindBf16, false, 1, kStagesBF16>(ta, tb, g, grid, s);
 }
 
-GemmArgs dense_args(int M, int N, int K, int splits, int epi, unsigned *err, int kb) {
+// K elements per 128-byte column block: 64 (bf16) or 128 (fp8).
+GemmArgs dense_args(int M, int N, int K, int splits, int epi, unsigned *err, int kb, int k_block = 64) {
     GemmArgs g;
     std::memset(&g, 0, sizeof(g));
     g.M = M; g.N = N; g.K = K;
     g.m_tiles = static_cast<int>(cdiv(M, kBM));
     g.n_tiles = static_cast<int>(cdiv(N, kBN));
-    g.k_tiles = static_cast<int>(cdiv(K / 64, kb));
+    g.k_tiles = static_cast<int>(cdiv(cdiv(K, k_block), kb));
     g.kt_per_split = static_cast<int>(cdiv(g.k_tiles, splits));
     g.k_splits = static_cast<int>(cdiv(g.k_tiles, g.kt_per_split));
     g.epi = epi;
@@ -376,6 +395,40 @@ lmoe_status lmoe_quantize_nvfp4(const void *src, lmoe_dtype dt, int64_t rows, in
     return LMOE_OK;
 }
 
+lmoe_status lmoe_quantize_fp8(const void *src, lmoe_dtype dt, int64_t n, float amax, uint8_t *codes,
+                              float *tensor_scale, lmoe_stream stream) {
+    if (n < 0 || n % 16 != 0 || (dt != LMOE_BF16 && dt != LMOE_FP32)) return LMOE_EINVAL;
+    if (n == 0) return LMOE_OK;
+    if (!src || !codes || !tensor_scale) return LMOE_EINVAL;
+    if (amax != amax) return LMOE_EINVAL;
+    if (reinterpret_cast<uintptr_t>(src) % 16 || reinterpret_cast<uintptr_t>(codes) % 16) return LMOE_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned *bits = reinterpret_cast<unsigned *>(tensor_scale);   // holds amax bits until the end
+    if (amax < 0.0f) {
+        LMOE_CUDA(cudaMemsetAsync(bits, 0, sizeof(unsigned), s));
+        const int agrid = static_cast<int>(std::min<int64_t>(cdiv(n, 256), 148 * 8));
+        if (dt == LMOE_BF16)
+            amax_kernel<__nv_bfloat16><<<agrid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(src), n, bits);
+        else
+            amax_kernel<float><<<agrid, 256, 0, s>>>(static_cast<const float *>(src), n, bits);
+        LMOE_LAUNCH();
+    } else {
+        unsigned ab;
+        std::memcpy(&ab, &amax, sizeof(ab));
+        LMOE_CUDA(cudaMemcpyAsync(bits, &ab, sizeof(ab), cudaMemcpyHostToDevice, s));
+    }
+    const int qgrid = static_cast<int>(std::min<int64_t>(cdiv(n / 16, 256), 148 * 16));
+    if (dt == LMOE_BF16)
+        quantize_fp8_kernel<__nv_bfloat16><<<qgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(src), n,
+                                                                -1.0f, bits, codes);
+    else
+        quantize_fp8_kernel<float><<<qgrid, 256, 0, s>>>(static_cast<const float *>(src), n, -1.0f, bits, codes);
+    LMOE_LAUNCH();
+    fp8_tensor_scale_kernel<<<1, 32, 0, s>>>(bits, tensor_scale);
+    LMOE_LAUNCH();
+    return LMOE_OK;
+}
+
 lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights *w,
                         lmoe_stream stream, lmoe_ctx **out) {
     if (!out) return LMOE_EINVAL;
@@ -385,6 +438,10 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
     if (l > 4096) return LMOE_EINVAL;
     if (k < 1 || k > 32 || E < k || E > 1024 || E % 4) return LMOE_EINVAL;
     if (!(w->amax_z > 0.0f) || !(w->amax_h > 0.0f)) return LMOE_EINVAL;
+    const bool has_shared = w->ws1 != nullptr;
+    if (has_shared && (!w->ws2 || w->shared_ffn <= 0 || w->shared_ffn % 64 || !(w->amax_xs > 0.0f) ||
+                       !(w->amax_hs > 0.0f)))
+        return LMOE_EINVAL;
     int dev = 0;
     LMOE_CUDA(cudaGetDevice(&dev));
     cudaDeviceProp prop;
@@ -395,10 +452,12 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
         static std::once_flag once;
         static cudaError_t attr_err = cudaSuccess;
         std::call_once(once, [] {
-            cudaError_t a = set_smem_attr<true, false, 1, kStagesF4>();
-            cudaError_t b = set_smem_attr<false, false, 1, kStagesBF16>();
-            if (a == cudaSuccess) a = set_smem_attr<true, true, 2, kStagesF4Small>();
-            if (b == cudaSuccess) b = set_smem_attr<false, true, 2, kStagesBF16Small>();
+            cudaError_t a = set_smem_attr<kKindNvf4, false, 1, kStagesF4>();
+            cudaError_t b = set_smem_attr<kKindBf16, false, 1, kStagesBF16>();
+            if (a == cudaSuccess) a = set_smem_attr<kKindNvf4, true, 2, kStagesF4Small>();
+            if (b == cudaSuccess) b = set_smem_attr<kKindBf16, true, 2, kStagesBF16Small>();
+            if (a == cudaSuccess) a = set_smem_attr<kKindFp8, false, 1, kStagesF8>();
+            if (a == cudaSuccess) a = set_smem_attr<kKindFp8, true, 2, kStagesF8Small>();
             cudaError_t r = cudaFuncSetAttribute(router_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  kRouterLogitsSmem);
             if (r == cudaSuccess)
@@ -488,6 +547,43 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
         for (cudaError_t e : {e1, e2, e3, e4})
             if (e != cudaSuccess) return fail(cuda_status(e));
     }
+    // shared expert: per-matrix amax, FP8 E4M3 codes, and the fp32 scale products
+    if (has_shared) {
+        const int FS = w->shared_ffn;
+        const int64_t n = static_cast<int64_t>(FS) * d;
+        c->shared_ffn = FS;
+        c->amax_xs = w->amax_xs;
+        c->amax_hs = w->amax_hs;
+        CREATE_CUDA(cudaMalloc(&c->ws1_codes, n));
+        CREATE_CUDA(cudaMalloc(&c->ws2_codes, n));
+        unsigned *bits = c->amax_bits;   // reused: [0] ws1, [1] ws2 (the expert amax is done)
+        CREATE_CUDA(cudaMemsetAsync(bits, 0, 2 * sizeof(unsigned), s));
+        amax_segments_kernel<<<dim3(c->num_sms * 4, 1), 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->ws1), n, bits);
+        amax_segments_kernel<<<dim3(c->num_sms * 4, 1), 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->ws2), n, bits + 1);
+        CREATE_CUDA(cudaGetLastError());
+        const int qg = static_cast<int>(std::min<int64_t>(cdiv(n / 16, 256), c->num_sms * 16));
+        quantize_fp8_kernel<__nv_bfloat16><<<qg, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->ws1), n, -1.0f,
+                                                             bits, c->ws1_codes);
+        quantize_fp8_kernel<__nv_bfloat16><<<qg, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->ws2), n, -1.0f,
+                                                             bits + 1, c->ws2_codes);
+        CREATE_CUDA(cudaGetLastError());
+        unsigned hb[2];
+        CREATE_CUDA(cudaMemcpyAsync(hb, bits, sizeof(hb), cudaMemcpyDeviceToHost, s));
+        CREATE_CUDA(cudaStreamSynchronize(s));
+        float a1, a2;
+        std::memcpy(&a1, &hb[0], 4);
+        std::memcpy(&a2, &hb[1], 4);
+        c->ws1_sdec = fp8scale_from_amax(a1).s_dec;
+        c->ws2_sdec = fp8scale_from_amax(a2).s_dec;
+        volatile float p1 = fp8scale_from_amax(c->amax_xs).s_dec * c->ws1_sdec;
+        volatile float p2 = fp8scale_from_amax(c->amax_hs).s_dec * c->ws2_sdec;
+        c->alpha_s1 = p1;
+        c->alpha_s2 = p2;
+        c->s_enc_hs = fp8scale_from_amax(c->amax_hs).s_enc;
+        if (!make_map(&c->tm_ws1, false, c->ws1_codes, d, FS, d) ||
+            !make_map(&c->tm_ws2, false, c->ws2_codes, FS, d, FS))
+            return fail(LMOE_ECUDA);
+    }
     bool ok = make_map(&c->tm_wd, true, c->w_down, d, l, static_cast<uint64_t>(d) * 2) &&
               make_map(&c->tm_wu, true, c->w_up, l, d, static_cast<uint64_t>(l) * 2) &&
               make_map(&c->tm_w1, false, c->w1_codes, l / 2, static_cast<uint64_t>(E) * ffn, l / 2) &&
@@ -503,7 +599,7 @@ void lmoe_destroy(lmoe_ctx *c) {
     cudaDeviceSynchronize();
     void *ptrs[] = {c->w_down, c->w_up, c->w_router, c->b_router, c->w1_codes, c->w1_sf,
                     c->w2_codes, c->w2_sf, c->w1_sdec, c->w2_sdec, c->alpha1, c->alpha2,
-                    c->amax_bits, c->err, c->route_ws};
+                    c->amax_bits, c->err, c->route_ws, c->ws1_codes, c->ws2_codes};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     for (cudaEvent_t e : c->ev)
@@ -560,6 +656,10 @@ lmoe_status lmoe_workspace_range(const lmoe_ctx *c, int64_t T, int stage, size_t
     case LMOE_STAGE_HQ_CODES: *offset = L.h_codes; *bytes = L.R * F / 2; break;
     case LMOE_STAGE_HQ_SF: *offset = L.h_sf; *bytes = L.R * F / 16; break;
     case LMOE_STAGE_NROWS: *offset = L.nrows; *bytes = 4; break;
+    case LMOE_STAGE_XS_Q: *offset = L.xs_q; *bytes = c->shared_ffn ? T * c->d : 0; break;
+    case LMOE_STAGE_HS: *offset = L.hs_dbg; *bytes = c->debug ? T * c->shared_ffn * 2 : 0; break;
+    case LMOE_STAGE_HS_Q: *offset = L.hs_q; *bytes = T * c->shared_ffn; break;
+    case LMOE_STAGE_S: *offset = L.s_out; *bytes = c->shared_ffn ? T * c->d * 2 : 0; break;
     default: return LMOE_EINVAL;
     }
     return LMOE_OK;
@@ -625,6 +725,10 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     float *c_acc = static_cast<float *>(at(L.c_acc));
     __nv_bfloat16 *cb = static_cast<__nv_bfloat16 *>(at(L.c));
     float *yacc = static_cast<float *>(at(L.yacc));
+    uint8_t *xs_q = static_cast<uint8_t *>(at(L.xs_q));
+    uint8_t *hs_q = static_cast<uint8_t *>(at(L.hs_q));
+    __nv_bfloat16 *hs_dbg = c->debug ? static_cast<__nv_bfloat16 *>(at(L.hs_dbg)) : nullptr;
+    __nv_bfloat16 *s_out = static_cast<__nv_bfloat16 *>(at(L.s_out));
     const int d = c->d, l = c->l, E = c->E, k = c->k, F = c->ffn;
     const bool small_a = T <= kSmallAMaxT;   // no GEMM tile then has more than 32 valid rows
     if (c->profile) {
@@ -647,7 +751,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
             g.topk = k; g.idx = idx; g.slot_off = slot_off; g.seg_start = seg;
             g.a_codes = a_codes; g.a_sf = a_sf; g.row_slot_out = row_slot;
         }
-        LMOE_CUDA((launch_gemm<false>(tx, c->tm_wd, g,
+        LMOE_CUDA((launch_gemm<kKindBf16>(tx, c->tm_wd, g,
                                       grid_for(int64_t(g.m_tiles) * g.n_tiles * g.k_splits, c->num_sms), small_a, ds)));
         prof_mark(c, "down_proj", ds);
         return LMOE_OK;
@@ -712,7 +816,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         g.sfa = a_sf; g.sfb = c->w1_sf; g.NB = static_cast<int>(cdiv(F, 128));
         g.epi = EPI_H_QUANT; g.q = c->qh; g.q_codes = h_codes; g.q_sf = h_sf; g.dbg = h_dbg;
         g.alpha = c->alpha1; g.err = c->err;
-        LMOE_CUDA((launch_gemm<true>(ta, c->tm_w1, g, c->num_sms, small_a, s)));
+        LMOE_CUDA((launch_gemm<kKindNvf4>(ta, c->tm_w1, g, c->num_sms, small_a, s)));
         prof_mark(c, "expert_up", s);
     }
     // 6. latent-down grouped GEMM, routing weight, combine into c_acc
@@ -728,17 +832,41 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         g.sfa = h_sf; g.sfb = c->w2_sf; g.NB = static_cast<int>(cdiv(l, 128));
         g.epi = EPI_COMBINE; g.out = c_acc; g.ld_out = l;
         g.alpha = c->alpha2; g.row_slot = row_slot; g.route_w = rw; g.topk = k; g.err = c->err;
-        LMOE_CUDA((launch_gemm<true>(ta, c->tm_w2, g, c->num_sms, small_a, s)));
+        LMOE_CUDA((launch_gemm<kKindNvf4>(ta, c->tm_w2, g, c->num_sms, small_a, s)));
         prof_mark(c, "expert_down", s);
     }
     // 7. c = bf16(c_acc)
     {
         const int grid = static_cast<int>(std::min<int64_t>(cdiv(T * l / 8, 256), c->num_sms * 8));
         LMOE_CUDA(launch_pdl(f32_to_bf16_kernel, dim3(grid), dim3(256), 0, s, static_cast<const float *>(c_acc),
-                             T * l, cb));
+                             T * l, cb, static_cast<const __nv_bfloat16 *>(nullptr)));
         prof_mark(c, "combine_cast", s);
     }
-    // 8. up-projection y = c Wu^T
+    // 7b. shared expert at width d (FP8): xs = q8(x); hs = q8(bf16(relu(alpha_s1 xs Ws1q^T)^2));
+    //     s = bf16(alpha_s2 hs Ws2q^T), added to the up-projection before its rounding
+    if (c->shared_ffn) {
+        const int FS = c->shared_ffn;
+        const int qg = static_cast<int>(std::min<int64_t>(cdiv(T * d / 16, 256), c->num_sms * 16));
+        LMOE_CUDA(launch_pdl(quantize_fp8_kernel<__nv_bfloat16>, dim3(qg), dim3(256), 0, s,
+                             static_cast<const __nv_bfloat16 *>(x), T * d, c->amax_xs,
+                             static_cast<const unsigned *>(nullptr), xs_q));
+        prof_mark(c, "shared_quant_x", s);
+        CUtensorMap txs, ths;
+        if (!make_map(&txs, false, xs_q, d, T, d, kABoxRows) || !make_map(&ths, false, hs_q, FS, T, FS, kABoxRows))
+            return LMOE_ECUDA;
+        GemmArgs g1 = dense_args(static_cast<int>(T), FS, d, 1, EPI_FP8_SQRELU, c->err, kb_for(small_a), 128);
+        g1.alpha_s = c->alpha_s1; g1.s_enc8 = c->s_enc_hs; g1.q_codes = hs_q; g1.dbg = hs_dbg;
+        LMOE_CUDA((launch_gemm<kKindFp8>(txs, c->tm_ws1, g1, grid_for(int64_t(g1.m_tiles) * g1.n_tiles, c->num_sms),
+                                         small_a, s)));
+        prof_mark(c, "shared_up", s);
+        GemmArgs g2 = dense_args(static_cast<int>(T), d, FS, 1, EPI_STORE_SCALED, c->err, kb_for(small_a), 128);
+        g2.alpha_s = c->alpha_s2; g2.out = s_out; g2.ld_out = d;
+        LMOE_CUDA((launch_gemm<kKindFp8>(ths, c->tm_ws2, g2, grid_for(int64_t(g2.m_tiles) * g2.n_tiles, c->num_sms),
+                                         small_a, s)));
+        prof_mark(c, "shared_down", s);
+    }
+    const __nv_bfloat16 *y_add = c->shared_ffn ? s_out : nullptr;
+    // 8. up-projection y = c Wu^T (+ s)
     {
         CUtensorMap tc;
         if (!make_map(&tc, true, cb, l, T, static_cast<uint64_t>(l) * 2, kABoxRows)) return LMOE_ECUDA;
@@ -746,13 +874,14 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
                                 L.split_up ? EPI_RED_F32 : EPI_STORE_BF16, c->err, kb_for(small_a));
         g.out = L.split_up ? static_cast<void *>(yacc) : y;
         g.ld_out = d;
-        LMOE_CUDA((launch_gemm<false>(tc, c->tm_wu, g,
+        if (!L.split_up) g.addend = y_add;
+        LMOE_CUDA((launch_gemm<kKindBf16>(tc, c->tm_wu, g,
                                                    grid_for(int64_t(g.m_tiles) * g.n_tiles * g.k_splits, c->num_sms), small_a, s)));
         prof_mark(c, "up_proj", s);
         if (L.split_up) {
             const int grid = static_cast<int>(std::min<int64_t>(cdiv(T * d / 8, 256), c->num_sms * 8));
             LMOE_CUDA(launch_pdl(f32_to_bf16_kernel, dim3(grid), dim3(256), 0, s, static_cast<const float *>(yacc),
-                                 T * d, static_cast<__nv_bfloat16 *>(y)));
+                                 T * d, static_cast<__nv_bfloat16 *>(y), y_add));
             prof_mark(c, "y_cast", s);
         }
     }
@@ -797,13 +926,25 @@ lmoe_status lmoe_get_expert_nvfp4(const lmoe_ctx *c, int which, int e, uint8_t *
     return LMOE_OK;
 }
 
+lmoe_status lmoe_get_shared_fp8(const lmoe_ctx *c, int which, uint8_t *codes, float *s_dec,
+                                lmoe_stream stream) {
+    if (!c || !c->shared_ffn || (which != 1 && which != 2) || !codes || !s_dec) return LMOE_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t n = static_cast<size_t>(c->shared_ffn) * c->d;
+    LMOE_CUDA(cudaMemcpyAsync(codes, which == 1 ? c->ws1_codes : c->ws2_codes, n, cudaMemcpyDeviceToDevice, s));
+    LMOE_CUDA(cudaStreamSynchronize(s));
+    *s_dec = which == 1 ? c->ws1_sdec : c->ws2_sdec;
+    return LMOE_OK;
+}
+
 int lmoe_forward_kernel_count(const lmoe_ctx *c, int64_t T) {
     if (!c || T <= 0) return 0;
     const WsLayout L = layout(c, T);
     // router logits, top-k, segments, down-proj, expert-up, expert-down, combine cast,
     // up-proj, plus one finalize per split projection (and, for a split down-projection run
-    // beside the router, the clearing of its accumulator)
-    return 8 + (L.split_down ? 2 : 0) + (L.split_up ? 1 : 0);
+    // beside the router, the clearing of its accumulator), plus the shared expert's
+    // quantization of x and its two GEMMs
+    return 8 + (L.split_down ? 2 : 0) + (L.split_up ? 1 : 0) + (c->shared_ffn ? 3 : 0);
 }
 
 lmoe_status lmoe_set_profile(lmoe_ctx *c, int on) {

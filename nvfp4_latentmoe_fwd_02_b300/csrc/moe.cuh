@@ -117,15 +117,23 @@ __global__ void transpose_f32_kernel(const float *__restrict__ in, int64_t R, in
     }
 }
 
-// acc [n] fp32 -> out [n] bf16 (n % 8 == 0).
+// out [n] bf16 = bf16(acc [n] fp32 (+ add [n] bf16, if given)) (n % 8 == 0).
 __global__ void f32_to_bf16_kernel(const float *__restrict__ acc, int64_t n,
-                                   __nv_bfloat16 *__restrict__ out) {
+                                   __nv_bfloat16 *__restrict__ out,
+                                   const __nv_bfloat16 *__restrict__ add) {
     pdl_wait();
     pdl_trigger();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n / 8;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const float4 a = __ldg(reinterpret_cast<const float4 *>(acc) + 2 * i);
-        const float4 b = __ldg(reinterpret_cast<const float4 *>(acc) + 2 * i + 1);
+        float4 a = __ldg(reinterpret_cast<const float4 *>(acc) + 2 * i);
+        float4 b = __ldg(reinterpret_cast<const float4 *>(acc) + 2 * i + 1);
+        if (add) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(add) + i);
+            a.x = __fadd_rn(a.x, __uint_as_float(u.x << 16)); a.y = __fadd_rn(a.y, __uint_as_float(u.x & 0xFFFF0000u));
+            a.z = __fadd_rn(a.z, __uint_as_float(u.y << 16)); a.w = __fadd_rn(a.w, __uint_as_float(u.y & 0xFFFF0000u));
+            b.x = __fadd_rn(b.x, __uint_as_float(u.z << 16)); b.y = __fadd_rn(b.y, __uint_as_float(u.z & 0xFFFF0000u));
+            b.z = __fadd_rn(b.z, __uint_as_float(u.w << 16)); b.w = __fadd_rn(b.w, __uint_as_float(u.w & 0xFFFF0000u));
+        }
         reinterpret_cast<uint4 *>(out)[i] =
             make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
                        pack_bf16x2(b.z, b.w));

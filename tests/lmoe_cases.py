@@ -41,11 +41,16 @@ class Case:
         host = {n: getattr(L, n).float().cpu().numpy() for n in
                 ("w_down", "w_up", "w_router", "b_router")}
         self._w1, self._w2 = L.w1, L.w2
+        shared = None
+        if dims.shared_ffn:
+            self.dev["ws1"], self.dev["ws2"] = L.ws1.cuda(), L.ws2.cuda()
+            shared = (L.ws1.float().cpu().numpy(), L.ws2.float().cpu().numpy())
         self.ol = oracle.OracleLayer(dims.d, dims.l, dims.E, dims.k, dims.ffn, host["w_down"],
                                      host["w_up"], host["w_router"], host["b_router"],
-                                     self._expert_master)
+                                     self._expert_master, shared=shared)
         xc = lmoe_synth.calibration_tokens(calib_T, dims.d, seed, gen_device).float().cpu().numpy()
         self.amax_z, self.amax_h = self.ol.calibrate(xc)
+        self.amax_xs, self.amax_hs = self.ol.calibrate_shared(xc) if shared else (0.0, 0.0)
         self.moe = None
 
     def _expert_master(self, e):
@@ -57,7 +62,9 @@ class Case:
             D = self.dev
             self.moe = self.lm.LatentMoE(d.d, d.l, d.E, d.k, d.ffn, D["w_down"], D["w_up"],
                                          D["w_router"], D["b_router"], D["w1"], D["w2"],
-                                         self.amax_z, self.amax_h, debug=debug)
+                                         self.amax_z, self.amax_h, debug=debug,
+                                         ws1=D.get("ws1"), ws2=D.get("ws2"),
+                                         amax_xs=self.amax_xs, amax_hs=self.amax_hs)
         return self.moe
 
     def tokens(self, T, seed_offset=0):
