@@ -5,7 +5,8 @@ Workload (one "step" = one whole forward of the layer over one batch):
   headline: decode-size batch, T = 8 tokens at Ultra dims (d = 8192, l = 2048, E = 512,
             top-22, ffn = 2048), uniform routing, NVFP4 experts, BF16 projections;
   also:     prefill, T = 4096 at Ultra dims with a Zipf(1.1) router bias (reported under
-            "prefill").
+            "prefill"), and one long prompt, T = 32768 at Ultra dims plus the FP8 shared expert
+            (d = shared ffn = 8192), uniform routing (reported under "long_shared").
 Inputs are seeded synthetic tensors (lmoe_synth); the static activation scales come from
 tests/golden/calibration.json (the oracle's calibration pass, written by
 tests/golden/make_calibration.py).
@@ -37,6 +38,7 @@ import lmoe_synth  # noqa: E402
 L2_FLUSH_BYTES = 256 << 20
 HEADLINE = "ultra_decode_T8"
 PREFILL = "ultra_prefill_T4096_zipf1.1"
+LONG = "ultra_long_T32768_shared"
 
 
 def args_():
@@ -46,10 +48,14 @@ def args_():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="lmoe", choices=["lmoe", "reference"])
     p.add_argument("--no-prefill", action="store_true")
+    p.add_argument("--no-long", action="store_true")
+    p.add_argument("--long-steps", type=int, default=5)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--prefill-steps", type=int, default=20)
     p.add_argument("--only-prefill", action="store_true",
                    help="profiling aid: build and run only the prefill workload, print its line")
+    p.add_argument("--only-long", action="store_true",
+                   help="profiling aid: build and run only the long-prompt workload, print its line")
     return p.parse_args()
 
 
@@ -190,6 +196,22 @@ def build_layers(names):
     L.w1 = L.w2 = None            # the contexts hold the quantized experts; masters not kept
     torch.cuda.empty_cache()
     return L, out
+
+
+def build_long():
+    """The long-prompt layer with its FP8 shared expert (own weights draw of the same seed)."""
+    import nvfp4_latentmoe_fwd_02_b300 as lm
+    c = lmoe_synth.CONFIGS[LONG]
+    dims = c["dims"]
+    L = lmoe_synth.layer(dims, c["seed"], "cuda", c["zipf"])
+    cal = calibration(LONG)
+    moe = lm.LatentMoE(dims.d, dims.l, dims.E, dims.k, dims.ffn, L.w_down, L.w_up, L.w_router,
+                       L.b_router, L.w1, L.w2, cal["amax_z"], cal["amax_h"], ws1=L.ws1, ws2=L.ws2,
+                       amax_xs=cal["amax_xs"], amax_hs=cal["amax_hs"])
+    torch.cuda.synchronize()
+    del L
+    torch.cuda.empty_cache()
+    return moe
 
 
 class Runner:
@@ -369,9 +391,11 @@ def run_reference(a, dist):
 def workload_config(name):
     c = lmoe_synth.CONFIGS[name]
     d = c["dims"]
+    sh = f", + FP8 shared expert ffn={d.shared_ffn}" if d.shared_ffn else ""
     return {"workload": f"LatentMoE forward, T={c['T']}, d={d.d}, l={d.l}, E={d.E}, top-{d.k}, "
-                        f"ffn={d.ffn}, routing {'uniform' if c['zipf'] == 0 else 'Zipf(%g)' % c['zipf']}",
+                        f"ffn={d.ffn}, routing {'uniform' if c['zipf'] == 0 else 'Zipf(%g)' % c['zipf']}{sh}",
             "T": c["T"], "d": d.d, "l": d.l, "E": d.E, "k": d.k, "ffn": d.ffn,
+            **({"shared_ffn": d.shared_ffn} if d.shared_ffn else {}),
             "routing": "uniform" if c["zipf"] == 0 else f"zipf{c['zipf']}",
             "l2": "flushed before every step (256 MB write + 256 MB read, outside the step's events)",
             "graph": "one CUDA graph replay per step"}
@@ -387,6 +411,50 @@ def roofline_entry(prof, moe, T, pk):
             "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": ncu_traffic(f"{dom}_T{T}"),
             "algorithmic_bytes": eb[dom], "launch_ms": ms,
             "peak_src": f"{pk['src']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"}, eb
+
+
+def long_entry(a, dist, pk):
+    """The long-prompt point: T = 32768 plus the FP8 shared expert."""
+    c = lmoe_synth.CONFIGS[LONG]
+    moe = build_long()
+    T = c["T"]
+    r = Runner(moe, T, c["seed"], pool=2)
+    K = max(3, a.long_steps)
+    with Clocks(torch.cuda.current_device()) as clk:
+        ms = r.timed_steps(K, 3)
+    tot = dist.max(sum(ms))
+    prof = r.profile(reps=2)
+    times = dict(prof)
+    d, FS = moe.d, moe.shared_ffn
+    # per-kernel FLOPs of the contractions (dense math of the definitions)
+    eb = expert_bytes(moe, T)
+    flops = {"shared_up": 2 * T * d * FS, "shared_down": 2 * T * d * FS,
+             "down_proj": 2 * T * d * moe.l, "up_proj": 2 * T * d * moe.l,
+             "expert_up": 2 * eb["slots"] * moe.l * moe.ffn,
+             "expert_down": 2 * eb["slots"] * moe.l * moe.ffn,
+             "router_logits": 2 * T * d * moe.E}
+    ratio = {"shared_up": 2.0, "shared_down": 2.0, "expert_up": 6.0, "expert_down": 6.0,
+             "down_proj": 1.0, "up_proj": 1.0, "router_logits": 1.0}
+    dom = max(flops, key=lambda n: times.get(n, 0.0))
+    ach = flops[dom] / (times[dom] * 1e-3) / 1e12
+    peak = pk["bf16_tflops"] * ratio[dom]
+    dtype = {2.0: "fp8", 6.0: "nvfp4", 1.0: "bf16"}[ratio[dom]]
+    if dom == "router_logits":
+        dtype = "fp32 CUDA cores (bf16 tensor peak as the whole-layer reference)"
+    moe.close()
+    del r
+    torch.cuda.empty_cache()
+    return {
+        "config": workload_config(LONG), "steps": K,
+        "tokens_per_s": T * K * dist.world / (tot * 1e-3), "ms_per_step": tot / K,
+        "per_kernel_ms": {n: round(v, 4) for n, v in prof},
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak,
+                     "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                     "dtype": dtype, "flops_per_launch": flops[dom], "launch_ms": times[dom],
+                     "peak_src": f"{pk['src']} bf16 cuBLAS (MEASURED_PEAKS.json bf16_tflops) x "
+                                 f"{ratio[dom]:g}, the nominal {dtype}/bf16 dense ratio"},
+        "clocks": clk.summary(),
+    }
 
 
 def main():
@@ -406,6 +474,12 @@ def main():
         if dist.rank == 0:
             print(json.dumps({"workload": PREFILL, "ms_per_step": sum(pms) / len(pms),
                               "per_kernel_ms": dict(pr.profile(reps=2))}), flush=True)
+        dist.close()
+        return
+    if a.only_long:
+        e = long_entry(a, dist, pk)
+        if dist.rank == 0:
+            print(json.dumps({"workload": LONG, **e}), flush=True)
         dist.close()
         return
     names = [HEADLINE] + ([] if a.no_prefill else [PREFILL])
@@ -489,6 +563,10 @@ def main():
                              "touched_experts": peb["touched"], "slots": peb["slots"]},
             "clocks": clk2.summary(),
         }
+
+    # ---- long prompt with the shared expert (its own layer and context)
+    if not a.no_long:
+        line["long_shared"] = long_entry(a, dist, pk)
 
     # ---- CPU baseline (rank 0, N = 1)
     if dist.world == 1 and not a.no_cpu_baseline:

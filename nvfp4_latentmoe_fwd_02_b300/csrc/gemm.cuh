@@ -9,9 +9,10 @@
 //     epilogue; NVIDIA AI releases Nemotron 3 Ultra, quantization paragraph).
 // D[m][n] = sum_k A[m][k] * B[n][k]: A = activations (rows = tokens), B = weights (rows = output
 // features); both K-major.  Tile 128 x 128, one SW128 row of 128 bytes per operand per stage
-// (64 bf16, 128 e4m3 or 256 e2m1 elements of K).  A is fetched in 32-row boxes, only as many as the tile
-// has valid rows (a decode tile of one token moves 4 KB of A per stage, not 16 KB); rows past
-// the loaded boxes hold stale data whose accumulator rows the epilogue never reads.
+// (64 bf16, 128 e4m3 or 256 e2m1 elements of K).  A is fetched as one box per column block:
+// 32 rows at decode (a tile of one token moves 4 KB of A per stage, not 16 KB; rows past the
+// box hold stale data whose accumulator rows the epilogue never reads), 128 rows otherwise
+// (one TMA request instead of four: the request count, not the bytes, limited the loads).
 //
 // Warp roles (384 threads, one CTA per SM):
 //   warp 0      TMA producer (one elected lane): operand tiles + scale atoms -> smem ring
@@ -49,7 +50,7 @@ enum EpiMode : int {
 
 constexpr int kBM = 128, kBN = 128;
 constexpr int kTileBytes = kBM * 128;     // 16 KB per operand per stage
-constexpr int kABoxRows = 32;             // A is loaded in 32-row boxes: only the valid rows
+constexpr int kABoxRows = 32;             // decode: A is loaded as one 32-row box per column block
 constexpr int kABoxBytes = kABoxRows * 128;
 constexpr int kSfStageBytes = 4 * 512;    // 4 scale atoms (4 x K64) per operand per stage
 
@@ -314,6 +315,36 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs &g, const Tile &tl
     }
 }
 
+// Combine through shared memory (prefill tiles): the warp parks its 32 rows x 32 scaled values
+// in a 4 KB staging buffer (16-byte chunk c of row r at chunk slot c ^ (r % 8): conflict-free
+// both ways), then reads them back four rows per instruction, so each red.add.v4 instruction
+// covers four whole 128-byte lines of c_acc instead of 32 scattered 16-byte pieces.  Rows of
+// padding (invalid) take part in the exchange but issue no reduction.  Warp-synchronous.
+__device__ __forceinline__ void combine_staged(const GemmArgs &g, const Tile &tl, const EpiRow &er,
+                                               int c0, const uint32_t (&r)[32], float4 *stg,
+                                               int lane) {
+    const float ws = er.wslot, a = er.alpha;
+    float4 *mine = stg + lane * 8;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        mine[c ^ (lane & 7)] = make_float4(__fmul_rn(ws, __fmul_rn(a, __uint_as_float(r[4 * c]))),
+                                           __fmul_rn(ws, __fmul_rn(a, __uint_as_float(r[4 * c + 1]))),
+                                           __fmul_rn(ws, __fmul_rn(a, __uint_as_float(r[4 * c + 2]))),
+                                           __fmul_rn(ws, __fmul_rn(a, __uint_as_float(r[4 * c + 3]))));
+    __syncwarp();
+    const int col = tl.n0 + c0;
+    const int cc = lane & 7;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int rr = it * 4 + (lane >> 3);
+        const float4 v = stg[rr * 8 + (cc ^ (rr & 7))];
+        const int64_t orow = __shfl_sync(0xffffffffu, er.orow, rr);
+        const bool ok = __shfl_sync(0xffffffffu, er.valid ? 1 : 0, rr) != 0;
+        if (ok) red_add_v4_f32(static_cast<float *>(g.out) + orow * g.ld_out + col + 4 * cc, v.x, v.y, v.z, v.w);
+    }
+    __syncwarp();
+}
+
 // KIND: kKindBf16, kKindNvf4 or kKindFp8.  SMALLA (decode): every tile has at most 32 valid A rows, so each column block of a stage
 // keeps only one 4 KB A box; the MMA still reads 128 rows from the block's A base, and rows
 // 32..127 fall on the following boxes (or on the slack after the last one): they only feed
@@ -332,13 +363,16 @@ struct GemmCfg {
     static constexpr int kTmaXPerBlock = KIND == kKindBf16 ? 64 : 128;  // tensor-map x units per block
     static constexpr int kStepsPerBlock = 4;                          // MMA K steps per block
     static constexpr int kSfCols = NVF4 ? 32 * KB : 0;                // TMEM columns per stage
+    static constexpr bool kStagedCombine = NVF4 && !SMALLA;           // combine via smem staging
+    static constexpr int kStgBytes = kStagedCombine ? 8 * 4096 : 0;   // one 4 KB buffer per epilogue warp
 };
 
 template <int KIND, bool SMALLA, int KB>
 constexpr int gemm_smem_bytes(int stages) {
     using C = GemmCfg<KIND, SMALLA, KB>;
     return 1024 + stages * (C::kAStage + C::kBStage + 2 * C::kSfStage) + C::kSlack + 256 +
-           (C::NVF4 ? static_cast<int>(sizeof(SmemTables)) : 0);
+           (C::NVF4 ? static_cast<int>((sizeof(SmemTables) + 15) & ~static_cast<size_t>(15)) : 0) +
+           C::kStgBytes;
 }
 
 constexpr int kEpiWarps = 8;
@@ -365,6 +399,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(cdrain + 2);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     SmemTables *tb = reinterpret_cast<SmemTables *>(bars + 256 / 8);
+    float4 *stg_all = reinterpret_cast<float4 *>(reinterpret_cast<uint8_t *>(tb) +
+                                                 (NVF4 ? ((sizeof(SmemTables) + 15) & ~static_cast<size_t>(15)) : 0));
 
     constexpr uint32_t kAccCols = kBN;
     constexpr uint32_t kTmemCols = NVF4 ? 512 : 256;
@@ -415,22 +451,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t sSFA0 = smem_u32(sSFA), sSFB0 = smem_u32(sSFB);
             for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x) {
                 const Tile tl = decode_tile(g, tb, t);
-                const int nbox = SMALLA ? 1 : (tl.rows + kABoxRows - 1) / kABoxRows;
                 const uint8_t *sfa_tile = NVF4 ? g.sfa + static_cast<size_t>(tl.a_row0 >> 7) * K64 * 512 : nullptr;
                 const uint8_t *sfb_tile = NVF4 ? g.sfb + (static_cast<size_t>(tl.e) * g.NB + (tl.n0 >> 7)) * K64 * 512 : nullptr;
                 for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
                     if (!role_wait(&empty[stage], phase ^ 1, s_abort, g.err)) break;
                     const int kb0 = kt * KB;
                     const int nsteps = NVF4 ? min(4 * KB, K64 - 4 * kb0) : 4 * KB;
-                    const uint32_t bytes = KB * (nbox * kABoxBytes + kTileBytes) + (NVF4 ? 2 * nsteps * 512 : 0);
+                    const uint32_t bytes = KB * (C::kACol + kTileBytes) + (NVF4 ? 2 * nsteps * 512 : 0);
                     uint64_t *fb = &full[stage];
                     mbar_arrive_expect_tx(fb, bytes);
                     const uint32_t a_st = sA0 + stage * C::kAStage, b_st = sB0 + stage * C::kBStage;
 #pragma unroll
                     for (int b = 0; b < KB; ++b) {
                         const int kx = (kb0 + b) * C::kTmaXPerBlock;
-                        for (int j = 0; j < nbox; ++j)
-                            tma_load_2d_u32(a_st + b * C::kACol + j * kABoxBytes, &tmA, fb, kx, tl.a_row0 + j * kABoxRows);
+                        tma_load_2d_u32(a_st + b * C::kACol, &tmA, fb, kx, tl.a_row0);
                         tma_load_2d_u32(b_st + b * kTileBytes, &tmB, fb, kx, tl.b_row0);
                     }
                     if (NVF4) {
@@ -566,7 +600,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     uint32_t r[32];
                     tmem_ld32(taddr + ch * 32, r);
                     tmem_wait_ld();
-                    epilogue_chunk(g, tl, er, row, ch * 32, r);
+                    if (C::kStagedCombine && g.epi == EPI_COMBINE)
+                        combine_staged(g, tl, er, ch * 32, r, stg_all + (warp - kEpiWarp0) * 256, lane);
+                    else
+                        epilogue_chunk(g, tl, er, row, ch * 32, r);
                 }
             }
             tc_fence_before();

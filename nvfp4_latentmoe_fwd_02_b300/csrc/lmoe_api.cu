@@ -731,6 +731,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     __nv_bfloat16 *s_out = static_cast<__nv_bfloat16 *>(at(L.s_out));
     const int d = c->d, l = c->l, E = c->E, k = c->k, F = c->ffn;
     const bool small_a = T <= kSmallAMaxT;   // no GEMM tile then has more than 32 valid rows
+    const uint32_t a_box = small_a ? kABoxRows : kBM;   // rows of the activation TMA box
     if (c->profile) {
         c->nprof = 0;
         cudaEventRecord(c->ev[0], s);
@@ -741,7 +742,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     const bool fork = L.split_down && !c->profile;
     auto down_proj = [&](cudaStream_t ds) -> lmoe_status {
         CUtensorMap tx;
-        if (!make_map(&tx, true, x, d, T, static_cast<uint64_t>(d) * 2, kABoxRows)) return LMOE_ECUDA;
+        if (!make_map(&tx, true, x, d, T, static_cast<uint64_t>(d) * 2, a_box)) return LMOE_ECUDA;
         GemmArgs g = dense_args(static_cast<int>(T), l, d, L.down_splits,
                                 L.split_down ? EPI_RED_F32 : EPI_Z_QUANT, c->err, kb_for(small_a));
         if (L.split_down) {
@@ -806,7 +807,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     // 5. latent-up grouped GEMM + relu^2 + requantize
     {
         CUtensorMap ta;
-        if (!make_map(&ta, false, a_codes, l / 2, L.R, l / 2, kABoxRows)) return LMOE_ECUDA;
+        if (!make_map(&ta, false, a_codes, l / 2, L.R, l / 2, a_box)) return LMOE_ECUDA;
         GemmArgs g;
         std::memset(&g, 0, sizeof(g));
         g.M = static_cast<int>(L.R); g.N = F; g.K = l;
@@ -822,7 +823,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     // 6. latent-down grouped GEMM, routing weight, combine into c_acc
     {
         CUtensorMap ta;
-        if (!make_map(&ta, false, h_codes, F / 2, L.R, F / 2, kABoxRows)) return LMOE_ECUDA;
+        if (!make_map(&ta, false, h_codes, F / 2, L.R, F / 2, a_box)) return LMOE_ECUDA;
         GemmArgs g;
         std::memset(&g, 0, sizeof(g));
         g.M = static_cast<int>(L.R); g.N = l; g.K = F;
@@ -852,7 +853,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
                              static_cast<const unsigned *>(nullptr), xs_q));
         prof_mark(c, "shared_quant_x", s);
         CUtensorMap txs, ths;
-        if (!make_map(&txs, false, xs_q, d, T, d, kABoxRows) || !make_map(&ths, false, hs_q, FS, T, FS, kABoxRows))
+        if (!make_map(&txs, false, xs_q, d, T, d, a_box) || !make_map(&ths, false, hs_q, FS, T, FS, a_box))
             return LMOE_ECUDA;
         GemmArgs g1 = dense_args(static_cast<int>(T), FS, d, 1, EPI_FP8_SQRELU, c->err, kb_for(small_a), 128);
         g1.alpha_s = c->alpha_s1; g1.s_enc8 = c->s_enc_hs; g1.q_codes = hs_q; g1.dbg = hs_dbg;
@@ -869,7 +870,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     // 8. up-projection y = c Wu^T (+ s)
     {
         CUtensorMap tc;
-        if (!make_map(&tc, true, cb, l, T, static_cast<uint64_t>(l) * 2, kABoxRows)) return LMOE_ECUDA;
+        if (!make_map(&tc, true, cb, l, T, static_cast<uint64_t>(l) * 2, a_box)) return LMOE_ECUDA;
         GemmArgs g = dense_args(static_cast<int>(T), d, l, L.up_splits,
                                 L.split_up ? EPI_RED_F32 : EPI_STORE_BF16, c->err, kb_for(small_a));
         g.out = L.split_up ? static_cast<void *>(yacc) : y;
