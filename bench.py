@@ -432,15 +432,13 @@ def long_entry(a, dist, pk):
              "down_proj": 2 * T * d * moe.l, "up_proj": 2 * T * d * moe.l,
              "expert_up": 2 * eb["slots"] * moe.l * moe.ffn,
              "expert_down": 2 * eb["slots"] * moe.l * moe.ffn,
-             "router_logits": 2 * T * d * moe.E}
+             "router_approx": 2 * T * 2 * d * moe.E}
     ratio = {"shared_up": 2.0, "shared_down": 2.0, "expert_up": 6.0, "expert_down": 6.0,
-             "down_proj": 1.0, "up_proj": 1.0, "router_logits": 1.0}
+             "down_proj": 1.0, "up_proj": 1.0, "router_approx": 1.0}
     dom = max(flops, key=lambda n: times.get(n, 0.0))
     ach = flops[dom] / (times[dom] * 1e-3) / 1e12
     peak = pk["bf16_tflops"] * ratio[dom]
     dtype = {2.0: "fp8", 6.0: "nvfp4", 1.0: "bf16"}[ratio[dom]]
-    if dom == "router_logits":
-        dtype = "fp32 CUDA cores (bf16 tensor peak as the whole-layer reference)"
     moe.close()
     del r
     torch.cuda.empty_cache()

@@ -80,7 +80,7 @@ typedef struct {
 /* Create a layer context: validates the dims, allocates the context buffers, quantizes every
  * expert matrix to NVFP4 (one FP32 tensor scale per expert per matrix, computed from its amax)
  * and lays the block scales out for the tensor cores; synchronizes `stream` once at the end.
- * Dims: d, l and ffn multiples of 64; l <= 4096; 1 <= k <= 32; k <= E <= 1024; E % 4 == 0;
+ * Dims: d, l and ffn multiples of 64; d <= 16384; l <= 4096; 1 <= k <= 32; k <= E <= 1024; E % 4 == 0;
  * with a shared expert, shared_ffn a multiple of 64 and amax_xs, amax_hs > 0.
  * (The Ultra layer: d = 8192, l = 2048, E = 512, k = 22; ffn is not given by the pages.)
  * Errors: LMOE_EINVAL (dims / NULL pointers / amax <= 0), LMOE_ENOMEM, LMOE_ECUDA,
@@ -116,9 +116,13 @@ lmoe_status lmoe_quantize_fp8(const void *src, lmoe_dtype dt, int64_t n, float a
  *   idx     device int32 [T][k]  selected experts, ascending expert id per token
  *   w       device float [T][k]  softmax over the k selected logits, same order as idx
  *   counts  device int32 [E]     tokens per expert (may be NULL)
- * Logits are computed in the canonical fp32 order (64-element fma chunks; chunk partials added
- * left to right in groups of 16; group sums added left to right; then the bias), so idx and
- * counts are exact.  Uses context-owned scratch
+ * The selection is the one the canonical fp32 logits make (64-element fma chunks; chunk
+ * partials added left to right in groups of 16; group sums added left to right; then the
+ * bias), so idx and counts are exact.  T <= 64: every canonical logit is computed.  T > 64:
+ * tensor-core logits (bf16 hi/lo split of the weights, fp32 accumulation) bound every canonical
+ * logit within a certified margin, and the canonical logits of the candidates the margin
+ * leaves undecided are computed exactly; w is then the softmax of the selected logits as known
+ * (canonical where computed, tensor-core otherwise: within about 1e-5 relative).  Uses context-owned scratch
  * (grown with cudaMallocAsync on first use for a larger T).  T >= 0. */
 lmoe_status lmoe_route(lmoe_ctx *ctx, const void *x, int64_t T, int32_t *idx, float *w,
                        int32_t *counts, lmoe_stream stream);
@@ -185,7 +189,9 @@ typedef enum {
     LMOE_STAGE_XS_Q = 12,    /* uint8 [T][d]      shared expert: E4M3 codes of x        */
     LMOE_STAGE_HS = 13,      /* bf16  [T][shared_ffn] shared expert h, debug mode only   */
     LMOE_STAGE_HS_Q = 14,    /* uint8 [T][shared_ffn] shared expert: E4M3 codes of h     */
-    LMOE_STAGE_S = 15        /* bf16  [T][d]      shared expert output s                */
+    LMOE_STAGE_S = 15,       /* bf16  [T][d]      shared expert output s                */
+    LMOE_STAGE_ROUTER = 16   /* fp32  router scratch: T > 64: tensor-core logits [T][E]
+                                without the bias; T <= 64: group sums [T][d/1024][E]   */
 } lmoe_stage;
 lmoe_status lmoe_workspace_range(const lmoe_ctx *ctx, int64_t T, int stage, size_t *offset,
                                  size_t *bytes);

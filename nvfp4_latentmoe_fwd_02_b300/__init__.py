@@ -23,6 +23,7 @@ LMOE_BF16, LMOE_FP32 = 0, 1
 STAGES = {
     "idx": 0, "w": 1, "counts": 2, "zq_codes": 3, "zq_sf": 4, "c": 5, "z": 6, "rows": 7, "h": 8,
     "hq_codes": 9, "hq_sf": 10, "nrows": 11, "xs_q": 12, "hs": 13, "hs_q": 14, "s": 15,
+    "router": 16,
 }
 
 

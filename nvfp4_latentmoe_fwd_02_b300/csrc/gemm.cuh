@@ -85,6 +85,7 @@ struct GemmArgs {
     float alpha_s;
     float s_enc8;
     const __nv_bfloat16 *addend; // EPI_STORE_BF16: bf16 [M][ld_out] added before the rounding
+    int a_kwrap;                 // > 0: A's K coordinate wraps at this many elements (B is K-concatenated)
     unsigned *err;
 };
 
@@ -246,9 +247,11 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs &g, const Tile &tl
         break;
     }
     case EPI_RED_F32: {
+        // columns past the tile's valid ones (N % 32 != 0, e.g. N = E experts) are skipped
         float *o = static_cast<float *>(g.out) + grow * g.ld_out + col;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) red_add_v4_f32(o + 4 * i, v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        for (int i = 0; i < 8; ++i)
+            if (c0 + 4 * i < tl.cols) red_add_v4_f32(o + 4 * i, v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         break;
     }
     case EPI_Z_QUANT:
@@ -464,7 +467,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                     for (int b = 0; b < KB; ++b) {
                         const int kx = (kb0 + b) * C::kTmaXPerBlock;
-                        tma_load_2d_u32(a_st + b * C::kACol, &tmA, fb, kx, tl.a_row0);
+                        const int kxa = g.a_kwrap > 0 ? kx % g.a_kwrap : kx;
+                        tma_load_2d_u32(a_st + b * C::kACol, &tmA, fb, kxa, tl.a_row0);
                         tma_load_2d_u32(b_st + b * kTileBytes, &tmB, fb, kx, tl.b_row0);
                     }
                     if (NVF4) {

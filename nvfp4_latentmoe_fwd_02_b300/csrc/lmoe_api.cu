@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -109,7 +110,13 @@ struct lmoe_ctx {
     int d, l, E, k, ffn;
     int dev, num_sms;
     __nv_bfloat16 *w_down, *w_up;
-    float *w_router, *b_router;   // w_router transposed: [d][E]
+    float *w_router, *b_router;   // w_router transposed: [d][E] (small-T router)
+    // large-T router: bf16 planes [E][2d] (hi | lo) for the tensor-core logits, fp32 rows [E][d]
+    // for the canonical recompute, per-expert norm bounds; host copies of max norm and max |b|
+    __nv_bfloat16 *w_split;
+    float *w_rows, *wnorm;
+    float wn_max, bmax;
+    CUtensorMap tm_wsplit;
     uint8_t *w1_codes, *w1_sf, *w2_codes, *w2_sf;
     float *w1_sdec, *w2_sdec, *alpha1, *alpha2;
     unsigned *amax_bits;   // [2E]
@@ -275,8 +282,10 @@ lmoe_status check_error_word(lmoe_ctx *c) {
     return LMOE_OK;
 }
 
-// The router on x: chunk partials (small T) or logits (large T) into `scratch`, then top-k,
-// softmax and counts.
+// The router on x.  Small T: canonical chunk-group sums into `scratch`, then top-k, softmax and
+// counts; the first kernel also clears the ranges in `zr`.  Large T: a clearing kernel (zr and
+// the logits), tensor-core logits into `scratch` (bf16 hi/lo planes of the weights, K split
+// over the SMs, fp32 reductions), then the certified selection against the canonical order.
 lmoe_status launch_router(lmoe_ctx *c, const __nv_bfloat16 *x, int64_t T, float *scratch,
                           int32_t *idx, float *w, int32_t *counts, int32_t *slot_off,
                           const ZeroRanges &zr, cudaStream_t s) {
@@ -288,18 +297,43 @@ lmoe_status launch_router(lmoe_ctx *c, const __nv_bfloat16 *x, int64_t T, float 
                              dim3(static_cast<unsigned>(cdiv(c->E, kSmallEG)), static_cast<unsigned>(cdiv(C, kSmallCG))),
                              dim3(kSmallEG * kSmallCG), kRouterSmallSmem, s, x,
                              static_cast<const float *>(c->w_router), static_cast<int>(T), c->d, c->E, scratch, zr));
-    } else {
-        dim3 grid(static_cast<unsigned>(cdiv(T, kRT)), static_cast<unsigned>(cdiv(c->E, kRE)));
-        LMOE_CUDA(launch_pdl(router_logits_kernel, grid, dim3(128), kRouterLogitsSmem, s, x,
-                             static_cast<const float *>(c->w_router), static_cast<const float *>(c->b_router),
-                             static_cast<int>(T), c->d, c->E, scratch, zr));
+        prof_mark(c, "router_small", s);
+        LMOE_CUDA(launch_pdl(router_topk_kernel, dim3(static_cast<unsigned>(T)), dim3(kTopkThreads), 0, s,
+                             static_cast<const float *>(scratch), NG, static_cast<const float *>(c->b_router),
+                             static_cast<int>(T), c->E, c->k, idx, w, counts, slot_off));
+        prof_mark(c, "router_topk", s);
+        return LMOE_OK;
     }
-    prof_mark(c, small ? "router_small" : "router_logits", s);
-    LMOE_CUDA(launch_pdl(router_topk_kernel, dim3(static_cast<unsigned>(T)), dim3(kTopkThreads), 0, s,
-                         static_cast<const float *>(scratch), small ? NG : 0,
-                         static_cast<const float *>(small ? c->b_router : nullptr), static_cast<int>(T), c->E,
-                         c->k, idx, w, counts, slot_off));
-    prof_mark(c, "router_topk", s);
+    ZeroRanges z = zr;
+    int free_slot = -1;
+    for (int i = 0; i < kZeroRanges; ++i)
+        if (!z.p[i] && free_slot < 0) free_slot = i;
+    if (free_slot < 0) return LMOE_EINVAL;
+    z.p[free_slot] = reinterpret_cast<uint4 *>(scratch);
+    z.n16[free_slot] = T * c->E * 4 / 16;
+    LMOE_CUDA(launch_pdl(zero_kernel, dim3(c->num_sms * 2), dim3(256), 0, s, z));
+    prof_mark(c, "router_zero", s);
+    const int d = c->d, E = c->E;
+    CUtensorMap tx;
+    if (!make_map(&tx, true, x, d, T, static_cast<uint64_t>(d) * 2, kBM)) return LMOE_ECUDA;
+    const int m_tiles = static_cast<int>(cdiv(T, kBM)), n_tiles = static_cast<int>(cdiv(E, kBN));
+    const int k_tiles = 2 * d / 64;
+    const int splits = std::min<int>(k_tiles, std::max<int>(8, static_cast<int>(cdiv(2 * c->num_sms, int64_t(m_tiles) * n_tiles))));
+    GemmArgs g = dense_args(static_cast<int>(T), E, 2 * d, splits, EPI_RED_F32, c->err, 1);
+    g.out = scratch;
+    g.ld_out = E;
+    g.a_kwrap = d;
+    LMOE_CUDA((launch_gemm<kKindBf16>(tx, c->tm_wsplit, g, grid_for(int64_t(g.m_tiles) * g.n_tiles * g.k_splits, c->num_sms),
+                                      false, s)));
+    prof_mark(c, "router_approx", s);
+    // accumulation bound: per K-slice 4 block steps per k-tile (+2), plus the fp32 sum of the
+    // slices, each within 2^-23 of the running magnitude; times a margin of 4
+    const float coef = 4.0f * static_cast<float>(4 * g.kt_per_split + 2 + g.k_splits) * 0x1p-23f;
+    LMOE_CUDA(launch_pdl(router_select_kernel, dim3(static_cast<unsigned>(T)), dim3(kSelThreads),
+                         router_select_smem(d), s, static_cast<const float *>(scratch),
+                         static_cast<const float *>(c->b_router), x, static_cast<const float *>(c->w_rows),
+                         static_cast<int>(T), d, E, c->k, coef, c->wn_max, c->bmax, idx, w, counts, slot_off));
+    prof_mark(c, "router_select", s);
     return LMOE_OK;
 }
 
@@ -435,7 +469,7 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
     *out = nullptr;
     if (!w || !w->w_down || !w->w_up || !w->w_router || !w->w1 || !w->w2) return LMOE_EINVAL;
     if (d <= 0 || l <= 0 || ffn <= 0 || d % 64 || l % 64 || ffn % 64) return LMOE_EINVAL;
-    if (l > 4096) return LMOE_EINVAL;
+    if (l > 4096 || d > kSelMaxD) return LMOE_EINVAL;
     if (k < 1 || k > 32 || E < k || E > 1024 || E % 4) return LMOE_EINVAL;
     if (!(w->amax_z > 0.0f) || !(w->amax_h > 0.0f)) return LMOE_EINVAL;
     const bool has_shared = w->ws1 != nullptr;
@@ -458,8 +492,8 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
             if (b == cudaSuccess) b = set_smem_attr<kKindBf16, true, 2, kStagesBF16Small>();
             if (a == cudaSuccess) a = set_smem_attr<kKindFp8, false, 1, kStagesF8>();
             if (a == cudaSuccess) a = set_smem_attr<kKindFp8, true, 2, kStagesF8Small>();
-            cudaError_t r = cudaFuncSetAttribute(router_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 kRouterLogitsSmem);
+            cudaError_t r = cudaFuncSetAttribute(router_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 router_select_smem(kSelMaxD));
             if (r == cudaSuccess)
                 r = cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kRouterSmallSmem);
@@ -491,6 +525,9 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
     CREATE_CUDA(cudaMalloc(&c->w_up, static_cast<size_t>(d) * l * 2));
     CREATE_CUDA(cudaMalloc(&c->w_router, static_cast<size_t>(E) * d * 4));
     CREATE_CUDA(cudaMalloc(&c->b_router, static_cast<size_t>(E) * 4));
+    CREATE_CUDA(cudaMalloc(&c->w_split, static_cast<size_t>(E) * 2 * d * 2));
+    CREATE_CUDA(cudaMalloc(&c->w_rows, static_cast<size_t>(E) * d * 4));
+    CREATE_CUDA(cudaMalloc(&c->wnorm, static_cast<size_t>(E) * 4));
     CREATE_CUDA(cudaMalloc(&c->w1_codes, static_cast<size_t>(E) * ffn * l / 2));
     CREATE_CUDA(cudaMalloc(&c->w2_codes, static_cast<size_t>(E) * l * ffn / 2));
     CREATE_CUDA(cudaMalloc(&c->w1_sf, w1_sf_bytes));
@@ -514,6 +551,9 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
         CREATE_CUDA(cudaMemcpyAsync(c->b_router, w->b_router, E * 4, cudaMemcpyDeviceToDevice, s));
     else
         CREATE_CUDA(cudaMemsetAsync(c->b_router, 0, E * 4, s));
+    CREATE_CUDA(cudaMemcpyAsync(c->w_rows, w->w_router, static_cast<size_t>(E) * d * 4, cudaMemcpyDeviceToDevice, s));
+    router_split_kernel<<<E, 256, 0, s>>>(c->w_rows, E, d, c->w_split, c->wnorm);
+    CREATE_CUDA(cudaGetLastError());
     CREATE_CUDA(cudaMemsetAsync(c->w1_sf, 0, w1_sf_bytes, s));
     CREATE_CUDA(cudaMemsetAsync(c->w2_sf, 0, w2_sf_bytes, s));
     CREATE_CUDA(cudaMemsetAsync(c->amax_bits, 0, 2 * E * 4, s));
@@ -545,6 +585,21 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
         cudaError_t e4 = cudaMemcpy(c->alpha2, a2, E * 4, cudaMemcpyHostToDevice);
         delete[] sd1; delete[] sd2; delete[] a1; delete[] a2;
         for (cudaError_t e : {e1, e2, e3, e4})
+            if (e != cudaSuccess) return fail(cuda_status(e));
+    }
+    // large-T router: the largest expert norm bound and the largest |bias|
+    {
+        float *wn = new float[E], *bb = new float[E];
+        cudaError_t e1 = cudaMemcpy(wn, c->wnorm, E * 4, cudaMemcpyDeviceToHost);
+        cudaError_t e2 = cudaMemcpy(bb, c->b_router, E * 4, cudaMemcpyDeviceToHost);
+        c->wn_max = 0.0f;
+        c->bmax = 0.0f;
+        for (int e = 0; e < E; ++e) {
+            c->wn_max = std::max(c->wn_max, wn[e]);
+            c->bmax = std::max(c->bmax, std::fabs(bb[e]));
+        }
+        delete[] wn; delete[] bb;
+        for (cudaError_t e : {e1, e2})
             if (e != cudaSuccess) return fail(cuda_status(e));
     }
     // shared expert: per-matrix amax, FP8 E4M3 codes, and the fp32 scale products
@@ -584,7 +639,8 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
             !make_map(&c->tm_ws2, false, c->ws2_codes, FS, d, FS))
             return fail(LMOE_ECUDA);
     }
-    bool ok = make_map(&c->tm_wd, true, c->w_down, d, l, static_cast<uint64_t>(d) * 2) &&
+    bool ok = make_map(&c->tm_wsplit, true, c->w_split, 2 * d, E, static_cast<uint64_t>(2 * d) * 2) &&
+              make_map(&c->tm_wd, true, c->w_down, d, l, static_cast<uint64_t>(d) * 2) &&
               make_map(&c->tm_wu, true, c->w_up, l, d, static_cast<uint64_t>(l) * 2) &&
               make_map(&c->tm_w1, false, c->w1_codes, l / 2, static_cast<uint64_t>(E) * ffn, l / 2) &&
               make_map(&c->tm_w2, false, c->w2_codes, ffn / 2, static_cast<uint64_t>(E) * l, ffn / 2);
@@ -599,7 +655,8 @@ void lmoe_destroy(lmoe_ctx *c) {
     cudaDeviceSynchronize();
     void *ptrs[] = {c->w_down, c->w_up, c->w_router, c->b_router, c->w1_codes, c->w1_sf,
                     c->w2_codes, c->w2_sf, c->w1_sdec, c->w2_sdec, c->alpha1, c->alpha2,
-                    c->amax_bits, c->err, c->route_ws, c->ws1_codes, c->ws2_codes};
+                    c->amax_bits, c->err, c->route_ws, c->ws1_codes, c->ws2_codes, c->w_split,
+                    c->w_rows, c->wnorm};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     for (cudaEvent_t e : c->ev)
@@ -660,6 +717,7 @@ lmoe_status lmoe_workspace_range(const lmoe_ctx *c, int64_t T, int stage, size_t
     case LMOE_STAGE_HS: *offset = L.hs_dbg; *bytes = c->debug ? T * c->shared_ffn * 2 : 0; break;
     case LMOE_STAGE_HS_Q: *offset = L.hs_q; *bytes = T * c->shared_ffn; break;
     case LMOE_STAGE_S: *offset = L.s_out; *bytes = c->shared_ffn ? T * c->d * 2 : 0; break;
+    case LMOE_STAGE_ROUTER: *offset = L.router; *bytes = route_scratch_bytes(c, T); break;
     default: return LMOE_EINVAL;
     }
     return LMOE_OK;
@@ -941,11 +999,11 @@ lmoe_status lmoe_get_shared_fp8(const lmoe_ctx *c, int which, uint8_t *codes, fl
 int lmoe_forward_kernel_count(const lmoe_ctx *c, int64_t T) {
     if (!c || T <= 0) return 0;
     const WsLayout L = layout(c, T);
-    // router logits, top-k, segments, down-proj, expert-up, expert-down, combine cast,
-    // up-proj, plus one finalize per split projection (and, for a split down-projection run
+    // router (small T: chunk sums, top-k; large T: clearing, tensor-core logits, selection),
+    // segments, down-proj, expert-up, expert-down, combine cast, up-proj, plus one finalize per split projection (and, for a split down-projection run
     // beside the router, the clearing of its accumulator), plus the shared expert's
     // quantization of x and its two GEMMs
-    return 8 + (L.split_down ? 2 : 0) + (L.split_up ? 1 : 0) + (c->shared_ffn ? 3 : 0);
+    return 8 + (T > kSmallMaxT ? 1 : 0) + (L.split_down ? 2 : 0) + (L.split_up ? 1 : 0) + (c->shared_ffn ? 3 : 0);
 }
 
 lmoe_status lmoe_set_profile(lmoe_ctx *c, int on) {

@@ -6,15 +6,16 @@
 //   the d axis is cut into chunks of 64; p_c = fmaf chain over the chunk in ascending index
 //   starting from +0; chunks form groups of 16; a group sum is ((0 + p_c0) + p_c0+1) + ...
 //   over its chunks; logit = ((0 + G_0) + G_1) + ... over the groups; then + bias.
-// The router weights are kept transposed, Wt[d][E], so that consecutive experts are
-// consecutive in memory (coalesced loads for threads that own one expert each).
-// Two paths produce exactly these fp32 operations:
-//   small T  router_small_kernel computes the group sums G_g(t, e) into G[t][g][e] (a block
-//            owns one group of 16 chunks); the top-k kernel adds them in ascending g and the
-//            bias;
-//   large T  router_logits_kernel: register-tiled, each thread walks the chunks in order.
 // Selection: logit descending, lower expert index first on ties.  Weights: softmax (fp32,
 // expf) over the k selected logits.  Output slots are in ascending expert id.
+// Two paths give exactly the selection of these fp32 operations:
+//   small T  (memory bound: the weights are streamed once) router_small_kernel computes the
+//            group sums G_g(t, e) into G[t][g][e] from the transposed weights Wt[d][E]
+//            (consecutive experts consecutive in memory; a block owns one group of 16 chunks);
+//            router_topk_kernel adds them in ascending g, adds the bias and selects;
+//   large T  (compute bound) tensor-core logits from bf16 hi/lo planes of the weights bound
+//            every canonical logit within a certified margin; router_select_kernel decides
+//            what the margin leaves open with canonical logits computed on the spot (below).
 #pragma once
 #include "common.cuh"
 
@@ -25,15 +26,16 @@ constexpr int kChunk = 64;
 // Buffers the first kernel of a forward clears (up to four ranges of 16-byte words), so that
 // no separate clearing launch is needed: the expert histogram before the top-k kernel counts
 // into it, and the fp32 accumulators before the GEMMs reduce into them.
+constexpr int kZeroRanges = 6;
 struct ZeroRanges {
-    uint4 *p[4];
-    int64_t n16[4];
+    uint4 *p[kZeroRanges];
+    int64_t n16[kZeroRanges];
 };
 __device__ __forceinline__ void zero_ranges(const ZeroRanges &z) {
     const int64_t nthreads = (int64_t)gridDim.x * gridDim.y * blockDim.x;
     const int64_t tid = ((int64_t)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int r = 0; r < kZeroRanges; ++r)
         for (int64_t i = tid; i < z.n16[r]; i += nthreads) z.p[r][i] = make_uint4(0, 0, 0, 0);
 }
 __global__ void zero_kernel(ZeroRanges z) {
@@ -109,151 +111,6 @@ __global__ void __launch_bounds__(kSmallEG * kSmallCG) router_small_kernel(
             float gs = 0.0f;
             for (int q = 0; q < ncg; ++q) gs = __fadd_rn(gs, ps[(tt * kSmallCG + q) * kSmallEG + lane]);
             G[(static_cast<int64_t>(t0 + tt) * ng + blockIdx.y) * E + e] = gs;
-        }
-    }
-}
-
-// Large T: logits[t][e] (bias added).  Tile 128 tokens x 64 experts per block of 128 threads,
-// each thread 8 tokens x 8 experts.  Each 64-element chunk is staged through shared memory in
-// two halves of 32 (double-buffered: the next half's global loads are in flight while the
-// current half is multiplied); the per-chunk fma chain runs across both halves before it is
-// added to acc.  The fmas are issued as fma.rn.f32x2 on expert pairs: two independent IEEE
-// fp32 fmas, so every (t, e) chain is exactly the scalar canonical one.  Dynamic smem.
-constexpr int kRT = 128, kRE = 64, kHalf = 32;
-constexpr int kXsStride = kRT + 4, kWsStride = kRE + 4;
-constexpr int kRouterLogitsSmem = 2 * kHalf * (kXsStride + kWsStride) * 4 + 128 * 64 * 4;
-
-__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-
-__global__ void __launch_bounds__(128) router_logits_kernel(
-    const __nv_bfloat16 *__restrict__ x, const float *__restrict__ Wt,
-    const float *__restrict__ bias, int T, int d, int E, float *__restrict__ logits, ZeroRanges zr) {
-    pdl_wait();
-    pdl_trigger();
-    zero_ranges(zr);
-    extern __shared__ __align__(16) float rl_smem[];
-    float *xs = rl_smem;                              // [2][kHalf][kXsStride]
-    float *ws = rl_smem + 2 * kHalf * kXsStride;      // [2][kHalf][kWsStride]
-    float4 *gsum = reinterpret_cast<float4 *>(ws + 2 * kHalf * kWsStride) + threadIdx.x;   // [16][128] float4: this thread's group sums
-    const int tid = threadIdx.x;
-    const int ty = tid >> 3, tx = tid & 7;
-    const int t_base = blockIdx.x * kRT, e_base = blockIdx.y * kRE;
-    float acc[8][8];
-    uint64_t p[8][4];
-#pragma unroll
-    for (int a = 0; a < 8; ++a)
-#pragma unroll
-        for (int b = 0; b < 8; ++b) acc[a][b] = 0.0f;
-#pragma unroll
-    for (int m = 0; m < 16; ++m) gsum[m * 128] = make_float4(0.f, 0.f, 0.f, 0.f);
-    uint4 xr[4];
-    float4 wr[4];
-    auto load = [&](int h) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int i = tid + 128 * j;            // x: 128 tokens x 4 uint4
-            const int t = i >> 2, q = i & 3;
-            xr[j] = t_base + t < T ? __ldg(reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(t_base + t) * d + h * kHalf + q * 8))
-                                   : make_uint4(0, 0, 0, 0);
-            const int r = i >> 4, qe = i & 15;      // Wt: 32 rows x 16 float4 of 4 experts
-            wr[j] = e_base + qe * 4 < E ? __ldg(reinterpret_cast<const float4 *>(Wt + static_cast<int64_t>(h * kHalf + r) * E + e_base + qe * 4))
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    };
-    auto store = [&](int buf) {
-        float *X = xs + buf * kHalf * kXsStride;
-        float *W = ws + buf * kHalf * kWsStride;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int i = tid + 128 * j;
-            const int t = i >> 2, q = i & 3;
-            const uint32_t ww[4] = {xr[j].x, xr[j].y, xr[j].z, xr[j].w};
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                X[(q * 8 + 2 * m) * kXsStride + t] = __uint_as_float(ww[m] << 16);
-                X[(q * 8 + 2 * m + 1) * kXsStride + t] = __uint_as_float(ww[m] & 0xFFFF0000u);
-            }
-            const int r = i >> 4, qe = i & 15;
-            *reinterpret_cast<float4 *>(W + r * kWsStride + qe * 4) = wr[j];
-        }
-    };
-    const int H = d / kHalf;
-    load(0);
-    store(0);
-    __syncthreads();
-    for (int h = 0; h < H; ++h) {
-        const int buf = h & 1;
-        if (h + 1 < H) load(h + 1);
-        if ((h & 1) == 0) {
-#pragma unroll
-            for (int a = 0; a < 8; ++a)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) p[a][q] = 0ull;
-        }
-        const float *X = xs + buf * kHalf * kXsStride;
-        const float *W = ws + buf * kHalf * kWsStride;
-#pragma unroll 4
-        for (int i = 0; i < kHalf; ++i) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(X + i * kXsStride + ty * 8);
-            const float4 a1 = *reinterpret_cast<const float4 *>(X + i * kXsStride + ty * 8 + 4);
-            const float4 b0 = *reinterpret_cast<const float4 *>(W + i * kWsStride + tx * 8);
-            const float4 b1 = *reinterpret_cast<const float4 *>(W + i * kWsStride + tx * 8 + 4);
-            const uint64_t bp[4] = {pack2(b0.x, b0.y), pack2(b0.z, b0.w), pack2(b1.x, b1.y), pack2(b1.z, b1.w)};
-            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-#pragma unroll
-            for (int a = 0; a < 8; ++a) {
-                const uint64_t aa = pack2(av[a], av[a]);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) p[a][q] = ffma2(aa, bp[q], p[a][q]);
-            }
-        }
-        if (h & 1) {
-            // chunk done: add it to the group sum; at a group's end add that to acc
-            const int chunk = h >> 1;
-            const bool group_end = ((chunk + 1) % kGroupChunks == 0) || (h + 1 == H);
-#pragma unroll
-            for (int a = 0; a < 8; ++a) {
-                float4 g0 = gsum[(2 * a) * 128], g1 = gsum[(2 * a + 1) * 128];
-                float lo, hi;
-                unpack2(p[a][0], lo, hi); g0.x = __fadd_rn(g0.x, lo); g0.y = __fadd_rn(g0.y, hi);
-                unpack2(p[a][1], lo, hi); g0.z = __fadd_rn(g0.z, lo); g0.w = __fadd_rn(g0.w, hi);
-                unpack2(p[a][2], lo, hi); g1.x = __fadd_rn(g1.x, lo); g1.y = __fadd_rn(g1.y, hi);
-                unpack2(p[a][3], lo, hi); g1.z = __fadd_rn(g1.z, lo); g1.w = __fadd_rn(g1.w, hi);
-                if (group_end) {
-                    acc[a][0] = __fadd_rn(acc[a][0], g0.x); acc[a][1] = __fadd_rn(acc[a][1], g0.y);
-                    acc[a][2] = __fadd_rn(acc[a][2], g0.z); acc[a][3] = __fadd_rn(acc[a][3], g0.w);
-                    acc[a][4] = __fadd_rn(acc[a][4], g1.x); acc[a][5] = __fadd_rn(acc[a][5], g1.y);
-                    acc[a][6] = __fadd_rn(acc[a][6], g1.z); acc[a][7] = __fadd_rn(acc[a][7], g1.w);
-                    g0 = make_float4(0.f, 0.f, 0.f, 0.f);
-                    g1 = g0;
-                }
-                gsum[(2 * a) * 128] = g0;
-                gsum[(2 * a + 1) * 128] = g1;
-            }
-        }
-        if (h + 1 < H) store(buf ^ 1);
-        __syncthreads();
-    }
-#pragma unroll
-    for (int a = 0; a < 8; ++a) {
-        const int t = t_base + ty * 8 + a;
-        if (t >= T) continue;
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const int e = e_base + tx * 8 + b;
-            if (e < E) logits[static_cast<int64_t>(t) * E + e] = __fadd_rn(acc[a][b], bias ? bias[e] : 0.0f);
         }
     }
 }
@@ -400,6 +257,246 @@ __global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(
             if (slot_off) slot_off[static_cast<int64_t>(t) * k + rank] = off;
         }
     }
+}
+
+// ------------------------------------------------------------------------------------
+// Large T: selection certified against the canonical order, with tensor-core logits.
+//
+// A bf16 tensor-core GEMM gives approximate logits a = x (Whi + Wlo)^T, where Whi = bf16(w)
+// and Wlo = bf16(w - Whi) (w - Whi - Wlo is at most 2^-18 |w|), accumulated in fp32 over
+// `splits` K-slices and summed with fp32 reductions.  For token t every |a_e + b_e -
+// canonical_e| is at most delta_t = |x_t| max_e |w_e| (coef + 2^-16) + 2^-22 max|b|: coef
+// bounds the tensor-core accumulation (1024 block steps at d = 8192 split 8 ways, each within
+// 2^-23 of the running magnitude, times a margin of 4), 2^-16 the split and the canonical
+// order's own rounding (at most 88 roundings of 2^-24), Cauchy-Schwarz bounds sum |x_i w_i|.
+// Then, with a_(k) the k-th largest approximate logit:
+//   * the true top-k lies inside U = { e : a_e >= a_(k) - 2 delta };
+//   * e in U is certainly selected when at most k - 1 others have a_f >= a_e - 2 delta;
+//   * the rest of U is decided by exact canonical logits computed here (one warp each).
+// Should U not fit in the sorted top 32, or the counts not add up, the block computes every
+// canonical logit of the token and selects from those.  The routing weights are the softmax
+// over the selected logits as known here (canonical where computed, otherwise a + b).
+// ------------------------------------------------------------------------------------
+
+// Whi / Wlo planes [E][2d] (row e: Whi then Wlo) and an upper bound of |w_e| per expert.
+// One block per expert.
+__global__ void router_split_kernel(const float *__restrict__ W, int E, int d,
+                                    __nv_bfloat16 *__restrict__ wsplit, float *__restrict__ wnorm) {
+    __shared__ double part[8];
+    const int e = blockIdx.x;
+    const float *w = W + static_cast<int64_t>(e) * d;
+    __nv_bfloat16 *o = wsplit + static_cast<int64_t>(e) * 2 * d;
+    double ss = 0.0;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) {
+        const float v = w[i];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(__fsub_rn(v, __bfloat162float(hi)));
+        o[i] = hi;
+        o[d + i] = lo;
+        ss += static_cast<double>(v) * static_cast<double>(v);
+    }
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) t += part[i];
+        wnorm[e] = __fmul_ru(__double2float_ru(sqrt(t)), 1.0f + 0x1p-20f);
+    }
+}
+
+constexpr int kSelThreads = 256;
+constexpr int kSelMaxD = 16384;
+__host__ __device__ constexpr int router_select_smem(int d) {
+    return (d / kChunk) * (kChunk + 1) * 4 + 8 * (d / kChunk) * 4;
+}
+
+// The canonical logit (64-element fma chunks, 16-chunk groups, then the bias) of one expert,
+// by one warp, for the token staged in xs ([C][65] fp32, padded so that lane-strided reads
+// hit distinct banks).  part: C floats of this warp's scratch.  Every lane returns the value.
+__device__ __forceinline__ float warp_canonical_logit(const float *xs, const float *__restrict__ wrow,
+                                                      int C, float bias, float *part, int lane) {
+    for (int c = lane; c < C; c += 32) {
+        const float *xc = xs + c * (kChunk + 1);
+        const float4 *wc = reinterpret_cast<const float4 *>(wrow + c * kChunk);
+        float p = 0.0f;
+#pragma unroll 4
+        for (int j = 0; j < kChunk / 4; ++j) {
+            const float4 w4 = __ldg(wc + j);
+            p = fmaf(xc[4 * j], w4.x, p);
+            p = fmaf(xc[4 * j + 1], w4.y, p);
+            p = fmaf(xc[4 * j + 2], w4.z, p);
+            p = fmaf(xc[4 * j + 3], w4.w, p);
+        }
+        part[c] = p;
+    }
+    __syncwarp();
+    const int G = (C + kGroupChunks - 1) / kGroupChunks;   // <= 32 for d <= 32768
+    float gs = 0.0f;
+    if (lane < G)
+        for (int q = lane * kGroupChunks; q < min(C, (lane + 1) * kGroupChunks); ++q) gs = __fadd_rn(gs, part[q]);
+    float acc = 0.0f;
+    for (int g = 0; g < G; ++g) acc = __fadd_rn(acc, __shfl_sync(0xffffffffu, gs, g));
+    __syncwarp();
+    return __fadd_rn(acc, bias);
+}
+
+// Sorted top 32 selection keys of the block's E values (vals(e)), left in lists[0].
+template <typename F>
+__device__ __forceinline__ void block_top32(uint64_t (*lists)[32], int E, F vals, int warp, int lane) {
+    uint64_t key[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int e = warp * 128 + 4 * lane + r;
+        key[r] = e < E ? topk_key(vals(e), e) : 0ull;
+    }
+    warp_sort128_desc(key, lane);
+    if (lane < 8) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) lists[warp][4 * lane + r] = key[r];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int n = 8; n > 1; n >>= 1) {
+        uint64_t res = 0;
+        if (warp < n / 2) res = merge_top32(lists[2 * warp][lane], lists[2 * warp + 1][31 - lane], lane);
+        __syncthreads();
+        if (warp < n / 2) lists[warp][lane] = res;
+        __syncthreads();
+    }
+}
+
+// Warp 0: write the selected experts (lanes with sel) in ascending expert id, the softmax of
+// their values, counts and slot offsets.
+__device__ __forceinline__ void emit_selection(int t, int k, bool sel, int e, float v, int lane,
+                                               int32_t *idx_out, float *w_out, int32_t *counts,
+                                               int32_t *slot_off) {
+    const int my_idx = sel ? e : 0x7fffffff;
+    const float my_val = sel ? v : -INFINITY;
+    int rank = 0;
+    for (int r = 0; r < 32; ++r) rank += (__shfl_sync(0xffffffffu, my_idx, r) < my_idx) ? 1 : 0;
+    float m = my_val;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float ex = sel ? expf(my_val - m) : 0.0f;
+    float ssum = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+    if (sel) {
+        idx_out[static_cast<int64_t>(t) * k + rank] = my_idx;
+        w_out[static_cast<int64_t>(t) * k + rank] = __fdiv_rn(ex, ssum);
+        if (counts) {
+            const int off = atomicAdd(counts + my_idx, 1);
+            if (slot_off) slot_off[static_cast<int64_t>(t) * k + rank] = off;
+        }
+    }
+}
+
+// One block of 256 threads per token.  approx: [T][E] fp32 sums of the tensor-core GEMM (no
+// bias); wrows: router weights [E][d] fp32; coef: the accumulation bound described above.
+__global__ void __launch_bounds__(kSelThreads) router_select_kernel(
+    const float *__restrict__ approx, const float *__restrict__ bias, const __nv_bfloat16 *__restrict__ x,
+    const float *__restrict__ wrows, int T, int d, int E, int k, float coef, float wn_max, float bmax,
+    int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts,
+    int32_t *__restrict__ slot_off) {
+    extern __shared__ __align__(16) float sel_smem[];
+    __shared__ uint64_t lists[8][32];
+    __shared__ float red[8];
+    __shared__ float vexact[32];
+    __shared__ float exall[1024];
+    __shared__ uint32_t s_mask[3];   // certain, uncertain, slow-path flag
+    __shared__ int s_need;
+    const int C = d / kChunk;
+    float *xs = sel_smem;                                  // [C][65]
+    const int t = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float *part = xs + C * (kChunk + 1) + warp * C;        // [8][C]
+    pdl_wait();
+    pdl_trigger();
+    // the token in shared memory (fp32, padded chunks) and its squared norm
+    const __nv_bfloat16 *xt = x + static_cast<int64_t>(t) * d;
+    float ss = 0.0f;
+    for (int i = tid; i < d; i += kSelThreads) {
+        const float v = __bfloat162float(xt[i]);
+        xs[(i / kChunk) * (kChunk + 1) + (i % kChunk)] = v;
+        ss = fmaf(v, v, ss);
+    }
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+    if (lane == 0) red[warp] = ss;
+    const float *at = approx + static_cast<int64_t>(t) * E;
+    block_top32(lists, E, [&](int e) { return __fadd_rn(__ldg(at + e), __ldg(bias + e)); }, warp, lane);
+    // (block_top32 ends with __syncthreads: red[] and lists[0] are visible)
+    const uint64_t mykey = lists[0][lane];
+    const float v = key_value(mykey);                      // NaN for padding (E < 32)
+    const int e_l = key_index(mykey);
+    if (warp == 0) {
+        float tot = 0.0f;
+        for (int i = 0; i < 8; ++i) tot += red[i];
+        // an upper bound of |x_t| (the fp32 sum of d squares is within d * 2^-24 of exact)
+        const float nx = __fmul_ru(sqrtf(tot), 1.0f + 0x1p-10f);
+        const float delta = __fadd_ru(__fmul_ru(__fmul_ru(nx, wn_max), __fadd_ru(coef, 0x1p-16f)),
+                                      __fmul_ru(bmax, 0x1p-22f));
+        const float two_d = __fmul_ru(2.0f, delta);
+        const float vk = __shfl_sync(0xffffffffu, v, k - 1);
+        const bool in_u = v >= __fsub_rd(vk, two_d);
+        const bool overflow = __shfl_sync(0xffffffffu, in_u ? 1 : 0, 31) != 0;
+        const float lo = __fsub_rd(v, two_d);
+        int cnt = 0;
+        for (int j = 0; j < 32; ++j) {
+            const float vj = __shfl_sync(0xffffffffu, v, j);
+            cnt += (j != lane && vj >= lo) ? 1 : 0;
+        }
+        const bool certain = in_u && cnt <= k - 1;
+        const uint32_t cm = __ballot_sync(0xffffffffu, certain);
+        const uint32_t um = __ballot_sync(0xffffffffu, in_u && !certain);
+        const int need = k - __popc(cm);
+        if (lane == 0) {
+            s_mask[0] = cm;
+            s_mask[1] = um;
+            s_mask[2] = (overflow || need < 0 || need > __popc(um)) ? 1u : 0u;
+            s_need = need;
+        }
+    }
+    __syncthreads();
+    if (!s_mask[2]) {
+        const uint32_t um = s_mask[1];
+        // exact canonical logits of the uncertain candidates, one warp each
+        for (int p = 0; p < 32; ++p) {
+            if (!((um >> p) & 1u)) continue;
+            if (__popc(um & ((1u << p) - 1u)) % 8 != warp) continue;
+            const int e = key_index(lists[0][p]);
+            const float ve = warp_canonical_logit(xs, wrows + static_cast<int64_t>(e) * d, C, __ldg(bias + e), part, lane);
+            if (lane == 0) vexact[p] = ve;
+        }
+        __syncthreads();
+        if (warp != 0) return;
+        const bool unc = (um >> lane) & 1u;
+        const float ve = unc ? vexact[lane] : v;
+        // rank of an uncertain candidate among the uncertain by its exact key
+        const uint64_t kx = unc ? topk_key(ve, e_l) : 0ull;
+        int r = 0;
+        for (int j = 0; j < 32; ++j) {
+            const uint64_t kj = (static_cast<uint64_t>(__shfl_sync(0xffffffffu, static_cast<uint32_t>(kx >> 32), j)) << 32) |
+                                __shfl_sync(0xffffffffu, static_cast<uint32_t>(kx), j);
+            r += (((um >> j) & 1u) && kj > kx) ? 1 : 0;
+        }
+        const bool sel = ((s_mask[0] >> lane) & 1u) || (unc && r < s_need);
+        emit_selection(t, k, sel, e_l, ve, lane, idx_out, w_out, counts, slot_off);
+        return;
+    }
+    // slow path: every canonical logit of the token, then the top k of those
+    __syncthreads();
+    for (int e = warp; e < E; e += 8) {
+        const float ve = warp_canonical_logit(xs, wrows + static_cast<int64_t>(e) * d, C, __ldg(bias + e), part, lane);
+        if (lane == 0) exall[e] = ve;
+    }
+    __syncthreads();
+    block_top32(lists, E, [&](int e) { return exall[e]; }, warp, lane);
+    if (warp != 0) return;
+    const uint64_t kb = lists[0][lane];
+    emit_selection(t, k, lane < k, key_index(kb), key_value(kb), lane, idx_out, w_out, counts, slot_off);
 }
 
 }  // namespace lmoe

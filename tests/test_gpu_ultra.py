@@ -12,7 +12,7 @@ import torch
 
 import lmoe_synth
 import oracle
-from lmoe_cases import Case, rel_l2_rows
+from lmoe_cases import Case, rel_l2_rows, w_tol
 
 pytestmark = pytest.mark.gpu
 
@@ -45,7 +45,7 @@ def _check_tokens(case, T, x, y, sample):
     ref = case.ol.forward(xs, quant=True, want=("z", "c", "y"))
     assert np.array_equal(idx[sample], ref["idx"])
     w = moe.stage("w", T, torch.float32).view(T, d.k).cpu().numpy()
-    assert np.allclose(w[sample], ref["w"], rtol=2e-6, atol=1e-7)
+    assert np.allclose(w[sample], ref["w"], **w_tol(T))
     z = moe.stage("z", T, torch.bfloat16).view(T, d.l).float().cpu().numpy()[sample]
     assert rel_l2_rows(z, ref["z"]).max() <= TOL_INTER
     zc = moe.stage("zq_codes", T).view(T, d.l // 2).cpu().numpy()[sample]
@@ -97,3 +97,28 @@ def test_ultra_prefill_T4096_zipf(ultra_zipf):
     sample[0] = 0
     sample[-1] = T - 1
     _check_tokens(case, T, x, y, sample)
+
+
+def test_ultra_router_margin_and_routing_on_many_tokens(ultra_zipf):
+    """T = 4096: routing of 256 sampled tokens against the oracle, and the tensor-core logits
+    against the canonical ones: the observed error must sit far inside the certified margin
+    (whose floor is 2^-16 |x| max|w_e|)."""
+    case = ultra_zipf
+    moe = case.gpu(debug=True)
+    d = case.dims
+    T = 4096
+    x = case.tokens(T, seed_offset=31).cuda()
+    moe.forward(x)
+    moe.check()
+    sample = np.sort(np.random.default_rng(1).choice(T, 256, replace=False))
+    xs = x[sample].float().cpu().numpy()
+    logits, oidx, ow, _ = oracle.router(xs, case.ol.w_router, case.ol.b_router, d.k)
+    idx = moe.stage("idx", T, torch.int32).view(T, d.k).cpu().numpy()[sample]
+    assert np.array_equal(idx, oidx)
+    approx = moe.stage("router", T, torch.float32).view(T, d.E).cpu().numpy()[sample]
+    approx = (approx + case.ol.b_router[None, :]).astype(np.float64)
+    nx = np.linalg.norm(xs.astype(np.float64), axis=1)
+    wn = np.linalg.norm(case.ol.w_router.astype(np.float64), axis=1).max()
+    ratio = (np.abs(approx - logits) / (nx * wn)[:, None]).max()
+    print(f"max |tensor-core - canonical| / (|x| max|w|) = {ratio:.3e} (margin floor 2^-16 = {2**-16:.3e})")
+    assert ratio < 2.0 ** -16 / 4
