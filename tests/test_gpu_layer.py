@@ -13,6 +13,7 @@ import torch
 import lmoe_synth
 import oracle
 from lmoe_cases import Case, atoms_to_rows, rel_l2_rows, w_tol
+from test_oracle_quant import dequant
 
 pytestmark = pytest.mark.gpu
 
@@ -157,3 +158,69 @@ def test_invalid_arguments(tiny):
         lm.lmoe_create(100, 64, 16, 4, 128, *[tiny.dev[n] for n in ("w_down", "w_up", "w_router", "b_router", "w1", "w2")], 1.0, 1.0)
     assert ei.value.status == lm.LMOE_EINVAL
     lm.lmoe_forward(moe.ctx, x, 0, y, ws, 16)   # T = 0 is a no-op
+
+
+@pytest.fixture(scope="module")
+def mid():
+    """ℓ = ffn = 512 (four n-tiles per expert GEMM), Zipf(1.1) routing over 32 experts: several
+    M tiles per hot expert, empty experts, ragged segments."""
+    case = Case(lmoe_synth.Dims(d=1024, l=512, E=32, k=4, ffn=512), seed=9, zipf=1.1, calib_T=64)
+    yield case
+    case.close()
+
+
+@pytest.mark.parametrize("T", [8, 40, 300, 1000])
+def test_forward_mid_size_stage_by_stage(mid, T):
+    """Each stage against the oracle's arithmetic applied to the GPU's own inputs of that stage
+    (decoded independently), then c and y against the oracle end to end.  A token whose z sits on
+    a rounding boundary can get one zq code other than the oracle's (both are correct
+    quantizations of their own z); its hq and c then differ legitimately, so the end-to-end check
+    covers the tokens whose zq equals the oracle's, and such tokens must be rare."""
+    moe = mid.gpu(debug=True)
+    d = mid.dims
+    x = mid.tokens(T, seed_offset=3000 + T)
+    y = moe.forward(x.cuda())
+    moe.check()
+    sample = np.arange(T) if T <= 300 else np.sort(np.random.default_rng(T).choice(T, 200, replace=False))
+    ref = mid.ol.forward(x[sample].float().numpy(), quant=True, want=("z", "zq_codes", "c", "y"))
+    idx = moe.stage("idx", T, torch.int32).view(T, d.k).cpu().numpy()[sample]
+    assert np.array_equal(idx, ref["idx"])
+    w = moe.stage("w", T, torch.float32).view(T, d.k).cpu().numpy()[sample]
+    # z within tolerance; the GPU's zq is the oracle's quantizer on the GPU's z
+    z = moe.stage("z", T, torch.bfloat16).view(T, d.l).float().cpu().numpy()[sample]
+    assert rel_l2_rows(z, ref["z"]).max() <= TOL_INTER
+    zc = moe.stage("zq_codes", T).view(T, d.l // 2).cpu().numpy()[sample]
+    zs = moe.stage("zq_sf", T).view(T, d.l // 16).cpu().numpy()[sample]
+    oc, os_, sdz = oracle.quantize_nvfp4(z, mid.amax_z)
+    assert np.array_equal(zc, oc) and np.array_equal(zs, os_)
+    same_zq = np.all(zc == ref["zq_codes"], axis=1)
+    assert same_zq.mean() >= 0.98
+    # h of every slot from the GPU's zq; hq = the oracle's quantizer on the GPU's h; c from the
+    # GPU's hq and routing weights
+    nrows = int(moe.stage("nrows", T, torch.int32).cpu()[0])
+    R = moe.stage("rows", T, torch.int32).numel()
+    rows = moe.stage("rows", T, torch.int32).cpu().numpy()[:nrows]
+    h = moe.stage("h", T, torch.bfloat16).view(R, d.ffn)[:nrows].float().cpu().numpy()
+    hc = moe.stage("hq_codes", T).view(R, d.ffn // 2)[:nrows].cpu().numpy()
+    hsf = atoms_to_rows(moe.stage("hq_sf", T).cpu().numpy()[: R * d.ffn // 16], R, d.ffn)[:nrows]
+    pos = {int(sl): i for i, sl in enumerate(rows) if sl >= 0}
+    zdec = dequant(zc, zs, sdz)
+    _, _, sdh = oracle.quantize_nvfp4(np.ones((1, 16), np.float32), mid.amax_h)
+    c = moe.stage("c", T, torch.bfloat16).view(T, d.l).float().cpu().numpy()[sample]
+    for n, t in enumerate(sample):
+        acc = np.zeros(d.l)
+        for j in range(d.k):
+            e = int(idx[n, j])
+            c1, s1, d1, c2, s2, d2 = mid.ol.quantized(e)
+            r = pos[int(t) * d.k + j]
+            u = dequant(c1, s1, d1) @ zdec[n]
+            href = torch.from_numpy(np.maximum(u, 0.0) ** 2).to(torch.bfloat16).double().numpy()
+            assert rel_l2_rows(h[r:r + 1], href[None]).max() <= TOL_INTER
+            qc, qs, _ = oracle.quantize_nvfp4(h[r:r + 1], mid.amax_h)
+            assert np.array_equal(hc[r:r + 1], qc) and np.array_equal(hsf[r:r + 1], qs)
+            acc += float(w[n, j]) * (dequant(c2, s2, d2) @ dequant(hc[r:r + 1], hsf[r:r + 1], sdh)[0])
+        cref = torch.from_numpy(acc).to(torch.bfloat16).double().numpy()
+        assert rel_l2_rows(c[n:n + 1], cref[None]).max() <= TOL_INTER
+    # end to end, tokens whose zq equals the oracle's
+    assert rel_l2_rows(c[same_zq], ref["c"][same_zq]).max() <= TOL_OUT
+    assert rel_l2_rows(y[sample].float().cpu().numpy()[same_zq], ref["y"][same_zq]).max() <= TOL_OUT
