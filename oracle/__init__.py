@@ -82,6 +82,9 @@ def lib():
             L.oracle_quantize_nvfp4.restype = None
             L.oracle_quantize_nvfp4.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_float,
                                                 C.c_void_p, C.c_void_p, C.c_void_p, C.c_int]
+            L.oracle_quantize_nvfp4_2d.restype = None
+            L.oracle_quantize_nvfp4_2d.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_float,
+                                                   C.c_void_p, C.c_void_p, C.c_void_p, C.c_int]
             L.oracle_nvfp4_dot.restype = C.c_double
             L.oracle_nvfp4_dot.argtypes = [C.c_void_p] * 4 + [C.c_int64]
             L.oracle_quantize_fp8.restype = None
@@ -163,6 +166,18 @@ def quantize_nvfp4(x, amax: float = -1.0, nthreads: int = 0):
     return codes, sf, float(sdec[0])
 
 
+def quantize_nvfp4_2d(x, amax: float = -1.0, nthreads: int = 0):
+    """x: [R][K] (R % 16 == 0) -> (codes [R][K/2], sf [R][K/16], s_dec): 16 x 16 weight blocks."""
+    x = _f32(x)
+    R, K = x.shape
+    assert K % 16 == 0 and R % 16 == 0
+    codes = np.empty((R, K // 2), np.uint8)
+    sf = np.empty((R, K // 16), np.uint8)
+    sdec = np.zeros(1, np.float32)
+    lib().oracle_quantize_nvfp4_2d(_p(x), R, K, float(amax), _p(codes), _p(sf), _p(sdec), nthreads)
+    return codes, sf, float(sdec[0])
+
+
 def nvfp4_dot(qa, sfa, qb, sfb) -> float:
     qa, sfa, qb, sfb = (np.ascontiguousarray(a, np.uint8) for a in (qa, sfa, qb, sfb))
     return lib().oracle_nvfp4_dot(_p(qa), _p(sfa), _p(qb), _p(sfb), qa.size * 2)
@@ -218,7 +233,8 @@ class OracleLayer:
     """
 
     def __init__(self, d, l, E, k, ffn, w_down, w_up, w_router, b_router, expert_fn,
-                 amax_z=0.0, amax_h=0.0, nthreads=0, shared=None, amax_xs=0.0, amax_hs=0.0):
+                 amax_z=0.0, amax_h=0.0, nthreads=0, shared=None, amax_xs=0.0, amax_hs=0.0,
+                 weight_blocks_2d=False):
         self.d, self.l, self.E, self.k, self.ffn = d, l, E, k, ffn
         self.w_down = _f32(w_down)
         self.w_up = _f32(w_up)
@@ -231,6 +247,7 @@ class OracleLayer:
         self.shared = None if shared is None else (_f32(shared[0]), _f32(shared[1]))
         self.shared_ffn = 0 if shared is None else self.shared[0].shape[0]
         self.amax_xs, self.amax_hs = float(amax_xs), float(amax_hs)
+        self.weight_blocks_2d = bool(weight_blocks_2d)   # 16 x 16 expert weight blocks
         self._sq = None    # (ws1 codes, ws1 s_dec, ws2 codes, ws2 s_dec)
         self._q = {}       # e -> (c1, s1, d1, c2, s2, d2)
         self._m = {}       # e -> (w1, w2) float32 masters
@@ -247,8 +264,9 @@ class OracleLayer:
         """Oracle-quantized expert e: (w1 codes, w1 sf, w1 s_dec, w2 codes, w2 sf, w2 s_dec)."""
         if e not in self._q:
             w1, w2 = self.master(e)
-            c1, s1, d1 = quantize_nvfp4(w1, -1.0, self.nthreads)
-            c2, s2, d2 = quantize_nvfp4(w2, -1.0, self.nthreads)
+            qf = quantize_nvfp4_2d if self.weight_blocks_2d else quantize_nvfp4
+            c1, s1, d1 = qf(w1, -1.0, self.nthreads)
+            c2, s2, d2 = qf(w2, -1.0, self.nthreads)
             self._q[e] = (c1, s1, d1, c2, s2, d2)
         return self._q[e]
 

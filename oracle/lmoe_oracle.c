@@ -199,6 +199,65 @@ void oracle_quantize_nvfp4(const float *src, int64_t R, int64_t K, float amax,
     if (s_dec_out) *s_dec_out = s_dec;
 }
 
+/* 2-D variant ([NEWS] architecture paragraph: NVFP4 pretraining with weights quantized in */
+/* two-dimensional blocks; 16 x 16 is this project's reading, matching the 16-element      */
+/* contraction blocks).  One E4M3 scale per 16 rows x 16 contraction elements, from the     */
+/* block's amax; the same fp32 steps as the 1-D quantizer otherwise.  The scale is written  */
+/* for every row of the block, so sf keeps the 1-D layout [R][K/16] (R % 16 == 0).          */
+typedef struct { const float *src; int64_t K; float s_enc6, s_dec; uint8_t *codes, *sf; } quant2d_job;
+
+static void quant2d_groups(int64_t gb, int64_t ge, void *arg) {
+    quant2d_job *j = (quant2d_job *)arg;
+    const int64_t K = j->K;
+    for (int64_t g = gb; g < ge; ++g) {               /* 16-row group */
+        for (int64_t b = 0; b < K / 16; ++b) {
+            float amax_b = 0.0f;
+            for (int r = 0; r < 16; ++r)
+                for (int i = 0; i < 16; ++i) {
+                    float a = fabsf(j->src[(g * 16 + r) * K + 16 * b + i]);
+                    if (a > amax_b) amax_b = a;
+                }
+            uint8_t s = oracle_f32_to_e4m3(amax_b * j->s_enc6);
+            float bd = (float)g_e4m3[s] * j->s_dec;
+            float rcp = (bd > 0.0f) ? 1.0f / bd : 0.0f;
+            for (int r = 0; r < 16; ++r) {
+                const float *xb = j->src + (g * 16 + r) * K + 16 * b;
+                uint8_t *cb = j->codes + (g * 16 + r) * (K / 2) + 8 * b;
+                for (int i = 0; i < 16; i += 2) {
+                    uint8_t q0 = oracle_f32_to_e2m1(xb[i] * rcp);
+                    uint8_t q1 = oracle_f32_to_e2m1(xb[i + 1] * rcp);
+                    cb[i / 2] = (uint8_t)(q0 | (q1 << 4));
+                }
+                j->sf[(g * 16 + r) * (K / 16) + b] = s;
+            }
+        }
+    }
+}
+
+void oracle_quantize_nvfp4_2d(const float *src, int64_t R, int64_t K, float amax,
+                              uint8_t *codes, uint8_t *sf, float *s_dec_out, int nthreads) {
+    pthread_once(&g_once, init_tables);
+    if (amax < 0.0f) {
+        amax = 0.0f;
+        for (int64_t i = 0; i < R * K; ++i) {
+            float a = fabsf(src[i]);
+            if (a > amax) amax = a;
+        }
+    }
+    if (amax == 0.0f) {
+        memset(codes, 0, (size_t)(R * K / 2));
+        memset(sf, 0, (size_t)(R * K / 16));
+        if (s_dec_out) *s_dec_out = 1.0f;
+        return;
+    }
+    const float S = 2688.0f;
+    float s_enc = S / amax;
+    float s_dec = amax / S;
+    quant2d_job j = {src, K, s_enc / 6.0f, s_dec, codes, sf};
+    parallel_for(R / 16, nthreads, quant2d_groups, &j);
+    if (s_dec_out) *s_dec_out = s_dec;
+}
+
 /* Exact block-scaled dot: inside a block, 2*e2m1 values are small integers, so the     */
 /* 16-term dot is an exact integer; it is scaled by 1/4 and the two E4M3 block scales    */
 /* (all exact in fp64).  Blocks are summed in fp64.                                      */

@@ -58,6 +58,12 @@ double oracle_fp8_dot(const uint8_t *a, const uint8_t *b, int64_t K);
 void oracle_quantize_nvfp4(const float *src, int64_t R, int64_t K, float amax,
                            uint8_t *codes, uint8_t *sf, float *s_dec, int nthreads);
 
+/* The 2-D weight-block variant: one E4M3 scale per 16 rows x 16 contraction elements (same
+ * arithmetic, block amax over the 16 x 16 block), written for every row of the block so sf
+ * keeps the [R][K/16] layout.  R % 16 == 0. */
+void oracle_quantize_nvfp4_2d(const float *src, int64_t R, int64_t K, float amax,
+                              uint8_t *codes, uint8_t *sf, float *s_dec, int nthreads);
+
 /* Exact NVFP4 x NVFP4 dot product over K elements (K % 16 == 0), block scales applied,
  * tensor scales NOT applied. */
 double oracle_nvfp4_dot(const uint8_t *qa, const uint8_t *sfa,
