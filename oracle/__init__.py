@@ -85,6 +85,8 @@ def lib():
             L.oracle_quantize_nvfp4_2d.restype = None
             L.oracle_quantize_nvfp4_2d.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_float,
                                                    C.c_void_p, C.c_void_p, C.c_void_p, C.c_int]
+            L.oracle_nvfp4_dense_dot.restype = C.c_double
+            L.oracle_nvfp4_dense_dot.argtypes = [C.c_void_p] * 3 + [C.c_int64]
             L.oracle_nvfp4_dot.restype = C.c_double
             L.oracle_nvfp4_dot.argtypes = [C.c_void_p] * 4 + [C.c_int64]
             L.oracle_quantize_fp8.restype = None
@@ -316,6 +318,8 @@ class OracleLayer:
 
     def forward(self, x, quant=True, want=("y",)):
         """Run the layer on the token rows x [T][d]; returns a dict of requested outputs.
+        quant: True (NVFP4 weights and activations), "w4a16" (NVFP4 weights, bf16 activations)
+        or False (fp64 masters, no quantization).
 
         Available: z, zq_codes, zq_sf, logits, idx, w, counts, h, hq_codes, hq_sf, c64, c,
         y64, y, and with a shared expert xs_q, hs, hs_q, s.  idx / w / counts are always
@@ -338,9 +342,9 @@ class OracleLayer:
         names = set(want) | {"idx", "w", "counts"}
         res = {n: np.zeros(*shapes[n]) for n in names}
         out = _Out(**{n: _p(res[n]) for n in names})
-        st, keep = self._struct(experts, quant)
-        rc = lib().oracle_layer_forward(C.byref(st), _p(x), T, 1 if quant else 0, C.byref(out),
-                                        self.nthreads)
+        mode = 2 if quant == "w4a16" else (1 if quant else 0)
+        st, keep = self._struct(experts, mode != 0)
+        rc = lib().oracle_layer_forward(C.byref(st), _p(x), T, mode, C.byref(out), self.nthreads)
         if rc != 0:
             raise RuntimeError("oracle_layer_forward: missing expert weights")
         del keep

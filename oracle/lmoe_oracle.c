@@ -276,6 +276,23 @@ double oracle_nvfp4_dot(const uint8_t *qa, const uint8_t *sfa,
     return acc;
 }
 
+/* Dense x NVFP4 dot (the W4A16 form): sum over blocks of value(sfb) * sum_i a_i * e2m1(q_i),  */
+/* in fp64; every product of a bf16 activation with an E2M1 value is exact in fp64.          */
+double oracle_nvfp4_dense_dot(const float *a, const uint8_t *qb, const uint8_t *sfb, int64_t K) {
+    pthread_once(&g_once, init_tables);
+    double acc = 0.0;
+    for (int64_t b = 0; b < K / 16; ++b) {
+        double blk = 0.0;
+        for (int i = 0; i < 8; ++i) {
+            uint8_t c = qb[8 * b + i];
+            blk += (double)a[16 * b + 2 * i] * (0.5 * g_e2m1x2[c & 15]) +
+                   (double)a[16 * b + 2 * i + 1] * (0.5 * g_e2m1x2[c >> 4]);
+        }
+        acc += blk * g_e4m3[sfb[b]];
+    }
+    return acc;
+}
+
 /* ------------------------------------------------------------------------------------ */
 /* FP8 E4M3 with one per-tensor scale ([NEWS] quantization paragraph: the shared expert is */
 /* FP8).  The scale arithmetic is this project's reading, in IEEE fp32: s_enc = 448/amax,  */
@@ -519,7 +536,9 @@ int oracle_calibrate_shared(const oracle_layer *L, const float *x, int64_t T,
 /*   y  = bf16( c Wu^T )                      up-projection l -> d, BF16                 */
 /*        (+ s, the shared expert above, before the rounding, when the layer has one)    */
 /* In unquantized mode (quant = 0) the same steps run in fp64 on the master weights with  */
-/* no quantization and no rounding.                                                      */
+/* no quantization and no rounding.  W4A16 mode (quant = 2; [NEWS] quantization paragraph: */
+/* the NVFP4 checkpoint runs as W4A16 on Hopper): NVFP4 weights, bf16 z and h unquantized: */
+/*   u = s_w1e (z . dq(W1q_e)), h = bf16(max(u,0)^2), o = s_w2e (h . dq(W2q_e)).           */
 /* ------------------------------------------------------------------------------------ */
 typedef struct {
     const oracle_layer *L; const float *x; int quant; oracle_out *out;
@@ -563,7 +582,7 @@ static void layer_rows(int64_t tb, int64_t te, void *arg) {
             zf[j] = (float)z64[j];
         }
         if (O->z) memcpy(O->z + t * l, zf, sizeof(float) * l);
-        if (J->quant) {
+        if (J->quant == 1) {
             float sd;
             oracle_quantize_nvfp4(zf, 1, l, J->amax_z, zc, zs, &sd, 1);
             if (O->zq_codes) memcpy(O->zq_codes + t * (l / 2), zc, (size_t)l / 2);
@@ -585,7 +604,25 @@ static void layer_rows(int64_t tb, int64_t te, void *arg) {
         float s_dec_h = (J->amax_h == 0.0f) ? 1.0f : J->amax_h / 2688.0f;
         for (int jj = 0; jj < k; ++jj) {
             int e = idx[jj];
-            if (J->quant) {
+            if (J->quant == 2) {
+                /* W4A16: NVFP4 weights, bf16 activations (no activation quantization) */
+                if (!L->w1_codes[e] || !L->w1_sf[e] || !L->w2_codes[e] || !L->w2_sf[e]) {
+                    J->error = 1; continue;
+                }
+                for (int f = 0; f < F; ++f) {
+                    double u = (double)L->w1_sdec[e] *
+                               oracle_nvfp4_dense_dot(zf, L->w1_codes[e] + (int64_t)f * (l / 2),
+                                                      L->w1_sf[e] + (int64_t)f * (l / 16), l);
+                    double r = u > 0.0 ? u : 0.0;
+                    hf[f] = (float)oracle_round_bf16(r * r);
+                }
+                for (int j = 0; j < l; ++j) {
+                    double o = (double)L->w2_sdec[e] *
+                               oracle_nvfp4_dense_dot(hf, L->w2_codes[e] + (int64_t)j * (F / 2),
+                                                      L->w2_sf[e] + (int64_t)j * (F / 16), F);
+                    c64[j] += w64[jj] * o;
+                }
+            } else if (J->quant) {
                 if (!L->w1_codes[e] || !L->w1_sf[e] || !L->w2_codes[e] || !L->w2_sf[e]) {
                     J->error = 1; continue;
                 }

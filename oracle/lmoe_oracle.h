@@ -69,6 +69,10 @@ void oracle_quantize_nvfp4_2d(const float *src, int64_t R, int64_t K, float amax
 double oracle_nvfp4_dot(const uint8_t *qa, const uint8_t *sfa,
                         const uint8_t *qb, const uint8_t *sfb, int64_t K);
 
+/* Dense x NVFP4 dot over K elements (W4A16): a holds the dense operand (bf16 values), block
+ * scales applied, tensor scale NOT applied; fp64. */
+double oracle_nvfp4_dense_dot(const float *a, const uint8_t *qb, const uint8_t *sfb, int64_t K);
+
 /* Router: canonical fp32 logits (64-element fmaf chunks; chunk partials summed left to right
  * in groups of 16 chunks; group sums summed left to right; then the bias), top-k by
  * (logit desc, index asc), softmax over the
@@ -131,8 +135,9 @@ typedef struct {               /* every pointer optional (NULL = not wanted)    
     float   *s;        /* [T][d]            shared expert output (bf16 values) */
 } oracle_out;
 
-/* quant = 1: the NVFP4 layer.  quant = 0: the same layer in plain fp64 with the master
- * weights and no rounding of any intermediate (used by the structural pins).
+/* quant = 1: the NVFP4 layer.  quant = 2: W4A16 (NVFP4 weights, bf16 activations, no activation
+ * quantization).  quant = 0: the same layer in plain fp64 with the master weights and no
+ * rounding of any intermediate (used by the structural pins).
  * Returns 0, or -1 if an expert that a token selects has no weights. */
 int oracle_layer_forward(const oracle_layer *L, const float *x, int64_t T, int quant,
                          oracle_out *out, int nthreads);
