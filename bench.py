@@ -49,6 +49,7 @@ def args_():
     p.add_argument("--impl", default="lmoe", choices=["lmoe", "reference"])
     p.add_argument("--no-prefill", action="store_true")
     p.add_argument("--no-long", action="store_true")
+    p.add_argument("--no-w4a16", action="store_true")
     p.add_argument("--long-steps", type=int, default=5)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--prefill-steps", type=int, default=20)
@@ -537,6 +538,34 @@ def main():
         "clocks": clk.summary(),
         "csrc_hash": csrc_hash(),
     }
+
+    # ---- the W4A16 form of the same decode step (NVFP4 weights decoded in smem, bf16 z and h)
+    if not a.no_w4a16:
+        import nvfp4_latentmoe_fwd_02_b300 as lm2
+        Lw = lmoe_synth.layer(cfg["dims"], cfg["seed"], "cuda", cfg["zipf"])
+        cal = calibration(HEADLINE)
+        d_ = cfg["dims"]
+        mw = lm2.LatentMoE(d_.d, d_.l, d_.E, d_.k, d_.ffn, Lw.w_down, Lw.w_up, Lw.w_router, Lw.b_router,
+                           Lw.w1, Lw.w2, cal["amax_z"], cal["amax_h"], w4a16=True)
+        del Lw
+        torch.cuda.empty_cache()
+        rw = Runner(mw, T, cfg["seed"])
+        with Clocks(torch.cuda.current_device()) as clkw:
+            wms = rw.timed_steps(a.steps, max(3, a.warmup))
+        wtot = dist.max(sum(wms))
+        wprof = rw.profile()
+        web = expert_bytes(mw, T)
+        wt = dict(wprof)
+        line["w4a16_decode"] = {
+            "config": {**workload_config(HEADLINE), "experts": "W4A16 (NVFP4 weights, bf16 activations)"},
+            "tokens_per_s": T * a.steps * dist.world / (wtot * 1e-3), "ms_per_step": wtot / a.steps,
+            "per_kernel_ms": {n: round(v, 5) for n, v in wprof},
+            "expert_up_hbm_frac": web["expert_up"] / (wt["expert_up"] * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "clocks": clkw.summary(),
+        }
+        mw.close()
+        del rw
+        torch.cuda.empty_cache()
 
     # ---- prefill point
     if not a.no_prefill:

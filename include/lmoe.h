@@ -75,6 +75,16 @@ typedef struct {
     int shared_ffn;         /* multiple of 64 when ws1 != NULL                                */
     float amax_xs;          /* static amax of x for its FP8 quantization (calibration); > 0    */
     float amax_hs;          /* static amax of the shared h (calibration); > 0                 */
+    /* Expert weight blocks: 0 = one E4M3 scale per 1 x 16 contraction elements; 1 = one scale
+     * per 16 output rows x 16 contraction elements (two-dimensional weight blocks, NVIDIA AI
+     * releases Nemotron 3 Ultra, architecture paragraph).  The GEMMs are the same: a 2-D
+     * block's scale is stored for each of its 16 rows. */
+    int weight_blocks_2d;
+    /* Expert arithmetic: 0 = W4A4 (z and h quantized to NVFP4, native FP4 MMAs); 1 = W4A16
+     * (NVIDIA AI releases Nemotron 3 Ultra, quantization paragraph: the Hopper form of the
+     * checkpoint): NVFP4 weights decoded to bf16 in shared memory and bf16 z and h, with
+     * u = s_w1 (z . dq(W1q)), h = bf16(relu(u)^2), o = s_w2 (h . dq(W2q)). */
+    int expert_w4a16;
 } lmoe_weights;
 
 /* Create a layer context: validates the dims, allocates the context buffers, quantizes every
@@ -100,6 +110,13 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
 lmoe_status lmoe_quantize_nvfp4(const void *src, lmoe_dtype dt, int64_t rows, int64_t K,
                                 float amax, uint8_t *codes, uint8_t *sf, float *tensor_scale,
                                 lmoe_stream stream);
+
+/* The same with two-dimensional blocks: one E4M3 scale per 16 rows x 16 elements of K, from
+ * the block's amax, written to each of the block's 16 rows of sf (so sf has the layout above).
+ * rows % 16 == 0, K % 16 == 0. */
+lmoe_status lmoe_quantize_nvfp4_2d(const void *src, lmoe_dtype dt, int64_t rows, int64_t K,
+                                   float amax, uint8_t *codes, uint8_t *sf, float *tensor_scale,
+                                   lmoe_stream stream);
 
 /* FP8 E4M3 quantization with one FP32 per-tensor scale (the shared expert's format):
  *   src          device, bf16 or fp32 per `dt`, n elements (n % 16 == 0, n >= 0; 0 is a no-op)
@@ -182,9 +199,9 @@ typedef enum {
     LMOE_STAGE_C = 5,        /* bf16  [T][l]      combine output                       */
     LMOE_STAGE_Z = 6,        /* bf16  [T][l]      debug mode only                       */
     LMOE_STAGE_ROWS = 7,     /* int32 [R] slot (token*k + j) of each permuted row, -1 = pad */
-    LMOE_STAGE_H = 8,        /* bf16  [R][ffn]    debug mode only, permuted rows        */
-    LMOE_STAGE_HQ_CODES = 9, /* uint8 [R][ffn/2]  permuted rows                         */
-    LMOE_STAGE_HQ_SF = 10,   /* uint8 [R/128][ffn/64][512] tensor-core scale atoms      */
+    LMOE_STAGE_H = 8,        /* bf16  [R][ffn]    permuted rows; W4A4: debug mode only  */
+    LMOE_STAGE_HQ_CODES = 9, /* uint8 [R][ffn/2]  permuted rows (W4A4 only)             */
+    LMOE_STAGE_HQ_SF = 10,   /* uint8 [R/128][ffn/64][512] tensor-core scale atoms (W4A4) */
     LMOE_STAGE_NROWS = 11,   /* int32 [1]         R actually used                       */
     LMOE_STAGE_XS_Q = 12,    /* uint8 [T][d]      shared expert: E4M3 codes of x        */
     LMOE_STAGE_HS = 13,      /* bf16  [T][shared_ffn] shared expert h, debug mode only   */

@@ -38,7 +38,8 @@ class _Weights(C.Structure):
                 ("b_router", C.c_void_p), ("w1", C.c_void_p), ("w2", C.c_void_p),
                 ("amax_z", C.c_float), ("amax_h", C.c_float),
                 ("ws1", C.c_void_p), ("ws2", C.c_void_p), ("shared_ffn", C.c_int),
-                ("amax_xs", C.c_float), ("amax_hs", C.c_float)]
+                ("amax_xs", C.c_float), ("amax_hs", C.c_float), ("weight_blocks_2d", C.c_int),
+                ("expert_w4a16", C.c_int)]
 
 
 _lib = None
@@ -60,6 +61,7 @@ def lib() -> C.CDLL:
         "lmoe_status_string": (C.c_char_p, [C.c_int]),
         "lmoe_create": (C.c_int, [C.c_int] * 5 + [C.POINTER(_Weights), vp, C.POINTER(vp)]),
         "lmoe_quantize_nvfp4": (C.c_int, [vp, C.c_int, i64, i64, C.c_float, vp, vp, vp, vp]),
+        "lmoe_quantize_nvfp4_2d": (C.c_int, [vp, C.c_int, i64, i64, C.c_float, vp, vp, vp, vp]),
         "lmoe_quantize_fp8": (C.c_int, [vp, C.c_int, i64, C.c_float, vp, vp, vp]),
         "lmoe_get_shared_fp8": (C.c_int, [vp, C.c_int, vp, C.POINTER(C.c_float), vp]),
         "lmoe_route": (C.c_int, [vp, vp, i64, vp, vp, vp, vp]),
@@ -128,6 +130,21 @@ def lmoe_quantize_nvfp4(src: torch.Tensor, amax: float = -1.0, codes=None, sf=No
     return codes, sf, tensor_scale
 
 
+def lmoe_quantize_nvfp4_2d(src: torch.Tensor, amax: float = -1.0, codes=None, sf=None,
+                           tensor_scale=None, stream=None):
+    """NVFP4 with 16 x 16 blocks of a [rows][K] bf16/fp32 device tensor (rows % 16 == 0)."""
+    assert src.is_cuda and src.dim() == 2 and src.is_contiguous()
+    rows, K = src.shape
+    dt = {torch.bfloat16: LMOE_BF16, torch.float32: LMOE_FP32}[src.dtype]
+    dev = src.device
+    codes = codes if codes is not None else torch.empty((rows, K // 2), dtype=torch.uint8, device=dev)
+    sf = sf if sf is not None else torch.empty((rows, K // 16), dtype=torch.uint8, device=dev)
+    tensor_scale = tensor_scale if tensor_scale is not None else torch.empty(1, dtype=torch.float32, device=dev)
+    _check(lib().lmoe_quantize_nvfp4_2d(_ptr(src), dt, rows, K, float(amax), _ptr(codes), _ptr(sf),
+                                        _ptr(tensor_scale), _stream(stream)), "lmoe_quantize_nvfp4_2d")
+    return codes, sf, tensor_scale
+
+
 def lmoe_quantize_fp8(src: torch.Tensor, amax: float = -1.0, codes=None, tensor_scale=None,
                       stream=None):
     """FP8 E4M3 per-tensor quantization of a bf16/fp32 device tensor -> (codes, tensor_scale)."""
@@ -141,7 +158,8 @@ def lmoe_quantize_fp8(src: torch.Tensor, amax: float = -1.0, codes=None, tensor_
 
 
 def lmoe_create(d, l, E, k, ffn, w_down, w_up, w_router, b_router, w1, w2, amax_z, amax_h,
-                stream=None, ws1=None, ws2=None, amax_xs=0.0, amax_hs=0.0) -> int:
+                stream=None, ws1=None, ws2=None, amax_xs=0.0, amax_hs=0.0,
+                weight_blocks_2d=False, w4a16=False) -> int:
     """Create a context from device tensors: w_down bf16 [l][d], w_up bf16 [d][l], w_router fp32
     [E][d], b_router fp32 [E] or None, w1 bf16 [E][ffn][l], w2 bf16 [E][l][ffn]; optional
     shared expert ws1 bf16 [shared_ffn][d], ws2 bf16 [d][shared_ffn]."""
@@ -149,7 +167,8 @@ def lmoe_create(d, l, E, k, ffn, w_down, w_up, w_router, b_router, w1, w2, amax_
         assert t.is_cuda and t.is_contiguous()
     ws = _Weights(_ptr(w_down), _ptr(w_up), _ptr(w_router), _ptr(b_router), _ptr(w1), _ptr(w2),
                   float(amax_z), float(amax_h), _ptr(ws1), _ptr(ws2),
-                  0 if ws1 is None else ws1.shape[0], float(amax_xs), float(amax_hs))
+                  0 if ws1 is None else ws1.shape[0], float(amax_xs), float(amax_hs),
+                  1 if weight_blocks_2d else 0, 1 if w4a16 else 0)
     out = C.c_void_p()
     _check(lib().lmoe_create(d, l, E, k, ffn, C.byref(ws), _stream(stream), C.byref(out)), "lmoe_create")
     return out.value
@@ -241,11 +260,13 @@ class LatentMoE:
     """Owns one context and a workspace; forward(x) -> y.  Marshalling only."""
 
     def __init__(self, d, l, E, k, ffn, w_down, w_up, w_router, b_router, w1, w2, amax_z, amax_h,
-                 debug=False, stream=None, ws1=None, ws2=None, amax_xs=0.0, amax_hs=0.0):
+                 debug=False, stream=None, ws1=None, ws2=None, amax_xs=0.0, amax_hs=0.0,
+                 weight_blocks_2d=False, w4a16=False):
         self.d, self.l, self.E, self.k, self.ffn = d, l, E, k, ffn
         self.shared_ffn = 0 if ws1 is None else ws1.shape[0]
         self.ctx = lmoe_create(d, l, E, k, ffn, w_down, w_up, w_router, b_router, w1, w2,
-                               amax_z, amax_h, stream, ws1, ws2, amax_xs, amax_hs)
+                               amax_z, amax_h, stream, ws1, ws2, amax_xs, amax_hs, weight_blocks_2d,
+                               w4a16)
         if debug:
             lmoe_set_debug(self.ctx, True)
         self.ws = None

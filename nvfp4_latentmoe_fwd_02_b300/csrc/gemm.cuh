@@ -36,7 +36,9 @@
 namespace lmoe {
 
 // Operand kinds (template argument KIND).
-constexpr int kKindBf16 = 0, kKindNvf4 = 1, kKindFp8 = 2;
+// kKindW4A16: bf16 activations times NVFP4 weights that converter warps decode into bf16 tiles
+// in shared memory (E2M1 x E4M3 is exact in bf16), then kind::f16 MMAs.
+constexpr int kKindBf16 = 0, kKindNvf4 = 1, kKindFp8 = 2, kKindW4A16 = 3;
 
 enum EpiMode : int {
     EPI_STORE_BF16 = 0,   // out bf16 [M][ld] = acc (+ addend bf16 [M][ld], if given)
@@ -45,7 +47,8 @@ enum EpiMode : int {
     EPI_H_QUANT = 3,      // h = bf16(relu(alpha_e acc)^2); hq = NVFP4(h) (scale atoms); dbg = h
     EPI_COMBINE = 4,      // c_acc[token] += w_slot * alpha_e * acc
     EPI_FP8_SQRELU = 5,   // h = bf16(relu(alpha_s acc)^2); q_codes [M][N] = e4m3(h * s_enc8); dbg = h
-    EPI_STORE_SCALED = 6  // out bf16 [M][ld] = alpha_s * acc
+    EPI_STORE_SCALED = 6, // out bf16 [M][ld] = alpha_s * acc
+    EPI_H_BF16 = 7        // W4A16 latent-up: out bf16 [M][N] = bf16(relu(alpha_e acc)^2)
 };
 
 constexpr int kBM = 128, kBN = 128;
@@ -86,6 +89,8 @@ struct GemmArgs {
     float s_enc8;
     const __nv_bfloat16 *addend; // EPI_STORE_BF16: bf16 [M][ld_out] added before the rounding
     int a_kwrap;                 // > 0: A's K coordinate wraps at this many elements (B is K-concatenated)
+    int bn;                      // tile width (output columns): the kernel's BN
+    __nv_bfloat16 *a_bf16;       // W4A16 z epilogue: bf16 z rows copied into the expert segments [R][N]
     unsigned *err;
 };
 
@@ -118,9 +123,9 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &g, const SmemTables 
         tl.e = e;
         tl.a_row0 = tb->seg[e] + m * kBM;
         tl.rows = min(kBM, tb->cnt[e] - m * kBM);
-        tl.n0 = n * kBN;
-        tl.b_row0 = e * g.N + n * kBN;
-        tl.cols = min(kBN, g.N - n * kBN);
+        tl.n0 = n * g.bn;
+        tl.b_row0 = e * g.N + n * g.bn;
+        tl.cols = min(g.bn, g.N - n * g.bn);
         tl.kt0 = 0;
         tl.kt1 = g.k_tiles;
     } else {
@@ -130,9 +135,9 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &g, const SmemTables 
         tl.e = 0;
         tl.a_row0 = m * kBM;
         tl.rows = min(kBM, g.M - m * kBM);
-        tl.n0 = n * kBN;
-        tl.b_row0 = n * kBN;
-        tl.cols = min(kBN, g.N - n * kBN);
+        tl.n0 = n * g.bn;
+        tl.b_row0 = n * g.bn;
+        tl.cols = min(g.bn, g.N - n * g.bn);
         tl.kt0 = s * g.kt_per_split;
         tl.kt1 = min(g.k_tiles, tl.kt0 + g.kt_per_split);
     }
@@ -171,7 +176,7 @@ __device__ __forceinline__ EpiRow epilogue_row(const GemmArgs &g, const Tile &tl
     EpiRow er;
     er.alpha = 1.0f; er.wslot = 0.0f; er.orow = 0;
     er.valid = row < tl.rows;
-    if (g.epi == EPI_H_QUANT || g.epi == EPI_COMBINE) er.alpha = __ldg(g.alpha + tl.e);
+    if (g.epi == EPI_H_QUANT || g.epi == EPI_COMBINE || g.epi == EPI_H_BF16) er.alpha = __ldg(g.alpha + tl.e);
     if (g.epi == EPI_COMBINE && er.valid) {
         const int slot = __ldg(g.row_slot + tl.a_row0 + row);
         if (slot < 0) {
@@ -288,18 +293,38 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs &g, const Tile &tl
         const uint16_t s2 = static_cast<uint16_t>(s[0] | (s[1] << 8));
         if (g.epi == EPI_Z_QUANT) {
             *reinterpret_cast<uint16_t *>(g.q_sf + grow * (g.N / 16) + col / 16) = s2;
-            // the token's k expert-segment rows get the same codes and scales
+            // the token's k expert-segment rows get the same codes and scales (W4A16: bf16 z)
             for (int j = 0; j < g.topk; ++j) {
                 const int64_t slot = grow * g.topk + j;
                 const int row = __ldg(g.seg_start + __ldg(g.idx + slot)) + __ldg(g.slot_off + slot);
-                *reinterpret_cast<uint4 *>(g.a_codes + static_cast<int64_t>(row) * (g.N / 2) + col / 2) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint16_t *>(g.a_sf + sf_atom_offset(row, col / 16, g.N / 64)) = s2;
+                if (g.a_bf16) {
+                    uint4 *o = reinterpret_cast<uint4 *>(g.a_bf16 + static_cast<int64_t>(row) * g.N + col);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) o[i] = make_uint4(hb[4 * i], hb[4 * i + 1], hb[4 * i + 2], hb[4 * i + 3]);
+                } else {
+                    *reinterpret_cast<uint4 *>(g.a_codes + static_cast<int64_t>(row) * (g.N / 2) + col / 2) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint16_t *>(g.a_sf + sf_atom_offset(row, col / 16, g.N / 64)) = s2;
+                }
                 if (col == 0) g.row_slot_out[row] = static_cast<int32_t>(slot);
             }
         } else {
             *reinterpret_cast<uint16_t *>(g.q_sf + sf_atom_offset(grow, col / 16, g.N / 64)) = s2;
         }
+        break;
+    }
+    case EPI_H_BF16: {
+        const float a = er.alpha;
+        uint32_t hb[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float u0 = fmaxf(__fmul_rn(a, v[2 * i]), 0.0f);
+            const float u1 = fmaxf(__fmul_rn(a, v[2 * i + 1]), 0.0f);
+            hb[i] = pack_bf16x2(__fmul_rn(u0, u0), __fmul_rn(u1, u1));
+        }
+        uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(g.out) + grow * g.N + col);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = make_uint4(hb[4 * i], hb[4 * i + 1], hb[4 * i + 2], hb[4 * i + 3]);
         break;
     }
     case EPI_COMBINE: {
@@ -354,40 +379,88 @@ __device__ __forceinline__ void combine_staged(const GemmArgs &g, const Tile &tl
 // accumulator rows the epilogue never reads.  KB: 128-byte column blocks (256 e2m1 or 64 bf16
 // elements of K each; 128 e4m3) per pipeline stage; KB = 2 halves the per-stage barrier handshakes and
 // copies when each stage carries little MMA work (decode).
-template <int KIND, bool SMALLA, int KB>
+template <int KIND, bool SMALLA, int KB, int BN = kBN>
 struct GemmCfg {
     static constexpr bool NVF4 = KIND == kKindNvf4;
+    static constexpr bool W4 = KIND == kKindW4A16;
+    static constexpr bool kTables = NVF4 || W4;                       // grouped launches: tables in smem
+    static constexpr int kRawBlock = W4 ? 128 * 32 + 512 : 0;         // E2M1 codes + one scale atom per block
+    static constexpr int kRawStage = KB * kRawBlock;
+    static constexpr int kEpi0 = W4 ? 8 : 4;                          // first epilogue warp
+    static constexpr int kThreads = 32 * (kEpi0 + 8);
     static constexpr int kACol = SMALLA ? kABoxBytes : kTileBytes;   // A bytes per column block
     static constexpr int kAStage = KB * kACol;
-    static constexpr int kBStage = KB * kTileBytes;
+    static constexpr int kBStage = KB * BN * 128;                     // B tile: BN rows of 128 bytes
     static constexpr int kSfStage = NVF4 ? KB * kSfStageBytes : 0;   // per operand
     static constexpr int kSlack = SMALLA ? kTileBytes - kABoxBytes : 0;
     static constexpr int kElemsPerBlock = NVF4 ? 256 : (KIND == kKindFp8 ? 128 : 64);
-    static constexpr int kTmaXPerBlock = KIND == kKindBf16 ? 64 : 128;  // tensor-map x units per block
+    static constexpr int kTmaXPerBlock = (KIND == kKindBf16 || W4) ? 64 : 128;  // tensor-map x units per block
     static constexpr int kStepsPerBlock = 4;                          // MMA K steps per block
     static constexpr int kSfCols = NVF4 ? 32 * KB : 0;                // TMEM columns per stage
     static constexpr bool kStagedCombine = NVF4 && !SMALLA;           // combine via smem staging
     static constexpr int kStgBytes = kStagedCombine ? 8 * 4096 : 0;   // one 4 KB buffer per epilogue warp
 };
 
-template <int KIND, bool SMALLA, int KB>
+template <int KIND, bool SMALLA, int KB, int BN = kBN>
 constexpr int gemm_smem_bytes(int stages) {
-    using C = GemmCfg<KIND, SMALLA, KB>;
+    using C = GemmCfg<KIND, SMALLA, KB, BN>;
     return 1024 + stages * (C::kAStage + C::kBStage + 2 * C::kSfStage) + C::kSlack + 256 +
-           (C::NVF4 ? static_cast<int>((sizeof(SmemTables) + 15) & ~static_cast<size_t>(15)) : 0) +
-           C::kStgBytes;
+           stages * C::kRawStage +
+           (C::kTables ? static_cast<int>((sizeof(SmemTables) + 15) & ~static_cast<size_t>(15)) : 0) +
+           C::kStgBytes + (C::W4 ? 1024 : 0);
 }
 
 constexpr int kEpiWarps = 8;
 constexpr int kEpiWarp0 = 4;
 constexpr int kGemmThreads = 32 * (kEpiWarp0 + kEpiWarps);
+constexpr int kConvWarps = 6;   // W4A16: warps 2..7 decode the weight tiles
 
-template <int KIND, bool SMALLA, int KB, int STAGES>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+// E2M1 code -> bf16 bits (sign kept; E2M1 values 0, .5, 1, 1.5, 2, 3, 4, 6 are exact in bf16).
+__device__ __forceinline__ uint32_t e2m1_bf16_bits(uint32_t c) {
+    const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+    const uint32_t mag = e == 0 ? (m ? 0x3F00u : 0u) : (((126u + e) << 7) | (m << 6));
+    return mag | ((c & 8u) << 12);
+}
+
+// The W4A16 converter: block b of stage `raw` (128 rows x 32 bytes of E2M1 codes, then one
+// 512-byte scale atom) -> a 128 x 64 bf16 tile in the SW128 layout at `dst` (16-byte chunk c
+// of row r at chunk slot c ^ (r % 8)).  Thread `ct` of `nct` takes (row, 16-element group)
+// units; each element is value(code) * value(scale) in bf16, exact.
+__device__ __forceinline__ void w4_convert_block(const uint8_t *raw, uint8_t *dst, const uint32_t *lut,
+                                                 int ct, int nct) {
+    for (int u = ct; u < 128 * 4; u += nct) {
+        const int r = u >> 2, grp = u & 3;
+        const uint2 codes = *reinterpret_cast<const uint2 *>(raw + r * 32 + grp * 8);
+        const uint32_t sfb = raw[4096 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + grp];
+        const uint32_t sbits = __float_as_uint(e4m3_to_f32(sfb)) >> 16;   // exact: <= 4 significant bits
+        const __nv_bfloat162 sc = __halves2bfloat162(__ushort_as_bfloat16(static_cast<unsigned short>(sbits)),
+                                                     __ushort_as_bfloat16(static_cast<unsigned short>(sbits)));
+        const uint32_t cw[2] = {codes.x, codes.y};
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t byte = (cw[i >> 2] >> (8 * (i & 3))) & 0xFFu;
+            uint32_t v = lut[byte];
+            __nv_bfloat162 p = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&v), sc);
+            o[i] = *reinterpret_cast<uint32_t *>(&p);
+        }
+        uint8_t *row = dst + r * 128;
+        *reinterpret_cast<uint4 *>(row + (((2 * grp) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4 *>(row + (((2 * grp + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+// BN: tile width, 128 or (dense kinds without scale factors) 256: a 256-column tile moves
+// 48 KB of operands per 64-element K block for twice the outputs of a 128-column one.
+template <int KIND, bool SMALLA, int KB, int STAGES, int BN = kBN>
+__global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmArgs g) {
-    using C = GemmCfg<KIND, SMALLA, KB>;
+    using C = GemmCfg<KIND, SMALLA, KB, BN>;
+    static_assert(BN == 128 || (BN == 256 && (KIND == kKindBf16 || KIND == kKindFp8)), "tile width");
     constexpr bool NVF4 = C::NVF4;
+    constexpr bool W4 = C::W4;
+    constexpr int kEpi0 = C::kEpi0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -395,7 +468,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint8_t *sB = sA + STAGES * C::kAStage + C::kSlack;
     uint8_t *sSFA = sB + STAGES * C::kBStage;
     uint8_t *sSFB = sSFA + STAGES * C::kSfStage;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sSFB + STAGES * C::kSfStage);
+    uint8_t *sRaw = sSFB + STAGES * C::kSfStage;              // W4A16: raw weight blocks
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sRaw + STAGES * C::kRawStage);
     uint64_t *full = bars, *empty = bars + STAGES, *sfready = bars + 2 * STAGES;
     uint64_t *tfull = bars + 3 * STAGES, *tempty = tfull + 2, *drain = tempty + 2;
     uint64_t *cdrain = drain + 1;   // [2]: one per scale copier
@@ -403,20 +477,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
     SmemTables *tb = reinterpret_cast<SmemTables *>(bars + 256 / 8);
     float4 *stg_all = reinterpret_cast<float4 *>(reinterpret_cast<uint8_t *>(tb) +
-                                                 (NVF4 ? ((sizeof(SmemTables) + 15) & ~static_cast<size_t>(15)) : 0));
+                                                 (C::kTables ? ((sizeof(SmemTables) + 15) & ~static_cast<size_t>(15)) : 0));
+    uint32_t *lut = reinterpret_cast<uint32_t *>(stg_all);    // W4A16: code byte -> two bf16
 
-    constexpr uint32_t kAccCols = kBN;
-    constexpr uint32_t kTmemCols = NVF4 ? 512 : 256;
+    constexpr uint32_t kAccCols = BN;
+    constexpr uint32_t kTmemCols = NVF4 ? 512 : 2 * BN;
     constexpr uint32_t kSfCol0 = 2 * kAccCols;
     static_assert(!NVF4 || kSfCol0 + STAGES * C::kSfCols <= 512, "TMEM budget");
     static_assert(3 * STAGES + 8 <= 32, "barrier area");
+    static_assert(!W4 || kEpi0 == 2 + kConvWarps, "warp roles");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&sfready[s], 2);
+            mbar_init(&sfready[s], W4 ? kConvWarps : 2);   // scales copied / weights decoded
         }
         for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], kEpiWarps); }
         mbar_init(drain, 1);
@@ -429,7 +505,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 1) { tmem_alloc(s_tmem, kTmemCols); tmem_relinquish(); }
     pdl_wait();      // the previous kernel's outputs (tables, activations) are complete
     pdl_trigger();
-    if (NVF4 && g.grouped) {
+    if (W4)
+        for (int i = threadIdx.x; i < 256; i += blockDim.x)
+            lut[i] = e2m1_bf16_bits(i & 15u) | (e2m1_bf16_bits(i >> 4) << 16);
+    if (C::kTables && g.grouped) {
         for (int i = threadIdx.x; i <= g.E; i += blockDim.x) {
             tb->mt[i] = __ldg(g.mt_start + i);
             if (i < g.E) { tb->seg[i] = __ldg(g.seg_start + i); tb->cnt[i] = __ldg(g.counts + i); }
@@ -455,21 +534,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x) {
                 const Tile tl = decode_tile(g, tb, t);
                 const uint8_t *sfa_tile = NVF4 ? g.sfa + static_cast<size_t>(tl.a_row0 >> 7) * K64 * 512 : nullptr;
-                const uint8_t *sfb_tile = NVF4 ? g.sfb + (static_cast<size_t>(tl.e) * g.NB + (tl.n0 >> 7)) * K64 * 512 : nullptr;
+                const uint8_t *sfb_tile = (NVF4 || W4) ? g.sfb + (static_cast<size_t>(tl.e) * g.NB + (tl.n0 >> 7)) * K64 * 512 : nullptr;
                 for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
                     if (!role_wait(&empty[stage], phase ^ 1, s_abort, g.err)) break;
                     const int kb0 = kt * KB;
-                    const int nsteps = NVF4 ? min(4 * KB, K64 - 4 * kb0) : 4 * KB;
-                    const uint32_t bytes = KB * (C::kACol + kTileBytes) + (NVF4 ? 2 * nsteps * 512 : 0);
                     uint64_t *fb = &full[stage];
-                    mbar_arrive_expect_tx(fb, bytes);
                     const uint32_t a_st = sA0 + stage * C::kAStage, b_st = sB0 + stage * C::kBStage;
+                    if constexpr (W4) {
+                        // activations (bf16), raw E2M1 codes and the scale atom of each 64-element block
+                        const int nb = min(KB, K64 - kb0);
+                        mbar_arrive_expect_tx(fb, nb * (C::kACol + C::kRawBlock));
+                        const uint32_t r_st = smem_u32(sRaw) + stage * C::kRawStage;
+                        for (int b = 0; b < nb; ++b) {
+                            tma_load_2d_u32(a_st + b * C::kACol, &tmA, fb, (kb0 + b) * 64, tl.a_row0);
+                            tma_load_2d_u32(r_st + b * C::kRawBlock, &tmB, fb, (kb0 + b) * 32, tl.b_row0);
+                            bulk_load_u32(r_st + b * C::kRawBlock + 4096, sfb_tile + (kb0 + b) * 512, 512, fb);
+                        }
+                        issued |= 1u << stage;
+                        issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                        continue;
+                    }
+                    const int nsteps = NVF4 ? min(4 * KB, K64 - 4 * kb0) : 4 * KB;
+                    const uint32_t bytes = KB * (C::kACol + BN * 128) + (NVF4 ? 2 * nsteps * 512 : 0);
+                    mbar_arrive_expect_tx(fb, bytes);
 #pragma unroll
                     for (int b = 0; b < KB; ++b) {
                         const int kx = (kb0 + b) * C::kTmaXPerBlock;
                         const int kxa = g.a_kwrap > 0 ? kx % g.a_kwrap : kx;
                         tma_load_2d_u32(a_st + b * C::kACol, &tmA, fb, kxa, tl.a_row0);
-                        tma_load_2d_u32(b_st + b * kTileBytes, &tmB, fb, kx, tl.b_row0);
+                        tma_load_2d_u32(b_st + b * (BN * 128), &tmB, fb, kx, tl.b_row0);
                     }
                     if (NVF4) {
                         bulk_load_u32(sSFA0 + stage * C::kSfStage, sfa_tile + kb0 * 2048, nsteps * 512, fb);
@@ -493,8 +587,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = NVF4 ? idesc_nvf4(kBM, kBN)
-                                        : (KIND == kKindFp8 ? idesc_f8(kBM, kBN) : idesc_bf16(kBM, kBN));
+            const uint32_t idesc = NVF4 ? idesc_nvf4(kBM, BN)
+                                        : (KIND == kKindFp8 ? idesc_f8(kBM, BN) : idesc_bf16(kBM, BN));
             // descriptors of stage 0; a stage adds its byte offset >> 4 to the start address
             const uint64_t adesc0 = sdesc_sw128(smem_u32(sA)), bdesc0 = sdesc_sw128(smem_u32(sB));
             int stage = 0;
@@ -510,7 +604,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 bool ok = true;
                 for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
                     if (!role_wait(&full[stage], phase, s_abort, g.err)) { ok = false; break; }
-                    if (NVF4 && !role_wait(&sfready[stage], phase, s_abort, g.err)) { ok = false; break; }
+                    if ((NVF4 || W4) && !role_wait(&sfready[stage], phase, s_abort, g.err)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t ad = adesc0 + ((stage * C::kAStage) >> 4);
                     const uint64_t bd = bdesc0 + ((stage * C::kBStage) >> 4);
@@ -522,20 +616,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         for (int kk = 0; kk < 4 * KB; ++kk) {
                             if (kk < nsteps)
                                 mma_nvf4(d_tmem, ad + (((kk >> 2) * C::kACol + (kk & 3) * 32) >> 4),
-                                         bd + (((kk >> 2) * kTileBytes + (kk & 3) * 32) >> 4), idesc,
+                                         bd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4), idesc,
                                          sf_t + kk * 4, sf_t + 16 * KB + kk * 4, (acc_flag0 | kk) ? 1u : 0u);
                         }
+                    } else if constexpr (W4) {
+                        const int nb = min(KB, K64 - kt * KB);    // 64-element blocks present
+                        for (int kk = 0; kk < 4 * nb; ++kk)
+                            mma_bf16(d_tmem, ad + (((kk >> 2) * C::kACol + (kk & 3) * 32) >> 4),
+                                     bd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4), idesc,
+                                     (acc_flag0 | kk) ? 1u : 0u);
                     } else if constexpr (KIND == kKindFp8) {
 #pragma unroll
                         for (int kk = 0; kk < 4 * KB; ++kk)
                             mma_f8(d_tmem, ad + (((kk >> 2) * C::kACol + (kk & 3) * 32) >> 4),
-                                   bd + (((kk >> 2) * kTileBytes + (kk & 3) * 32) >> 4), idesc,
+                                   bd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4), idesc,
                                    (acc_flag0 | kk) ? 1u : 0u);
                     } else {
 #pragma unroll
                         for (int kk = 0; kk < 4 * KB; ++kk)
                             mma_bf16(d_tmem, ad + (((kk >> 2) * C::kACol + (kk & 3) * 32) >> 4),
-                                     bd + (((kk >> 2) * kTileBytes + (kk & 3) * 32) >> 4), idesc,
+                                     bd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4), idesc,
                                      (acc_flag0 | kk) ? 1u : 0u);
                     }
                     mma_commit(&empty[stage]);
@@ -548,6 +648,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mma_commit(drain);
             const long long t0 = clock64();
             while (!mbar_try_wait(drain, 0) && clock64() - t0 < kWaitLimitCycles) {}
+        }
+    } else if (W4 && warp < kEpi0) {
+        // ---------------------------------------------------------------- weight decoders
+        const int ct = (warp - 2) * 32 + lane;
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x) {
+            const Tile tl = decode_tile(g, tb, t);
+            bool ok = true;
+            for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
+                if (!role_wait(&full[stage], phase, s_abort, g.err)) { ok = false; break; }
+                const int nb = min(KB, K64 - kt * KB);
+                for (int b = 0; b < nb; ++b)
+                    w4_convert_block(sRaw + stage * C::kRawStage + b * C::kRawBlock,
+                                     sB + stage * C::kBStage + b * (BN * 128), lut, ct, kConvWarps * 32);
+                fence_proxy_async();          // the tensor core reads what these threads wrote
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sfready[stage]);
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            }
+            if (!ok) break;
         }
     } else if (warp == 2 || warp == 3) {
         // ---------------------------------------------------------------- scale copiers
@@ -583,7 +704,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // ---------------------------------------------------------------- epilogue
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
-        const int ch0 = ((warp - kEpiWarp0) / 4) * (kBN / 32 / 2);   // this warp's half of the columns
+        const int ch0 = ((warp - kEpi0) / 4) * (BN / 32 / 2);   // this warp's half of the columns
         int it = 0;
         for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x, ++it) {
             const Tile tl = decode_tile(g, tb, t);
@@ -599,13 +720,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t taddr = tmem + acc * kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
             if (live) {
 #pragma unroll 1
-                for (int ch = ch0; ch < ch0 + kBN / 32 / 2; ++ch) {
+                for (int ch = ch0; ch < ch0 + BN / 32 / 2; ++ch) {
                     if (ch * 32 >= tl.cols) break;
                     uint32_t r[32];
                     tmem_ld32(taddr + ch * 32, r);
                     tmem_wait_ld();
                     if (C::kStagedCombine && g.epi == EPI_COMBINE)
-                        combine_staged(g, tl, er, ch * 32, r, stg_all + (warp - kEpiWarp0) * 256, lane);
+                        combine_staged(g, tl, er, ch * 32, r, stg_all + (warp - kEpi0) * 256, lane);
                     else
                         epilogue_chunk(g, tl, er, row, ch * 32, r);
                 }

@@ -35,8 +35,14 @@ constexpr int kStagesF4Small = 4;     // decode (T <= 32): 4 KB A boxes, 2 colum
 constexpr int kStagesBF16Small = 5;
 constexpr int kStagesF8 = 6;          // FP8 stages have the BF16 byte layout
 constexpr int kStagesF8Small = 5;
+constexpr int kStagesWide = 4;        // bf16 / fp8 with 256-column tiles: 48 KB per stage
+constexpr int kBNWide = 256;
+constexpr int kStagesW4 = 5;          // W4A16: bf16 A + decoded bf16 B + raw E2M1 block per stage
+constexpr int kStagesW4Small = 4;
 constexpr int kSmallAMaxT = 32;
 inline int kb_for(bool small_a) { return small_a ? 2 : 1; }   // column blocks per stage
+// tile width of the dense (bf16 / fp8) GEMMs: 256 outside decode (fewer operand bytes per output)
+inline int bn_for(bool small_a) { return small_a ? 128 : 256; }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -74,6 +80,21 @@ bool make_map(CUtensorMap *m, bool bf16, const void *ptr, uint64_t inner, uint64
     return r == CUDA_SUCCESS;
 }
 
+// Raw (unswizzled) byte map of E2M1 weight codes [rows][K/2] for the W4A16 decoders: a box
+// of 32 bytes (64 elements) by 128 rows lands in smem as [128][32].
+bool make_map_raw(CUtensorMap *m, const void *ptr, uint64_t inner_bytes, uint64_t rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner_bytes, rows};
+    cuuint64_t strides[1] = {inner_bytes};
+    cuuint32_t box[2] = {32u, 128u};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Launch with programmatic stream serialization: the kernel's CTAs may be scheduled while the
@@ -98,7 +119,7 @@ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct WsLayout {
     size_t idx, w, counts, seg, mt, slot_off, nrows, row_slot, router, zacc, zq_codes, zq_sf, z_dbg,
-        a_codes, a_sf, h_codes, h_sf, h_dbg, c_acc, c, yacc, xs_q, hs_q, hs_dbg, s_out, total;
+        a_codes, a_sf, h_codes, h_sf, h_dbg, c_acc, c, yacc, xs_q, hs_q, hs_dbg, s_out, a_bf16, h_bf16, total;
     int64_t R;   // row capacity of the permuted buffers (multiple of 128)
     bool small_router, split_down, split_up;
     int down_splits, up_splits;
@@ -123,12 +144,15 @@ struct lmoe_ctx {
     float amax_z, amax_h;
     QScale qz, qh;
     CUtensorMap tm_wd, tm_wu, tm_w1, tm_w2;
+    CUtensorMap tm_wd_w, tm_wu_w;     // 256-row boxes for the wide (256-column) tiles
+    int w4a16;                        // experts in W4A16 form (bf16 z, h; weights decoded in smem)
+    CUtensorMap tm_w1raw, tm_w2raw;   // unswizzled code maps for the W4A16 decoders
     // shared expert (FP8 E4M3, per-tensor scales); shared_ffn == 0: none
     int shared_ffn;
     uint8_t *ws1_codes, *ws2_codes;
     float ws1_sdec, ws2_sdec, amax_xs, amax_hs;
     float alpha_s1, alpha_s2, s_enc_hs;
-    CUtensorMap tm_ws1, tm_ws2;
+    CUtensorMap tm_ws1, tm_ws2, tm_ws1_w, tm_ws2_w;
     unsigned *err;
     int debug;
     void *route_ws;
@@ -180,8 +204,9 @@ WsLayout layout(const lmoe_ctx *c, int64_t T) {
     L.small_router = T <= kSmallMaxT;
     const int mt = static_cast<int>(cdiv(T, 128));
     const int kb = kb_for(T <= kSmallAMaxT);
-    L.down_splits = plan_splits(mt, static_cast<int>(cdiv(l, 128)), static_cast<int>(cdiv(d / 64, kb)), c->num_sms);
-    L.up_splits = plan_splits(mt, static_cast<int>(cdiv(d, 128)), static_cast<int>(cdiv(l / 64, kb)), c->num_sms);
+    const int bn = bn_for(T <= kSmallAMaxT);
+    L.down_splits = plan_splits(mt, static_cast<int>(cdiv(l, bn)), static_cast<int>(cdiv(d / 64, kb)), c->num_sms);
+    L.up_splits = plan_splits(mt, static_cast<int>(cdiv(d, bn)), static_cast<int>(cdiv(l / 64, kb)), c->num_sms);
     L.split_down = L.down_splits > 1;
     L.split_up = L.up_splits > 1;
     size_t off = 0;
@@ -199,11 +224,14 @@ WsLayout layout(const lmoe_ctx *c, int64_t T) {
     L.zq_codes = take(T * l / 2);
     L.zq_sf = take(T * l / 16);
     L.z_dbg = take(c->debug ? T * l * 2 : 0);
-    L.a_codes = take(L.R * l / 2);
-    L.a_sf = take(L.R * l / 16);
-    L.h_codes = take(L.R * F / 2);
-    L.h_sf = take(L.R * F / 16);
-    L.h_dbg = take(c->debug ? L.R * F * 2 : 0);
+    const bool w4 = c->w4a16 != 0;
+    L.a_codes = take(w4 ? 0 : L.R * l / 2);
+    L.a_sf = take(w4 ? 0 : L.R * l / 16);
+    L.h_codes = take(w4 ? 0 : L.R * F / 2);
+    L.h_sf = take(w4 ? 0 : L.R * F / 16);
+    L.h_dbg = take(c->debug && !w4 ? L.R * F * 2 : 0);
+    L.a_bf16 = take(w4 ? L.R * l * 2 : 0);
+    L.h_bf16 = take(w4 ? L.R * F * 2 : 0);
     L.c_acc = take(T * l * 4);
     L.c = take(T * l * 2);
     L.yacc = take(L.split_up ? T * d * 4 : 0);
@@ -216,19 +244,20 @@ WsLayout layout(const lmoe_ctx *c, int64_t T) {
     return L;
 }
 
-template <int KIND, bool SMALLA, int KB, int STAGES>
+template <int KIND, bool SMALLA, int KB, int STAGES, int BN = kBN>
 cudaError_t set_smem_attr() {
-    static_assert(gemm_smem_bytes<KIND, SMALLA, KB>(STAGES) <= 232448, "shared memory budget");
-    return cudaFuncSetAttribute(gemm_kernel<KIND, SMALLA, KB, STAGES>,
+    static_assert(gemm_smem_bytes<KIND, SMALLA, KB, BN>(STAGES) <= 232448, "shared memory budget");
+    return cudaFuncSetAttribute(gemm_kernel<KIND, SMALLA, KB, STAGES, BN>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                gemm_smem_bytes<KIND, SMALLA, KB>(STAGES));
+                                gemm_smem_bytes<KIND, SMALLA, KB, BN>(STAGES));
 }
 
-template <int KIND, bool SMALLA, int KB, int STAGES>
+template <int KIND, bool SMALLA, int KB, int STAGES, int BN = kBN>
 cudaError_t launch_gemm_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int grid,
                             cudaStream_t s) {
-    return launch_pdl(gemm_kernel<KIND, SMALLA, KB, STAGES>, dim3(grid), dim3(kGemmThreads),
-                      gemm_smem_bytes<KIND, SMALLA, KB>(STAGES), s, ta, tb, g);
+    return launch_pdl(gemm_kernel<KIND, SMALLA, KB, STAGES, BN>, dim3(grid),
+                      dim3(GemmCfg<KIND, SMALLA, KB, BN>::kThreads), gemm_smem_bytes<KIND, SMALLA, KB, BN>(STAGES),
+                      s, ta, tb, g);
 }
 
 // small_a: every tile has at most 32 valid A rows (T <= 32); such launches use two column
@@ -241,18 +270,23 @@ cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const Gemm
                        : launch_gemm_cfg<kKindNvf4, false, 1, kStagesF4>(ta, tb, g, grid, s);
     if (KIND == kKindFp8)
         return small_a ? launch_gemm_cfg<kKindFp8, true, 2, kStagesF8Small>(ta, tb, g, grid, s)
-                       : launch_gemm_cfg<kKindFp8, false, 1, kStagesF8>(ta, tb, g, grid, s);
+                       : launch_gemm_cfg<kKindFp8, false, 1, kStagesWide, kBNWide>(ta, tb, g, grid, s);
+    if (KIND == kKindW4A16)
+        return small_a ? launch_gemm_cfg<kKindW4A16, true, 2, kStagesW4Small>(ta, tb, g, grid, s)
+                       : launch_gemm_cfg<kKindW4A16, false, 1, kStagesW4>(ta, tb, g, grid, s);
     return small_a ? launch_gemm_cfg<kKindBf16, true, 2, kStagesBF16Small>(ta, tb, g, grid, s)
-                   : launch_gemm_cfg<kKindBf16, false, 1, kStagesBF16>(ta, tb, g, grid, s);
+                   : launch_gemm_cfg<kKindBf16, false, 1, kStagesWide, kBNWide>(ta, tb, g, grid, s);
 }
 
 // K elements per 128-byte column block: 64 (bf16) or 128 (fp8).
-GemmArgs dense_args(int M, int N, int K, int splits, int epi, unsigned *err, int kb, int k_block = 64) {
+GemmArgs dense_args(int M, int N, int K, int splits, int epi, unsigned *err, int kb, int k_block = 64,
+                    int bn = kBN) {
     GemmArgs g;
     std::memset(&g, 0, sizeof(g));
     g.M = M; g.N = N; g.K = K;
+    g.bn = bn;
     g.m_tiles = static_cast<int>(cdiv(M, kBM));
-    g.n_tiles = static_cast<int>(cdiv(N, kBN));
+    g.n_tiles = static_cast<int>(cdiv(N, bn));
     g.k_tiles = static_cast<int>(cdiv(cdiv(K, k_block), kb));
     g.kt_per_split = static_cast<int>(cdiv(g.k_tiles, splits));
     g.k_splits = static_cast<int>(cdiv(g.k_tiles, g.kt_per_split));
@@ -316,10 +350,10 @@ lmoe_status launch_router(lmoe_ctx *c, const __nv_bfloat16 *x, int64_t T, float 
     const int d = c->d, E = c->E;
     CUtensorMap tx;
     if (!make_map(&tx, true, x, d, T, static_cast<uint64_t>(d) * 2, kBM)) return LMOE_ECUDA;
-    const int m_tiles = static_cast<int>(cdiv(T, kBM)), n_tiles = static_cast<int>(cdiv(E, kBN));
+    const int m_tiles = static_cast<int>(cdiv(T, kBM)), n_tiles = static_cast<int>(cdiv(E, kBNWide));
     const int k_tiles = 2 * d / 64;
     const int splits = std::min<int>(k_tiles, std::max<int>(8, static_cast<int>(cdiv(2 * c->num_sms, int64_t(m_tiles) * n_tiles))));
-    GemmArgs g = dense_args(static_cast<int>(T), E, 2 * d, splits, EPI_RED_F32, c->err, 1);
+    GemmArgs g = dense_args(static_cast<int>(T), E, 2 * d, splits, EPI_RED_F32, c->err, 1, 64, kBNWide);
     g.out = scratch;
     g.ld_out = E;
     g.a_kwrap = d;
@@ -329,10 +363,19 @@ lmoe_status launch_router(lmoe_ctx *c, const __nv_bfloat16 *x, int64_t T, float 
     // accumulation bound: per K-slice 4 block steps per k-tile (+2), plus the fp32 sum of the
     // slices, each within 2^-23 of the running magnitude; times a margin of 4
     const float coef = 4.0f * static_cast<float>(4 * g.kt_per_split + 2 + g.k_splits) * 0x1p-23f;
-    LMOE_CUDA(launch_pdl(router_select_kernel, dim3(static_cast<unsigned>(T)), dim3(kSelThreads),
-                         router_select_smem(d), s, static_cast<const float *>(scratch),
-                         static_cast<const float *>(c->b_router), x, static_cast<const float *>(c->w_rows),
-                         static_cast<int>(T), d, E, c->k, coef, c->wn_max, c->bmax, idx, w, counts, slot_off));
+    const dim3 sgrid(static_cast<unsigned>(cdiv(T, kSelWarps))), sblock(32 * kSelWarps);
+    const float *ap = scratch;
+    const float *wr = c->w_rows;
+    const float *bp = c->b_router;
+    if (E <= 128)
+        LMOE_CUDA(launch_pdl(router_select_kernel<4>, sgrid, sblock, 0, s, ap, bp, x, wr, static_cast<int>(T), d, E,
+                             c->k, coef, c->wn_max, c->bmax, idx, w, counts, slot_off));
+    else if (E <= 512)
+        LMOE_CUDA(launch_pdl(router_select_kernel<16>, sgrid, sblock, 0, s, ap, bp, x, wr, static_cast<int>(T), d, E,
+                             c->k, coef, c->wn_max, c->bmax, idx, w, counts, slot_off));
+    else
+        LMOE_CUDA(launch_pdl(router_select_kernel<32>, sgrid, sblock, 0, s, ap, bp, x, wr, static_cast<int>(T), d, E,
+                             c->k, coef, c->wn_max, c->bmax, idx, w, counts, slot_off));
     prof_mark(c, "router_select", s);
     return LMOE_OK;
 }
@@ -392,10 +435,11 @@ const char *lmoe_status_string(lmoe_status s) {
     return "unknown status";
 }
 
-lmoe_status lmoe_quantize_nvfp4(const void *src, lmoe_dtype dt, int64_t rows, int64_t K, float amax,
-                                uint8_t *codes, uint8_t *sf, float *tensor_scale,
-                                lmoe_stream stream) {
+static lmoe_status quantize_nvfp4_impl(const void *src, lmoe_dtype dt, int64_t rows, int64_t K, float amax,
+                                       uint8_t *codes, uint8_t *sf, float *tensor_scale, lmoe_stream stream,
+                                       bool two_d) {
     if (rows < 0 || K <= 0 || K % 16 != 0 || (dt != LMOE_BF16 && dt != LMOE_FP32)) return LMOE_EINVAL;
+    if (two_d && rows % 16 != 0) return LMOE_EINVAL;
     if (rows == 0) return LMOE_OK;
     if (!src || !codes || !sf || !tensor_scale) return LMOE_EINVAL;
     if (amax != amax) return LMOE_EINVAL;
@@ -417,16 +461,35 @@ lmoe_status lmoe_quantize_nvfp4(const void *src, lmoe_dtype dt, int64_t rows, in
         std::memcpy(&ab, &amax, sizeof(ab));
         LMOE_CUDA(cudaMemcpyAsync(bits, &ab, sizeof(ab), cudaMemcpyHostToDevice, s));
     }
-    if (dt == LMOE_BF16)
+    if (two_d) {
+        const int g2 = static_cast<int>(std::min<int64_t>(cdiv(blocks / 16, 256), 148 * 16));
+        if (dt == LMOE_BF16)
+            quantize_rows_2d_kernel<__nv_bfloat16><<<g2, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(src),
+                                                                     rows, K, -1.0f, bits, codes, sf);
+        else
+            quantize_rows_2d_kernel<float><<<g2, 256, 0, s>>>(static_cast<const float *>(src), rows, K, -1.0f,
+                                                             bits, codes, sf);
+    } else if (dt == LMOE_BF16) {
         quantize_rows_kernel<__nv_bfloat16><<<qgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(src),
                                                                  rows, K, -1.0f, bits, codes, sf);
-    else
+    } else {
         quantize_rows_kernel<float><<<qgrid, 256, 0, s>>>(static_cast<const float *>(src), rows, K, -1.0f,
                                                          bits, codes, sf);
+    }
     LMOE_LAUNCH();
     tensor_scale_kernel<<<1, 32, 0, s>>>(bits, 1, tensor_scale);
     LMOE_LAUNCH();
     return LMOE_OK;
+}
+
+lmoe_status lmoe_quantize_nvfp4(const void *src, lmoe_dtype dt, int64_t rows, int64_t K, float amax,
+                                uint8_t *codes, uint8_t *sf, float *tensor_scale, lmoe_stream stream) {
+    return quantize_nvfp4_impl(src, dt, rows, K, amax, codes, sf, tensor_scale, stream, false);
+}
+
+lmoe_status lmoe_quantize_nvfp4_2d(const void *src, lmoe_dtype dt, int64_t rows, int64_t K, float amax,
+                                   uint8_t *codes, uint8_t *sf, float *tensor_scale, lmoe_stream stream) {
+    return quantize_nvfp4_impl(src, dt, rows, K, amax, codes, sf, tensor_scale, stream, true);
 }
 
 lmoe_status lmoe_quantize_fp8(const void *src, lmoe_dtype dt, int64_t n, float amax, uint8_t *codes,
@@ -472,6 +535,8 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
     if (l > 4096 || d > kSelMaxD) return LMOE_EINVAL;
     if (k < 1 || k > 32 || E < k || E > 1024 || E % 4) return LMOE_EINVAL;
     if (!(w->amax_z > 0.0f) || !(w->amax_h > 0.0f)) return LMOE_EINVAL;
+    if (w->weight_blocks_2d != 0 && w->weight_blocks_2d != 1) return LMOE_EINVAL;
+    if (w->expert_w4a16 != 0 && w->expert_w4a16 != 1) return LMOE_EINVAL;
     const bool has_shared = w->ws1 != nullptr;
     if (has_shared && (!w->ws2 || w->shared_ffn <= 0 || w->shared_ffn % 64 || !(w->amax_xs > 0.0f) ||
                        !(w->amax_hs > 0.0f)))
@@ -491,12 +556,13 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
             if (a == cudaSuccess) a = set_smem_attr<kKindNvf4, true, 2, kStagesF4Small>();
             if (b == cudaSuccess) b = set_smem_attr<kKindBf16, true, 2, kStagesBF16Small>();
             if (a == cudaSuccess) a = set_smem_attr<kKindFp8, false, 1, kStagesF8>();
+            if (a == cudaSuccess) a = set_smem_attr<kKindW4A16, false, 1, kStagesW4>();
+            if (a == cudaSuccess) a = set_smem_attr<kKindBf16, false, 1, kStagesWide, kBNWide>();
+            if (a == cudaSuccess) a = set_smem_attr<kKindFp8, false, 1, kStagesWide, kBNWide>();
+            if (a == cudaSuccess) a = set_smem_attr<kKindW4A16, true, 2, kStagesW4Small>();
             if (a == cudaSuccess) a = set_smem_attr<kKindFp8, true, 2, kStagesF8Small>();
-            cudaError_t r = cudaFuncSetAttribute(router_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 router_select_smem(kSelMaxD));
-            if (r == cudaSuccess)
-                r = cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kRouterSmallSmem);
+            cudaError_t r = cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kRouterSmallSmem);
             attr_err = a != cudaSuccess ? a : (b != cudaSuccess ? b : r);
         });
         if (attr_err != cudaSuccess) return cuda_status(attr_err);
@@ -512,6 +578,7 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
     c->amax_h = w->amax_h;
     c->qz = qscale_from_amax(w->amax_z);
     c->qh = qscale_from_amax(w->amax_h);
+    c->w4a16 = w->expert_w4a16;
     auto fail = [&](lmoe_status st) { lmoe_destroy(c); return st; };
 #define CREATE_CUDA(call)                                   \
     do {                                                    \
@@ -563,10 +630,17 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
     amax_segments_kernel<<<dim3(16, E), 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->w2), seg2, c->amax_bits + E);
     CREATE_CUDA(cudaGetLastError());
     const int qgrid = c->num_sms * 16;
-    quantize_experts_kernel<<<qgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->w1), E, ffn, l,
-                                                  c->amax_bits, c->w1_codes, c->w1_sf);
-    quantize_experts_kernel<<<qgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->w2), E, l, ffn,
-                                                  c->amax_bits + E, c->w2_codes, c->w2_sf);
+    if (w->weight_blocks_2d) {
+        quantize_experts_2d_kernel<<<qgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->w1), E, ffn, l,
+                                                         c->amax_bits, c->w1_codes, c->w1_sf);
+        quantize_experts_2d_kernel<<<qgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->w2), E, l, ffn,
+                                                         c->amax_bits + E, c->w2_codes, c->w2_sf);
+    } else {
+        quantize_experts_kernel<<<qgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->w1), E, ffn, l,
+                                                      c->amax_bits, c->w1_codes, c->w1_sf);
+        quantize_experts_kernel<<<qgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->w2), E, l, ffn,
+                                                      c->amax_bits + E, c->w2_codes, c->w2_sf);
+    }
     tensor_scale_kernel<<<cdiv(E, 256), 256, 0, s>>>(c->amax_bits, E, c->w1_sdec);
     tensor_scale_kernel<<<cdiv(E, 256), 256, 0, s>>>(c->amax_bits + E, E, c->w2_sdec);
     CREATE_CUDA(cudaGetLastError());
@@ -636,10 +710,16 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
         c->alpha_s2 = p2;
         c->s_enc_hs = fp8scale_from_amax(c->amax_hs).s_enc;
         if (!make_map(&c->tm_ws1, false, c->ws1_codes, d, FS, d) ||
-            !make_map(&c->tm_ws2, false, c->ws2_codes, FS, d, FS))
+            !make_map(&c->tm_ws2, false, c->ws2_codes, FS, d, FS) ||
+            !make_map(&c->tm_ws1_w, false, c->ws1_codes, d, FS, d, kBNWide) ||
+            !make_map(&c->tm_ws2_w, false, c->ws2_codes, FS, d, FS, kBNWide))
             return fail(LMOE_ECUDA);
     }
-    bool ok = make_map(&c->tm_wsplit, true, c->w_split, 2 * d, E, static_cast<uint64_t>(2 * d) * 2) &&
+    bool ok = make_map_raw(&c->tm_w1raw, c->w1_codes, l / 2, static_cast<uint64_t>(E) * ffn) &&
+              make_map_raw(&c->tm_w2raw, c->w2_codes, ffn / 2, static_cast<uint64_t>(E) * l) &&
+              make_map(&c->tm_wsplit, true, c->w_split, 2 * d, E, static_cast<uint64_t>(2 * d) * 2, kBNWide) &&
+              make_map(&c->tm_wd_w, true, c->w_down, d, l, static_cast<uint64_t>(d) * 2, kBNWide) &&
+              make_map(&c->tm_wu_w, true, c->w_up, l, d, static_cast<uint64_t>(l) * 2, kBNWide) &&
               make_map(&c->tm_wd, true, c->w_down, d, l, static_cast<uint64_t>(d) * 2) &&
               make_map(&c->tm_wu, true, c->w_up, l, d, static_cast<uint64_t>(l) * 2) &&
               make_map(&c->tm_w1, false, c->w1_codes, l / 2, static_cast<uint64_t>(E) * ffn, l / 2) &&
@@ -709,9 +789,12 @@ lmoe_status lmoe_workspace_range(const lmoe_ctx *c, int64_t T, int stage, size_t
     case LMOE_STAGE_C: *offset = L.c; *bytes = T * l * 2; break;
     case LMOE_STAGE_Z: *offset = L.z_dbg; *bytes = c->debug ? T * l * 2 : 0; break;
     case LMOE_STAGE_ROWS: *offset = L.row_slot; *bytes = L.R * 4; break;
-    case LMOE_STAGE_H: *offset = L.h_dbg; *bytes = c->debug ? L.R * F * 2 : 0; break;
-    case LMOE_STAGE_HQ_CODES: *offset = L.h_codes; *bytes = L.R * F / 2; break;
-    case LMOE_STAGE_HQ_SF: *offset = L.h_sf; *bytes = L.R * F / 16; break;
+    case LMOE_STAGE_H:
+        if (c->w4a16) { *offset = L.h_bf16; *bytes = L.R * F * 2; }
+        else { *offset = L.h_dbg; *bytes = c->debug ? L.R * F * 2 : 0; }
+        break;
+    case LMOE_STAGE_HQ_CODES: *offset = L.h_codes; *bytes = c->w4a16 ? 0 : L.R * F / 2; break;
+    case LMOE_STAGE_HQ_SF: *offset = L.h_sf; *bytes = c->w4a16 ? 0 : L.R * F / 16; break;
     case LMOE_STAGE_NROWS: *offset = L.nrows; *bytes = 4; break;
     case LMOE_STAGE_XS_Q: *offset = L.xs_q; *bytes = c->shared_ffn ? T * c->d : 0; break;
     case LMOE_STAGE_HS: *offset = L.hs_dbg; *bytes = c->debug ? T * c->shared_ffn * 2 : 0; break;
@@ -783,6 +866,8 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     float *c_acc = static_cast<float *>(at(L.c_acc));
     __nv_bfloat16 *cb = static_cast<__nv_bfloat16 *>(at(L.c));
     float *yacc = static_cast<float *>(at(L.yacc));
+    __nv_bfloat16 *a_bf16 = c->w4a16 ? static_cast<__nv_bfloat16 *>(at(L.a_bf16)) : nullptr;
+    __nv_bfloat16 *h_bf16 = c->w4a16 ? static_cast<__nv_bfloat16 *>(at(L.h_bf16)) : nullptr;
     uint8_t *xs_q = static_cast<uint8_t *>(at(L.xs_q));
     uint8_t *hs_q = static_cast<uint8_t *>(at(L.hs_q));
     __nv_bfloat16 *hs_dbg = c->debug ? static_cast<__nv_bfloat16 *>(at(L.hs_dbg)) : nullptr;
@@ -802,15 +887,15 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         CUtensorMap tx;
         if (!make_map(&tx, true, x, d, T, static_cast<uint64_t>(d) * 2, a_box)) return LMOE_ECUDA;
         GemmArgs g = dense_args(static_cast<int>(T), l, d, L.down_splits,
-                                L.split_down ? EPI_RED_F32 : EPI_Z_QUANT, c->err, kb_for(small_a));
+                                L.split_down ? EPI_RED_F32 : EPI_Z_QUANT, c->err, kb_for(small_a), 64, bn_for(small_a));
         if (L.split_down) {
             g.out = zacc; g.ld_out = l;
         } else {
             g.q = c->qz; g.q_codes = zq_codes; g.q_sf = zq_sf; g.dbg = z_dbg;
             g.topk = k; g.idx = idx; g.slot_off = slot_off; g.seg_start = seg;
-            g.a_codes = a_codes; g.a_sf = a_sf; g.row_slot_out = row_slot;
+            g.a_codes = a_codes; g.a_sf = a_sf; g.row_slot_out = row_slot; g.a_bf16 = a_bf16;
         }
-        LMOE_CUDA((launch_gemm<kKindBf16>(tx, c->tm_wd, g,
+        LMOE_CUDA((launch_gemm<kKindBf16>(tx, small_a ? c->tm_wd : c->tm_wd_w, g,
                                       grid_for(int64_t(g.m_tiles) * g.n_tiles * g.k_splits, c->num_sms), small_a, ds)));
         prof_mark(c, "down_proj", ds);
         return LMOE_OK;
@@ -858,40 +943,62 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
             LMOE_CUDA(launch_pdl(z_finalize_kernel, dim3(static_cast<unsigned>(cdiv(T, tpb))), dim3(tpb * nb), 0, s,
                                  static_cast<const float *>(zacc), T, l, c->qz, zq_codes, zq_sf, z_dbg,
                                  static_cast<const int32_t *>(idx), static_cast<const int32_t *>(slot_off),
-                                 static_cast<const int32_t *>(seg), k, row_slot, a_codes, a_sf));
+                                 static_cast<const int32_t *>(seg), k, row_slot, a_codes, a_sf, a_bf16));
             prof_mark(c, "z_finalize", s);
         }
     }
-    // 5. latent-up grouped GEMM + relu^2 + requantize
+    // 5. latent-up grouped GEMM + relu^2 (+ requantize to NVFP4; W4A16: bf16 h)
     {
         CUtensorMap ta;
-        if (!make_map(&ta, false, a_codes, l / 2, L.R, l / 2, a_box)) return LMOE_ECUDA;
+        const bool ok = c->w4a16 ? make_map(&ta, true, a_bf16, l, L.R, static_cast<uint64_t>(l) * 2, a_box)
+                                 : make_map(&ta, false, a_codes, l / 2, L.R, l / 2, a_box);
+        if (!ok) return LMOE_ECUDA;
         GemmArgs g;
         std::memset(&g, 0, sizeof(g));
         g.M = static_cast<int>(L.R); g.N = F; g.K = l;
+        g.bn = kBN;
         g.n_tiles = static_cast<int>(cdiv(F, kBN));
-        g.k_tiles = static_cast<int>(cdiv(l, 256 * kb_for(small_a)));
         g.grouped = 1; g.E = E; g.mt_start = mt; g.seg_start = seg; g.counts = counts;
-        g.sfa = a_sf; g.sfb = c->w1_sf; g.NB = static_cast<int>(cdiv(F, 128));
-        g.epi = EPI_H_QUANT; g.q = c->qh; g.q_codes = h_codes; g.q_sf = h_sf; g.dbg = h_dbg;
-        g.alpha = c->alpha1; g.err = c->err;
-        LMOE_CUDA((launch_gemm<kKindNvf4>(ta, c->tm_w1, g, c->num_sms, small_a, s)));
+        g.sfb = c->w1_sf; g.NB = static_cast<int>(cdiv(F, 128));
+        g.err = c->err;
+        if (c->w4a16) {
+            g.k_tiles = static_cast<int>(cdiv(l / 64, kb_for(small_a)));
+            g.epi = EPI_H_BF16; g.out = h_bf16; g.alpha = c->w1_sdec;
+            LMOE_CUDA((launch_gemm<kKindW4A16>(ta, c->tm_w1raw, g, c->num_sms, small_a, s)));
+        } else {
+            g.k_tiles = static_cast<int>(cdiv(l, 256 * kb_for(small_a)));
+            g.sfa = a_sf;
+            g.epi = EPI_H_QUANT; g.q = c->qh; g.q_codes = h_codes; g.q_sf = h_sf; g.dbg = h_dbg;
+            g.alpha = c->alpha1;
+            LMOE_CUDA((launch_gemm<kKindNvf4>(ta, c->tm_w1, g, c->num_sms, small_a, s)));
+        }
         prof_mark(c, "expert_up", s);
     }
     // 6. latent-down grouped GEMM, routing weight, combine into c_acc
     {
         CUtensorMap ta;
-        if (!make_map(&ta, false, h_codes, F / 2, L.R, F / 2, a_box)) return LMOE_ECUDA;
+        const bool ok = c->w4a16 ? make_map(&ta, true, h_bf16, F, L.R, static_cast<uint64_t>(F) * 2, a_box)
+                                 : make_map(&ta, false, h_codes, F / 2, L.R, F / 2, a_box);
+        if (!ok) return LMOE_ECUDA;
         GemmArgs g;
         std::memset(&g, 0, sizeof(g));
         g.M = static_cast<int>(L.R); g.N = l; g.K = F;
+        g.bn = kBN;
         g.n_tiles = static_cast<int>(cdiv(l, kBN));
-        g.k_tiles = static_cast<int>(cdiv(F, 256 * kb_for(small_a)));
         g.grouped = 1; g.E = E; g.mt_start = mt; g.seg_start = seg; g.counts = counts;
-        g.sfa = h_sf; g.sfb = c->w2_sf; g.NB = static_cast<int>(cdiv(l, 128));
+        g.sfb = c->w2_sf; g.NB = static_cast<int>(cdiv(l, 128));
         g.epi = EPI_COMBINE; g.out = c_acc; g.ld_out = l;
-        g.alpha = c->alpha2; g.row_slot = row_slot; g.route_w = rw; g.topk = k; g.err = c->err;
-        LMOE_CUDA((launch_gemm<kKindNvf4>(ta, c->tm_w2, g, c->num_sms, small_a, s)));
+        g.row_slot = row_slot; g.route_w = rw; g.topk = k; g.err = c->err;
+        if (c->w4a16) {
+            g.k_tiles = static_cast<int>(cdiv(F / 64, kb_for(small_a)));
+            g.alpha = c->w2_sdec;
+            LMOE_CUDA((launch_gemm<kKindW4A16>(ta, c->tm_w2raw, g, c->num_sms, small_a, s)));
+        } else {
+            g.k_tiles = static_cast<int>(cdiv(F, 256 * kb_for(small_a)));
+            g.sfa = h_sf;
+            g.alpha = c->alpha2;
+            LMOE_CUDA((launch_gemm<kKindNvf4>(ta, c->tm_w2, g, c->num_sms, small_a, s)));
+        }
         prof_mark(c, "expert_down", s);
     }
     // 7. c = bf16(c_acc)
@@ -913,14 +1020,16 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         CUtensorMap txs, ths;
         if (!make_map(&txs, false, xs_q, d, T, d, a_box) || !make_map(&ths, false, hs_q, FS, T, FS, a_box))
             return LMOE_ECUDA;
-        GemmArgs g1 = dense_args(static_cast<int>(T), FS, d, 1, EPI_FP8_SQRELU, c->err, kb_for(small_a), 128);
+        GemmArgs g1 = dense_args(static_cast<int>(T), FS, d, 1, EPI_FP8_SQRELU, c->err, kb_for(small_a), 128,
+                                 bn_for(small_a));
         g1.alpha_s = c->alpha_s1; g1.s_enc8 = c->s_enc_hs; g1.q_codes = hs_q; g1.dbg = hs_dbg;
-        LMOE_CUDA((launch_gemm<kKindFp8>(txs, c->tm_ws1, g1, grid_for(int64_t(g1.m_tiles) * g1.n_tiles, c->num_sms),
+        LMOE_CUDA((launch_gemm<kKindFp8>(txs, small_a ? c->tm_ws1 : c->tm_ws1_w, g1, grid_for(int64_t(g1.m_tiles) * g1.n_tiles, c->num_sms),
                                          small_a, s)));
         prof_mark(c, "shared_up", s);
-        GemmArgs g2 = dense_args(static_cast<int>(T), d, FS, 1, EPI_STORE_SCALED, c->err, kb_for(small_a), 128);
+        GemmArgs g2 = dense_args(static_cast<int>(T), d, FS, 1, EPI_STORE_SCALED, c->err, kb_for(small_a), 128,
+                                 bn_for(small_a));
         g2.alpha_s = c->alpha_s2; g2.out = s_out; g2.ld_out = d;
-        LMOE_CUDA((launch_gemm<kKindFp8>(ths, c->tm_ws2, g2, grid_for(int64_t(g2.m_tiles) * g2.n_tiles, c->num_sms),
+        LMOE_CUDA((launch_gemm<kKindFp8>(ths, small_a ? c->tm_ws2 : c->tm_ws2_w, g2, grid_for(int64_t(g2.m_tiles) * g2.n_tiles, c->num_sms),
                                          small_a, s)));
         prof_mark(c, "shared_down", s);
     }
@@ -930,11 +1039,11 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         CUtensorMap tc;
         if (!make_map(&tc, true, cb, l, T, static_cast<uint64_t>(l) * 2, a_box)) return LMOE_ECUDA;
         GemmArgs g = dense_args(static_cast<int>(T), d, l, L.up_splits,
-                                L.split_up ? EPI_RED_F32 : EPI_STORE_BF16, c->err, kb_for(small_a));
+                                L.split_up ? EPI_RED_F32 : EPI_STORE_BF16, c->err, kb_for(small_a), 64, bn_for(small_a));
         g.out = L.split_up ? static_cast<void *>(yacc) : y;
         g.ld_out = d;
         if (!L.split_up) g.addend = y_add;
-        LMOE_CUDA((launch_gemm<kKindBf16>(tc, c->tm_wu, g,
+        LMOE_CUDA((launch_gemm<kKindBf16>(tc, small_a ? c->tm_wu : c->tm_wu_w, g,
                                                    grid_for(int64_t(g.m_tiles) * g.n_tiles * g.k_splits, c->num_sms), small_a, s)));
         prof_mark(c, "up_proj", s);
         if (L.split_up) {

@@ -52,13 +52,14 @@ __device__ __forceinline__ int slot_row(const int32_t *idx, const int32_t *slot_
 
 // Split-K finalize of the down-projection, one thread per (token, 16-block): z = bf16(zacc),
 // zq = NVFP4(z) into the row-major buffers and into the token's k segment rows (codes and
-// scale atoms); row_slot records the slot of each written row.  A block covers whole tokens
+// scale atoms; or, for W4A16, the bf16 z itself); row_slot records the slot of each row.  A block covers whole tokens
 // (blockDim / (l/16) of them); their k segment rows are looked up once into shared memory.
 __global__ void __launch_bounds__(256) z_finalize_kernel(
     const float *__restrict__ zacc, int64_t T, int l, QScale q, uint8_t *__restrict__ codes,
     uint8_t *__restrict__ sf, __nv_bfloat16 *__restrict__ z_out, const int32_t *__restrict__ idx,
     const int32_t *__restrict__ slot_off, const int32_t *__restrict__ seg_start, int k,
-    int32_t *__restrict__ row_slot, uint8_t *__restrict__ a_codes, uint8_t *__restrict__ a_sf) {
+    int32_t *__restrict__ row_slot, uint8_t *__restrict__ a_codes, uint8_t *__restrict__ a_sf,
+    __nv_bfloat16 *__restrict__ a_bf16) {
     __shared__ int rows_s[256];   // [tokens per block][k]
     pdl_wait();
     pdl_trigger();
@@ -82,10 +83,10 @@ __global__ void __launch_bounds__(256) z_finalize_kernel(
     load16<float>(zacc + i * 16, x);
 #pragma unroll
     for (int j = 0; j < 16; ++j) x[j] = bf16_bits_to_f32(f32_to_bf16_bits(x[j]));
-    if (z_out) {
-        uint32_t zb[8];
+    uint32_t zb[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) zb[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
+    for (int j = 0; j < 8; ++j) zb[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
+    if (z_out) {
         uint4 *zo = reinterpret_cast<uint4 *>(z_out + i * 16);
         zo[0] = make_uint4(zb[0], zb[1], zb[2], zb[3]);
         zo[1] = make_uint4(zb[4], zb[5], zb[6], zb[7]);
@@ -96,8 +97,14 @@ __global__ void __launch_bounds__(256) z_finalize_kernel(
     sf[i] = static_cast<uint8_t>(s);
     for (int j = 0; j < k; ++j) {
         const int row = rows_s[tl * k + j];
-        reinterpret_cast<uint2 *>(a_codes + static_cast<int64_t>(row) * (l / 2))[b] = make_uint2(lo, hi);
-        a_sf[sf_atom_offset(row, b, K64)] = static_cast<uint8_t>(s);
+        if (a_bf16) {       // W4A16: the bf16 z itself goes to the expert segments
+            uint4 *o = reinterpret_cast<uint4 *>(a_bf16 + static_cast<int64_t>(row) * l + b * 16);
+            o[0] = make_uint4(zb[0], zb[1], zb[2], zb[3]);
+            o[1] = make_uint4(zb[4], zb[5], zb[6], zb[7]);
+        } else {
+            reinterpret_cast<uint2 *>(a_codes + static_cast<int64_t>(row) * (l / 2))[b] = make_uint2(lo, hi);
+            a_sf[sf_atom_offset(row, b, K64)] = static_cast<uint8_t>(s);
+        }
     }
 }
 

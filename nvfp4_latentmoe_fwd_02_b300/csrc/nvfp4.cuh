@@ -82,6 +82,17 @@ __device__ __forceinline__ uint32_t quant_block16(const float (&x)[16], const QS
     return sf;
 }
 
+// 16 codes of a block whose scale is already decided (rcp = 1 / (value(sf) * s_dec), or 0).
+__device__ __forceinline__ void block_codes16(const float (&x)[16], float rcp, uint32_t &lo, uint32_t &hi) {
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t b = f32x2_to_e2m1x2(__fmul_rn(x[2 * i], rcp), __fmul_rn(x[2 * i + 1], rcp));
+        w[i >> 2] |= b << (8 * (i & 3));
+    }
+    lo = w[0]; hi = w[1];
+}
+
 // Byte offset of the scale of (row r, 16-block b) in the tensor-core scale-factor layout:
 // atoms of 128 rows x 4 blocks (512 B), ordered [r / 128][b / 4]; inside an atom row r
 // sits at (r % 32) * 16 + ((r / 32) % 4) * 4 and block b at + (b % 4).
@@ -207,6 +218,80 @@ __global__ void quantize_experts_kernel(const __nv_bfloat16 *__restrict__ src, i
         reinterpret_cast<uint2 *>(codes)[i] = make_uint2(lo, hi);
         sf_atoms[static_cast<size_t>(e) * NB * K64 * 512 + sf_atom_offset(r, b, K64)] =
             static_cast<uint8_t>(s);
+    }
+}
+
+// 2-D weight blocks (NVIDIA AI releases Nemotron 3 Ultra, architecture paragraph: weights
+// quantized in two-dimensional blocks; 16 x 16 here): one E4M3 scale per 16 rows x 16
+// contraction elements from the block's amax, the 1-D arithmetic otherwise.  One thread per
+// block; it writes the scale for each of the 16 rows, so the GEMMs read the usual per-row
+// layout.  quantize_block2d: rows [r0, r0 + 16) x elements [16 b, 16 b + 16) of src [.][K].
+template <typename T, typename SfAt>
+__device__ __forceinline__ void quantize_block2d(const T *src, int64_t K, int64_t r0, int64_t b,
+                                                 const QScale &q, uint8_t *codes, SfAt sf_at) {
+    float amax_b = 0.0f;
+#pragma unroll 4
+    for (int r = 0; r < 16; ++r) {
+        float x[16];
+        load16<T>(src + (r0 + r) * K + 16 * b, x);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax_b = fmaxf(amax_b, fabsf(x[i]));
+    }
+    uint32_t s = 0u;
+    float rcp = 0.0f;
+    if (!q.zero) {
+        s = f32_to_e4m3_satfinite(__fmul_rn(amax_b, q.s_enc6));
+        const float bd = __fmul_rn(e4m3_to_f32(s), q.s_dec);
+        rcp = bd > 0.0f ? __frcp_rn(bd) : 0.0f;
+    }
+#pragma unroll 4
+    for (int r = 0; r < 16; ++r) {
+        float x[16];
+        load16<T>(src + (r0 + r) * K + 16 * b, x);
+        uint32_t lo = 0u, hi = 0u;
+        if (!q.zero) block_codes16(x, rcp, lo, hi);
+        reinterpret_cast<uint2 *>(codes + (r0 + r) * (K / 2))[b] = make_uint2(lo, hi);
+        *sf_at(r0 + r, b) = static_cast<uint8_t>(s);
+    }
+}
+
+// Row-major 2-D quantization of src [rows][K] (rows % 16 == 0); sf [rows][K/16] per row.
+template <typename T>
+__global__ void quantize_rows_2d_kernel(const T *__restrict__ src, int64_t rows, int64_t K, float amax,
+                                        const unsigned *__restrict__ amax_bits, uint8_t *__restrict__ codes,
+                                        uint8_t *__restrict__ sf) {
+    const float a = amax >= 0.0f ? amax : __uint_as_float(*amax_bits);
+    const QScale q = qscale_from_amax(a);
+    const int64_t nb = K / 16;
+    const int64_t total = (rows / 16) * nb;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t g = i / nb, b = i - g * nb;
+        quantize_block2d<T>(src, K, g * 16, b, q, codes,
+                            [&](int64_t r, int64_t bb) { return sf + r * nb + bb; });
+    }
+}
+
+// Expert weights with 2-D blocks: src [E][N][K] bf16 -> codes [E][N][K/2] and the scale atoms
+// [E][ceil(N/128)][K/64][512] (N % 16 == 0), one FP32 tensor scale per expert.
+__global__ void quantize_experts_2d_kernel(const __nv_bfloat16 *__restrict__ src, int E, int N, int K,
+                                           const unsigned *__restrict__ amax_bits,
+                                           uint8_t *__restrict__ codes, uint8_t *__restrict__ sf_atoms) {
+    const int64_t nb = K / 16;
+    const int64_t per_e = static_cast<int64_t>(N / 16) * nb;
+    const int64_t total = per_e * E;
+    const int64_t K64 = K / 64;
+    const int64_t NB = (N + 127) / 128;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t e = i / per_e;
+        const int64_t rem = i - e * per_e;
+        const int64_t g = rem / nb, b = rem - g * nb;
+        const QScale q = qscale_from_amax(__uint_as_float(amax_bits[e]));
+        uint8_t *atoms = sf_atoms + static_cast<size_t>(e) * NB * K64 * 512;
+        quantize_block2d<__nv_bfloat16>(src + static_cast<int64_t>(e) * N * K, K, g * 16, b, q,
+                                        codes + static_cast<int64_t>(e) * N * (K / 2),
+                                        [&](int64_t r, int64_t bb) { return atoms + sf_atom_offset(r, bb, K64); });
     }
 }
 

@@ -272,8 +272,8 @@ __global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(
 // Then, with a_(k) the k-th largest approximate logit:
 //   * the true top-k lies inside U = { e : a_e >= a_(k) - 2 delta };
 //   * e in U is certainly selected when at most k - 1 others have a_f >= a_e - 2 delta;
-//   * the rest of U is decided by exact canonical logits computed here (one warp each).
-// Should U not fit in the sorted top 32, or the counts not add up, the block computes every
+//   * the rest of U is decided by exact canonical logits computed here by the token's warp.
+// Should U not fit in the sorted top 32, or the counts not add up, the warp computes every
 // canonical logit of the token and selects from those.  The routing weights are the softmax
 // over the selected logits as known here (canonical where computed, otherwise a + b).
 // ------------------------------------------------------------------------------------
@@ -306,69 +306,99 @@ __global__ void router_split_kernel(const float *__restrict__ W, int E, int d,
     }
 }
 
-constexpr int kSelThreads = 256;
+constexpr int kSelWarps = 8;                 // tokens per block: one warp per token
 constexpr int kSelMaxD = 16384;
-__host__ __device__ constexpr int router_select_smem(int d) {
-    return (d / kChunk) * (kChunk + 1) * 4 + 8 * (d / kChunk) * 4;
-}
 
-// The canonical logit (64-element fma chunks, 16-chunk groups, then the bias) of one expert,
-// by one warp, for the token staged in xs ([C][65] fp32, padded so that lane-strided reads
-// hit distinct banks).  part: C floats of this warp's scratch.  Every lane returns the value.
-__device__ __forceinline__ float warp_canonical_logit(const float *xs, const float *__restrict__ wrow,
-                                                      int C, float bias, float *part, int lane) {
-    for (int c = lane; c < C; c += 32) {
-        const float *xc = xs + c * (kChunk + 1);
-        const float4 *wc = reinterpret_cast<const float4 *>(wrow + c * kChunk);
-        float p = 0.0f;
-#pragma unroll 4
-        for (int j = 0; j < kChunk / 4; ++j) {
-            const float4 w4 = __ldg(wc + j);
-            p = fmaf(xc[4 * j], w4.x, p);
-            p = fmaf(xc[4 * j + 1], w4.y, p);
-            p = fmaf(xc[4 * j + 2], w4.z, p);
-            p = fmaf(xc[4 * j + 3], w4.w, p);
-        }
-        part[c] = p;
-    }
-    __syncwarp();
-    const int G = (C + kGroupChunks - 1) / kGroupChunks;   // <= 32 for d <= 32768
-    float gs = 0.0f;
-    if (lane < G)
-        for (int q = lane * kGroupChunks; q < min(C, (lane + 1) * kGroupChunks); ++q) gs = __fadd_rn(gs, part[q]);
+// The canonical logit (64-element fma chunks, 16-chunk groups, then the bias) of one expert
+// for one token, by one warp straight from global memory: lane L takes chunks L, L + 32, ...
+// (128-byte rows of bf16 x, 256-byte rows of fp32 w: vector loads), each an fma chain in
+// ascending index; a 16-chunk group is the half-warp of one round, summed in order through
+// shuffles; the group sums are added in order.  Every lane returns the value.
+__device__ __forceinline__ float warp_canonical_logit_g(const __nv_bfloat16 *__restrict__ xt,
+                                                        const float *__restrict__ wrow, int C, float bias,
+                                                        int lane) {
     float acc = 0.0f;
-    for (int g = 0; g < G; ++g) acc = __fadd_rn(acc, __shfl_sync(0xffffffffu, gs, g));
-    __syncwarp();
+    for (int r = 0; r * 32 < C; ++r) {
+        const int c = r * 32 + lane;
+        float p = 0.0f;
+        if (c < C) {
+            const uint4 *xc = reinterpret_cast<const uint4 *>(xt + c * kChunk);
+            const float4 *wc = reinterpret_cast<const float4 *>(wrow + c * kChunk);
+#pragma unroll
+            for (int q = 0; q < kChunk / 8; ++q) {
+                const uint4 u = __ldg(xc + q);
+                const float4 w0 = __ldg(wc + 2 * q), w1 = __ldg(wc + 2 * q + 1);
+                p = fmaf(__uint_as_float(u.x << 16), w0.x, p);
+                p = fmaf(__uint_as_float(u.x & 0xFFFF0000u), w0.y, p);
+                p = fmaf(__uint_as_float(u.y << 16), w0.z, p);
+                p = fmaf(__uint_as_float(u.y & 0xFFFF0000u), w0.w, p);
+                p = fmaf(__uint_as_float(u.z << 16), w1.x, p);
+                p = fmaf(__uint_as_float(u.z & 0xFFFF0000u), w1.y, p);
+                p = fmaf(__uint_as_float(u.w << 16), w1.z, p);
+                p = fmaf(__uint_as_float(u.w & 0xFFFF0000u), w1.w, p);
+            }
+        }
+        // chunks past C contribute +0 at the end of their group (only a zero's sign can change)
+        float gs = 0.0f;
+        const int base = lane & 16;
+#pragma unroll
+        for (int q = 0; q < kGroupChunks; ++q) gs = __fadd_rn(gs, __shfl_sync(0xffffffffu, p, base + q));
+        const float g0 = __shfl_sync(0xffffffffu, gs, 0), g1 = __shfl_sync(0xffffffffu, gs, 16);
+        acc = __fadd_rn(acc, g0);
+        if (r * 32 + 16 < C) acc = __fadd_rn(acc, g1);
+    }
     return __fadd_rn(acc, bias);
 }
 
-// Sorted top 32 selection keys of the block's E values (vals(e)), left in lists[0].
-template <typename F>
-__device__ __forceinline__ void block_top32(uint64_t (*lists)[32], int E, F vals, int warp, int lane) {
-    uint64_t key[4];
+// The 32 largest keys of the warp (R keys per lane, distinct except padding 0), sorted
+// descending, lane j holding the j-th: the 32nd largest key is built bit by bit from the top
+// (a candidate is kept while at least 32 keys reach it), the keys at or above it are packed
+// through `slots` (32 entries of warp scratch), then a bitonic sort across the lanes.
+template <int R>
+__device__ __forceinline__ uint64_t warp_top32(const uint64_t (&key)[R], uint64_t *slots, int lane) {
+    uint64_t tau = 0;
+    for (int bit = 63; bit >= 0; --bit) {
+        const uint64_t cand = tau | (1ull << bit);
+        int cnt = 0;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int e = warp * 128 + 4 * lane + r;
-        key[r] = e < E ? topk_key(vals(e), e) : 0ull;
+        for (int i = 0; i < R; ++i) cnt += key[i] >= cand ? 1 : 0;
+        if (__reduce_add_sync(0xffffffffu, cnt) >= 32) tau = cand;
     }
-    warp_sort128_desc(key, lane);
-    if (lane < 8) {
+    // keys >= tau: exactly 32 when at least 32 keys are non-zero; otherwise pad with zeros
+    slots[lane] = 0;
+    __syncwarp();
+    int mine = 0;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) lists[warp][4 * lane + r] = key[r];
-    }
-    __syncthreads();
+    for (int i = 0; i < R; ++i) mine += (key[i] >= tau && key[i] != 0) ? 1 : 0;
+    int pos = mine;
 #pragma unroll
-    for (int n = 8; n > 1; n >>= 1) {
-        uint64_t res = 0;
-        if (warp < n / 2) res = merge_top32(lists[2 * warp][lane], lists[2 * warp + 1][31 - lane], lane);
-        __syncthreads();
-        if (warp < n / 2) lists[warp][lane] = res;
-        __syncthreads();
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, pos, o);
+        if (lane >= o) pos += v;
     }
+    pos -= mine;                                           // exclusive prefix
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+        if (key[i] >= tau && key[i] != 0 && pos < 32) slots[pos++] = key[i];
+    __syncwarp();
+    uint64_t a = slots[lane];
+    __syncwarp();
+    // bitonic sort, descending by lane
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j >= 1; j >>= 1) {
+            const uint64_t o = shfl_xor64(a, j);
+            const bool lower = (lane & j) == 0;
+            const bool desc = (lane & k) == 0;
+            a = (lower == desc) ? (a > o ? a : o) : (a < o ? a : o);
+        }
+    }
+    return a;
 }
 
-// Warp 0: write the selected experts (lanes with sel) in ascending expert id, the softmax of
-// their values, counts and slot offsets.
+// Output of one token's selection by its warp: the selected lanes (sel) in ascending expert
+// id, the softmax of their values, counts and slot offsets.
 __device__ __forceinline__ void emit_selection(int t, int k, bool sel, int e, float v, int lane,
                                                int32_t *idx_out, float *w_out, int32_t *counts,
                                                int32_t *slot_off) {
@@ -393,88 +423,76 @@ __device__ __forceinline__ void emit_selection(int t, int k, bool sel, int e, fl
     }
 }
 
-// One block of 256 threads per token.  approx: [T][E] fp32 sums of the tensor-core GEMM (no
-// bias); wrows: router weights [E][d] fp32; coef: the accumulation bound described above.
-__global__ void __launch_bounds__(kSelThreads) router_select_kernel(
+// One warp per token (kSelWarps tokens per block).  approx: [T][E] fp32 sums of the tensor-core
+// GEMM (no bias); wrows: router weights [E][d] fp32; coef: the accumulation bound described
+// above.  R: keys per lane (E <= 32 R).
+template <int R>
+__global__ void __launch_bounds__(32 * kSelWarps) router_select_kernel(
     const float *__restrict__ approx, const float *__restrict__ bias, const __nv_bfloat16 *__restrict__ x,
     const float *__restrict__ wrows, int T, int d, int E, int k, float coef, float wn_max, float bmax,
     int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts,
     int32_t *__restrict__ slot_off) {
-    extern __shared__ __align__(16) float sel_smem[];
-    __shared__ uint64_t lists[8][32];
-    __shared__ float red[8];
-    __shared__ float vexact[32];
-    __shared__ float exall[1024];
-    __shared__ uint32_t s_mask[3];   // certain, uncertain, slow-path flag
-    __shared__ int s_need;
-    const int C = d / kChunk;
-    float *xs = sel_smem;                                  // [C][65]
-    const int t = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    float *part = xs + C * (kChunk + 1) + warp * C;        // [8][C]
+    __shared__ uint64_t slots_all[kSelWarps][32];
     pdl_wait();
     pdl_trigger();
-    // the token in shared memory (fp32, padded chunks) and its squared norm
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = blockIdx.x * kSelWarps + warp;
+    if (t >= T) return;
+    uint64_t *slots = slots_all[warp];
+    const int C = d / kChunk;
     const __nv_bfloat16 *xt = x + static_cast<int64_t>(t) * d;
+    // an upper bound of |x_t| (the fp32 sum of d squares is within d * 2^-24 of exact)
     float ss = 0.0f;
-    for (int i = tid; i < d; i += kSelThreads) {
-        const float v = __bfloat162float(xt[i]);
-        xs[(i / kChunk) * (kChunk + 1) + (i % kChunk)] = v;
-        ss = fmaf(v, v, ss);
+    for (int i = lane * 8; i < d; i += 256) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(xt + i));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float a = __uint_as_float(w[j] << 16), b = __uint_as_float(w[j] & 0xFFFF0000u);
+            ss = fmaf(a, a, ss);
+            ss = fmaf(b, b, ss);
+        }
     }
 #pragma unroll
-    for (int m = 16; m > 0; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-    if (lane == 0) red[warp] = ss;
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float nx = __fmul_ru(sqrtf(ss), 1.0f + 0x1p-10f);
+    const float delta = __fadd_ru(__fmul_ru(__fmul_ru(nx, wn_max), __fadd_ru(coef, 0x1p-16f)),
+                                  __fmul_ru(bmax, 0x1p-22f));
+    const float two_d = __fmul_ru(2.0f, delta);
+    // approximate logits + bias -> selection keys
     const float *at = approx + static_cast<int64_t>(t) * E;
-    block_top32(lists, E, [&](int e) { return __fadd_rn(__ldg(at + e), __ldg(bias + e)); }, warp, lane);
-    // (block_top32 ends with __syncthreads: red[] and lists[0] are visible)
-    const uint64_t mykey = lists[0][lane];
-    const float v = key_value(mykey);                      // NaN for padding (E < 32)
-    const int e_l = key_index(mykey);
-    if (warp == 0) {
-        float tot = 0.0f;
-        for (int i = 0; i < 8; ++i) tot += red[i];
-        // an upper bound of |x_t| (the fp32 sum of d squares is within d * 2^-24 of exact)
-        const float nx = __fmul_ru(sqrtf(tot), 1.0f + 0x1p-10f);
-        const float delta = __fadd_ru(__fmul_ru(__fmul_ru(nx, wn_max), __fadd_ru(coef, 0x1p-16f)),
-                                      __fmul_ru(bmax, 0x1p-22f));
-        const float two_d = __fmul_ru(2.0f, delta);
-        const float vk = __shfl_sync(0xffffffffu, v, k - 1);
-        const bool in_u = v >= __fsub_rd(vk, two_d);
-        const bool overflow = __shfl_sync(0xffffffffu, in_u ? 1 : 0, 31) != 0;
-        const float lo = __fsub_rd(v, two_d);
-        int cnt = 0;
-        for (int j = 0; j < 32; ++j) {
-            const float vj = __shfl_sync(0xffffffffu, v, j);
-            cnt += (j != lane && vj >= lo) ? 1 : 0;
-        }
-        const bool certain = in_u && cnt <= k - 1;
-        const uint32_t cm = __ballot_sync(0xffffffffu, certain);
-        const uint32_t um = __ballot_sync(0xffffffffu, in_u && !certain);
-        const int need = k - __popc(cm);
-        if (lane == 0) {
-            s_mask[0] = cm;
-            s_mask[1] = um;
-            s_mask[2] = (overflow || need < 0 || need > __popc(um)) ? 1u : 0u;
-            s_need = need;
-        }
+    uint64_t key[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        const int e = i * 32 + lane;
+        key[i] = e < E ? topk_key(__fadd_rn(__ldg(at + e), __ldg(bias + e)), e) : 0ull;
     }
-    __syncthreads();
-    if (!s_mask[2]) {
-        const uint32_t um = s_mask[1];
-        // exact canonical logits of the uncertain candidates, one warp each
-        for (int p = 0; p < 32; ++p) {
-            if (!((um >> p) & 1u)) continue;
-            if (__popc(um & ((1u << p) - 1u)) % 8 != warp) continue;
-            const int e = key_index(lists[0][p]);
-            const float ve = warp_canonical_logit(xs, wrows + static_cast<int64_t>(e) * d, C, __ldg(bias + e), part, lane);
-            if (lane == 0) vexact[p] = ve;
+    uint64_t top = warp_top32<R>(key, slots, lane);
+    float v = key_value(top);                              // NaN for padding (E < 32)
+    int e_l = key_index(top);
+    const float vk = __shfl_sync(0xffffffffu, v, k - 1);
+    const bool in_u = v >= __fsub_rd(vk, two_d);
+    const bool overflow = __shfl_sync(0xffffffffu, in_u ? 1 : 0, 31) != 0;
+    const float lo = __fsub_rd(v, two_d);
+    int cnt = 0;
+    for (int j = 0; j < 32; ++j) {
+        const float vj = __shfl_sync(0xffffffffu, v, j);
+        cnt += (j != lane && vj >= lo) ? 1 : 0;
+    }
+    const bool certain = in_u && cnt <= k - 1;
+    const uint32_t cm = __ballot_sync(0xffffffffu, certain);
+    const uint32_t um = __ballot_sync(0xffffffffu, in_u && !certain);
+    const int need = k - __popc(cm);
+    if (!overflow && need >= 0 && need <= __popc(um)) {
+        // canonical logits of the uncertain candidates
+        float ve = v;
+        for (uint32_t m = um; m; m &= m - 1) {
+            const int p = __ffs(m) - 1;
+            const int e = __shfl_sync(0xffffffffu, e_l, p);
+            const float c = warp_canonical_logit_g(xt, wrows + static_cast<int64_t>(e) * d, C, __ldg(bias + e), lane);
+            if (lane == p) ve = c;
         }
-        __syncthreads();
-        if (warp != 0) return;
         const bool unc = (um >> lane) & 1u;
-        const float ve = unc ? vexact[lane] : v;
-        // rank of an uncertain candidate among the uncertain by its exact key
         const uint64_t kx = unc ? topk_key(ve, e_l) : 0ull;
         int r = 0;
         for (int j = 0; j < 32; ++j) {
@@ -482,21 +500,24 @@ __global__ void __launch_bounds__(kSelThreads) router_select_kernel(
                                 __shfl_sync(0xffffffffu, static_cast<uint32_t>(kx), j);
             r += (((um >> j) & 1u) && kj > kx) ? 1 : 0;
         }
-        const bool sel = ((s_mask[0] >> lane) & 1u) || (unc && r < s_need);
+        const bool sel = ((cm >> lane) & 1u) || (unc && r < need);
         emit_selection(t, k, sel, e_l, ve, lane, idx_out, w_out, counts, slot_off);
         return;
     }
     // slow path: every canonical logit of the token, then the top k of those
-    __syncthreads();
-    for (int e = warp; e < E; e += 8) {
-        const float ve = warp_canonical_logit(xs, wrows + static_cast<int64_t>(e) * d, C, __ldg(bias + e), part, lane);
-        if (lane == 0) exall[e] = ve;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        const int e0 = i * 32;
+        float mine = 0.0f;
+        for (int q = 0; q < 32 && e0 + q < E; ++q) {
+            const float c = warp_canonical_logit_g(xt, wrows + static_cast<int64_t>(e0 + q) * d, C, __ldg(bias + e0 + q), lane);
+            if (lane == q) mine = c;
+        }
+        const int e = e0 + lane;
+        key[i] = e < E ? topk_key(mine, e) : 0ull;
     }
-    __syncthreads();
-    block_top32(lists, E, [&](int e) { return exall[e]; }, warp, lane);
-    if (warp != 0) return;
-    const uint64_t kb = lists[0][lane];
-    emit_selection(t, k, lane < k, key_index(kb), key_value(kb), lane, idx_out, w_out, counts, slot_off);
+    top = warp_top32<R>(key, slots, lane);
+    emit_selection(t, k, lane < k, key_index(top), key_value(top), lane, idx_out, w_out, counts, slot_off);
 }
 
 }  // namespace lmoe

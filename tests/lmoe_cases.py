@@ -37,10 +37,12 @@ class Case:
     """A layer (dims, seed, routing skew) with its calibration, on the GPU and in the oracle."""
 
     def __init__(self, dims: lmoe_synth.Dims, seed: int, zipf: float = 0.0, calib_T: int = 64,
-                 gen_device: str = "cpu"):
+                 gen_device: str = "cpu", weight_blocks_2d: bool = False, w4a16: bool = False):
         import nvfp4_latentmoe_fwd_02_b300 as lm
         self.lm = lm
         self.dims, self.seed, self.zipf = dims, seed, zipf
+        self.weight_blocks_2d = weight_blocks_2d
+        self.w4a16 = w4a16
         L = lmoe_synth.layer(dims, seed, gen_device, zipf)
         self.L = L
         self.dev = {n: getattr(L, n).cuda() for n in
@@ -54,7 +56,8 @@ class Case:
             shared = (L.ws1.float().cpu().numpy(), L.ws2.float().cpu().numpy())
         self.ol = oracle.OracleLayer(dims.d, dims.l, dims.E, dims.k, dims.ffn, host["w_down"],
                                      host["w_up"], host["w_router"], host["b_router"],
-                                     self._expert_master, shared=shared)
+                                     self._expert_master, shared=shared,
+                                     weight_blocks_2d=weight_blocks_2d)
         xc = lmoe_synth.calibration_tokens(calib_T, dims.d, seed, gen_device).float().cpu().numpy()
         self.amax_z, self.amax_h = self.ol.calibrate(xc)
         self.amax_xs, self.amax_hs = self.ol.calibrate_shared(xc) if shared else (0.0, 0.0)
@@ -71,7 +74,8 @@ class Case:
                                          D["w_router"], D["b_router"], D["w1"], D["w2"],
                                          self.amax_z, self.amax_h, debug=debug,
                                          ws1=D.get("ws1"), ws2=D.get("ws2"),
-                                         amax_xs=self.amax_xs, amax_hs=self.amax_hs)
+                                         amax_xs=self.amax_xs, amax_hs=self.amax_hs,
+                                         weight_blocks_2d=self.weight_blocks_2d, w4a16=self.w4a16)
         return self.moe
 
     def tokens(self, T, seed_offset=0):

@@ -122,3 +122,39 @@ def test_ultra_router_margin_and_routing_on_many_tokens(ultra_zipf):
     ratio = (np.abs(approx - logits) / (nx * wn)[:, None]).max()
     print(f"max |tensor-core - canonical| / (|x| max|w|) = {ratio:.3e} (margin floor 2^-16 = {2**-16:.3e})")
     assert ratio < 2.0 ** -16 / 4
+
+
+def test_ultra_drift_against_bf16_experts(ultra_uniform):
+    """Layer-level drift at Ultra dims, T = 8: the GPU's NVFP4 layer against the oracle's
+    BF16-expert layer (unquantized mode: fp64, bf16 master weights, no quantization), with the
+    flush-to-zero rates of the GPU's z and h.  A measurement; the bounds only catch a broken
+    quantized path."""
+    case = ultra_uniform
+    moe = case.gpu(debug=True)
+    d = case.dims
+    T = 8
+    x = case.tokens(T, seed_offset=55).cuda()
+    y = moe.forward(x)
+    moe.check()
+    u = case.ol.forward(x.float().cpu().numpy(), quant=False, want=("c64", "y64"))
+    idx = moe.stage("idx", T, torch.int32).view(T, d.k).cpu().numpy()
+    ry = rel_l2_rows(y.float().cpu().numpy(), u["y64"])
+    c = moe.stage("c", T, torch.bfloat16).view(T, d.l).float().cpu().numpy()
+    z = moe.stage("z", T, torch.bfloat16).view(T, d.l).float().cpu().numpy()
+    zc = moe.stage("zq_codes", T).view(T, d.l // 2).cpu().numpy()
+    zn = np.stack([zc & 15, zc >> 4], -1).reshape(T, -1)
+    nrows = int(moe.stage("nrows", T, torch.int32).cpu()[0])
+    R = moe.stage("rows", T, torch.int32).numel()
+    live = moe.stage("rows", T, torch.int32).cpu().numpy()[:nrows] >= 0
+    h = moe.stage("h", T, torch.bfloat16).view(R, d.ffn)[:nrows].float().cpu().numpy()[live]
+    hc = moe.stage("hq_codes", T).view(R, d.ffn // 2)[:nrows].cpu().numpy()[live]
+    hn = np.stack([hc & 15, hc >> 4], -1).reshape(hc.shape[0], -1)
+    r = {"y_rel_l2_mean": float(ry.mean()), "y_rel_l2_max": float(ry.max()),
+         "c_rel_l2_mean": float(rel_l2_rows(c, u["c64"]).mean()),
+         "routing_agreement": float((idx == u["idx"]).all(axis=1).mean()),
+         "ftz_rate_z": float((((zn & 7) == 0) & (z != 0)).sum() / max(1, (z != 0).sum())),
+         "ftz_rate_h": float((((hn & 7) == 0) & (h != 0)).sum() / max(1, (h != 0).sum()))}
+    print("drift ultra T=8:", r)
+    assert r["routing_agreement"] == 1.0
+    assert 0.05 < r["y_rel_l2_mean"] < 0.35 and r["y_rel_l2_max"] < 0.6
+    assert r["ftz_rate_z"] < 0.15 and r["ftz_rate_h"] < 0.5
