@@ -150,7 +150,7 @@ lmoe_status lmoe_route(lmoe_ctx *ctx, const void *x, int64_t T, int32_t *idx, fl
  * loops whose device memory is fixed at start-up, and hosts that embed the library without
  * handing it any allocator.  lmoe_route may grow a context-owned scratch with cudaMallocAsync;
  * lmoe_route_static never allocates or frees.  It has lmoe_route's arguments and results, but
- * keeps the router's scratch (fp32 group sums, T x ceil(d/1024) x E, when T <= 64; fp32
+ * keeps the router's scratch (fp32 group sums, T x E x ceil(d/1024), when T <= 64; fp32
  * logits, T x E, above) in one fixed array of LMOE_ROUTE_STATIC_SCRATCH_BYTES compiled into
  * liblmoe.so, which every GPU that loads the library holds until the process exits.
  *   - That scratch must fit in LMOE_ROUTE_STATIC_SCRATCH_BYTES (at d = 8192, E = 512: every
@@ -208,7 +208,7 @@ typedef enum {
     LMOE_STAGE_HS_Q = 14,    /* uint8 [T][shared_ffn] shared expert: E4M3 codes of h     */
     LMOE_STAGE_S = 15,       /* bf16  [T][d]      shared expert output s                */
     LMOE_STAGE_ROUTER = 16   /* fp32  router scratch: T > 64: tensor-core logits [T][E]
-                                without the bias; T <= 64: group sums [T][d/1024][E]   */
+                                without the bias; T <= 64: group sums [T][E][d/1024]   */
 } lmoe_stage;
 lmoe_status lmoe_workspace_range(const lmoe_ctx *ctx, int64_t T, int stage, size_t *offset,
                                  size_t *bytes);

@@ -213,7 +213,7 @@ WsLayout layout(const lmoe_ctx *c, int64_t T) {
     auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
     L.idx = take(T * k * 4);
     L.w = take(T * k * 4);
-    L.counts = take(E * 4);
+    L.counts = take(E * 4 + 16);   // + the routing kernels' done counter (cleared with the counts)
     L.seg = take((E + 1) * 4);
     L.mt = take((E + 1) * 4);
     L.slot_off = take(T * k * 4);
@@ -320,9 +320,15 @@ lmoe_status check_error_word(lmoe_ctx *c) {
 // counts; the first kernel also clears the ranges in `zr`.  Large T: a clearing kernel (zr and
 // the logits), tensor-core logits into `scratch` (bf16 hi/lo planes of the weights, K split
 // over the SMs, fp32 reductions), then the certified selection against the canonical order.
+// seg (optional, with done / mt / nrows): the routing kernel's last warp lays out the expert
+// segments (done: a zeroed counter).
+struct SegOut {
+    int *done;
+    int32_t *seg, *mt, *nrows;
+};
 lmoe_status launch_router(lmoe_ctx *c, const __nv_bfloat16 *x, int64_t T, float *scratch,
                           int32_t *idx, float *w, int32_t *counts, int32_t *slot_off,
-                          const ZeroRanges &zr, cudaStream_t s) {
+                          const ZeroRanges &zr, cudaStream_t s, SegOut so = {nullptr, nullptr, nullptr, nullptr}) {
     const bool small = T <= kSmallMaxT;
     const int C = c->d / kChunk;
     const int NG = static_cast<int>(cdiv(C, kGroupChunks));
@@ -334,7 +340,8 @@ lmoe_status launch_router(lmoe_ctx *c, const __nv_bfloat16 *x, int64_t T, float 
         prof_mark(c, "router_small", s);
         LMOE_CUDA(launch_pdl(router_topk_kernel, dim3(static_cast<unsigned>(T)), dim3(kTopkThreads), 0, s,
                              static_cast<const float *>(scratch), NG, static_cast<const float *>(c->b_router),
-                             static_cast<int>(T), c->E, c->k, idx, w, counts, slot_off));
+                             static_cast<int>(T), c->E, c->k, idx, w, counts, slot_off, so.done, so.seg, so.mt,
+                             so.nrows));
         prof_mark(c, "router_topk", s);
         return LMOE_OK;
     }
@@ -369,13 +376,16 @@ lmoe_status launch_router(lmoe_ctx *c, const __nv_bfloat16 *x, int64_t T, float 
     const float *bp = c->b_router;
     if (E <= 128)
         LMOE_CUDA(launch_pdl(router_select_kernel<4>, sgrid, sblock, 0, s, ap, bp, x, wr, static_cast<int>(T), d, E,
-                             c->k, coef, c->wn_max, c->bmax, idx, w, counts, slot_off));
+                             c->k, coef, c->wn_max, c->bmax, idx, w, counts, slot_off, so.done, so.seg, so.mt,
+                             so.nrows));
     else if (E <= 512)
         LMOE_CUDA(launch_pdl(router_select_kernel<16>, sgrid, sblock, 0, s, ap, bp, x, wr, static_cast<int>(T), d, E,
-                             c->k, coef, c->wn_max, c->bmax, idx, w, counts, slot_off));
+                             c->k, coef, c->wn_max, c->bmax, idx, w, counts, slot_off, so.done, so.seg, so.mt,
+                             so.nrows));
     else
         LMOE_CUDA(launch_pdl(router_select_kernel<32>, sgrid, sblock, 0, s, ap, bp, x, wr, static_cast<int>(T), d, E,
-                             c->k, coef, c->wn_max, c->bmax, idx, w, counts, slot_off));
+                             c->k, coef, c->wn_max, c->bmax, idx, w, counts, slot_off, so.done, so.seg, so.mt,
+                             so.nrows));
     prof_mark(c, "router_select", s);
     return LMOE_OK;
 }
@@ -916,18 +926,15 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     {
         ZeroRanges z;
         std::memset(&z, 0, sizeof(z));
-        z.p[0] = reinterpret_cast<uint4 *>(counts); z.n16[0] = cdiv(E * 4, 16);
+        z.p[0] = reinterpret_cast<uint4 *>(counts); z.n16[0] = cdiv(E * 4 + 16, 16);   // counts + done
         z.p[1] = reinterpret_cast<uint4 *>(c_acc); z.n16[1] = T * l * 4 / 16;
         if (L.split_down && !fork) { z.p[2] = reinterpret_cast<uint4 *>(zacc); z.n16[2] = T * l * 4 / 16; }
         if (L.split_up) { z.p[3] = reinterpret_cast<uint4 *>(yacc); z.n16[3] = T * d * 4 / 16; }
+        SegOut so = {counts + E, seg, mt, nrows};
         lmoe_status st = launch_router(c, static_cast<const __nv_bfloat16 *>(x), T,
-                                       static_cast<float *>(at(L.router)), idx, rw, counts, slot_off, z, s);
+                                       static_cast<float *>(at(L.router)), idx, rw, counts, slot_off, z, s, so);
         if (st != LMOE_OK) return st;
     }
-    // 2. per-expert segments
-    LMOE_CUDA(launch_pdl(segments_kernel, dim3(E), dim3(128), 0, s, static_cast<const int32_t *>(counts), E,
-                         seg, mt, row_slot, nrows));
-    prof_mark(c, "segments", s);
     // 3. down-projection z = x Wd^T, quantized to NVFP4
     {
         if (fork) {
@@ -1108,11 +1115,11 @@ lmoe_status lmoe_get_shared_fp8(const lmoe_ctx *c, int which, uint8_t *codes, fl
 int lmoe_forward_kernel_count(const lmoe_ctx *c, int64_t T) {
     if (!c || T <= 0) return 0;
     const WsLayout L = layout(c, T);
-    // router (small T: chunk sums, top-k; large T: clearing, tensor-core logits, selection),
-    // segments, down-proj, expert-up, expert-down, combine cast, up-proj, plus one finalize per split projection (and, for a split down-projection run
+    // router (small T: chunk sums, top-k; large T: clearing, tensor-core logits, selection;
+    // its last warp lays out the segments), down-proj, expert-up, expert-down, combine cast, up-proj, plus one finalize per split projection (and, for a split down-projection run
     // beside the router, the clearing of its accumulator), plus the shared expert's
     // quantization of x and its two GEMMs
-    return 8 + (T > kSmallMaxT ? 1 : 0) + (L.split_down ? 2 : 0) + (L.split_up ? 1 : 0) + (c->shared_ffn ? 3 : 0);
+    return 7 + (T > kSmallMaxT ? 1 : 0) + (L.split_down ? 2 : 0) + (L.split_up ? 1 : 0) + (c->shared_ffn ? 3 : 0);
 }
 
 lmoe_status lmoe_set_profile(lmoe_ctx *c, int on) {

@@ -1,48 +1,17 @@
 // moe.cuh -- per-expert segments, gather of the latent tokens, and the small element-wise
 // passes around the GEMMs (zeroing, z finalize + quantize, combine finalize, y finalize).
 //
-// Segments: expert e owns rows [seg_start[e], seg_start[e] + counts[e]) of the permuted
-// buffers; each segment is padded to a multiple of 128 rows (one tensor-core M tile) so that
-// every tile's block scales sit in whole 128-row scale atoms.  row_slot[row] is the routing
-// slot (token * k + j) of a row, -1 for padding.  mt_start[e] is the prefix sum of M tiles.
-// A slot's row inside its segment is the histogram's old value when the top-k kernel counted
-// it (atomic-arrival order: the grouping, not the order inside a segment, is fixed).
+// Segments (laid out by the routing kernels' last warp, router.cuh): expert e owns rows
+// [seg_start[e], seg_start[e] + counts[e]) of the permuted buffers, padded to a multiple of
+// 128 rows.  row_slot[row] is the routing slot (token * k + j) of a real row; padding rows are
+// never written or read.  A slot's row inside its segment is the histogram's old value when
+// the routing kernel counted it (atomic-arrival order: the grouping, not the order inside a
+// segment, is fixed).
 #pragma once
 #include "common.cuh"
 #include "nvfp4.cuh"
 
 namespace lmoe {
-
-// One block per expert e: its segment start is the sum of the padded counts of experts < e
-// (a block reduction over the histogram); the block also marks the segment's padding rows.
-// Block E - 1 writes the totals.  grid = E, block = 128.
-__global__ void __launch_bounds__(128) segments_kernel(
-    const int32_t *__restrict__ counts, int E, int32_t *__restrict__ seg_start,
-    int32_t *__restrict__ mt_start, int32_t *__restrict__ row_slot, int32_t *__restrict__ nrows) {
-    __shared__ int part[4];
-    const int e = blockIdx.x;
-    pdl_wait();
-    pdl_trigger();
-    int sum = 0;
-    for (int i = threadIdx.x; i < e; i += blockDim.x) sum += (__ldg(counts + i) + 127) & ~127;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = sum;
-    __syncthreads();
-    const int start = part[0] + part[1] + part[2] + part[3];
-    const int cnt = __ldg(counts + e);
-    const int padded = (cnt + 127) & ~127;
-    if (threadIdx.x == 0) {
-        seg_start[e] = start;
-        mt_start[e] = start >> 7;
-        if (e == E - 1) {
-            seg_start[E] = start + padded;
-            mt_start[E] = (start + padded) >> 7;
-            *nrows = start + padded;
-        }
-    }
-    for (int r = start + cnt + threadIdx.x; r < start + padded; r += blockDim.x) row_slot[r] = -1;
-}
 
 // Where the k copies of token t's quantized latent vector go: segment row of each slot.
 __device__ __forceinline__ int slot_row(const int32_t *idx, const int32_t *slot_off,

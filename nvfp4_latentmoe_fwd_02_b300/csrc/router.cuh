@@ -10,7 +10,7 @@
 // expf) over the k selected logits.  Output slots are in ascending expert id.
 // Two paths give exactly the selection of these fp32 operations:
 //   small T  (memory bound: the weights are streamed once) router_small_kernel computes the
-//            group sums G_g(t, e) into G[t][g][e] from the transposed weights Wt[d][E]
+//            group sums G_g(t, e) into G[t][e][g] from the transposed weights Wt[d][E]
 //            (consecutive experts consecutive in memory; a block owns one group of 16 chunks);
 //            router_topk_kernel adds them in ascending g, adds the bias and selects;
 //   large T  (compute bound) tensor-core logits from bf16 hi/lo planes of the weights bound
@@ -44,7 +44,7 @@ __global__ void zero_kernel(ZeroRanges z) {
     zero_ranges(z);
 }
 
-// Small T: group sums G[t][g][e].  Block: 32 experts (lanes) x the 16 chunks of group g
+// Small T: group sums G[t][e][g].  Block: 32 experts (lanes) x the 16 chunks of group g
 // (warps); thread (e, c) loads its 64 weights once (one coalesced 128-byte load per element
 // across the warp) and runs one fmaf chain per token; the block then adds its 16 chunk
 // partials in order per (token, expert) from shared memory.  Tokens are staged 16 at a time
@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(kSmallEG * kSmallCG) router_small_kernel(
         if (tt < nt && e < E) {
             float gs = 0.0f;
             for (int q = 0; q < ncg; ++q) gs = __fadd_rn(gs, ps[(tt * kSmallCG + q) * kSmallEG + lane]);
-            G[(static_cast<int64_t>(t0 + tt) * ng + blockIdx.y) * E + e] = gs;
+            G[(static_cast<int64_t>(t0 + tt) * E + e) * ng + blockIdx.y] = gs;
         }
     }
 }
@@ -185,78 +185,6 @@ __device__ __forceinline__ uint64_t merge_top32(uint64_t a_i, uint64_t b_rev_i, 
         c = lower ? (c > o ? c : o) : (c < o ? c : o);
     }
     return c;
-}
-
-// One block of 256 threads (8 warps) per token: each warp sorts 128 selection keys (E <= 1024),
-// the per-warp top-32 lists are merged pairwise (8 -> 4 -> 2 -> 1) through shared memory,
-// then warp 0 holds the top-k: softmax over their logits, write idx / w in ascending expert
-// id, count tokens per expert and record each slot's offset inside its expert's segment.
-constexpr int kTopkThreads = 256;
-// src: logits[T][E] (C == 0) or group sums G[T][C][E] (C > 0 groups: summed here in
-// ascending group order, then the bias).
-__global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(
-    const float *__restrict__ src, int C, const float *__restrict__ bias, int T, int E, int k,
-    int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts,
-    int32_t *__restrict__ slot_off) {
-    __shared__ uint64_t lists[8][32];
-    const int t = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    pdl_wait();
-    pdl_trigger();
-    uint64_t key[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int e = warp * 128 + 4 * lane + r;
-        float v = 0.0f;
-        if (e < E) {
-            if (C == 0) {
-                v = __ldg(src + static_cast<int64_t>(t) * E + e);
-            } else {
-                const float *pt = src + static_cast<int64_t>(t) * C * E + e;
-                float acc = 0.0f;
-                for (int g = 0; g < C; ++g) acc = __fadd_rn(acc, __ldg(pt + static_cast<int64_t>(g) * E));
-                v = __fadd_rn(acc, bias ? bias[e] : 0.0f);
-            }
-        }
-        key[r] = e < E ? topk_key(v, e) : 0ull;             // padding sorts last
-    }
-    warp_sort128_desc(key, lane);
-    // positions 0..31 (lanes 0..7) -> list of this warp
-    if (lane < 8) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) lists[warp][4 * lane + r] = key[r];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int n = 8; n > 1; n >>= 1) {
-        uint64_t res = 0;
-        if (warp < n / 2) res = merge_top32(lists[2 * warp][lane], lists[2 * warp + 1][31 - lane], lane);
-        __syncthreads();
-        if (warp < n / 2) lists[warp][lane] = res;
-        __syncthreads();
-    }
-    if (warp != 0) return;
-    const uint64_t best = lists[0][lane];
-    const int my_idx = lane < k ? key_index(best) : 0x7fffffff;
-    const float my_val = lane < k ? key_value(best) : -INFINITY;
-    int rank = 0;
-    for (int r = 0; r < k; ++r) rank += (__shfl_sync(0xffffffffu, my_idx, r) < my_idx) ? 1 : 0;
-    float m = my_val;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const float ex = lane < k ? expf(my_val - m) : 0.0f;
-    float ssum = ex;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
-    if (lane < k) {
-        idx_out[static_cast<int64_t>(t) * k + rank] = my_idx;
-        w_out[static_cast<int64_t>(t) * k + rank] = __fdiv_rn(ex, ssum);
-        if (counts) {
-            // the histogram's old value is this slot's row inside its expert's segment
-            const int off = atomicAdd(counts + my_idx, 1);
-            if (slot_off) slot_off[static_cast<int64_t>(t) * k + rank] = off;
-        }
-    }
 }
 
 // ------------------------------------------------------------------------------------
@@ -423,6 +351,118 @@ __device__ __forceinline__ void emit_selection(int t, int k, bool sel, int e, fl
     }
 }
 
+// The expert segments, by the last warp to finish routing (the routing kernels count every
+// slot into `counts` first): expert e owns rows [seg_start[e], seg_start[e] + counts[e]) of the
+// permuted buffers, its segment padded to a multiple of 128 rows (one tensor-core M tile) so
+// that every tile's block scales sit in whole scale atoms; mt_start is the prefix of M tiles.
+// Padding rows are never written or read (a tile's valid rows end at its expert's count).
+__device__ __forceinline__ void segments_if_last(int units, int *done, const int32_t *counts, int E,
+                                                 int32_t *seg_start, int32_t *mt_start, int32_t *nrows,
+                                                 int lane) {
+    __syncwarp();
+    __threadfence();                                       // this warp's counts are visible
+    int last = 0;
+    if (lane == 0) last = atomicAdd(done, 1) == units - 1;
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    __threadfence();
+    // every count first (independent loads), then the scan
+    int cv[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) cv[i] = i * 32 + lane < E ? __ldcg(counts + i * 32 + lane) : 0;
+    int run = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        if (i * 32 >= E) break;
+        const int e = i * 32 + lane;
+        const int p = (cv[i] + 127) & ~127;
+        int incl = p;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (e < E) {
+            seg_start[e] = run + incl - p;
+            mt_start[e] = (run + incl - p) >> 7;
+        }
+        run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+        seg_start[E] = run;
+        mt_start[E] = run >> 7;
+        *nrows = run;
+    }
+}
+
+// Small T: one block of 256 threads per token (at decode there are few tokens, so the work of
+// one token is spread over eight warps).  G: group sums [T][E][NG] (router_small_kernel); a
+// logit is their sum in ascending group order plus the bias (the canonical order).  Each warp
+// sorts 128 selection keys (4 per lane; E <= 1024), the per-warp top-32 lists are merged
+// pairwise through shared memory, and warp 0 emits the top k (softmax, counts, slot offsets);
+// the last block lays out the segments (when `done` is given).
+constexpr int kTopkThreads = 256;
+__global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(
+    const float *__restrict__ G, int NG, const float *__restrict__ bias, int T, int E, int k,
+    int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts,
+    int32_t *__restrict__ slot_off, int *__restrict__ done, int32_t *__restrict__ seg_start,
+    int32_t *__restrict__ mt_start, int32_t *__restrict__ nrows) {
+    __shared__ uint64_t lists[8][32];
+    pdl_wait();
+    pdl_trigger();
+    const int t = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // the group sums of one expert are contiguous: every load of this thread is independent
+    const float *gt = G + static_cast<int64_t>(t) * E * NG;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (NG % 4 == 0) {
+        for (int g0 = 0; g0 < NG; g0 += 4) {
+            float4 v[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int e = warp * 128 + 4 * lane + r;
+                v[r] = e < E ? __ldg(reinterpret_cast<const float4 *>(gt + static_cast<int64_t>(e) * NG + g0))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                acc[r] = __fadd_rn(acc[r], v[r].x); acc[r] = __fadd_rn(acc[r], v[r].y);
+                acc[r] = __fadd_rn(acc[r], v[r].z); acc[r] = __fadd_rn(acc[r], v[r].w);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int e = warp * 128 + 4 * lane + r;
+            if (e < E)
+                for (int g = 0; g < NG; ++g) acc[r] = __fadd_rn(acc[r], __ldg(gt + static_cast<int64_t>(e) * NG + g));
+        }
+    }
+    uint64_t key[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int e = warp * 128 + 4 * lane + r;
+        key[r] = e < E ? topk_key(__fadd_rn(acc[r], bias ? __ldg(bias + e) : 0.0f), e) : 0ull;
+    }
+    warp_sort128_desc(key, lane);
+    if (lane < 8) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) lists[warp][4 * lane + r] = key[r];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int n = 8; n > 1; n >>= 1) {
+        uint64_t res = 0;
+        if (warp < n / 2) res = merge_top32(lists[2 * warp][lane], lists[2 * warp + 1][31 - lane], lane);
+        __syncthreads();
+        if (warp < n / 2) lists[warp][lane] = res;
+        __syncthreads();
+    }
+    if (warp != 0) return;
+    const uint64_t best = lists[0][lane];
+    emit_selection(t, k, lane < k, key_index(best), key_value(best), lane, idx_out, w_out, counts, slot_off);
+    if (done) segments_if_last(T, done, counts, E, seg_start, mt_start, nrows, lane);
+}
+
 // One warp per token (kSelWarps tokens per block).  approx: [T][E] fp32 sums of the tensor-core
 // GEMM (no bias); wrows: router weights [E][d] fp32; coef: the accumulation bound described
 // above.  R: keys per lane (E <= 32 R).
@@ -431,7 +471,8 @@ __global__ void __launch_bounds__(32 * kSelWarps) router_select_kernel(
     const float *__restrict__ approx, const float *__restrict__ bias, const __nv_bfloat16 *__restrict__ x,
     const float *__restrict__ wrows, int T, int d, int E, int k, float coef, float wn_max, float bmax,
     int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts,
-    int32_t *__restrict__ slot_off) {
+    int32_t *__restrict__ slot_off, int *__restrict__ done, int32_t *__restrict__ seg_start,
+    int32_t *__restrict__ mt_start, int32_t *__restrict__ nrows) {
     __shared__ uint64_t slots_all[kSelWarps][32];
     pdl_wait();
     pdl_trigger();
@@ -502,6 +543,7 @@ __global__ void __launch_bounds__(32 * kSelWarps) router_select_kernel(
         }
         const bool sel = ((cm >> lane) & 1u) || (unc && r < need);
         emit_selection(t, k, sel, e_l, ve, lane, idx_out, w_out, counts, slot_off);
+        if (done) segments_if_last(T, done, counts, E, seg_start, mt_start, nrows, lane);
         return;
     }
     // slow path: every canonical logit of the token, then the top k of those
@@ -518,6 +560,7 @@ __global__ void __launch_bounds__(32 * kSelWarps) router_select_kernel(
     }
     top = warp_top32<R>(key, slots, lane);
     emit_selection(t, k, lane < k, key_index(top), key_value(top), lane, idx_out, w_out, counts, slot_off);
+    if (done) segments_if_last(T, done, counts, E, seg_start, mt_start, nrows, lane);
 }
 
 }  // namespace lmoe

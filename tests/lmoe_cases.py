@@ -18,6 +18,18 @@ def w_tol(T):
     return dict(rtol=2e-6, atol=1e-7) if T <= 64 else dict(rtol=1e-4, atol=1e-6)
 
 
+def real_rows(counts, nrows):
+    """Mask of the permuted rows that hold a routing slot: the first counts[e] rows of each
+    expert's 128-row-padded segment (padding rows are never written or read)."""
+    mask = np.zeros(nrows, bool)
+    start = 0
+    for c in np.asarray(counts):
+        mask[start:start + int(c)] = True
+        start += (int(c) + 127) // 128 * 128
+    assert start == nrows
+    return mask
+
+
 def rel_l2_rows(a, b):
     a = np.asarray(a, np.float64).reshape(a.shape[0], -1)
     b = np.asarray(b, np.float64).reshape(b.shape[0], -1)

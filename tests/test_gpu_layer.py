@@ -12,7 +12,7 @@ import torch
 
 import lmoe_synth
 import oracle
-from lmoe_cases import Case, atoms_to_rows, rel_l2_rows, w_tol
+from lmoe_cases import Case, atoms_to_rows, real_rows, rel_l2_rows, w_tol
 from test_oracle_quant import dequant
 
 pytestmark = pytest.mark.gpu
@@ -85,18 +85,17 @@ def test_forward_matches_oracle(tiny, T):
     oc, os_, _ = oracle.quantize_nvfp4(z, tiny.amax_z)
     assert np.array_equal(zs, os_) and np.array_equal(zc, oc)
 
-    # permuted rows: a valid grouping of all T*k slots by expert
+    # permuted rows: a valid grouping of all T*k slots by expert (padding rows carry no slot)
     nrows = int(moe.stage("nrows", T, torch.int32).cpu()[0])
     rows = moe.stage("rows", T, torch.int32).cpu().numpy()[:nrows]
-    slots = rows[rows >= 0]
+    live = real_rows(counts, nrows)
+    slots = rows[live]
     assert np.array_equal(np.sort(slots), np.arange(T * d.k))
     flat_idx = idx.ravel()
     start = 0
     for e in range(d.E):
         n = int(counts[e])
-        seg = rows[start:start + n]
-        assert np.all(flat_idx[seg] == e)
-        assert np.all(rows[start + n:start + ((n + 127) // 128) * 128] == -1)
+        assert np.all(flat_idx[rows[start:start + n]] == e)
         start += ((n + 127) // 128) * 128
     assert start == nrows
 
@@ -105,7 +104,6 @@ def test_forward_matches_oracle(tiny, T):
     h = moe.stage("h", T, torch.bfloat16).view(R, d.ffn)[:nrows].float().cpu().numpy()
     hc = moe.stage("hq_codes", T).view(R, d.ffn // 2)[:nrows].cpu().numpy()
     hs = atoms_to_rows(moe.stage("hq_sf", T).cpu().numpy()[: R * d.ffn // 16], R, d.ffn)[:nrows]
-    live = rows >= 0
     s = rows[live]
     ref_h = ref["h"].reshape(T * d.k, d.ffn)[s]
     assert rel_l2_rows(h[live], ref_h).max() <= TOL_INTER
@@ -203,7 +201,9 @@ def test_forward_mid_size_stage_by_stage(mid, T):
     h = moe.stage("h", T, torch.bfloat16).view(R, d.ffn)[:nrows].float().cpu().numpy()
     hc = moe.stage("hq_codes", T).view(R, d.ffn // 2)[:nrows].cpu().numpy()
     hsf = atoms_to_rows(moe.stage("hq_sf", T).cpu().numpy()[: R * d.ffn // 16], R, d.ffn)[:nrows]
-    pos = {int(sl): i for i, sl in enumerate(rows) if sl >= 0}
+    counts = moe.stage("counts", T, torch.int32).cpu().numpy()
+    live = real_rows(counts, nrows)
+    pos = {int(sl): i for i, sl in enumerate(rows) if live[i]}
     zdec = dequant(zc, zs, sdz)
     _, _, sdh = oracle.quantize_nvfp4(np.ones((1, 16), np.float32), mid.amax_h)
     c = moe.stage("c", T, torch.bfloat16).view(T, d.l).float().cpu().numpy()[sample]

@@ -12,7 +12,7 @@ import torch
 
 import lmoe_synth
 import oracle
-from lmoe_cases import Case, rel_l2_rows, w_tol
+from lmoe_cases import Case, real_rows, rel_l2_rows, w_tol
 
 pytestmark = pytest.mark.gpu
 
@@ -145,7 +145,7 @@ def test_ultra_drift_against_bf16_experts(ultra_uniform):
     zn = np.stack([zc & 15, zc >> 4], -1).reshape(T, -1)
     nrows = int(moe.stage("nrows", T, torch.int32).cpu()[0])
     R = moe.stage("rows", T, torch.int32).numel()
-    live = moe.stage("rows", T, torch.int32).cpu().numpy()[:nrows] >= 0
+    live = real_rows(moe.stage("counts", T, torch.int32).cpu().numpy(), nrows)
     h = moe.stage("h", T, torch.bfloat16).view(R, d.ffn)[:nrows].float().cpu().numpy()[live]
     hc = moe.stage("hq_codes", T).view(R, d.ffn // 2)[:nrows].cpu().numpy()[live]
     hn = np.stack([hc & 15, hc >> 4], -1).reshape(hc.shape[0], -1)

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import lmoe_synth
-from lmoe_cases import Case, rel_l2_rows, w_tol
+from lmoe_cases import Case, real_rows, rel_l2_rows, w_tol
 
 pytestmark = pytest.mark.gpu
 
@@ -39,7 +39,9 @@ def check_w4a16(case, T, x, y, sample):
     R = moe.stage("rows", T, torch.int32).numel()
     rows = moe.stage("rows", T, torch.int32).cpu().numpy()[:nrows]
     h = moe.stage("h", T, torch.bfloat16).view(R, d.ffn)[:nrows].float().cpu().numpy()
-    pos = {int(sl): i for i, sl in enumerate(rows) if sl >= 0}
+    counts = moe.stage("counts", T, torch.int32).cpu().numpy()
+    live = real_rows(counts, nrows)
+    pos = {int(sl): i for i, sl in enumerate(rows) if live[i]}
     hr = np.stack([h[pos[int(t) * d.k + j]] for t in sample for j in range(d.k)])
     assert rel_l2_rows(hr, ref["h"].reshape(-1, d.ffn)).max() <= TOL_INTER
     c = moe.stage("c", T, torch.bfloat16).view(T, d.l).float().cpu().numpy()[sample]
