@@ -223,7 +223,7 @@ WsLayout layout(const lmoe_ctx *c, int64_t T) {
     L.zacc = take(L.split_down ? T * l * 4 : 0);
     L.zq_codes = take(T * l / 2);
     L.zq_sf = take(T * l / 16);
-    L.z_dbg = take(c->debug ? T * l * 2 : 0);
+    L.z_dbg = take(c->debug || c->w4a16 ? T * l * 2 : 0);   // W4A16: the scatter copies z rows
     const bool w4 = c->w4a16 != 0;
     L.a_codes = take(w4 ? 0 : L.R * l / 2);
     L.a_sf = take(w4 ? 0 : L.R * l / 16);
@@ -867,7 +867,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     float *zacc = static_cast<float *>(at(L.zacc));
     uint8_t *zq_codes = static_cast<uint8_t *>(at(L.zq_codes));
     uint8_t *zq_sf = static_cast<uint8_t *>(at(L.zq_sf));
-    __nv_bfloat16 *z_dbg = c->debug ? static_cast<__nv_bfloat16 *>(at(L.z_dbg)) : nullptr;
+    __nv_bfloat16 *z_dbg = c->debug || c->w4a16 ? static_cast<__nv_bfloat16 *>(at(L.z_dbg)) : nullptr;
     uint8_t *a_codes = static_cast<uint8_t *>(at(L.a_codes));
     uint8_t *a_sf = static_cast<uint8_t *>(at(L.a_sf));
     uint8_t *h_codes = static_cast<uint8_t *>(at(L.h_codes));
@@ -901,9 +901,11 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         if (L.split_down) {
             g.out = zacc; g.ld_out = l;
         } else {
+            // row-major zq (and, W4A16, z) only; scatter_rows_kernel copies the rows into the
+            // expert segments (a copy kernel with all SMs beats k scattered stores per row in
+            // the GEMM epilogue)
             g.q = c->qz; g.q_codes = zq_codes; g.q_sf = zq_sf; g.dbg = z_dbg;
-            g.topk = k; g.idx = idx; g.slot_off = slot_off; g.seg_start = seg;
-            g.a_codes = a_codes; g.a_sf = a_sf; g.row_slot_out = row_slot; g.a_bf16 = a_bf16;
+            g.topk = 0;
         }
         LMOE_CUDA((launch_gemm<kKindBf16>(tx, small_a ? c->tm_wd : c->tm_wd_w, g,
                                       grid_for(int64_t(g.m_tiles) * g.n_tiles * g.k_splits, c->num_sms), small_a, ds)));
@@ -942,6 +944,15 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         } else {
             lmoe_status st = down_proj(s);
             if (st != LMOE_OK) return st;
+        }
+        if (!L.split_down) {
+            const int64_t slots = T * k;
+            LMOE_CUDA(launch_pdl(scatter_rows_kernel, dim3(static_cast<unsigned>(cdiv(slots * 32, 256))), dim3(256), 0, s,
+                                 static_cast<const uint8_t *>(zq_codes), static_cast<const uint8_t *>(zq_sf),
+                                 static_cast<const __nv_bfloat16 *>(z_dbg), static_cast<const int32_t *>(idx),
+                                 static_cast<const int32_t *>(slot_off), static_cast<const int32_t *>(seg), slots, k, l,
+                                 a_codes, a_sf, a_bf16, row_slot));
+            prof_mark(c, "scatter", s);
         }
         if (L.split_down) {
             // whole tokens per block: 256 threads cover 256 / (l/16) tokens (l <= 4096, k * tokens <= 256)
@@ -1119,7 +1130,7 @@ int lmoe_forward_kernel_count(const lmoe_ctx *c, int64_t T) {
     // its last warp lays out the segments), down-proj, expert-up, expert-down, combine cast, up-proj, plus one finalize per split projection (and, for a split down-projection run
     // beside the router, the clearing of its accumulator), plus the shared expert's
     // quantization of x and its two GEMMs
-    return 7 + (T > kSmallMaxT ? 1 : 0) + (L.split_down ? 2 : 0) + (L.split_up ? 1 : 0) + (c->shared_ffn ? 3 : 0);
+    return 7 + (T > kSmallMaxT ? 1 : 0) + (L.split_down ? 2 : 1) + (L.split_up ? 1 : 0) + (c->shared_ffn ? 3 : 0);
 }
 
 lmoe_status lmoe_set_profile(lmoe_ctx *c, int on) {

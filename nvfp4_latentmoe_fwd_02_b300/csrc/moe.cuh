@@ -77,6 +77,39 @@ __global__ void __launch_bounds__(256) z_finalize_kernel(
     }
 }
 
+// Copies of each token's quantized latent row into its k expert-segment rows (large T: the
+// down-projection epilogue then only writes the row-major zq), one warp per routing slot:
+// the codes (l/2 bytes) as 16-byte stores, the scales (l/16 bytes, row-major) as 4-byte groups
+// into the scale atoms, the slot into row_slot.  W4A16: the bf16 z row instead (a_bf16 set).
+__global__ void __launch_bounds__(256) scatter_rows_kernel(
+    const uint8_t *__restrict__ zq_codes, const uint8_t *__restrict__ zq_sf,
+    const __nv_bfloat16 *__restrict__ z, const int32_t *__restrict__ idx,
+    const int32_t *__restrict__ slot_off, const int32_t *__restrict__ seg_start, int64_t slots, int k,
+    int l, uint8_t *__restrict__ a_codes, uint8_t *__restrict__ a_sf, __nv_bfloat16 *__restrict__ a_bf16,
+    int32_t *__restrict__ row_slot) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t slot = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (slot >= slots) return;
+    const int64_t t = slot / k;
+    const int row = slot_row(idx, slot_off, seg_start, slot);
+    if (lane == 0) row_slot[row] = static_cast<int32_t>(slot);
+    if (a_bf16) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(z + t * l);
+        uint4 *dst = reinterpret_cast<uint4 *>(a_bf16 + static_cast<int64_t>(row) * l);
+        for (int i = lane; i < l / 8; i += 32) dst[i] = __ldg(src + i);
+        return;
+    }
+    const uint4 *src = reinterpret_cast<const uint4 *>(zq_codes + t * (l / 2));
+    uint4 *dst = reinterpret_cast<uint4 *>(a_codes + static_cast<int64_t>(row) * (l / 2));
+    for (int i = lane; i < l / 32; i += 32) dst[i] = __ldg(src + i);
+    const int K64 = l / 64;
+    const uint32_t *sf4 = reinterpret_cast<const uint32_t *>(zq_sf + t * (l / 16));
+    for (int j = lane; j < K64; j += 32)   // the four scales of 16-blocks 4j..4j+3 sit together in atom j
+        *reinterpret_cast<uint32_t *>(a_sf + sf_atom_offset(row, 4 * j, K64)) = __ldg(sf4 + j);
+}
+
 // out[c][r] = in[r][c] for an [R][Cn] fp32 matrix (router weights, once at create).
 __global__ void transpose_f32_kernel(const float *__restrict__ in, int64_t R, int64_t Cn,
                                      float *__restrict__ out) {
