@@ -186,9 +186,11 @@ lmoe_status cuda_status(cudaError_t e) {
     } while (0)
 
 // Split-K plan for a dense projection: spread small-M problems over the SMs.
-int plan_splits(int m_tiles, int n_tiles, int k_tiles, int num_sms) {
+// fill: split only while tiles * fill <= SMs (a split costs a finalize kernel and fp32
+// reduction traffic; with N = d the up-projection already has enough tiles unsplit).
+int plan_splits(int m_tiles, int n_tiles, int k_tiles, int num_sms, int fill = 2) {
     const int tiles = m_tiles * n_tiles;
-    if (tiles * 2 > num_sms) return 1;
+    if (tiles * fill > num_sms) return 1;
     int s = std::max(1, num_sms / tiles);
     s = std::min(s, k_tiles);
     const int per = static_cast<int>(cdiv(k_tiles, s));
@@ -206,7 +208,7 @@ WsLayout layout(const lmoe_ctx *c, int64_t T) {
     const int kb = kb_for(T <= kSmallAMaxT);
     const int bn = bn_for(T <= kSmallAMaxT);
     L.down_splits = plan_splits(mt, static_cast<int>(cdiv(l, bn)), static_cast<int>(cdiv(d / 64, kb)), c->num_sms);
-    L.up_splits = plan_splits(mt, static_cast<int>(cdiv(d, bn)), static_cast<int>(cdiv(l / 64, kb)), c->num_sms);
+    L.up_splits = plan_splits(mt, static_cast<int>(cdiv(d, bn)), static_cast<int>(cdiv(l / 64, kb)), c->num_sms, 4);
     L.split_down = L.down_splits > 1;
     L.split_up = L.up_splits > 1;
     size_t off = 0;
@@ -946,11 +948,10 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
             if (st != LMOE_OK) return st;
         }
         if (!L.split_down) {
-            const int64_t slots = T * k;
-            LMOE_CUDA(launch_pdl(scatter_rows_kernel, dim3(static_cast<unsigned>(cdiv(slots * 32, 256))), dim3(256), 0, s,
+            LMOE_CUDA(launch_pdl(scatter_rows_kernel, dim3(static_cast<unsigned>(cdiv(T * 32, 256))), dim3(256), 0, s,
                                  static_cast<const uint8_t *>(zq_codes), static_cast<const uint8_t *>(zq_sf),
                                  static_cast<const __nv_bfloat16 *>(z_dbg), static_cast<const int32_t *>(idx),
-                                 static_cast<const int32_t *>(slot_off), static_cast<const int32_t *>(seg), slots, k, l,
+                                 static_cast<const int32_t *>(slot_off), static_cast<const int32_t *>(seg), T, k, l,
                                  a_codes, a_sf, a_bf16, row_slot));
             prof_mark(c, "scatter", s);
         }

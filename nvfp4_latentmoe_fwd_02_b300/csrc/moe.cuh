@@ -78,36 +78,63 @@ __global__ void __launch_bounds__(256) z_finalize_kernel(
 }
 
 // Copies of each token's quantized latent row into its k expert-segment rows (large T: the
-// down-projection epilogue then only writes the row-major zq), one warp per routing slot:
-// the codes (l/2 bytes) as 16-byte stores, the scales (l/16 bytes, row-major) as 4-byte groups
-// into the scale atoms, the slot into row_slot.  W4A16: the bf16 z row instead (a_bf16 set).
+// down-projection epilogue then only writes the row-major zq), one warp per token: the row is
+// read once into registers (codes as 16-byte pieces, scales as 4-byte groups), then written to
+// each of the token's k rows (codes as 16-byte stores, the scales into the scale atoms) with
+// the slot into row_slot.  W4A16: the bf16 z row instead (a_bf16 set).  l <= 4096.
 __global__ void __launch_bounds__(256) scatter_rows_kernel(
     const uint8_t *__restrict__ zq_codes, const uint8_t *__restrict__ zq_sf,
     const __nv_bfloat16 *__restrict__ z, const int32_t *__restrict__ idx,
-    const int32_t *__restrict__ slot_off, const int32_t *__restrict__ seg_start, int64_t slots, int k,
+    const int32_t *__restrict__ slot_off, const int32_t *__restrict__ seg_start, int64_t T, int k,
     int l, uint8_t *__restrict__ a_codes, uint8_t *__restrict__ a_sf, __nv_bfloat16 *__restrict__ a_bf16,
     int32_t *__restrict__ row_slot) {
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
-    const int64_t slot = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    if (slot >= slots) return;
-    const int64_t t = slot / k;
-    const int row = slot_row(idx, slot_off, seg_start, slot);
-    if (lane == 0) row_slot[row] = static_cast<int32_t>(slot);
+    const int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (t >= T) return;
+    // the token's k rows (k <= 32): lane j looks up slot j
+    const int my_row = lane < k ? slot_row(idx, slot_off, seg_start, t * k + lane) : 0;
+    if (lane < k) row_slot[my_row] = static_cast<int32_t>(t * k + lane);
     if (a_bf16) {
+        const int n16 = l / 8;                             // uint4 per row
+        uint4 v[16];
         const uint4 *src = reinterpret_cast<const uint4 *>(z + t * l);
-        uint4 *dst = reinterpret_cast<uint4 *>(a_bf16 + static_cast<int64_t>(row) * l);
-        for (int i = lane; i < l / 8; i += 32) dst[i] = __ldg(src + i);
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+            if (q * 32 + lane < n16) v[q] = __ldg(src + q * 32 + lane);
+        for (int j = 0; j < k; ++j) {
+            const int row = __shfl_sync(0xffffffffu, my_row, j);
+            uint4 *dst = reinterpret_cast<uint4 *>(a_bf16 + static_cast<int64_t>(row) * l);
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                if (q * 32 + lane < n16) dst[q * 32 + lane] = v[q];
+        }
         return;
     }
+    const int n16 = l / 32;                                // uint4 of codes per row
+    const int K64 = l / 64;                                // 4-byte scale groups per row
+    uint4 cv[4];
+    uint32_t sv[2];
     const uint4 *src = reinterpret_cast<const uint4 *>(zq_codes + t * (l / 2));
-    uint4 *dst = reinterpret_cast<uint4 *>(a_codes + static_cast<int64_t>(row) * (l / 2));
-    for (int i = lane; i < l / 32; i += 32) dst[i] = __ldg(src + i);
-    const int K64 = l / 64;
     const uint32_t *sf4 = reinterpret_cast<const uint32_t *>(zq_sf + t * (l / 16));
-    for (int j = lane; j < K64; j += 32)   // the four scales of 16-blocks 4j..4j+3 sit together in atom j
-        *reinterpret_cast<uint32_t *>(a_sf + sf_atom_offset(row, 4 * j, K64)) = __ldg(sf4 + j);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        if (q * 32 + lane < n16) cv[q] = __ldg(src + q * 32 + lane);
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+        if (q * 32 + lane < K64) sv[q] = __ldg(sf4 + q * 32 + lane);
+    for (int j = 0; j < k; ++j) {
+        const int row = __shfl_sync(0xffffffffu, my_row, j);
+        uint4 *dst = reinterpret_cast<uint4 *>(a_codes + static_cast<int64_t>(row) * (l / 2));
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (q * 32 + lane < n16) dst[q * 32 + lane] = cv[q];
+#pragma unroll
+        for (int q = 0; q < 2; ++q)                        // scales of 16-blocks 4g..4g+3: atom g
+            if (q * 32 + lane < K64)
+                *reinterpret_cast<uint32_t *>(a_sf + sf_atom_offset(row, 4 * (q * 32 + lane), K64)) = sv[q];
+    }
 }
 
 // out[c][r] = in[r][c] for an [R][Cn] fp32 matrix (router weights, once at create).

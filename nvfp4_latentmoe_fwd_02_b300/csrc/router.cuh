@@ -279,41 +279,32 @@ __device__ __forceinline__ float warp_canonical_logit_g(const __nv_bfloat16 *__r
 }
 
 // The 32 largest keys of the warp (R keys per lane, distinct except padding 0), sorted
-// descending, lane j holding the j-th: the 32nd largest key is built bit by bit from the top
-// (a candidate is kept while at least 32 keys reach it), the keys at or above it are packed
-// through `slots` (32 entries of warp scratch), then a bitonic sort across the lanes.
+// descending, lane j holding the j-th.  Each lane sorts its own keys (in registers), then
+// rounds merge the lanes' r-th largest keys into a running top 32 (a bitonic sort of the 32
+// candidates and a bitonic merge with the list): after round r the list is the top 32 of every
+// key ranked <= r in its lane, so once no lane's next key beats the list's last the list is
+// final (with the top 32 spread over the lanes this takes a few rounds).
 template <int R>
-__device__ __forceinline__ uint64_t warp_top32(const uint64_t (&key)[R], uint64_t *slots, int lane) {
-    uint64_t tau = 0;
-    for (int bit = 63; bit >= 0; --bit) {
-        const uint64_t cand = tau | (1ull << bit);
-        int cnt = 0;
+__device__ __forceinline__ void sort_desc_local(uint64_t (&a)[R]) {
 #pragma unroll
-        for (int i = 0; i < R; ++i) cnt += key[i] >= cand ? 1 : 0;
-        if (__reduce_add_sync(0xffffffffu, cnt) >= 32) tau = cand;
-    }
-    // keys >= tau: exactly 32 when at least 32 keys are non-zero; otherwise pad with zeros
-    slots[lane] = 0;
-    __syncwarp();
-    int mine = 0;
+    for (int k = 2; k <= R; k <<= 1)
 #pragma unroll
-    for (int i = 0; i < R; ++i) mine += (key[i] >= tau && key[i] != 0) ? 1 : 0;
-    int pos = mine;
+        for (int j = k >> 1; j >= 1; j >>= 1)
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, pos, o);
-        if (lane >= o) pos += v;
-    }
-    pos -= mine;                                           // exclusive prefix
+            for (int i = 0; i < R; ++i) {
+                const int p = i ^ j;
+                if (p > i) {
+                    const bool desc = (i & k) == 0;
+                    const uint64_t x = a[i], y = a[p];
+                    const bool swap = desc ? (x < y) : (x > y);
+                    a[i] = swap ? y : x;
+                    a[p] = swap ? x : y;
+                }
+            }
+}
+__device__ __forceinline__ uint64_t warp_sort32_desc(uint64_t a, int lane) {
 #pragma unroll
-    for (int i = 0; i < R; ++i)
-        if (key[i] >= tau && key[i] != 0 && pos < 32) slots[pos++] = key[i];
-    __syncwarp();
-    uint64_t a = slots[lane];
-    __syncwarp();
-    // bitonic sort, descending by lane
-#pragma unroll
-    for (int k = 2; k <= 32; k <<= 1) {
+    for (int k = 2; k <= 32; k <<= 1)
 #pragma unroll
         for (int j = k >> 1; j >= 1; j >>= 1) {
             const uint64_t o = shfl_xor64(a, j);
@@ -321,8 +312,31 @@ __device__ __forceinline__ uint64_t warp_top32(const uint64_t (&key)[R], uint64_
             const bool desc = (lane & k) == 0;
             a = (lower == desc) ? (a > o ? a : o) : (a < o ? a : o);
         }
-    }
     return a;
+}
+template <int R>
+__device__ __forceinline__ uint64_t warp_top32(uint64_t (&key)[R], int lane) {
+    sort_desc_local<R>(key);
+    uint64_t list = warp_sort32_desc(key[0], lane);
+#pragma unroll
+    for (int r = 1; r < R; ++r) {
+        // stop when no lane's next key beats the 32nd of the list
+        uint64_t m = key[r];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const uint64_t v = shfl_xor64(m, o);
+            m = v > m ? v : m;
+        }
+        const uint64_t last = (static_cast<uint64_t>(__shfl_sync(0xffffffffu, static_cast<uint32_t>(list >> 32), 31)) << 32) |
+                              __shfl_sync(0xffffffffu, static_cast<uint32_t>(list), 31);
+        if (m <= last) break;
+        const uint64_t cand = warp_sort32_desc(key[r], lane);
+        // merge: the top 32 of (list, cand) -- list descending, cand reversed gives a bitonic 64
+        const uint64_t crev = (static_cast<uint64_t>(__shfl_sync(0xffffffffu, static_cast<uint32_t>(cand >> 32), 31 - lane)) << 32) |
+                              __shfl_sync(0xffffffffu, static_cast<uint32_t>(cand), 31 - lane);
+        list = merge_top32(list, crev, lane);
+    }
+    return list;
 }
 
 // Output of one token's selection by its warp: the selected lanes (sel) in ascending expert
@@ -473,13 +487,11 @@ __global__ void __launch_bounds__(32 * kSelWarps) router_select_kernel(
     int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts,
     int32_t *__restrict__ slot_off, int *__restrict__ done, int32_t *__restrict__ seg_start,
     int32_t *__restrict__ mt_start, int32_t *__restrict__ nrows) {
-    __shared__ uint64_t slots_all[kSelWarps][32];
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = blockIdx.x * kSelWarps + warp;
     if (t >= T) return;
-    uint64_t *slots = slots_all[warp];
     const int C = d / kChunk;
     const __nv_bfloat16 *xt = x + static_cast<int64_t>(t) * d;
     // an upper bound of |x_t| (the fp32 sum of d squares is within d * 2^-24 of exact)
@@ -508,7 +520,7 @@ __global__ void __launch_bounds__(32 * kSelWarps) router_select_kernel(
         const int e = i * 32 + lane;
         key[i] = e < E ? topk_key(__fadd_rn(__ldg(at + e), __ldg(bias + e)), e) : 0ull;
     }
-    uint64_t top = warp_top32<R>(key, slots, lane);
+    uint64_t top = warp_top32<R>(key, lane);
     float v = key_value(top);                              // NaN for padding (E < 32)
     int e_l = key_index(top);
     const float vk = __shfl_sync(0xffffffffu, v, k - 1);
@@ -558,7 +570,7 @@ __global__ void __launch_bounds__(32 * kSelWarps) router_select_kernel(
         const int e = e0 + lane;
         key[i] = e < E ? topk_key(mine, e) : 0ull;
     }
-    top = warp_top32<R>(key, slots, lane);
+    top = warp_top32<R>(key, lane);
     emit_selection(t, k, lane < k, key_index(top), key_value(top), lane, idx_out, w_out, counts, slot_off);
     if (done) segments_if_last(T, done, counts, E, seg_start, mt_start, nrows, lane);
 }
