@@ -14,17 +14,21 @@
 // box hold stale data whose accumulator rows the epilogue never reads), 128 rows otherwise
 // (one TMA request instead of four: the request count, not the bytes, limited the loads).
 //
-// Warp roles (384 threads, one CTA per SM):
+// Warp roles (one CTA per SM; 384 threads, 256 for the grouped NVFP4 GEMMs at prefill):
 //   warp 0      TMA producer (one elected lane): operand tiles + scale atoms -> smem ring
 //   warp 1      TMEM allocator and MMA issuer (one lane): tcgen05.mma into one of two
 //               128-column accumulators
 //   warps 2, 3  scale-factor copiers (NVFP4 only, one lane each): the A and the B scale atoms
-//               of a stage, smem -> TMEM with tcgen05.cp, then a commit on the stage's
+//               of a stage (loaded first, on their own barrier, so they land ahead of the
+//               operand tiles), smem -> TMEM with tcgen05.cp, then a commit on the stage's
 //               "scales ready" barrier.  Issuing a tensor-core op costs a single thread tens of
 //               cycles, so copies and MMAs are issued from three threads in parallel.
-//   warps 4..11 epilogue: tcgen05.ld of the accumulator (warp w reads lane quadrant w % 4;
-//               two warps per quadrant, each taking half of the tile's columns), fused
-//               output transform, global stores / reductions
+//   warps 4..   epilogue: tcgen05.ld of the accumulator (warp w reads lane quadrant w % 4;
+//               eight warps: two per quadrant, each taking half of the tile's columns; four
+//               warps: one per quadrant), fused output transform, global stores / reductions.
+//               A warp loads two 32-column chunks before one wait; the next tile's per-row
+//               scalars (expert scale, routing weight, output token) are fetched while the
+//               current tile is processed.
 // Barriers: full/empty per smem stage, tmem_full/tmem_empty per accumulator.  Every wait is
 // bounded (common.cuh); on a timeout the CTA records LMOE_ETIMEOUT, the roles leave their
 // loops, outstanding tensor-core work is drained with a bounded wait and TMEM is freed.
@@ -102,8 +106,8 @@ struct Tile {
 // decodes every tile, so the binary search must not walk global memory.
 struct SmemTables {
     int32_t mt[1025];    // mt_start[0..E]
-    int32_t seg[1024];   // seg_start[e]
     int32_t cnt[1024];   // counts[e]
+    float rcp_h[256];    // h quantizer: reciprocal of each block-scale byte (quant_block16_lut)
 };
 
 __device__ __forceinline__ Tile decode_tile(const GemmArgs &g, const SmemTables *tb, int t) {
@@ -121,7 +125,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &g, const SmemTables 
         const int local = t - mt0 * g.n_tiles;
         const int m = local % mt_e, n = local / mt_e;
         tl.e = e;
-        tl.a_row0 = tb->seg[e] + m * kBM;
+        tl.a_row0 = (mt0 + m) * kBM;          // segments are whole 128-row tiles: seg_start = 128 mt_start
         tl.rows = min(kBM, tb->cnt[e] - m * kBM);
         tl.n0 = n * g.bn;
         tl.b_row0 = e * g.N + n * g.bn;
@@ -189,8 +193,10 @@ __device__ __forceinline__ EpiRow epilogue_row(const GemmArgs &g, const Tile &tl
     return er;
 }
 
+// rcp_of: the h quantizer's reciprocal table in shared memory (grouped NVFP4 GEMMs), or null.
 __device__ __forceinline__ void epilogue_chunk(const GemmArgs &g, const Tile &tl, const EpiRow &er,
-                                               int row, int c0, const uint32_t (&r)[32]) {
+                                               int row, int c0, const uint32_t (&r)[32],
+                                               const float *rcp_of) {
     if (!er.valid) return;
     const int64_t grow = static_cast<int64_t>(tl.a_row0) + row;   // global row of A / output
     const int col = tl.n0 + c0;                                    // output column
@@ -287,7 +293,8 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs &g, const Tile &tl
             float x[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) x[i] = v[16 * b + i];
-            s[b] = quant_block16(x, g.q, w[2 * b], w[2 * b + 1]);
+            s[b] = rcp_of ? quant_block16_lut(x, g.q, rcp_of, w[2 * b], w[2 * b + 1])
+                          : quant_block16(x, g.q, w[2 * b], w[2 * b + 1]);
         }
         *reinterpret_cast<uint4 *>(g.q_codes + grow * (g.N / 2) + col / 2) = make_uint4(w[0], w[1], w[2], w[3]);
         const uint16_t s2 = static_cast<uint16_t>(s[0] | (s[1] << 8));
@@ -343,6 +350,60 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs &g, const Tile &tl
     }
 }
 
+// EPI_H_QUANT over two adjacent 32-column chunks (columns c0 .. c0 + 63, c0 a multiple of 64)
+// in one straight-line block, so the four 16-element blocks' dependency chains interleave.
+// Same arithmetic as epilogue_chunk's EPI_H_QUANT.
+__device__ __forceinline__ void hquant_pair(const GemmArgs &g, const Tile &tl, const EpiRow &er, int row,
+                                            int c0, const uint32_t (&r0)[32], const uint32_t (&r1)[32],
+                                            const float *rcp_of) {
+    if (!er.valid) return;
+    const int64_t grow = static_cast<int64_t>(tl.a_row0) + row;
+    const int col = tl.n0 + c0;
+    const float a = er.alpha;
+    float v[64];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const float u0 = fmaxf(__fmul_rn(a, __uint_as_float(r0[i])), 0.0f);
+        const float u1 = fmaxf(__fmul_rn(a, __uint_as_float(r1[i])), 0.0f);
+        v[i] = __fmul_rn(u0, u0);
+        v[32 + i] = __fmul_rn(u1, u1);
+    }
+    uint32_t hb[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        hb[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+        v[2 * i] = __uint_as_float(hb[i] << 16);
+        v[2 * i + 1] = __uint_as_float(hb[i] & 0xFFFF0000u);
+    }
+    if (g.dbg) {
+        uint4 *o = reinterpret_cast<uint4 *>(g.dbg + grow * g.N + col);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = make_uint4(hb[4 * i], hb[4 * i + 1], hb[4 * i + 2], hb[4 * i + 3]);
+    }
+    uint32_t w[8], s[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = v[16 * b + i];
+        s[b] = quant_block16_lut(x, g.q, rcp_of, w[2 * b], w[2 * b + 1]);
+    }
+    uint4 *q = reinterpret_cast<uint4 *>(g.q_codes + grow * (g.N / 2) + col / 2);
+    q[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    q[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    // blocks col/16 .. col/16 + 3 are the four bytes of one word of the row's scale atom
+    *reinterpret_cast<uint32_t *>(g.q_sf + sf_atom_offset(grow, col / 16, g.N / 64)) =
+        s[0] | (s[1] << 8) | (s[2] << 16) | (s[3] << 24);
+}
+
+// The output row of each of the eight rows this lane reduces (rows it * 4 + lane / 8), or -1
+// for padding: exchanged once per tile and shared by the tile's chunks.
+__device__ __forceinline__ void combine_rows(const EpiRow &er, int lane, int32_t (&orow)[8]) {
+    const int32_t mine = er.valid ? static_cast<int32_t>(er.orow) : -1;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) orow[it] = __shfl_sync(0xffffffffu, mine, it * 4 + (lane >> 3));
+}
+
 // Combine through shared memory (prefill tiles): the warp parks its 32 rows x 32 scaled values
 // in a 4 KB staging buffer (16-byte chunk c of row r at chunk slot c ^ (r % 8): conflict-free
 // both ways), then reads them back four rows per instruction, so each red.add.v4 instruction
@@ -350,7 +411,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs &g, const Tile &tl
 // padding (invalid) take part in the exchange but issue no reduction.  Warp-synchronous.
 __device__ __forceinline__ void combine_staged(const GemmArgs &g, const Tile &tl, const EpiRow &er,
                                                int c0, const uint32_t (&r)[32], float4 *stg,
-                                               int lane) {
+                                               int lane, const int32_t (&orow)[8]) {
     const float ws = er.wslot, a = er.alpha;
     float4 *mine = stg + lane * 8;
 #pragma unroll
@@ -366,9 +427,9 @@ __device__ __forceinline__ void combine_staged(const GemmArgs &g, const Tile &tl
     for (int it = 0; it < 8; ++it) {
         const int rr = it * 4 + (lane >> 3);
         const float4 v = stg[rr * 8 + (cc ^ (rr & 7))];
-        const int64_t orow = __shfl_sync(0xffffffffu, er.orow, rr);
-        const bool ok = __shfl_sync(0xffffffffu, er.valid ? 1 : 0, rr) != 0;
-        if (ok) red_add_v4_f32(static_cast<float *>(g.out) + orow * g.ld_out + col + 4 * cc, v.x, v.y, v.z, v.w);
+        if (orow[it] >= 0)
+            red_add_v4_f32(static_cast<float *>(g.out) + static_cast<int64_t>(orow[it]) * g.ld_out + col + 4 * cc,
+                           v.x, v.y, v.z, v.w);
     }
     __syncwarp();
 }
@@ -379,7 +440,7 @@ __device__ __forceinline__ void combine_staged(const GemmArgs &g, const Tile &tl
 // accumulator rows the epilogue never reads.  KB: 128-byte column blocks (256 e2m1 or 64 bf16
 // elements of K each; 128 e4m3) per pipeline stage; KB = 2 halves the per-stage barrier handshakes and
 // copies when each stage carries little MMA work (decode).
-template <int KIND, bool SMALLA, int KB, int BN = kBN>
+template <int KIND, bool SMALLA, int KB, int BN = kBN, bool STG = false>
 struct GemmCfg {
     static constexpr bool NVF4 = KIND == kKindNvf4;
     static constexpr bool W4 = KIND == kKindW4A16;
@@ -387,7 +448,12 @@ struct GemmCfg {
     static constexpr int kRawBlock = W4 ? 128 * 32 + 512 : 0;         // E2M1 codes + one scale atom per block
     static constexpr int kRawStage = KB * kRawBlock;
     static constexpr int kEpi0 = W4 ? 8 : 4;                          // first epilogue warp
-    static constexpr int kThreads = 32 * (kEpi0 + 8);
+    // epilogue warps: 4 for the grouped NVFP4 GEMMs at prefill (one per TMEM lane quadrant,
+    // four 32-column chunks each), 8 otherwise.  At prefill the MMA issuer and the TMA
+    // producer, not the epilogue, set the pace, and every epilogue warp competes with them for
+    // its SM sub-partition's issue slots: 4 warps run the grouped GEMMs faster than 8 or 16.
+    static constexpr int kEpiWarps = NVF4 && !SMALLA ? 4 : 8;
+    static constexpr int kThreads = 32 * (kEpi0 + kEpiWarps);
     static constexpr int kACol = SMALLA ? kABoxBytes : kTileBytes;   // A bytes per column block
     static constexpr int kAStage = KB * kACol;
     static constexpr int kBStage = KB * BN * 128;                     // B tile: BN rows of 128 bytes
@@ -397,22 +463,19 @@ struct GemmCfg {
     static constexpr int kTmaXPerBlock = (KIND == kKindBf16 || W4) ? 64 : 128;  // tensor-map x units per block
     static constexpr int kStepsPerBlock = 4;                          // MMA K steps per block
     static constexpr int kSfCols = NVF4 ? 32 * KB : 0;                // TMEM columns per stage
-    static constexpr bool kStagedCombine = NVF4 && !SMALLA;           // combine via smem staging
-    static constexpr int kStgBytes = kStagedCombine ? 8 * 4096 : 0;   // one 4 KB buffer per epilogue warp
+    static constexpr bool kStagedCombine = NVF4 && !SMALLA && STG;    // combine via smem staging
+    static constexpr int kStgBytes = kStagedCombine ? kEpiWarps * 4096 : 0;   // one 4 KB buffer per epilogue warp
 };
 
-template <int KIND, bool SMALLA, int KB, int BN = kBN>
+template <int KIND, bool SMALLA, int KB, int BN = kBN, bool STG = false>
 constexpr int gemm_smem_bytes(int stages) {
-    using C = GemmCfg<KIND, SMALLA, KB, BN>;
+    using C = GemmCfg<KIND, SMALLA, KB, BN, STG>;
     return 1024 + stages * (C::kAStage + C::kBStage + 2 * C::kSfStage) + C::kSlack + 256 +
            stages * C::kRawStage +
            (C::kTables ? static_cast<int>((sizeof(SmemTables) + 15) & ~static_cast<size_t>(15)) : 0) +
            C::kStgBytes + (C::W4 ? 1024 : 0);
 }
 
-constexpr int kEpiWarps = 8;
-constexpr int kEpiWarp0 = 4;
-constexpr int kGemmThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr int kConvWarps = 6;   // W4A16: warps 2..7 decode the weight tiles
 
 // E2M1 code -> bf16 bits (sign kept; E2M1 values 0, .5, 1, 1.5, 2, 3, 4, 6 are exact in bf16).
@@ -451,12 +514,15 @@ __device__ __forceinline__ void w4_convert_block(const uint8_t *raw, uint8_t *ds
 }
 
 // BN: tile width, 128 or (dense kinds without scale factors) 256: a 256-column tile moves
-// 48 KB of operands per 64-element K block for twice the outputs of a 128-column one.
-template <int KIND, bool SMALLA, int KB, int STAGES, int BN = kBN>
-__global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN>::kThreads, 1)
+// 48 KB of operands per 64-element K block for twice the outputs of a 128-column one.  (NVFP4
+// stays at 128: two 256-column accumulators would fill TMEM and leave no room for the scale
+// factors, and one accumulator serialises each tile's epilogue with the next tile's MMAs.)
+// STG: the staged combine (grouped NVFP4 latent-down at prefill; 16 KB of smem).
+template <int KIND, bool SMALLA, int KB, int STAGES, int BN = kBN, bool STG = false>
+__global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmArgs g) {
-    using C = GemmCfg<KIND, SMALLA, KB, BN>;
+    using C = GemmCfg<KIND, SMALLA, KB, BN, STG>;
     static_assert(BN == 128 || (BN == 256 && (KIND == kKindBf16 || KIND == kKindFp8)), "tile width");
     constexpr bool NVF4 = C::NVF4;
     constexpr bool W4 = C::W4;
@@ -471,7 +537,8 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN>::kThreads, 1)
     uint8_t *sRaw = sSFB + STAGES * C::kSfStage;              // W4A16: raw weight blocks
     uint64_t *bars = reinterpret_cast<uint64_t *>(sRaw + STAGES * C::kRawStage);
     uint64_t *full = bars, *empty = bars + STAGES, *sfready = bars + 2 * STAGES;
-    uint64_t *tfull = bars + 3 * STAGES, *tempty = tfull + 2, *drain = tempty + 2;
+    uint64_t *sffull = bars + 3 * STAGES;   // NVFP4: the stage's scale atoms have landed
+    uint64_t *tfull = bars + 4 * STAGES, *tempty = tfull + 2, *drain = tempty + 2;
     uint64_t *cdrain = drain + 1;   // [2]: one per scale copier
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(cdrain + 2);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
@@ -484,7 +551,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN>::kThreads, 1)
     constexpr uint32_t kTmemCols = NVF4 ? 512 : 2 * BN;
     constexpr uint32_t kSfCol0 = 2 * kAccCols;
     static_assert(!NVF4 || kSfCol0 + STAGES * C::kSfCols <= 512, "TMEM budget");
-    static_assert(3 * STAGES + 8 <= 32, "barrier area");
+    static_assert(4 * STAGES + 8 <= 32, "barrier area");
     static_assert(!W4 || kEpi0 == 2 + kConvWarps, "warp roles");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -493,8 +560,9 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN>::kThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
             mbar_init(&sfready[s], W4 ? kConvWarps : 2);   // scales copied / weights decoded
+            mbar_init(&sffull[s], 1);
         }
-        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], kEpiWarps); }
+        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], C::kEpiWarps); }
         mbar_init(drain, 1);
         mbar_init(&cdrain[0], 1);
         mbar_init(&cdrain[1], 1);
@@ -511,7 +579,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN>::kThreads, 1)
     if (C::kTables && g.grouped) {
         for (int i = threadIdx.x; i <= g.E; i += blockDim.x) {
             tb->mt[i] = __ldg(g.mt_start + i);
-            if (i < g.E) { tb->seg[i] = __ldg(g.seg_start + i); tb->cnt[i] = __ldg(g.counts + i); }
+            if (i < g.E) tb->cnt[i] = __ldg(g.counts + i);
         }
     }
     tc_fence_before();
@@ -556,18 +624,21 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN>::kThreads, 1)
                         continue;
                     }
                     const int nsteps = NVF4 ? min(4 * KB, K64 - 4 * kb0) : 4 * KB;
-                    const uint32_t bytes = KB * (C::kACol + BN * 128) + (NVF4 ? 2 * nsteps * 512 : 0);
-                    mbar_arrive_expect_tx(fb, bytes);
+                    if (NVF4) {
+                        // the scale atoms first, on their own barrier: they land ahead of the
+                        // operand tiles, so their smem -> TMEM copies are off the critical path
+                        uint64_t *sb = &sffull[stage];
+                        mbar_arrive_expect_tx(sb, 2 * nsteps * 512);
+                        bulk_load_u32(sSFA0 + stage * C::kSfStage, sfa_tile + kb0 * 2048, nsteps * 512, sb);
+                        bulk_load_u32(sSFB0 + stage * C::kSfStage, sfb_tile + kb0 * 2048, nsteps * 512, sb);
+                    }
+                    mbar_arrive_expect_tx(fb, KB * (C::kACol + BN * 128));
 #pragma unroll
                     for (int b = 0; b < KB; ++b) {
                         const int kx = (kb0 + b) * C::kTmaXPerBlock;
                         const int kxa = g.a_kwrap > 0 ? kx % g.a_kwrap : kx;
                         tma_load_2d_u32(a_st + b * C::kACol, &tmA, fb, kxa, tl.a_row0);
                         tma_load_2d_u32(b_st + b * (BN * 128), &tmB, fb, kx, tl.b_row0);
-                    }
-                    if (NVF4) {
-                        bulk_load_u32(sSFA0 + stage * C::kSfStage, sfa_tile + kb0 * 2048, nsteps * 512, fb);
-                        bulk_load_u32(sSFB0 + stage * C::kSfStage, sfb_tile + kb0 * 2048, nsteps * 512, fb);
                     }
                     issued |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -581,6 +652,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN>::kThreads, 1)
                     const uint32_t p = (issued_phase >> s) & 1u;
                     const long long t0 = clock64();
                     while (!mbar_try_wait(&full[s], p) && clock64() - t0 < kWaitLimitCycles / 8) {}
+                    while (NVF4 && !mbar_try_wait(&sffull[s], p) && clock64() - t0 < kWaitLimitCycles / 8) {}
                 }
             }
         }
@@ -682,7 +754,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN>::kThreads, 1)
                 const Tile tl = decode_tile(g, tb, t);
                 bool ok = true;
                 for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
-                    if (!role_wait(&full[stage], phase, s_abort, g.err)) { ok = false; break; }
+                    if (!role_wait(&sffull[stage], phase, s_abort, g.err)) { ok = false; break; }
                     tc_fence_after();
                     const int nsteps = min(4 * KB, K64 - 4 * kt * KB);
                     const uint32_t sf_t = tmem + kSfCol0 + stage * C::kSfCols + col_off;
@@ -704,13 +776,42 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN>::kThreads, 1)
         // ---------------------------------------------------------------- epilogue
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
-        const int ch0 = ((warp - kEpi0) / 4) * (BN / 32 / 2);   // this warp's half of the columns
+        constexpr int kChunks = BN / 32 / (C::kEpiWarps / 4);    // 32-column chunks per warp and tile
+        static_assert(kChunks == 1 || kChunks % 2 == 0, "chunks are loaded singly or in pairs");
+        const int ch0 = ((warp - kEpi0) / 4) * kChunks;          // this warp's share of the columns
+        const float *rcp_of = (C::kTables && g.grouped && g.epi == EPI_H_QUANT) ? tb->rcp_h : nullptr;
+        if (rcp_of) {
+            // the h quantizer's table, built by the epilogue warps alone (named barrier 1) so
+            // the producer and MMA roles start at once
+            for (int i = threadIdx.x - kEpi0 * 32; i < 256; i += C::kEpiWarps * 32)
+                tb->rcp_h[i] = quant_rcp_entry(g.q, i);
+            asm volatile("bar.sync 1, %0;" ::"r"(C::kEpiWarps * 32) : "memory");
+        }
+        float4 *stg = stg_all + (warp - kEpi0) * 256;
+        int32_t orow[8];
+        auto chunk = [&](const Tile &tl, const EpiRow &er, int ch, const uint32_t (&r)[32]) {
+            if (ch * 32 >= tl.cols) return;
+            if (C::kStagedCombine && g.epi == EPI_COMBINE)
+                combine_staged(g, tl, er, ch * 32, r, stg, lane, orow);
+            else
+                epilogue_chunk(g, tl, er, row, ch * 32, r, rcp_of);
+        };
         int it = 0;
-        for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x, ++it) {
-            const Tile tl = decode_tile(g, tb, t);
+        int t = blockIdx.x;
+        Tile tl{};
+        EpiRow er{};
+        if (t < num_tiles) { tl = decode_tile(g, tb, t); er = epilogue_row(g, tl, row); }
+        for (; t < num_tiles && !*s_abort; t += gridDim.x, ++it) {
+            // The next tile's row scalars (global loads, some dependent) are fetched before this
+            // tile is processed, so their latency overlaps this tile's work.
+            Tile tn = tl;
+            EpiRow en = er;
+            if (t + static_cast<int>(gridDim.x) < num_tiles) {
+                tn = decode_tile(g, tb, t + gridDim.x);
+                en = epilogue_row(g, tn, row);
+            }
             const int acc = it & 1;
             const uint32_t aphase = (it >> 1) & 1;
-            const EpiRow er = epilogue_row(g, tl, row);
             // A warp whose 32 rows are all past the tile's valid rows reads nothing; it still
             // waits for the accumulator before releasing it, which keeps the release phases
             // of all four warps in step.
@@ -719,21 +820,33 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN>::kThreads, 1)
             tc_fence_after();
             const uint32_t taddr = tmem + acc * kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
             if (live) {
-#pragma unroll 1
-                for (int ch = ch0; ch < ch0 + BN / 32 / 2; ++ch) {
-                    if (ch * 32 >= tl.cols) break;
-                    uint32_t r[32];
-                    tmem_ld32(taddr + ch * 32, r);
+                if (C::kStagedCombine && g.epi == EPI_COMBINE) combine_rows(er, lane, orow);
+                if constexpr (kChunks == 1) {
+                    uint32_t r0[32];
+                    tmem_ld32(taddr + ch0 * 32, r0);
                     tmem_wait_ld();
-                    if (C::kStagedCombine && g.epi == EPI_COMBINE)
-                        combine_staged(g, tl, er, ch * 32, r, stg_all + (warp - kEpi0) * 256, lane);
-                    else
-                        epilogue_chunk(g, tl, er, row, ch * 32, r);
+                    chunk(tl, er, ch0, r0);
+                }
+                // two chunks in flight per wait
+#pragma unroll 1
+                for (int cp = 0; kChunks > 1 && cp < kChunks; cp += 2) {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(taddr + (ch0 + cp) * 32, r0);
+                    tmem_ld32(taddr + (ch0 + cp + 1) * 32, r1);
+                    tmem_wait_ld();
+                    if (rcp_of && (ch0 + cp + 2) * 32 <= tl.cols) {
+                        hquant_pair(g, tl, er, row, (ch0 + cp) * 32, r0, r1, rcp_of);
+                    } else {
+                        chunk(tl, er, ch0 + cp, r0);
+                        chunk(tl, er, ch0 + cp + 1, r1);
+                    }
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
+            tl = tn;
+            er = en;
         }
     }
     tc_fence_before();

@@ -29,7 +29,8 @@ using namespace lmoe;
 
 namespace {
 
-constexpr int kStagesF4 = 5;
+constexpr int kStagesF4 = 6;          // NVFP4 prefill, latent-up: 36 KB per stage
+constexpr int kStagesF4Stg = 5;       // NVFP4 prefill, latent-down: + 16 KB of combine staging
 constexpr int kStagesBF16 = 6;
 constexpr int kStagesF4Small = 4;     // decode (T <= 32): 4 KB A boxes, 2 column blocks per stage
 constexpr int kStagesBF16Small = 5;
@@ -246,20 +247,20 @@ WsLayout layout(const lmoe_ctx *c, int64_t T) {
     return L;
 }
 
-template <int KIND, bool SMALLA, int KB, int STAGES, int BN = kBN>
+template <int KIND, bool SMALLA, int KB, int STAGES, int BN = kBN, bool STG = false>
 cudaError_t set_smem_attr() {
-    static_assert(gemm_smem_bytes<KIND, SMALLA, KB, BN>(STAGES) <= 232448, "shared memory budget");
-    return cudaFuncSetAttribute(gemm_kernel<KIND, SMALLA, KB, STAGES, BN>,
+    static_assert(gemm_smem_bytes<KIND, SMALLA, KB, BN, STG>(STAGES) <= 232448, "shared memory budget");
+    return cudaFuncSetAttribute(gemm_kernel<KIND, SMALLA, KB, STAGES, BN, STG>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                gemm_smem_bytes<KIND, SMALLA, KB, BN>(STAGES));
+                                gemm_smem_bytes<KIND, SMALLA, KB, BN, STG>(STAGES));
 }
 
-template <int KIND, bool SMALLA, int KB, int STAGES, int BN = kBN>
+template <int KIND, bool SMALLA, int KB, int STAGES, int BN = kBN, bool STG = false>
 cudaError_t launch_gemm_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int grid,
                             cudaStream_t s) {
-    return launch_pdl(gemm_kernel<KIND, SMALLA, KB, STAGES, BN>, dim3(grid),
-                      dim3(GemmCfg<KIND, SMALLA, KB, BN>::kThreads), gemm_smem_bytes<KIND, SMALLA, KB, BN>(STAGES),
-                      s, ta, tb, g);
+    return launch_pdl(gemm_kernel<KIND, SMALLA, KB, STAGES, BN, STG>, dim3(grid),
+                      dim3(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads),
+                      gemm_smem_bytes<KIND, SMALLA, KB, BN, STG>(STAGES), s, ta, tb, g);
 }
 
 // small_a: every tile has at most 32 valid A rows (T <= 32); such launches use two column
@@ -269,7 +270,8 @@ cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const Gemm
                         bool small_a, cudaStream_t s) {
     if (KIND == kKindNvf4)
         return small_a ? launch_gemm_cfg<kKindNvf4, true, 2, kStagesF4Small>(ta, tb, g, grid, s)
-                       : launch_gemm_cfg<kKindNvf4, false, 1, kStagesF4>(ta, tb, g, grid, s);
+               : g.epi == EPI_COMBINE ? launch_gemm_cfg<kKindNvf4, false, 1, kStagesF4Stg, kBN, true>(ta, tb, g, grid, s)
+                                      : launch_gemm_cfg<kKindNvf4, false, 1, kStagesF4>(ta, tb, g, grid, s);
     if (KIND == kKindFp8)
         return small_a ? launch_gemm_cfg<kKindFp8, true, 2, kStagesF8Small>(ta, tb, g, grid, s)
                        : launch_gemm_cfg<kKindFp8, false, 1, kStagesWide, kBNWide>(ta, tb, g, grid, s);
@@ -564,6 +566,7 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
         static cudaError_t attr_err = cudaSuccess;
         std::call_once(once, [] {
             cudaError_t a = set_smem_attr<kKindNvf4, false, 1, kStagesF4>();
+            if (a == cudaSuccess) a = set_smem_attr<kKindNvf4, false, 1, kStagesF4Stg, kBN, true>();
             cudaError_t b = set_smem_attr<kKindBf16, false, 1, kStagesBF16>();
             if (a == cudaSuccess) a = set_smem_attr<kKindNvf4, true, 2, kStagesF4Small>();
             if (b == cudaSuccess) b = set_smem_attr<kKindBf16, true, 2, kStagesBF16Small>();

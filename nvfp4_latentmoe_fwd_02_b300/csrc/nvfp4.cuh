@@ -82,6 +82,34 @@ __device__ __forceinline__ uint32_t quant_block16(const float (&x)[16], const QS
     return sf;
 }
 
+// quant_block16 with the reciprocal looked up: rcp_of[sf] holds the rcp that quant_block16
+// derives from the scale byte sf (the same fp32 operations, done once per byte value), so the
+// codes are identical.  The block maximum is taken as a tree (max is exact in any order).
+__device__ __forceinline__ uint32_t quant_block16_lut(const float (&x)[16], const QScale &q,
+                                                      const float *rcp_of, uint32_t &lo, uint32_t &hi) {
+    if (q.zero) { lo = hi = 0u; return 0u; }
+    float m[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m[i] = fmaxf(fabsf(x[2 * i]), fabsf(x[2 * i + 1]));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], m[i + 4]);
+    const float amax_b = fmaxf(fmaxf(m[0], m[2]), fmaxf(m[1], m[3]));
+    const uint32_t sf = f32_to_e4m3_satfinite(__fmul_rn(amax_b, q.s_enc6));
+    const float rcp = rcp_of[sf];
+    uint32_t b[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) b[i] = f32x2_to_e2m1x2(__fmul_rn(x[2 * i], rcp), __fmul_rn(x[2 * i + 1], rcp));
+    lo = (b[0] | (b[1] << 8)) | ((b[2] << 16) | (b[3] << 24));
+    hi = (b[4] | (b[5] << 8)) | ((b[6] << 16) | (b[7] << 24));
+    return sf;
+}
+// The table of quant_block16_lut for quantizer q (rcp_of[0..255]; all zero when q.zero).
+__device__ __forceinline__ float quant_rcp_entry(const QScale &q, uint32_t sf) {
+    if (q.zero) return 0.0f;
+    const float bd = __fmul_rn(e4m3_to_f32(sf), q.s_dec);
+    return bd > 0.0f ? __frcp_rn(bd) : 0.0f;
+}
+
 // 16 codes of a block whose scale is already decided (rcp = 1 / (value(sf) * s_dec), or 0).
 __device__ __forceinline__ void block_codes16(const float (&x)[16], float rcp, uint32_t &lo, uint32_t &hi) {
     uint32_t w[2] = {0u, 0u};
