@@ -71,6 +71,8 @@ struct GemmArgs {
     const uint8_t *sfa;          // activation scale atoms [rows/128][K/64][512]
     const uint8_t *sfb;          // weight scale atoms [E][NB][K/64][512]
     int NB;                      // ceil(N / 128)
+    int b_kt;                    // > 0: B (expert weight codes) in tile order with b_kt 128-byte
+                                 // column blocks per 128-row block (tiled_code_offset)
     int epi;
     void *out;                   // see EpiMode
     int64_t ld_out;
@@ -615,7 +617,10 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
                         const uint32_t r_st = smem_u32(sRaw) + stage * C::kRawStage;
                         for (int b = 0; b < nb; ++b) {
                             tma_load_2d_u32(a_st + b * C::kACol, &tmA, fb, (kb0 + b) * 64, tl.a_row0);
-                            tma_load_2d_u32(r_st + b * C::kRawBlock, &tmB, fb, (kb0 + b) * 32, tl.b_row0);
+                            // 32 code bytes of 64-element block kb0 + b: a quarter of a tiled box row
+                            const int kb = kb0 + b;
+                            tma_load_2d_u32(r_st + b * C::kRawBlock, &tmB, fb, (kb & 3) * 32,
+                                            ((tl.e * g.NB + (tl.n0 >> 7)) * g.b_kt + (kb >> 2)) * 128);
                             bulk_load_u32(r_st + b * C::kRawBlock + 4096, sfb_tile + (kb0 + b) * 512, 512, fb);
                         }
                         issued |= 1u << stage;
@@ -638,7 +643,11 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
                         const int kx = (kb0 + b) * C::kTmaXPerBlock;
                         const int kxa = g.a_kwrap > 0 ? kx % g.a_kwrap : kx;
                         tma_load_2d_u32(a_st + b * C::kACol, &tmA, fb, kxa, tl.a_row0);
-                        tma_load_2d_u32(b_st + b * (BN * 128), &tmB, fb, kx, tl.b_row0);
+                        if (NVF4)   // weight codes in tile order: box (expert, row block, column block)
+                            tma_load_2d_u32(b_st + b * (BN * 128), &tmB, fb, 0,
+                                            ((tl.e * g.NB + (tl.n0 >> 7)) * g.b_kt + kb0 + b) * 128);
+                        else
+                            tma_load_2d_u32(b_st + b * (BN * 128), &tmB, fb, kx, tl.b_row0);
                     }
                     issued |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);

@@ -610,8 +610,9 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
     CREATE_CUDA(cudaMalloc(&c->w_split, static_cast<size_t>(E) * 2 * d * 2));
     CREATE_CUDA(cudaMalloc(&c->w_rows, static_cast<size_t>(E) * d * 4));
     CREATE_CUDA(cudaMalloc(&c->wnorm, static_cast<size_t>(E) * 4));
-    CREATE_CUDA(cudaMalloc(&c->w1_codes, static_cast<size_t>(E) * ffn * l / 2));
-    CREATE_CUDA(cudaMalloc(&c->w2_codes, static_cast<size_t>(E) * l * ffn / 2));
+    const size_t w1_bytes = tiled_codes_bytes(E, ffn, l), w2_bytes = tiled_codes_bytes(E, l, ffn);
+    CREATE_CUDA(cudaMalloc(&c->w1_codes, w1_bytes));
+    CREATE_CUDA(cudaMalloc(&c->w2_codes, w2_bytes));
     CREATE_CUDA(cudaMalloc(&c->w1_sf, w1_sf_bytes));
     CREATE_CUDA(cudaMalloc(&c->w2_sf, w2_sf_bytes));
     CREATE_CUDA(cudaMalloc(&c->w1_sdec, E * 4));
@@ -645,16 +646,28 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
     amax_segments_kernel<<<dim3(16, E), 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->w2), seg2, c->amax_bits + E);
     CREATE_CUDA(cudaGetLastError());
     const int qgrid = c->num_sms * 16;
-    if (w->weight_blocks_2d) {
-        quantize_experts_2d_kernel<<<qgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->w1), E, ffn, l,
-                                                         c->amax_bits, c->w1_codes, c->w1_sf);
-        quantize_experts_2d_kernel<<<qgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->w2), E, l, ffn,
-                                                         c->amax_bits + E, c->w2_codes, c->w2_sf);
-    } else {
-        quantize_experts_kernel<<<qgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->w1), E, ffn, l,
-                                                      c->amax_bits, c->w1_codes, c->w1_sf);
-        quantize_experts_kernel<<<qgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->w2), E, l, ffn,
-                                                      c->amax_bits + E, c->w2_codes, c->w2_sf);
+    {
+        // quantize row-major into a scratch buffer, then lay the codes out in tile order
+        uint8_t *rowmajor = nullptr;
+        CREATE_CUDA(cudaMalloc(&rowmajor, static_cast<size_t>(E) * ffn * l / 2));
+        cudaError_t qe = cudaMemsetAsync(c->w1_codes, 0, w1_bytes, s);
+        if (qe == cudaSuccess) qe = cudaMemsetAsync(c->w2_codes, 0, w2_bytes, s);
+        for (int m = 0; m < 2 && qe == cudaSuccess; ++m) {
+            const int N = m == 0 ? ffn : l, K = m == 0 ? l : ffn;
+            const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(m == 0 ? w->w1 : w->w2);
+            unsigned *amax = c->amax_bits + m * E;
+            uint8_t *sf = m == 0 ? c->w1_sf : c->w2_sf;
+            if (w->weight_blocks_2d)
+                quantize_experts_2d_kernel<<<qgrid, 256, 0, s>>>(src, E, N, K, amax, rowmajor, sf);
+            else
+                quantize_experts_kernel<<<qgrid, 256, 0, s>>>(src, E, N, K, amax, rowmajor, sf);
+            tile_codes_kernel<<<qgrid, 256, 0, s>>>(rowmajor, E, N, K, m == 0 ? c->w1_codes : c->w2_codes);
+            qe = cudaGetLastError();
+        }
+        if (qe == cudaSuccess) qe = cudaStreamSynchronize(s);
+        const cudaError_t fe = cudaFree(rowmajor);
+        CREATE_CUDA(qe);
+        CREATE_CUDA(fe);
     }
     tensor_scale_kernel<<<cdiv(E, 256), 256, 0, s>>>(c->amax_bits, E, c->w1_sdec);
     tensor_scale_kernel<<<cdiv(E, 256), 256, 0, s>>>(c->amax_bits + E, E, c->w2_sdec);
@@ -730,15 +743,17 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
             !make_map(&c->tm_ws2_w, false, c->ws2_codes, FS, d, FS, kBNWide))
             return fail(LMOE_ECUDA);
     }
-    bool ok = make_map_raw(&c->tm_w1raw, c->w1_codes, l / 2, static_cast<uint64_t>(E) * ffn) &&
-              make_map_raw(&c->tm_w2raw, c->w2_codes, ffn / 2, static_cast<uint64_t>(E) * l) &&
+    // expert codes in tile order: rows of 128 bytes, one 128-row box per (expert, row block, column block)
+    const uint64_t w1_rows = w1_bytes / 128, w2_rows = w2_bytes / 128;
+    bool ok = make_map_raw(&c->tm_w1raw, c->w1_codes, 128, w1_rows) &&
+              make_map_raw(&c->tm_w2raw, c->w2_codes, 128, w2_rows) &&
               make_map(&c->tm_wsplit, true, c->w_split, 2 * d, E, static_cast<uint64_t>(2 * d) * 2, kBNWide) &&
               make_map(&c->tm_wd_w, true, c->w_down, d, l, static_cast<uint64_t>(d) * 2, kBNWide) &&
               make_map(&c->tm_wu_w, true, c->w_up, l, d, static_cast<uint64_t>(l) * 2, kBNWide) &&
               make_map(&c->tm_wd, true, c->w_down, d, l, static_cast<uint64_t>(d) * 2) &&
               make_map(&c->tm_wu, true, c->w_up, l, d, static_cast<uint64_t>(l) * 2) &&
-              make_map(&c->tm_w1, false, c->w1_codes, l / 2, static_cast<uint64_t>(E) * ffn, l / 2) &&
-              make_map(&c->tm_w2, false, c->w2_codes, ffn / 2, static_cast<uint64_t>(E) * l, ffn / 2);
+              make_map(&c->tm_w1, false, c->w1_codes, 128, w1_rows, 128) &&
+              make_map(&c->tm_w2, false, c->w2_codes, 128, w2_rows, 128);
     if (!ok) return fail(LMOE_ECUDA);
 #undef CREATE_CUDA
     *out = c;
@@ -982,6 +997,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         g.n_tiles = static_cast<int>(cdiv(F, kBN));
         g.grouped = 1; g.E = E; g.mt_start = mt; g.seg_start = seg; g.counts = counts;
         g.sfb = c->w1_sf; g.NB = static_cast<int>(cdiv(F, 128));
+        g.b_kt = static_cast<int>(cdiv(l, 256));
         g.err = c->err;
         if (c->w4a16) {
             g.k_tiles = static_cast<int>(cdiv(l / 64, kb_for(small_a)));
@@ -1009,6 +1025,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         g.n_tiles = static_cast<int>(cdiv(l, kBN));
         g.grouped = 1; g.E = E; g.mt_start = mt; g.seg_start = seg; g.counts = counts;
         g.sfb = c->w2_sf; g.NB = static_cast<int>(cdiv(l, 128));
+        g.b_kt = static_cast<int>(cdiv(F, 256));
         g.epi = EPI_COMBINE; g.out = c_acc; g.ld_out = l;
         g.row_slot = row_slot; g.route_w = rw; g.topk = k; g.err = c->err;
         if (c->w4a16) {
@@ -1105,10 +1122,11 @@ lmoe_status lmoe_get_expert_nvfp4(const lmoe_ctx *c, int which, int e, uint8_t *
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int N = which == 1 ? c->ffn : c->l;
     const int K = which == 1 ? c->l : c->ffn;
-    const uint8_t *src = (which == 1 ? c->w1_codes : c->w2_codes) + static_cast<size_t>(e) * N * K / 2;
     const size_t NB = cdiv(N, 128);
     const uint8_t *atoms = (which == 1 ? c->w1_sf : c->w2_sf) + static_cast<size_t>(e) * NB * (K / 64) * 512;
-    LMOE_CUDA(cudaMemcpyAsync(codes, src, static_cast<size_t>(N) * K / 2, cudaMemcpyDeviceToDevice, s));
+    untile_codes_kernel<<<static_cast<unsigned>(cdiv(static_cast<int64_t>(N) * K / 16, 256)), 256, 0, s>>>(
+        which == 1 ? c->w1_codes : c->w2_codes, e, N, K, codes);
+    LMOE_LAUNCH();
     sf_atoms_to_rows_kernel<<<static_cast<unsigned>(cdiv(static_cast<int64_t>(N) * K / 16, 256)), 256, 0, s>>>(atoms, N, K, sf);
     LMOE_LAUNCH();
     LMOE_CUDA(cudaMemcpyAsync(s_dec, (which == 1 ? c->w1_sdec : c->w2_sdec) + e, 4, cudaMemcpyDeviceToHost, s));

@@ -323,6 +323,47 @@ __global__ void quantize_experts_2d_kernel(const __nv_bfloat16 *__restrict__ src
     }
 }
 
+// Expert weight codes in tile order: for expert e, 128-row block nb and 128-byte column block
+// kt, the 128 x 128-byte box that one TMA copy of the GEMMs moves is contiguous (16 KB), so
+// the weight stream reads whole 16 KB runs of HBM instead of 128-byte pieces 1 KB apart.
+// Byte (e, r, c) of the row-major [E][N][K/2] codes sits at
+//   (((e * NB + r / 128) * KT + c / 128) * 128 + r % 128) * 128 + c % 128,
+// NB = ceil(N / 128), KT = ceil(K / 256); bytes past N rows or K/2 columns stay 0.
+__host__ __device__ __forceinline__ int64_t tiled_code_offset(int64_t e, int64_t r, int64_t c, int64_t NB,
+                                                              int64_t KT) {
+    return (((e * NB + (r >> 7)) * KT + (c >> 7)) * 128 + (r & 127)) * 128 + (c & 127);
+}
+__host__ __device__ __forceinline__ size_t tiled_codes_bytes(int64_t E, int64_t N, int64_t K) {
+    return static_cast<size_t>(E * ((N + 127) / 128) * ((K + 255) / 256)) * 16384;
+}
+// row-major codes [E][N][K/2] -> tile order (8-byte pieces: one 16-element block each)
+__global__ void tile_codes_kernel(const uint8_t *__restrict__ src, int E, int N, int K,
+                                  uint8_t *__restrict__ dst) {
+    const int64_t NB = (N + 127) / 128, KT = (K + 255) / 256;
+    const int64_t pr = K / 16;                                   // 8-byte pieces per row
+    const int64_t total = static_cast<int64_t>(E) * N * pr;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = i / pr, p = i - row * pr;           // row over E * N
+        const int64_t e = row / N, r = row - e * N;
+        *reinterpret_cast<uint2 *>(dst + tiled_code_offset(e, r, 8 * p, NB, KT)) =
+            reinterpret_cast<const uint2 *>(src)[i];
+    }
+}
+// One expert's codes from tile order back to row-major [N][K/2].
+__global__ void untile_codes_kernel(const uint8_t *__restrict__ tiled, int e, int N, int K,
+                                    uint8_t *__restrict__ out) {
+    const int64_t NB = (N + 127) / 128, KT = (K + 255) / 256;
+    const int64_t pr = K / 16;
+    const int64_t total = static_cast<int64_t>(N) * pr;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / pr, p = i - r * pr;
+        reinterpret_cast<uint2 *>(out)[i] =
+            *reinterpret_cast<const uint2 *>(tiled + tiled_code_offset(e, r, 8 * p, NB, KT));
+    }
+}
+
 // Atom layout -> row-major [N][K/16] for one matrix (used to hand scales back to callers).
 __global__ void sf_atoms_to_rows_kernel(const uint8_t *__restrict__ atoms, int N, int K,
                                         uint8_t *__restrict__ out) {
