@@ -516,7 +516,8 @@ __device__ __forceinline__ void w4_convert_block(const uint8_t *raw, uint8_t *ds
 }
 
 // BN: tile width, 128 or (dense kinds without scale factors) 256: a 256-column tile moves
-// 48 KB of operands per 64-element K block for twice the outputs of a 128-column one.  (NVFP4
+// 48 KB of operands per 64-element K block for twice the outputs of a 128-column one.  64 for
+// the bf16 up-projection at decode: twice the CTAs stream the weights, with no split-K.  (NVFP4
 // stays at 128: two 256-column accumulators would fill TMEM and leave no room for the scale
 // factors, and one accumulator serialises each tile's epilogue with the next tile's MMAs.)
 // STG: the staged combine (grouped NVFP4 latent-down at prefill; 16 KB of smem).
@@ -525,7 +526,8 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmArgs g) {
     using C = GemmCfg<KIND, SMALLA, KB, BN, STG>;
-    static_assert(BN == 128 || (BN == 256 && (KIND == kKindBf16 || KIND == kKindFp8)), "tile width");
+    static_assert(BN == 128 || (BN == 256 && (KIND == kKindBf16 || KIND == kKindFp8)) ||
+                      (BN == 64 && KIND == kKindBf16 && SMALLA), "tile width");
     constexpr bool NVF4 = C::NVF4;
     constexpr bool W4 = C::W4;
     constexpr int kEpi0 = C::kEpi0;

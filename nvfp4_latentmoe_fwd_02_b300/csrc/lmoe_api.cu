@@ -38,6 +38,7 @@ constexpr int kStagesF8 = 6;          // FP8 stages have the BF16 byte layout
 constexpr int kStagesF8Small = 5;
 constexpr int kStagesWide = 4;        // bf16 / fp8 with 256-column tiles: 48 KB per stage
 constexpr int kBNWide = 256;
+constexpr int kBNNarrow = 64;         // bf16 GEMMs at decode whose 128-column tiles leave SMs idle
 constexpr int kStagesW4 = 5;          // W4A16: bf16 A + decoded bf16 B + raw E2M1 block per stage
 constexpr int kStagesW4Small = 4;
 constexpr int kSmallAMaxT = 32;
@@ -124,6 +125,7 @@ struct WsLayout {
     int64_t R;   // row capacity of the permuted buffers (multiple of 128)
     bool small_router, split_down, split_up;
     int down_splits, up_splits;
+    int up_bn;                         // tile width of the up-projection
 };
 
 }  // namespace
@@ -146,6 +148,7 @@ struct lmoe_ctx {
     QScale qz, qh;
     CUtensorMap tm_wd, tm_wu, tm_w1, tm_w2;
     CUtensorMap tm_wd_w, tm_wu_w;     // 256-row boxes for the wide (256-column) tiles
+    CUtensorMap tm_wu_n;              // 64-row boxes: the up-projection's narrow tiles at decode
     int w4a16;                        // experts in W4A16 form (bf16 z, h; weights decoded in smem)
     CUtensorMap tm_w1raw, tm_w2raw;   // unswizzled code maps for the W4A16 decoders
     // shared expert (FP8 E4M3, per-tensor scales); shared_ffn == 0: none
@@ -198,6 +201,14 @@ int plan_splits(int m_tiles, int n_tiles, int k_tiles, int num_sms, int fill = 2
     return static_cast<int>(cdiv(k_tiles, per));
 }
 
+// Tile width of the up-projection: 64 at decode when 128-column tiles would leave more than a
+// quarter of the SMs idle and 64-column ones still fit in one wave; else the dense default.
+int up_bn(int64_t T, int64_t d, int num_sms) {
+    if (T > kSmallAMaxT) return bn_for(false);
+    const int64_t t128 = cdiv(d, kBN), t64 = cdiv(d, kBNNarrow);
+    return (4 * t128 < 3 * num_sms && t64 <= num_sms) ? kBNNarrow : kBN;
+}
+
 WsLayout layout(const lmoe_ctx *c, int64_t T) {
     WsLayout L;
     std::memset(&L, 0, sizeof(L));
@@ -209,7 +220,8 @@ WsLayout layout(const lmoe_ctx *c, int64_t T) {
     const int kb = kb_for(T <= kSmallAMaxT);
     const int bn = bn_for(T <= kSmallAMaxT);
     L.down_splits = plan_splits(mt, static_cast<int>(cdiv(l, bn)), static_cast<int>(cdiv(d / 64, kb)), c->num_sms);
-    L.up_splits = plan_splits(mt, static_cast<int>(cdiv(d, bn)), static_cast<int>(cdiv(l / 64, kb)), c->num_sms, 4);
+    L.up_bn = up_bn(T, d, c->num_sms);
+    L.up_splits = plan_splits(mt, static_cast<int>(cdiv(d, L.up_bn)), static_cast<int>(cdiv(l / 64, kb)), c->num_sms, 4);
     L.split_down = L.down_splits > 1;
     L.split_up = L.up_splits > 1;
     size_t off = 0;
@@ -278,6 +290,8 @@ cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const Gemm
     if (KIND == kKindW4A16)
         return small_a ? launch_gemm_cfg<kKindW4A16, true, 2, kStagesW4Small>(ta, tb, g, grid, s)
                        : launch_gemm_cfg<kKindW4A16, false, 1, kStagesW4>(ta, tb, g, grid, s);
+    if (small_a && g.bn == kBNNarrow)
+        return launch_gemm_cfg<kKindBf16, true, 2, kStagesBF16Small, kBNNarrow>(ta, tb, g, grid, s);
     return small_a ? launch_gemm_cfg<kKindBf16, true, 2, kStagesBF16Small>(ta, tb, g, grid, s)
                    : launch_gemm_cfg<kKindBf16, false, 1, kStagesWide, kBNWide>(ta, tb, g, grid, s);
 }
@@ -573,6 +587,7 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
             if (a == cudaSuccess) a = set_smem_attr<kKindFp8, false, 1, kStagesF8>();
             if (a == cudaSuccess) a = set_smem_attr<kKindW4A16, false, 1, kStagesW4>();
             if (a == cudaSuccess) a = set_smem_attr<kKindBf16, false, 1, kStagesWide, kBNWide>();
+            if (a == cudaSuccess) a = set_smem_attr<kKindBf16, true, 2, kStagesBF16Small, kBNNarrow>();
             if (a == cudaSuccess) a = set_smem_attr<kKindFp8, false, 1, kStagesWide, kBNWide>();
             if (a == cudaSuccess) a = set_smem_attr<kKindW4A16, true, 2, kStagesW4Small>();
             if (a == cudaSuccess) a = set_smem_attr<kKindFp8, true, 2, kStagesF8Small>();
@@ -752,6 +767,7 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
               make_map(&c->tm_wu_w, true, c->w_up, l, d, static_cast<uint64_t>(l) * 2, kBNWide) &&
               make_map(&c->tm_wd, true, c->w_down, d, l, static_cast<uint64_t>(d) * 2) &&
               make_map(&c->tm_wu, true, c->w_up, l, d, static_cast<uint64_t>(l) * 2) &&
+              make_map(&c->tm_wu_n, true, c->w_up, l, d, static_cast<uint64_t>(l) * 2, kBNNarrow) &&
               make_map(&c->tm_w1, false, c->w1_codes, 128, w1_rows, 128) &&
               make_map(&c->tm_w2, false, c->w2_codes, 128, w2_rows, 128);
     if (!ok) return fail(LMOE_ECUDA);
@@ -1078,11 +1094,12 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         CUtensorMap tc;
         if (!make_map(&tc, true, cb, l, T, static_cast<uint64_t>(l) * 2, a_box)) return LMOE_ECUDA;
         GemmArgs g = dense_args(static_cast<int>(T), d, l, L.up_splits,
-                                L.split_up ? EPI_RED_F32 : EPI_STORE_BF16, c->err, kb_for(small_a), 64, bn_for(small_a));
+                                L.split_up ? EPI_RED_F32 : EPI_STORE_BF16, c->err, kb_for(small_a), 64, L.up_bn);
         g.out = L.split_up ? static_cast<void *>(yacc) : y;
         g.ld_out = d;
         if (!L.split_up) g.addend = y_add;
-        LMOE_CUDA((launch_gemm<kKindBf16>(tc, small_a ? c->tm_wu : c->tm_wu_w, g,
+        const CUtensorMap &twu = !small_a ? c->tm_wu_w : (L.up_bn == kBNNarrow ? c->tm_wu_n : c->tm_wu);
+        LMOE_CUDA((launch_gemm<kKindBf16>(tc, twu, g,
                                                    grid_for(int64_t(g.m_tiles) * g.n_tiles * g.k_splits, c->num_sms), small_a, s)));
         prof_mark(c, "up_proj", s);
         if (L.split_up) {
