@@ -14,7 +14,8 @@
 // box hold stale data whose accumulator rows the epilogue never reads), 128 rows otherwise
 // (one TMA request instead of four: the request count, not the bytes, limited the loads).
 //
-// Warp roles (one CTA per SM; 384 threads, 256 for the grouped NVFP4 GEMMs at prefill):
+// Warp roles (one CTA per SM; 384 threads; 256 for the grouped NVFP4 GEMMs at prefill, 512 for
+// W4A16, whose warps 2..7 decode the weight tiles):
 //   warp 0      TMA producer (one elected lane): operand tiles + scale atoms -> smem ring
 //   warp 1      TMEM allocator and MMA issuer (one lane): tcgen05.mma into one of two
 //               128-column accumulators
