@@ -158,3 +158,32 @@ def test_ultra_drift_against_bf16_experts(ultra_uniform):
     assert r["routing_agreement"] == 1.0
     assert 0.05 < r["y_rel_l2_mean"] < 0.35 and r["y_rel_l2_max"] < 0.6
     assert r["ftz_rate_z"] < 0.15 and r["ftz_rate_h"] < 0.5
+
+
+@pytest.mark.parametrize("which,T", [("uniform", 8), ("zipf", 4096)])
+def test_ultra_timed_configuration(ultra_uniform, ultra_zipf, which, T):
+    """The benchmark times the layer with debug copies off; that forward (same kernels, no
+    intermediate copies) gives the oracle's routing on all sampled tokens and its outputs on
+    every sampled token whose zq equals the oracle's (a z on a rounding boundary can take the
+    neighbouring code, as in the stage-by-stage tests; such tokens must be rare)."""
+    case = ultra_uniform if which == "uniform" else ultra_zipf
+    moe = case.gpu(debug=True)
+    d = case.dims
+    x = case.tokens(T, seed_offset=5).cuda()
+    case.lm.lmoe_set_debug(moe.ctx, False)
+    try:
+        y = moe.forward(x)
+        moe.check()
+        idx = moe.stage("idx", T, torch.int32).view(T, d.k).cpu().numpy()
+        counts = moe.stage("counts", T, torch.int32).cpu().numpy()
+        zc = moe.stage("zq_codes", T).view(T, d.l // 2).cpu().numpy()
+        zs = moe.stage("zq_sf", T).view(T, d.l // 16).cpu().numpy()
+    finally:
+        case.lm.lmoe_set_debug(moe.ctx, True)
+    assert np.array_equal(counts, np.bincount(idx.ravel(), minlength=d.E))
+    sample = np.arange(T) if T <= 8 else np.array([0, 1, 777, 2048, 3001, T - 1])
+    ref = case.ol.forward(x[sample].float().cpu().numpy(), quant=True, want=("zq_codes", "zq_sf", "y"))
+    assert np.array_equal(idx[sample], ref["idx"])
+    same_zq = np.all(zc[sample] == ref["zq_codes"], axis=1) & np.all(zs[sample] == ref["zq_sf"], axis=1)
+    assert same_zq.sum() >= len(sample) - 1
+    assert rel_l2_rows(y[sample].float().cpu().numpy()[same_zq], ref["y"][same_zq]).max() <= TOL_OUT
