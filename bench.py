@@ -55,6 +55,9 @@ def args_():
     p.add_argument("--prefill-steps", type=int, default=20)
     p.add_argument("--only-prefill", action="store_true",
                    help="profiling aid: build and run only the prefill workload, print its line")
+    p.add_argument("--sweep", action="store_true",
+                   help="the full-block sweep instead (Ultra + FP8 shared expert, T x routing "
+                        "skew): one JSON line per point")
     p.add_argument("--only-long", action="store_true",
                    help="profiling aid: build and run only the long-prompt workload, print its line")
     return p.parse_args()
@@ -456,6 +459,70 @@ def long_entry(a, dist, pk):
     }
 
 
+def sweep(a, dist, pk):
+    """The full Ultra block with its FP8 shared expert over every T x routing skew of the sweep
+    (lmoe_synth.sweep_points): one weight draw, one context per skew, the long-prompt layer's
+    static scales.  Per point: tokens/s and two roofline fractions,
+      experts: max(touched expert bytes / HBM, expert FLOPs / NVFP4 peak) / expert-stage time,
+      layer:   max(algorithmic bytes / HBM, sum over precisions of FLOPs / peak) / step time,
+    peaks: measured HBM copy, measured bf16 x the nominal dense ratios (nvfp4 6, fp8 2)."""
+    import nvfp4_latentmoe_fwd_02_b300 as lm
+    base = lmoe_synth.CONFIGS[lmoe_synth.SWEEP_BASE]
+    dims, seed = base["dims"], base["seed"]
+    cal = calibration(lmoe_synth.SWEEP_BASE)
+    L = lmoe_synth.layer(dims, seed, "cuda", 0.0)
+    moes = {}
+    for s in lmoe_synth.SWEEP_SKEW:
+        _, b = lmoe_synth.router(dims, seed, "cuda", s)
+        moes[s] = lm.LatentMoE(dims.d, dims.l, dims.E, dims.k, dims.ffn, L.w_down, L.w_up,
+                               L.w_router, b, L.w1, L.w2, cal["amax_z"], cal["amax_h"],
+                               ws1=L.ws1, ws2=L.ws2, amax_xs=cal["amax_xs"], amax_hs=cal["amax_hs"])
+    torch.cuda.synchronize()
+    del L
+    torch.cuda.empty_cache()
+    bw = pk["hbm_gbs"] * 1e9
+    p_bf16 = pk["bf16_tflops"] * 1e12
+    d, l, E, F, FS = dims.d, dims.l, dims.E, dims.ffn, dims.shared_ffn
+    w_e = l * F // 2 + l * F // 16 + 4                  # one expert matrix: codes, scales, fp32
+    for p in lmoe_synth.sweep_points():
+        T, moe = p["T"], moes[p["zipf"]]
+        r = Runner(moe, T, p["seed"], pool=1)
+        K = 5 if T <= 4096 else 3
+        with Clocks(torch.cuda.current_device()) as clk:
+            ms = r.timed_steps(K, 3)
+        tot = dist.max(sum(ms))
+        prof = dict(r.profile(reps=1))
+        eb = expert_bytes(moe, T)
+        t_exp = (prof.get("expert_up", 0.0) + prof.get("expert_down", 0.0)) * 1e-3
+        fl_e = 4 * l * F * eb["slots"]
+        roof_e = max(2 * eb["touched"] * w_e / bw, fl_e / (6 * p_bf16))
+        bytes_layer = layer_bytes(moe, T, eb) + 2 * d * FS       # + the shared expert's FP8 weights
+        t_comp = fl_e / (6 * p_bf16) + (4 * T * d * l + 2 * T * d * E) / p_bf16 + 4 * T * d * FS / (2 * p_bf16)
+        roof_l = max(bytes_layer / bw, t_comp)
+        step = tot / K * 1e-3
+        if dist.rank == 0:
+            print(json.dumps({
+                "sweep_point": p["i"], "T": T, "routing": "uniform" if p["zipf"] == 0 else f"zipf{p['zipf']}",
+                "seed": p["seed"], "steps": K, "ms_per_step": tot / K,
+                "tokens_per_s": T * K * dist.world / (tot * 1e-3),
+                "touched_experts": eb["touched"], "slots": eb["slots"],
+                "expert_stage_ms": t_exp * 1e3,
+                "roofline_experts": {"time_ms": roof_e * 1e3, "frac": roof_e / t_exp if t_exp else None,
+                                     "bound": "hbm" if 2 * eb["touched"] * w_e / bw >= fl_e / (6 * p_bf16) else "nvfp4"},
+                "roofline_layer": {"time_ms": roof_l * 1e3, "frac": roof_l / step,
+                                   "bound": "hbm" if bytes_layer / bw >= t_comp else "compute"},
+                "per_kernel_ms": {n: round(v, 4) for n, v in prof.items()},
+                "clocks": clk.summary(),
+                "config": {"workload": f"LatentMoE forward + FP8 shared expert, T={T}, d={d}, l={l}, "
+                                       f"E={E}, top-{dims.k}, ffn={F}, shared ffn={FS}",
+                           "l2": "flushed before every step", "graph": "one CUDA graph replay per step"},
+            }), flush=True)
+        del r
+        torch.cuda.empty_cache()
+    for m in moes.values():
+        m.close()
+
+
 def main():
     a = args_()
     dist = Dist("nccl")
@@ -465,6 +532,10 @@ def main():
         return
     import nvfp4_latentmoe_fwd_02_b300 as lm
     pk = peaks()
+    if a.sweep:
+        sweep(a, dist, pk)
+        dist.close()
+        return
     if a.only_prefill:
         L, moes = build_layers([PREFILL])
         pc = lmoe_synth.CONFIGS[PREFILL]

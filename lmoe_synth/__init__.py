@@ -158,3 +158,20 @@ CONFIGS = {
     "ultra_long_T32768_shared": dict(dims=ULTRA_SHARED, seed=1, zipf=0.0, T=32768, calib_T=8,
                                      gen="cuda"),
 }
+
+# The full-block sweep (Ultra dims with the FP8 shared expert): every T against every routing
+# skew.  Point i (T-major order) draws its tokens with seed 100 + i; all points share the
+# weights of "ultra_long_T32768_shared" (seed 1, drawn on the GPU) and its static activation
+# scales; the router bias of a point is that seed's Zipf(s) bias (s = 0: none).
+SWEEP_T = (1, 8, 64, 512, 4096, 16384, 65536)
+SWEEP_SKEW = (0.0, 1.1, 2.0)
+SWEEP_BASE = "ultra_long_T32768_shared"
+
+
+def sweep_points():
+    """[{"i", "T", "zipf", "seed"}] in T-major order."""
+    pts = []
+    for T in SWEEP_T:
+        for s in SWEEP_SKEW:
+            pts.append(dict(i=len(pts), T=T, zipf=s, seed=100 + len(pts)))
+    return pts

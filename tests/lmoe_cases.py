@@ -49,7 +49,10 @@ class Case:
     """A layer (dims, seed, routing skew) with its calibration, on the GPU and in the oracle."""
 
     def __init__(self, dims: lmoe_synth.Dims, seed: int, zipf: float = 0.0, calib_T: int = 64,
-                 gen_device: str = "cpu", weight_blocks_2d: bool = False, w4a16: bool = False):
+                 gen_device: str = "cpu", weight_blocks_2d: bool = False, w4a16: bool = False,
+                 calib=None):
+        """calib: stored static scales (amax_z, amax_h, amax_xs, amax_hs) instead of the
+        oracle's calibration pass."""
         import nvfp4_latentmoe_fwd_02_b300 as lm
         self.lm = lm
         self.dims, self.seed, self.zipf = dims, seed, zipf
@@ -70,9 +73,14 @@ class Case:
                                      host["w_up"], host["w_router"], host["b_router"],
                                      self._expert_master, shared=shared,
                                      weight_blocks_2d=weight_blocks_2d)
-        xc = lmoe_synth.calibration_tokens(calib_T, dims.d, seed, gen_device).float().cpu().numpy()
-        self.amax_z, self.amax_h = self.ol.calibrate(xc)
-        self.amax_xs, self.amax_hs = self.ol.calibrate_shared(xc) if shared else (0.0, 0.0)
+        if calib is not None:
+            self.amax_z, self.amax_h, self.amax_xs, self.amax_hs = (float(v) for v in calib)
+            self.ol.amax_z, self.ol.amax_h = self.amax_z, self.amax_h
+            self.ol.amax_xs, self.ol.amax_hs = self.amax_xs, self.amax_hs
+        else:
+            xc = lmoe_synth.calibration_tokens(calib_T, dims.d, seed, gen_device).float().cpu().numpy()
+            self.amax_z, self.amax_h = self.ol.calibrate(xc)
+            self.amax_xs, self.amax_hs = self.ol.calibrate_shared(xc) if shared else (0.0, 0.0)
         self.moe = None
 
     def _expert_master(self, e):
