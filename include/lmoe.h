@@ -184,7 +184,12 @@ lmoe_status lmoe_forward(lmoe_ctx *ctx, const void *x, int64_t T, void *y, void 
 size_t lmoe_host_workspace_size(const lmoe_ctx *ctx, int64_t T);
 
 /* The forward from and to HOST memory: copies x_host (bf16 [T][d], pinned for best speed) to
- * the device, runs lmoe_forward, copies y back to y_host and synchronizes `stream`. */
+ * the device, runs lmoe_forward, copies y back to y_host and synchronizes `stream`.  On a
+ * created (non-default) stream the three steps are captured as one CUDA graph, kept in the
+ * context and replayed by later calls with the same T, x_host, y_host, ws, ws_bytes, stream
+ * and debug flag (the host buffers' contents are read and written at each replay); any other
+ * call captures anew.  If the capture is refused (e.g. pageable host memory) the steps run
+ * directly.  The legacy and per-thread default streams, and profiling mode, run directly. */
 lmoe_status lmoe_forward_host(lmoe_ctx *ctx, const void *x_host, int64_t T, void *y_host,
                               void *ws, size_t ws_bytes, lmoe_stream stream);
 

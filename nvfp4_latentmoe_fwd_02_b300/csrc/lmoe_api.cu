@@ -164,6 +164,15 @@ struct lmoe_ctx {
     // second stream: the split-K down-projection runs beside the router (fork / join events)
     cudaStream_t aux;
     cudaEvent_t ev_fork, ev_join;
+    // lmoe_forward_host: its copy-in, forward and copy-out as one CUDA graph, replayed while a
+    // call's arguments (and the debug flag) equal those it was captured with
+    cudaGraphExec_t host_exec;
+    int64_t host_T;
+    const void *host_x;
+    void *host_y, *host_ws;
+    size_t host_ws_bytes;
+    cudaStream_t host_stream;
+    int host_debug;
     // per-kernel timing (lmoe_set_profile)
     int profile;
     int nprof;
@@ -790,6 +799,7 @@ void lmoe_destroy(lmoe_ctx *c) {
     if (c->ev_fork) cudaEventDestroy(c->ev_fork);
     if (c->ev_join) cudaEventDestroy(c->ev_join);
     if (c->aux) cudaStreamDestroy(c->aux);
+    if (c->host_exec) cudaGraphExecDestroy(c->host_exec);
     delete c;
 }
 
@@ -1124,12 +1134,53 @@ lmoe_status lmoe_forward_host(lmoe_ctx *c, const void *x_host, int64_t T, void *
     uint8_t *W = static_cast<uint8_t *>(ws);
     void *xd = W + main, *yd = W + main + io;
     const size_t bytes = static_cast<size_t>(T) * c->d * 2;
-    LMOE_CUDA(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s));
-    lmoe_status st = lmoe_forward(c, xd, T, yd, ws, main, stream);
-    if (st != LMOE_OK) return st;
-    LMOE_CUDA(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s));
-    LMOE_CUDA(cudaStreamSynchronize(s));
-    return LMOE_OK;
+    auto direct = [&]() -> lmoe_status {
+        LMOE_CUDA(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s));
+        lmoe_status st = lmoe_forward(c, xd, T, yd, ws, main, stream);
+        if (st != LMOE_OK) return st;
+        LMOE_CUDA(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s));
+        LMOE_CUDA(cudaStreamSynchronize(s));
+        return LMOE_OK;
+    };
+    // the legacy / per-thread default streams cannot be captured; profiling times each kernel
+    const bool graphable = s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread && !c->profile;
+    if (!graphable) return direct();
+    if (c->host_exec && c->host_T == T && c->host_x == x_host && c->host_y == y_host && c->host_ws == ws &&
+        c->host_ws_bytes == ws_bytes && c->host_stream == s && c->host_debug == c->debug) {
+        LMOE_CUDA(cudaGraphLaunch(c->host_exec, s));
+        LMOE_CUDA(cudaStreamSynchronize(s));
+        return LMOE_OK;
+    }
+    // capture copy-in + forward + copy-out; if the capture cannot be made (e.g. pageable host
+    // memory), run the same work directly
+    cudaGraph_t graph = nullptr;
+    if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        cudaGetLastError();
+        return direct();
+    }
+    cudaError_t e = cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s);
+    lmoe_status st = e == cudaSuccess ? lmoe_forward(c, xd, T, yd, ws, main, stream) : LMOE_ECUDA;
+    if (st == LMOE_OK) e = cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s);
+    const cudaError_t ec = cudaStreamEndCapture(s, &graph);
+    if (st == LMOE_EINVAL || st == LMOE_ENOMEM) {        // argument errors: nothing ran
+        if (graph) cudaGraphDestroy(graph);
+        return st;
+    }
+    cudaGraphExec_t exec = nullptr;
+    if (st == LMOE_OK && e == cudaSuccess && ec == cudaSuccess && graph &&
+        cudaGraphInstantiate(&exec, graph, 0) == cudaSuccess) {
+        cudaGraphDestroy(graph);
+        if (c->host_exec) cudaGraphExecDestroy(c->host_exec);
+        c->host_exec = exec;
+        c->host_T = T; c->host_x = x_host; c->host_y = y_host; c->host_ws = ws;
+        c->host_ws_bytes = ws_bytes; c->host_stream = s; c->host_debug = c->debug;
+        LMOE_CUDA(cudaGraphLaunch(c->host_exec, s));
+        LMOE_CUDA(cudaStreamSynchronize(s));
+        return LMOE_OK;
+    }
+    if (graph) cudaGraphDestroy(graph);
+    cudaGetLastError();                                    // the failed capture's error
+    return direct();
 }
 
 lmoe_status lmoe_get_expert_nvfp4(const lmoe_ctx *c, int which, int e, uint8_t *codes, uint8_t *sf,

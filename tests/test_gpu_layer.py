@@ -130,6 +130,24 @@ def test_forward_host_matches_device(tiny):
     lm.lmoe_forward_host(moe.ctx, xh, T, yh, ws, nb)
     # combine uses fp32 atomics; results agree to the last bf16 place almost everywhere
     assert rel_l2_rows(yh.float().numpy(), y_dev.float().numpy()).max() <= 1e-2
+    # on a created stream: the first call captures a graph, the next ones replay it; a replay
+    # reads the current contents of x_host
+    st = torch.cuda.Stream()
+    x2 = tiny.tokens(T, seed_offset=78)
+    y2_dev = moe.forward(x2.cuda()).cpu()
+    for _ in range(3):
+        yh.zero_()
+        lm.lmoe_forward_host(moe.ctx, xh, T, yh, ws, nb, st)
+        assert rel_l2_rows(yh.float().numpy(), y_dev.float().numpy()).max() <= 1e-2
+    xh.copy_(x2)
+    lm.lmoe_forward_host(moe.ctx, xh, T, yh, ws, nb, st)
+    assert rel_l2_rows(yh.float().numpy(), y2_dev.float().numpy()).max() <= 1e-2
+    # another T captures anew
+    T3 = 5
+    xh3 = x2[:T3].contiguous().pin_memory()
+    yh3 = torch.empty_like(xh3).pin_memory()
+    lm.lmoe_forward_host(moe.ctx, xh3, T3, yh3, ws, nb, st)
+    assert rel_l2_rows(yh3.float().numpy(), y2_dev[:T3].float().numpy()).max() <= 1e-2
 
 
 def test_routing_is_deterministic_across_calls(tiny):
