@@ -343,6 +343,10 @@ double oracle_fp8_dot(const uint8_t *a, const uint8_t *b, int64_t K) {
 /* the bias.  Selection: logit descending, lower expert index first on ties.  Weights:    */
 /* softmax over the k selected logits (fp64).                                             */
 /* ------------------------------------------------------------------------------------ */
+/* The same source is compiled twice: for CPUs with the FMA instruction set fmaf becomes one  */
+/* inline fused multiply-add instead of a libm call (the operation is exactly specified, so  */
+/* both clones return the same bits; the loader picks the clone the host supports).          */
+__attribute__((target_clones("fma", "default")))
 static float canonical_logit(const float *x, const float *w, int d) {
     float acc = 0.0f;
     for (int g = 0; g < d; g += 16 * 64) {
