@@ -291,7 +291,11 @@ class Runner:
 
 
 def expert_bytes(moe, T):
-    """Algorithmic bytes of the two expert GEMM launches of the last forward (device counts)."""
+    """Algorithmic bytes of the two expert GEMM launches of the last forward (device counts):
+    the touched experts' weights only (codes, block scales, FP32 tensor scale of one matrix per
+    expert).  The activations these launches read and write (zq, hq, the fp32 combine
+    accumulator) are intermediates of the layer, which the algorithmic bytes exclude; they are
+    reported beside it as `with_activations`."""
     d = moe
     counts = moe.stage("counts", T, torch.int32).cpu()
     touched = int((counts > 0).sum())
@@ -302,8 +306,9 @@ def expert_bytes(moe, T):
     act_out_up = slots * (F // 2 + F // 16)
     act_in_dn = slots * (F // 2 + F // 16)
     out_dn = T * l * 4                               # fp32 combine accumulator (read-modify-write once)
-    return {"expert_up": touched * w_bytes + act_in_up + act_out_up,
-            "expert_down": touched * w_bytes + act_in_dn + out_dn,
+    return {"expert_up": touched * w_bytes, "expert_down": touched * w_bytes,
+            "with_activations": {"expert_up": touched * w_bytes + act_in_up + act_out_up,
+                                 "expert_down": touched * w_bytes + act_in_dn + out_dn},
             "touched": touched, "slots": slots}
 
 
@@ -413,8 +418,9 @@ def roofline_entry(prof, moe, T, pk):
     achieved = eb[dom] / (ms * 1e-3) / 1e9
     return {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": pk["hbm_gbs"],
             "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": ncu_traffic(f"{dom}_T{T}"),
-            "algorithmic_bytes": eb[dom], "launch_ms": ms,
-            "peak_src": f"{pk['src']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"}, eb
+            "algorithmic_bytes": eb[dom], "bytes_counted": "touched expert weights (intermediates excluded)",
+            "frac_with_activations": eb["with_activations"][dom] / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "launch_ms": ms, "peak_src": f"{pk['src']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"}, eb
 
 
 def long_entry(a, dist, pk):

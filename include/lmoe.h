@@ -25,7 +25,20 @@
  *  - Calls return a status and never abort, exit or throw.  Argument errors are detected on
  *    the host before anything is launched.  Launched work is asynchronous on `stream`;
  *    device-side errors (a bounded wait that ran out) latch into the context's error word and
- *    are reported by lmoe_check() and by the next call on that context.
+ *    are reported (and cleared) by the calls that synchronize: lmoe_check() and
+ *    lmoe_forward_host().  The asynchronous calls (lmoe_route, lmoe_route_static,
+ *    lmoe_forward) never read device memory, so they cannot report them.
+ *  - Every wait inside a kernel is bounded.  The GEMM pipeline waits give up after the
+ *    context's wait limit (lmoe_set_wait_limit; default about 1 s of SM clock), record
+ *    LMOE_ETIMEOUT, drain the kernel's outstanding copies and tensor-core work (with the
+ *    default bound) and return; the forward's outputs are then undefined, the context stays
+ *    usable and the next forward is unaffected.
+ *  - Fault injection for tests of the error paths (read from the environment by each call):
+ *    LMOE_FAULT=alloc:N makes the call's N-th device allocation fail (LMOE_ENOMEM, nothing
+ *    leaked); LMOE_FAULT=launch:N makes the call's N-th kernel launch fail before it launches
+ *    (LMOE_ECUDA); LMOE_FAULT=wait makes lmoe_forward's latent-up GEMM wait on a barrier that
+ *    nothing arrives at, so the wait runs out and lmoe_check() returns LMOE_ETIMEOUT.
+ *    LMOE_WAIT_LIMIT_CYCLES=n (read by lmoe_create) sets the new context's wait limit.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).
  *  - The caller owns every buffer it passes; the context owns the quantized weights.
  *  - A context must not run two forwards at once on overlapping workspaces.
@@ -140,7 +153,8 @@ lmoe_status lmoe_quantize_fp8(const void *src, lmoe_dtype dt, int64_t n, float a
  * logit within a certified margin, and the canonical logits of the candidates the margin
  * leaves undecided are computed exactly; w is then the softmax of the selected logits as known
  * (canonical where computed, tensor-core otherwise: within about 1e-5 relative).  Uses context-owned scratch
- * (grown with cudaMallocAsync on first use for a larger T).  T >= 0. */
+ * (grown with cudaMallocAsync on first use for a larger T).  T >= 0; x and counts 16-byte
+ * aligned (LMOE_EINVAL otherwise, before anything is launched). */
 lmoe_status lmoe_route(lmoe_ctx *ctx, const void *x, int64_t T, int32_t *idx, float *w,
                        int32_t *counts, lmoe_stream stream);
 
@@ -157,7 +171,10 @@ lmoe_status lmoe_route(lmoe_ctx *ctx, const void *x, int64_t T, int32_t *idx, fl
  *     T <= 8192); a larger T returns LMOE_EINVAL before anything is launched.
  *   - The first call on a device looks up the array's device address (once per device, with
  *     that device current; the context's device must be current).  Make that first call before
- *     any CUDA stream capture.
+ *     any CUDA stream capture.  The address is cached with the device's current CUDA context;
+ *     after a device reset (or a released and re-created primary context) the first call in
+ *     the new context looks it up again, so that call too must come before any capture.
+ *   - x and counts must be 16-byte aligned (LMOE_EINVAL otherwise, before anything launches).
  *   - Every call on a device shares the one array, and it keeps the last call's contents.  The
  *     scratch is fully written before it is read, and `counts` is zeroed by the call, so no
  *     earlier contents leak into a result; but two calls whose kernels overlap on the GPU (on
@@ -186,10 +203,14 @@ size_t lmoe_host_workspace_size(const lmoe_ctx *ctx, int64_t T);
 /* The forward from and to HOST memory: copies x_host (bf16 [T][d], pinned for best speed) to
  * the device, runs lmoe_forward, copies y back to y_host and synchronizes `stream`.  On a
  * created (non-default) stream the three steps are captured as one CUDA graph, kept in the
- * context and replayed by later calls with the same T, x_host, y_host, ws, ws_bytes, stream
- * and debug flag (the host buffers' contents are read and written at each replay); any other
- * call captures anew.  If the capture is refused (e.g. pageable host memory) the steps run
- * directly.  The legacy and per-thread default streams, and profiling mode, run directly. */
+ * context and replayed by later calls with the same T, x_host, y_host, ws, ws_bytes, stream,
+ * debug flag and wait limit (the host buffers' contents are read and written at each
+ * replay); any other call captures anew.  A call with LMOE_FAULT set runs the steps directly
+ * and keeps the cached graph.  If the capture is refused (e.g. pageable host memory) the steps run
+ * directly.  The legacy and per-thread default streams, and profiling mode, run directly.
+ * The call synchronizes `stream`, so a stream that is being captured is refused with
+ * LMOE_EINVAL before anything is enqueued.  After the synchronize it reads the context's
+ * error word: a device-side error of this forward returns LMOE_ETIMEOUT / LMOE_EDEVICE. */
 lmoe_status lmoe_forward_host(lmoe_ctx *ctx, const void *x_host, int64_t T, void *y_host,
                               void *ws, size_t ws_bytes, lmoe_stream stream);
 
@@ -221,6 +242,13 @@ lmoe_status lmoe_workspace_range(const lmoe_ctx *ctx, int64_t T, int stage, size
 /* Debug mode (0/1): when on, lmoe_forward also writes z and h (bf16) into its workspace,
  * which then needs lmoe_workspace_size() bytes computed after this call. */
 lmoe_status lmoe_set_debug(lmoe_ctx *ctx, int on);
+
+/* Wait limit of the GEMM pipeline waits, in SM clock cycles (cycles <= 0: the default, about
+ * 1 s at the maximum SM clock).  A wait that runs out makes its kernel record LMOE_ETIMEOUT in
+ * the context's error word and return early (see the conventions at the top).  The waits that
+ * drain a kernel's in-flight copies and tensor-core work before it exits keep the default
+ * bound.  Applies to the forwards launched after the call. */
+lmoe_status lmoe_set_wait_limit(lmoe_ctx *ctx, long long cycles);
 
 /* Copy expert e's quantized matrix (which = 1: W1 [ffn][l], which = 2: W2 [l][ffn]) out of the
  * context in the canonical layout: codes device uint8 [N][K/2], sf device uint8 [N][K/16]

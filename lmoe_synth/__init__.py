@@ -146,16 +146,17 @@ def calibration_tokens(T: int, d: int, seed: int, device="cpu") -> torch.Tensor:
     return tokens(T, d, seed + 1, device, tag="x_cal")
 
 
-# Named workloads.  "gen" is the device whose torch generator draws the inputs (Ultra-size
+# Named workloads.  calib_T: size of the calibration batch (1024 tokens drawn with seed + 1)
+# whose activation amax fixes the static scales.  "gen" is the device whose torch generator draws the inputs (Ultra-size
 # weights are drawn on the GPU, so their values are reproducible on the same GPU model).
 CONFIGS = {
-    "tiny": dict(dims=TINY, seed=0, zipf=0.0, T=64, calib_T=64, gen="cpu"),
-    "ultra_decode_T8": dict(dims=ULTRA, seed=1, zipf=0.0, T=8, calib_T=8, gen="cuda"),
-    "ultra_prefill_T4096_zipf1.1": dict(dims=ULTRA, seed=1, zipf=1.1, T=4096, calib_T=8,
+    "tiny": dict(dims=TINY, seed=0, zipf=0.0, T=64, calib_T=1024, gen="cpu"),
+    "ultra_decode_T8": dict(dims=ULTRA, seed=1, zipf=0.0, T=8, calib_T=1024, gen="cuda"),
+    "ultra_prefill_T4096_zipf1.1": dict(dims=ULTRA, seed=1, zipf=1.1, T=4096, calib_T=1024,
                                         gen="cuda"),
     # with the FP8 shared expert at width d
-    "tiny_shared": dict(dims=TINY_SHARED, seed=0, zipf=0.0, T=64, calib_T=64, gen="cpu"),
-    "ultra_long_T32768_shared": dict(dims=ULTRA_SHARED, seed=1, zipf=0.0, T=32768, calib_T=8,
+    "tiny_shared": dict(dims=TINY_SHARED, seed=0, zipf=0.0, T=64, calib_T=1024, gen="cpu"),
+    "ultra_long_T32768_shared": dict(dims=ULTRA_SHARED, seed=1, zipf=0.0, T=32768, calib_T=1024,
                                      gen="cuda"),
 }
 

@@ -72,6 +72,7 @@ def lib() -> C.CDLL:
         "lmoe_forward_host": (C.c_int, [vp, vp, i64, vp, vp, sz, vp]),
         "lmoe_workspace_range": (C.c_int, [vp, i64, C.c_int, C.POINTER(sz), C.POINTER(sz)]),
         "lmoe_set_debug": (C.c_int, [vp, C.c_int]),
+        "lmoe_set_wait_limit": (C.c_int, [vp, C.c_longlong]),
         "lmoe_get_expert_nvfp4": (C.c_int, [vp, C.c_int, C.c_int, vp, vp, C.POINTER(C.c_float), vp]),
         "lmoe_check": (C.c_int, [vp, vp]),
         "lmoe_forward_kernel_count": (C.c_int, [vp, i64]),
@@ -218,6 +219,10 @@ def lmoe_workspace_range(ctx, T, stage) -> tuple[int, int]:
 
 def lmoe_set_debug(ctx, on: bool):
     _check(lib().lmoe_set_debug(ctx, 1 if on else 0), "lmoe_set_debug")
+
+
+def lmoe_set_wait_limit(ctx, cycles: int):
+    _check(lib().lmoe_set_wait_limit(ctx, int(cycles)), "lmoe_set_wait_limit")
 
 
 def lmoe_get_expert_nvfp4(ctx, which, e, codes, sf, stream=None) -> float:

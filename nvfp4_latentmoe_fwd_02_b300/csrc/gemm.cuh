@@ -99,6 +99,9 @@ struct GemmArgs {
     int bn;                      // tile width (output columns): the kernel's BN
     __nv_bfloat16 *a_bf16;       // W4A16 z epilogue: bf16 z rows copied into the expert segments [R][N]
     unsigned *err;
+    long long wait_limit;        // SM cycles a pipeline wait may take before the CTA gives up
+    int inject_wait;             // fault injection: the MMA role first waits on a barrier that
+                                 // nothing arrives at, so the wait runs out (LMOE_FAULT=wait)
 };
 
 struct Tile {
@@ -151,15 +154,17 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &g, const SmemTables 
     return tl;
 }
 
-// Wait that also gives up when another role of the CTA has aborted.
+// Pipeline wait: gives up after `limit` SM cycles (recording LMOE_ETIMEOUT and telling the
+// other roles to stop), or as soon as another role of the CTA has given up.
 __device__ __forceinline__ bool role_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          unsigned *err) {
+                                          unsigned *err, long long limit) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (limit <= 0) limit = kWaitLimitCycles;       // unset: the library's default bound
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > limit) {
             *abort = 1;
             raise_error(err, kErrTimeout);
             return false;
@@ -609,7 +614,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
                 const uint8_t *sfa_tile = NVF4 ? g.sfa + static_cast<size_t>(tl.a_row0 >> 7) * K64 * 512 : nullptr;
                 const uint8_t *sfb_tile = (NVF4 || W4) ? g.sfb + (static_cast<size_t>(tl.e) * g.NB + (tl.n0 >> 7)) * K64 * 512 : nullptr;
                 for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
-                    if (!role_wait(&empty[stage], phase ^ 1, s_abort, g.err)) break;
+                    if (!role_wait(&empty[stage], phase ^ 1, s_abort, g.err, g.wait_limit)) break;
                     const int kb0 = kt * KB;
                     uint64_t *fb = &full[stage];
                     const uint32_t a_st = sA0 + stage * C::kAStage, b_st = sB0 + stage * C::kBStage;
@@ -678,17 +683,21 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
+            // Injected fault: `drain` gets its only arrival from the commit after the tile
+            // loop, so this wait cannot succeed; it runs out after g.wait_limit cycles and
+            // takes the CTA down the timeout path.
+            if (g.inject_wait) role_wait(drain, 0, s_abort, g.err, g.wait_limit);
             for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x, ++it) {
                 const Tile tl = decode_tile(g, tb, t);
                 const int acc = it & 1;
                 const uint32_t aphase = (it >> 1) & 1;
-                if (!role_wait(&tempty[acc], aphase ^ 1, s_abort, g.err)) break;
+                if (!role_wait(&tempty[acc], aphase ^ 1, s_abort, g.err, g.wait_limit)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + acc * kAccCols;
                 bool ok = true;
                 for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
-                    if (!role_wait(&full[stage], phase, s_abort, g.err)) { ok = false; break; }
-                    if ((NVF4 || W4) && !role_wait(&sfready[stage], phase, s_abort, g.err)) { ok = false; break; }
+                    if (!role_wait(&full[stage], phase, s_abort, g.err, g.wait_limit)) { ok = false; break; }
+                    if ((NVF4 || W4) && !role_wait(&sfready[stage], phase, s_abort, g.err, g.wait_limit)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t ad = adesc0 + ((stage * C::kAStage) >> 4);
                     const uint64_t bd = bdesc0 + ((stage * C::kBStage) >> 4);
@@ -742,7 +751,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
             const Tile tl = decode_tile(g, tb, t);
             bool ok = true;
             for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
-                if (!role_wait(&full[stage], phase, s_abort, g.err)) { ok = false; break; }
+                if (!role_wait(&full[stage], phase, s_abort, g.err, g.wait_limit)) { ok = false; break; }
                 const int nb = min(KB, K64 - kt * KB);
                 for (int b = 0; b < nb; ++b)
                     w4_convert_block(sRaw + stage * C::kRawStage + b * C::kRawBlock,
@@ -766,7 +775,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
                 const Tile tl = decode_tile(g, tb, t);
                 bool ok = true;
                 for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
-                    if (!role_wait(&sffull[stage], phase, s_abort, g.err)) { ok = false; break; }
+                    if (!role_wait(&sffull[stage], phase, s_abort, g.err, g.wait_limit)) { ok = false; break; }
                     tc_fence_after();
                     const int nsteps = min(4 * KB, K64 - 4 * kt * KB);
                     const uint32_t sf_t = tmem + kSfCol0 + stage * C::kSfCols + col_off;
@@ -828,7 +837,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
             // waits for the accumulator before releasing it, which keeps the release phases
             // of all four warps in step.
             const bool live = quad * 32 < tl.rows;
-            if (!role_wait(&tfull[acc], aphase, s_abort, g.err)) break;
+            if (!role_wait(&tfull[acc], aphase, s_abort, g.err, g.wait_limit)) break;
             tc_fence_after();
             const uint32_t taddr = tmem + acc * kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
             if (live) {

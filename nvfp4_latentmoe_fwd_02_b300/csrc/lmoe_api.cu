@@ -12,6 +12,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -29,7 +30,11 @@ using namespace lmoe;
 
 namespace {
 
-constexpr int kStagesF4 = 6;          // NVFP4 prefill, latent-up: 36 KB per stage
+// NVFP4 prefill, latent-up: two 128-byte column blocks (72 KB) per stage, three stages.  The
+// same bytes in flight as six one-block stages, but half the barrier handshakes, MMA commits
+// and scale-copy commits per byte (T = 4096, Zipf 1.1: 424 -> 381 us).
+constexpr int kKbF4Up = 2;
+constexpr int kStagesF4 = 3;
 constexpr int kStagesF4Stg = 5;       // NVFP4 prefill, latent-down: + 16 KB of combine staging
 constexpr int kStagesBF16 = 6;
 constexpr int kStagesF4Small = 4;     // decode (T <= 32): 4 KB A boxes, 2 column blocks per stage
@@ -99,12 +104,63 @@ bool make_map_raw(CUtensorMap *m, const void *ptr, uint64_t inner_bytes, uint64_
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// ---------------------------------------------------------------------------------------
+// Host-side fault injection (for tests of the error paths; nothing here touches the GPU):
+// the environment variable LMOE_FAULT, read at the start of each create / route / forward
+// call, selects one failure for that call:
+//   alloc:N   the call's N-th device allocation fails as if the device were out of memory
+//   launch:N  the call's N-th kernel launch fails before anything is launched
+//   wait      the forward's latent-up GEMM makes one pipeline wait on a barrier nothing
+//             arrives at, so that wait runs out after the context's wait limit and the
+//             kernel takes its timeout path (LMOE_ETIMEOUT from lmoe_check)
+// ---------------------------------------------------------------------------------------
+enum FaultKind { kFaultNone = 0, kFaultAlloc = 1, kFaultLaunch = 2, kFaultWait = 3 };
+struct Fault {
+    int kind = kFaultNone;
+    int n = 0;
+};
+Fault read_fault() {
+    Fault f;
+    const char *e = std::getenv("LMOE_FAULT");
+    if (!e) return f;
+    if (std::strncmp(e, "alloc:", 6) == 0) { f.kind = kFaultAlloc; f.n = std::atoi(e + 6); }
+    else if (std::strncmp(e, "launch:", 7) == 0) { f.kind = kFaultLaunch; f.n = std::atoi(e + 7); }
+    else if (std::strcmp(e, "wait") == 0) f.kind = kFaultWait;
+    if ((f.kind == kFaultAlloc || f.kind == kFaultLaunch) && f.n <= 0) f.kind = kFaultNone;
+    return f;
+}
+// Launches left before the injected launch failure in this thread's current call (0: none).
+thread_local int t_launch_fault = 0;
+// Allocations left before the injected allocation failure in this thread's current call.
+thread_local int t_alloc_fault = 0;
+inline bool injected_launch_failure() { return t_launch_fault > 0 && --t_launch_fault == 0; }
+// Arms the call's injected failures from LMOE_FAULT and disarms them when the call returns.
+struct FaultScope {
+    Fault f;
+    FaultScope() : f(read_fault()) {
+        t_launch_fault = f.kind == kFaultLaunch ? f.n : 0;
+        t_alloc_fault = f.kind == kFaultAlloc ? f.n : 0;
+    }
+    ~FaultScope() { t_launch_fault = 0; t_alloc_fault = 0; }
+};
+// cudaMalloc / cudaMallocAsync with the injected allocation failure.
+template <typename T>
+cudaError_t dev_malloc(T **p, size_t bytes) {
+    if (t_alloc_fault > 0 && --t_alloc_fault == 0) return cudaErrorMemoryAllocation;
+    return cudaMalloc(reinterpret_cast<void **>(p), bytes);
+}
+cudaError_t dev_malloc_async(void **p, size_t bytes, cudaStream_t s) {
+    if (t_alloc_fault > 0 && --t_alloc_fault == 0) return cudaErrorMemoryAllocation;
+    return cudaMallocAsync(p, bytes, s);
+}
+
 // Launch with programmatic stream serialization: the kernel's CTAs may be scheduled while the
 // previous kernel on the stream drains; each kernel of this library calls pdl_wait() before
 // its first global access (see common.cuh), so results are the same as a plain launch.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                        Args &&...args) {
+    if (injected_launch_failure()) return cudaErrorLaunchFailure;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -158,6 +214,7 @@ struct lmoe_ctx {
     float alpha_s1, alpha_s2, s_enc_hs;
     CUtensorMap tm_ws1, tm_ws2, tm_ws1_w, tm_ws2_w;
     unsigned *err;
+    long long wait_limit;             // SM cycles a GEMM pipeline wait may take (<= 0: default)
     int debug;
     void *route_ws;
     size_t route_ws_bytes;
@@ -173,6 +230,7 @@ struct lmoe_ctx {
     size_t host_ws_bytes;
     cudaStream_t host_stream;
     int host_debug;
+    long long host_wait_limit;
     // per-kernel timing (lmoe_set_profile)
     int profile;
     int nprof;
@@ -292,7 +350,7 @@ cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const Gemm
     if (KIND == kKindNvf4)
         return small_a ? launch_gemm_cfg<kKindNvf4, true, 2, kStagesF4Small>(ta, tb, g, grid, s)
                : g.epi == EPI_COMBINE ? launch_gemm_cfg<kKindNvf4, false, 1, kStagesF4Stg, kBN, true>(ta, tb, g, grid, s)
-                                      : launch_gemm_cfg<kKindNvf4, false, 1, kStagesF4>(ta, tb, g, grid, s);
+                                      : launch_gemm_cfg<kKindNvf4, false, kKbF4Up, kStagesF4>(ta, tb, g, grid, s);
     if (KIND == kKindFp8)
         return small_a ? launch_gemm_cfg<kKindFp8, true, 2, kStagesF8Small>(ta, tb, g, grid, s)
                        : launch_gemm_cfg<kKindFp8, false, 1, kStagesWide, kBNWide>(ta, tb, g, grid, s);
@@ -306,7 +364,7 @@ cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const Gemm
 }
 
 // K elements per 128-byte column block: 64 (bf16) or 128 (fp8).
-GemmArgs dense_args(int M, int N, int K, int splits, int epi, unsigned *err, int kb, int k_block = 64,
+GemmArgs dense_args(int M, int N, int K, int splits, int epi, const lmoe_ctx *c, int kb, int k_block = 64,
                     int bn = kBN) {
     GemmArgs g;
     std::memset(&g, 0, sizeof(g));
@@ -318,7 +376,8 @@ GemmArgs dense_args(int M, int N, int K, int splits, int epi, unsigned *err, int
     g.kt_per_split = static_cast<int>(cdiv(g.k_tiles, splits));
     g.k_splits = static_cast<int>(cdiv(g.k_tiles, g.kt_per_split));
     g.epi = epi;
-    g.err = err;
+    g.err = c->err;
+    g.wait_limit = c->wait_limit;
     return g;
 }
 
@@ -387,7 +446,7 @@ lmoe_status launch_router(lmoe_ctx *c, const __nv_bfloat16 *x, int64_t T, float 
     const int m_tiles = static_cast<int>(cdiv(T, kBM)), n_tiles = static_cast<int>(cdiv(E, kBNWide));
     const int k_tiles = 2 * d / 64;
     const int splits = std::min<int>(k_tiles, std::max<int>(8, static_cast<int>(cdiv(2 * c->num_sms, int64_t(m_tiles) * n_tiles))));
-    GemmArgs g = dense_args(static_cast<int>(T), E, 2 * d, splits, EPI_RED_F32, c->err, 1, 64, kBNWide);
+    GemmArgs g = dense_args(static_cast<int>(T), E, 2 * d, splits, EPI_RED_F32, c, 1, 64, kBNWide);
     g.out = scratch;
     g.ld_out = E;
     g.a_kwrap = d;
@@ -441,15 +500,40 @@ __device__ __align__(256) unsigned char g_route_static_scratch[LMOE_ROUTE_STATIC
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mu;
 void *g_static_ptr[kMaxDevices] = {};
+CUcontext g_static_ctx[kMaxDevices] = {};   // the context each cached address belongs to
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+CtxGetCurrentFn ctx_get_current_fn() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    return fn;
+}
+
+// The device address of the fixed scratch on device `dev` (current).  Looked up once per device
+// and context: a device reset (or a released and re-created primary context) reloads the
+// library's module at a possibly different address, so a cached address is only reused while
+// the current context is the one it was looked up in.
 lmoe_status route_static_scratch(int dev, void **out) {
     if (dev < 0 || dev >= kMaxDevices) return LMOE_EUNSUPPORTED;
+    CtxGetCurrentFn get = ctx_get_current_fn();
+    if (!get) return LMOE_ECUDA;
+    CUcontext cur = nullptr;
+    if (get(&cur) != CUDA_SUCCESS || !cur) return LMOE_ECUDA;
     std::lock_guard<std::mutex> lock(g_static_mu);
-    if (!g_static_ptr[dev]) {
+    if (!g_static_ptr[dev] || g_static_ctx[dev] != cur) {
         void *p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_route_static_scratch);
         if (e != cudaSuccess || !p) return e != cudaSuccess ? cuda_status(e) : LMOE_ECUDA;
         g_static_ptr[dev] = p;
+        g_static_ctx[dev] = cur;
     }
     *out = g_static_ptr[dev];
     return LMOE_OK;
@@ -588,7 +672,7 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
         static std::once_flag once;
         static cudaError_t attr_err = cudaSuccess;
         std::call_once(once, [] {
-            cudaError_t a = set_smem_attr<kKindNvf4, false, 1, kStagesF4>();
+            cudaError_t a = set_smem_attr<kKindNvf4, false, kKbF4Up, kStagesF4>();
             if (a == cudaSuccess) a = set_smem_attr<kKindNvf4, false, 1, kStagesF4Stg, kBN, true>();
             cudaError_t b = set_smem_attr<kKindBf16, false, 1, kStagesBF16>();
             if (a == cudaSuccess) a = set_smem_attr<kKindNvf4, true, 2, kStagesF4Small>();
@@ -607,9 +691,11 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
         if (attr_err != cudaSuccess) return cuda_status(attr_err);
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    FaultScope fault_scope;
     lmoe_ctx *c = new (std::nothrow) lmoe_ctx;
     if (!c) return LMOE_ENOMEM;
     std::memset(c, 0, sizeof(*c));
+    if (const char *wl = std::getenv("LMOE_WAIT_LIMIT_CYCLES")) c->wait_limit = std::atoll(wl);
     c->d = d; c->l = l; c->E = E; c->k = k; c->ffn = ffn;
     c->dev = dev;
     c->num_sms = prop.multiProcessorCount;
@@ -627,24 +713,24 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
     const size_t NB1 = cdiv(ffn, 128), NB2 = cdiv(l, 128);
     const size_t w1_sf_bytes = static_cast<size_t>(E) * NB1 * (l / 64) * 512;
     const size_t w2_sf_bytes = static_cast<size_t>(E) * NB2 * (ffn / 64) * 512;
-    CREATE_CUDA(cudaMalloc(&c->w_down, static_cast<size_t>(l) * d * 2));
-    CREATE_CUDA(cudaMalloc(&c->w_up, static_cast<size_t>(d) * l * 2));
-    CREATE_CUDA(cudaMalloc(&c->w_router, static_cast<size_t>(E) * d * 4));
-    CREATE_CUDA(cudaMalloc(&c->b_router, static_cast<size_t>(E) * 4));
-    CREATE_CUDA(cudaMalloc(&c->w_split, static_cast<size_t>(E) * 2 * d * 2));
-    CREATE_CUDA(cudaMalloc(&c->w_rows, static_cast<size_t>(E) * d * 4));
-    CREATE_CUDA(cudaMalloc(&c->wnorm, static_cast<size_t>(E) * 4));
+    CREATE_CUDA(dev_malloc(&c->w_down, static_cast<size_t>(l) * d * 2));
+    CREATE_CUDA(dev_malloc(&c->w_up, static_cast<size_t>(d) * l * 2));
+    CREATE_CUDA(dev_malloc(&c->w_router, static_cast<size_t>(E) * d * 4));
+    CREATE_CUDA(dev_malloc(&c->b_router, static_cast<size_t>(E) * 4));
+    CREATE_CUDA(dev_malloc(&c->w_split, static_cast<size_t>(E) * 2 * d * 2));
+    CREATE_CUDA(dev_malloc(&c->w_rows, static_cast<size_t>(E) * d * 4));
+    CREATE_CUDA(dev_malloc(&c->wnorm, static_cast<size_t>(E) * 4));
     const size_t w1_bytes = tiled_codes_bytes(E, ffn, l), w2_bytes = tiled_codes_bytes(E, l, ffn);
-    CREATE_CUDA(cudaMalloc(&c->w1_codes, w1_bytes));
-    CREATE_CUDA(cudaMalloc(&c->w2_codes, w2_bytes));
-    CREATE_CUDA(cudaMalloc(&c->w1_sf, w1_sf_bytes));
-    CREATE_CUDA(cudaMalloc(&c->w2_sf, w2_sf_bytes));
-    CREATE_CUDA(cudaMalloc(&c->w1_sdec, E * 4));
-    CREATE_CUDA(cudaMalloc(&c->w2_sdec, E * 4));
-    CREATE_CUDA(cudaMalloc(&c->alpha1, E * 4));
-    CREATE_CUDA(cudaMalloc(&c->alpha2, E * 4));
-    CREATE_CUDA(cudaMalloc(&c->amax_bits, 2 * E * 4));
-    CREATE_CUDA(cudaMalloc(&c->err, sizeof(unsigned)));
+    CREATE_CUDA(dev_malloc(&c->w1_codes, w1_bytes));
+    CREATE_CUDA(dev_malloc(&c->w2_codes, w2_bytes));
+    CREATE_CUDA(dev_malloc(&c->w1_sf, w1_sf_bytes));
+    CREATE_CUDA(dev_malloc(&c->w2_sf, w2_sf_bytes));
+    CREATE_CUDA(dev_malloc(&c->w1_sdec, E * 4));
+    CREATE_CUDA(dev_malloc(&c->w2_sdec, E * 4));
+    CREATE_CUDA(dev_malloc(&c->alpha1, E * 4));
+    CREATE_CUDA(dev_malloc(&c->alpha2, E * 4));
+    CREATE_CUDA(dev_malloc(&c->amax_bits, 2 * E * 4));
+    CREATE_CUDA(dev_malloc(&c->err, sizeof(unsigned)));
     CREATE_CUDA(cudaStreamCreateWithFlags(&c->aux, cudaStreamNonBlocking));
     CREATE_CUDA(cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming));
     CREATE_CUDA(cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming));
@@ -673,7 +759,7 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
     {
         // quantize row-major into a scratch buffer, then lay the codes out in tile order
         uint8_t *rowmajor = nullptr;
-        CREATE_CUDA(cudaMalloc(&rowmajor, static_cast<size_t>(E) * ffn * l / 2));
+        CREATE_CUDA(dev_malloc(&rowmajor, static_cast<size_t>(E) * ffn * l / 2));
         cudaError_t qe = cudaMemsetAsync(c->w1_codes, 0, w1_bytes, s);
         if (qe == cudaSuccess) qe = cudaMemsetAsync(c->w2_codes, 0, w2_bytes, s);
         for (int m = 0; m < 2 && qe == cudaSuccess; ++m) {
@@ -735,8 +821,8 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
         c->shared_ffn = FS;
         c->amax_xs = w->amax_xs;
         c->amax_hs = w->amax_hs;
-        CREATE_CUDA(cudaMalloc(&c->ws1_codes, n));
-        CREATE_CUDA(cudaMalloc(&c->ws2_codes, n));
+        CREATE_CUDA(dev_malloc(&c->ws1_codes, n));
+        CREATE_CUDA(dev_malloc(&c->ws2_codes, n));
         unsigned *bits = c->amax_bits;   // reused: [0] ws1, [1] ws2 (the expert amax is done)
         CREATE_CUDA(cudaMemsetAsync(bits, 0, 2 * sizeof(unsigned), s));
         amax_segments_kernel<<<dim3(c->num_sms * 4, 1), 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w->ws1), n, bits);
@@ -808,7 +894,10 @@ lmoe_status lmoe_route_static(lmoe_ctx *c, const void *x, int64_t T, int32_t *id
     if (!c || T < 0) return LMOE_EINVAL;
     if (T == 0) return LMOE_OK;
     if (!x || !idx || !w) return LMOE_EINVAL;
+    if (reinterpret_cast<uintptr_t>(x) % 16 || (counts && reinterpret_cast<uintptr_t>(counts) % 16))
+        return LMOE_EINVAL;
     if (route_scratch_bytes(c, T) > LMOE_ROUTE_STATIC_SCRATCH_BYTES) return LMOE_EINVAL;
+    FaultScope fault_scope;
     int dev = -1;
     LMOE_CUDA(cudaGetDevice(&dev));
     if (dev != c->dev) return LMOE_EINVAL;
@@ -816,7 +905,6 @@ lmoe_status lmoe_route_static(lmoe_ctx *c, const void *x, int64_t T, int32_t *id
     const lmoe_status st = route_static_scratch(dev, &scratch);
     if (st != LMOE_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (counts && reinterpret_cast<uintptr_t>(counts) % 16) return LMOE_EINVAL;
     return launch_router(c, static_cast<const __nv_bfloat16 *>(x), T, static_cast<float *>(scratch),
                          idx, w, counts, nullptr, zero_counts(counts, c->E), s);
 }
@@ -868,21 +956,29 @@ lmoe_status lmoe_set_debug(lmoe_ctx *c, int on) {
     return LMOE_OK;
 }
 
+lmoe_status lmoe_set_wait_limit(lmoe_ctx *c, long long cycles) {
+    if (!c) return LMOE_EINVAL;
+    c->wait_limit = cycles > 0 ? cycles : 0;
+    return LMOE_OK;
+}
+
 lmoe_status lmoe_route(lmoe_ctx *c, const void *x, int64_t T, int32_t *idx, float *w,
                        int32_t *counts, lmoe_stream stream) {
     if (!c || T < 0) return LMOE_EINVAL;
     if (T == 0) return LMOE_OK;
     if (!x || !idx || !w) return LMOE_EINVAL;
+    if (reinterpret_cast<uintptr_t>(x) % 16 || (counts && reinterpret_cast<uintptr_t>(counts) % 16))
+        return LMOE_EINVAL;
+    FaultScope fault_scope;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const size_t need = route_scratch_bytes(c, T);
     if (need > c->route_ws_bytes) {
         if (c->route_ws) LMOE_CUDA(cudaFreeAsync(c->route_ws, s));
         c->route_ws = nullptr;
         c->route_ws_bytes = 0;
-        LMOE_CUDA(cudaMallocAsync(&c->route_ws, need, s));
+        LMOE_CUDA(dev_malloc_async(&c->route_ws, need, s));
         c->route_ws_bytes = need;
     }
-    if (counts && reinterpret_cast<uintptr_t>(counts) % 16) return LMOE_EINVAL;
     return launch_router(c, static_cast<const __nv_bfloat16 *>(x), T,
                          static_cast<float *>(c->route_ws), idx, w, counts, nullptr,
                          zero_counts(counts, c->E), s);
@@ -899,6 +995,8 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     if (reinterpret_cast<uintptr_t>(ws) % 256 || reinterpret_cast<uintptr_t>(x) % 16 ||
         reinterpret_cast<uintptr_t>(y) % 16)
         return LMOE_EINVAL;
+    FaultScope fault_scope;
+    const Fault &fault = fault_scope.f;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t *W = static_cast<uint8_t *>(ws);
     auto at = [&](size_t off) { return static_cast<void *>(W + off); };
@@ -943,7 +1041,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         CUtensorMap tx;
         if (!make_map(&tx, true, x, d, T, static_cast<uint64_t>(d) * 2, a_box)) return LMOE_ECUDA;
         GemmArgs g = dense_args(static_cast<int>(T), l, d, L.down_splits,
-                                L.split_down ? EPI_RED_F32 : EPI_Z_QUANT, c->err, kb_for(small_a), 64, bn_for(small_a));
+                                L.split_down ? EPI_RED_F32 : EPI_Z_QUANT, c, kb_for(small_a), 64, bn_for(small_a));
         if (L.split_down) {
             g.out = zacc; g.ld_out = l;
         } else {
@@ -1025,12 +1123,14 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         g.sfb = c->w1_sf; g.NB = static_cast<int>(cdiv(F, 128));
         g.b_kt = static_cast<int>(cdiv(l, 256));
         g.err = c->err;
+        g.wait_limit = c->wait_limit;
+        g.inject_wait = fault.kind == kFaultWait ? 1 : 0;
         if (c->w4a16) {
             g.k_tiles = static_cast<int>(cdiv(l / 64, kb_for(small_a)));
             g.epi = EPI_H_BF16; g.out = h_bf16; g.alpha = c->w1_sdec;
             LMOE_CUDA((launch_gemm<kKindW4A16>(ta, c->tm_w1raw, g, c->num_sms, small_a, s)));
         } else {
-            g.k_tiles = static_cast<int>(cdiv(l, 256 * kb_for(small_a)));
+            g.k_tiles = static_cast<int>(cdiv(l, 256 * (small_a ? kb_for(true) : kKbF4Up)));
             g.sfa = a_sf;
             g.epi = EPI_H_QUANT; g.q = c->qh; g.q_codes = h_codes; g.q_sf = h_sf; g.dbg = h_dbg;
             g.alpha = c->alpha1;
@@ -1054,6 +1154,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         g.b_kt = static_cast<int>(cdiv(F, 256));
         g.epi = EPI_COMBINE; g.out = c_acc; g.ld_out = l;
         g.row_slot = row_slot; g.route_w = rw; g.topk = k; g.err = c->err;
+        g.wait_limit = c->wait_limit;
         if (c->w4a16) {
             g.k_tiles = static_cast<int>(cdiv(F / 64, kb_for(small_a)));
             g.alpha = c->w2_sdec;
@@ -1085,13 +1186,13 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         CUtensorMap txs, ths;
         if (!make_map(&txs, false, xs_q, d, T, d, a_box) || !make_map(&ths, false, hs_q, FS, T, FS, a_box))
             return LMOE_ECUDA;
-        GemmArgs g1 = dense_args(static_cast<int>(T), FS, d, 1, EPI_FP8_SQRELU, c->err, kb_for(small_a), 128,
+        GemmArgs g1 = dense_args(static_cast<int>(T), FS, d, 1, EPI_FP8_SQRELU, c, kb_for(small_a), 128,
                                  bn_for(small_a));
         g1.alpha_s = c->alpha_s1; g1.s_enc8 = c->s_enc_hs; g1.q_codes = hs_q; g1.dbg = hs_dbg;
         LMOE_CUDA((launch_gemm<kKindFp8>(txs, small_a ? c->tm_ws1 : c->tm_ws1_w, g1, grid_for(int64_t(g1.m_tiles) * g1.n_tiles, c->num_sms),
                                          small_a, s)));
         prof_mark(c, "shared_up", s);
-        GemmArgs g2 = dense_args(static_cast<int>(T), d, FS, 1, EPI_STORE_SCALED, c->err, kb_for(small_a), 128,
+        GemmArgs g2 = dense_args(static_cast<int>(T), d, FS, 1, EPI_STORE_SCALED, c, kb_for(small_a), 128,
                                  bn_for(small_a));
         g2.alpha_s = c->alpha_s2; g2.out = s_out; g2.ld_out = d;
         LMOE_CUDA((launch_gemm<kKindFp8>(ths, small_a ? c->tm_ws2 : c->tm_ws2_w, g2, grid_for(int64_t(g2.m_tiles) * g2.n_tiles, c->num_sms),
@@ -1104,7 +1205,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         CUtensorMap tc;
         if (!make_map(&tc, true, cb, l, T, static_cast<uint64_t>(l) * 2, a_box)) return LMOE_ECUDA;
         GemmArgs g = dense_args(static_cast<int>(T), d, l, L.up_splits,
-                                L.split_up ? EPI_RED_F32 : EPI_STORE_BF16, c->err, kb_for(small_a), 64, L.up_bn);
+                                L.split_up ? EPI_RED_F32 : EPI_STORE_BF16, c, kb_for(small_a), 64, L.up_bn);
         g.out = L.split_up ? static_cast<void *>(yacc) : y;
         g.ld_out = d;
         if (!L.split_up) g.addend = y_add;
@@ -1134,22 +1235,29 @@ lmoe_status lmoe_forward_host(lmoe_ctx *c, const void *x_host, int64_t T, void *
     uint8_t *W = static_cast<uint8_t *>(ws);
     void *xd = W + main, *yd = W + main + io;
     const size_t bytes = static_cast<size_t>(T) * c->d * 2;
+    // The call synchronizes `stream`, which is not allowed while the stream is being captured.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    LMOE_CUDA(cudaStreamIsCapturing(s, &cap));
+    if (cap != cudaStreamCaptureStatusNone) return LMOE_EINVAL;
     auto direct = [&]() -> lmoe_status {
         LMOE_CUDA(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s));
         lmoe_status st = lmoe_forward(c, xd, T, yd, ws, main, stream);
         if (st != LMOE_OK) return st;
         LMOE_CUDA(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s));
         LMOE_CUDA(cudaStreamSynchronize(s));
-        return LMOE_OK;
+        return check_error_word(c);
     };
-    // the legacy / per-thread default streams cannot be captured; profiling times each kernel
-    const bool graphable = s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread && !c->profile;
+    // the legacy / per-thread default streams cannot be captured; profiling times each kernel;
+    // a call with an injected fault runs directly and leaves the cached graph alone
+    const bool graphable = s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread && !c->profile &&
+                           read_fault().kind == kFaultNone;
     if (!graphable) return direct();
     if (c->host_exec && c->host_T == T && c->host_x == x_host && c->host_y == y_host && c->host_ws == ws &&
-        c->host_ws_bytes == ws_bytes && c->host_stream == s && c->host_debug == c->debug) {
+        c->host_ws_bytes == ws_bytes && c->host_stream == s && c->host_debug == c->debug &&
+        c->host_wait_limit == c->wait_limit) {
         LMOE_CUDA(cudaGraphLaunch(c->host_exec, s));
         LMOE_CUDA(cudaStreamSynchronize(s));
-        return LMOE_OK;
+        return check_error_word(c);
     }
     // capture copy-in + forward + copy-out; if the capture cannot be made (e.g. pageable host
     // memory), run the same work directly
@@ -1174,9 +1282,10 @@ lmoe_status lmoe_forward_host(lmoe_ctx *c, const void *x_host, int64_t T, void *
         c->host_exec = exec;
         c->host_T = T; c->host_x = x_host; c->host_y = y_host; c->host_ws = ws;
         c->host_ws_bytes = ws_bytes; c->host_stream = s; c->host_debug = c->debug;
+        c->host_wait_limit = c->wait_limit;
         LMOE_CUDA(cudaGraphLaunch(c->host_exec, s));
         LMOE_CUDA(cudaStreamSynchronize(s));
-        return LMOE_OK;
+        return check_error_word(c);
     }
     if (graph) cudaGraphDestroy(graph);
     cudaGetLastError();                                    // the failed capture's error

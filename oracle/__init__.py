@@ -109,6 +109,9 @@ def lib():
             L.oracle_layer_forward.restype = C.c_int
             L.oracle_layer_forward.argtypes = [C.POINTER(_Layer), C.c_void_p, C.c_int64, C.c_int,
                                                C.POINTER(_Out), C.c_int]
+            L.oracle_layer_forward_zq.restype = C.c_int
+            L.oracle_layer_forward_zq.argtypes = [C.POINTER(_Layer), C.c_void_p, C.c_void_p,
+                                                  C.c_void_p, C.c_int64, C.POINTER(_Out), C.c_int]
             L.oracle_calibrate.restype = C.c_int
             L.oracle_calibrate.argtypes = [C.POINTER(_Layer), C.c_void_p, C.c_int64,
                                            C.POINTER(C.c_float), C.POINTER(C.c_float), C.c_int]
@@ -316,10 +319,14 @@ class OracleLayer:
         keep += [c1, s1, c2, s2, m1, m2, d1, d2]
         return st, keep
 
-    def forward(self, x, quant=True, want=("y",)):
+    def forward(self, x, quant=True, want=("y",), zq=None):
         """Run the layer on the token rows x [T][d]; returns a dict of requested outputs.
         quant: True (NVFP4 weights and activations), "w4a16" (NVFP4 weights, bf16 activations)
         or False (fp64 masters, no quantization).
+        zq: optional (codes [T][l/2], scales [T][l/16]) uint8: the NVFP4 layer's steps after the
+        quantization of z applied to this zq instead of the quantization of the oracle's own z
+        (a z from another fp32 accumulation order may sit one bf16 ulp away and quantize to
+        a neighbouring code; oracle_layer_forward_zq).
 
         Available: z, zq_codes, zq_sf, logits, idx, w, counts, h, hq_codes, hq_sf, c64, c,
         y64, y, and with a shared expert xs_q, hs, hs_q, s.  idx / w / counts are always
@@ -344,7 +351,14 @@ class OracleLayer:
         out = _Out(**{n: _p(res[n]) for n in names})
         mode = 2 if quant == "w4a16" else (1 if quant else 0)
         st, keep = self._struct(experts, mode != 0)
-        rc = lib().oracle_layer_forward(C.byref(st), _p(x), T, mode, C.byref(out), self.nthreads)
+        if zq is not None:
+            assert mode == 1
+            zc = np.ascontiguousarray(zq[0], dtype=np.uint8).reshape(T, l // 2)
+            zs = np.ascontiguousarray(zq[1], dtype=np.uint8).reshape(T, l // 16)
+            rc = lib().oracle_layer_forward_zq(C.byref(st), _p(x), _p(zc), _p(zs), T, C.byref(out),
+                                               self.nthreads)
+        else:
+            rc = lib().oracle_layer_forward(C.byref(st), _p(x), T, mode, C.byref(out), self.nthreads)
         if rc != 0:
             raise RuntimeError("oracle_layer_forward: missing expert weights")
         del keep

@@ -548,6 +548,9 @@ typedef struct {
     const oracle_layer *L; const float *x; int quant; oracle_out *out;
     float amax_z, amax_h;       /* used by the quantizers */
     float *amax_h_seen;         /* per-token max |h| (calibration), may be NULL */
+    /* optional (quant = 1): each token's zq ([T][l/2] codes, [T][l/16] scales) given instead */
+    /* of the quantization of this oracle's own z                                          */
+    const uint8_t *zq_codes_in, *zq_sf_in;
     volatile int error;
 } layer_job;
 
@@ -586,7 +589,12 @@ static void layer_rows(int64_t tb, int64_t te, void *arg) {
             zf[j] = (float)z64[j];
         }
         if (O->z) memcpy(O->z + t * l, zf, sizeof(float) * l);
-        if (J->quant == 1) {
+        if (J->quant == 1 && J->zq_codes_in) {
+            memcpy(zc, J->zq_codes_in + t * (l / 2), (size_t)l / 2);
+            memcpy(zs, J->zq_sf_in + t * (l / 16), (size_t)l / 16);
+            if (O->zq_codes) memcpy(O->zq_codes + t * (l / 2), zc, (size_t)l / 2);
+            if (O->zq_sf) memcpy(O->zq_sf + t * (l / 16), zs, (size_t)l / 16);
+        } else if (J->quant == 1) {
             float sd;
             oracle_quantize_nvfp4(zf, 1, l, J->amax_z, zc, zs, &sd, 1);
             if (O->zq_codes) memcpy(O->zq_codes + t * (l / 2), zc, (size_t)l / 2);
@@ -716,6 +724,29 @@ int oracle_layer_forward(const oracle_layer *L, const float *x, int64_t T, int q
                           out->counts, nthreads);
             free(idx);
         }
+    }
+    return J.error ? -1 : 0;
+}
+
+/* The NVFP4 layer (quant = 1) with each token's zq given: the steps after the quantization */
+/* of z (routing on x, the latent experts, the combine, the up-projection, the shared       */
+/* expert) applied to zq_codes [T][l/2] / zq_sf [T][l/16].  z = bf16(x Wd^T) is the bf16     */
+/* rounding of a sum whose fp32 accumulation order the method leaves open, so a z one bf16   */
+/* ulp away from this oracle's (its sum is exact) is as correct, and so is its              */
+/* quantization; this entry point gives the layer's output for such a zq.                    */
+int oracle_layer_forward_zq(const oracle_layer *L, const float *x, const uint8_t *zq_codes,
+                            const uint8_t *zq_sf, int64_t T, oracle_out *out, int nthreads) {
+    pthread_once(&g_once, init_tables);
+    if (!zq_codes || !zq_sf) return -1;
+    layer_job J;
+    memset(&J, 0, sizeof(J));
+    J.L = L; J.x = x; J.quant = 1; J.out = out;
+    J.amax_z = L->amax_z; J.amax_h = L->amax_h;
+    J.zq_codes_in = zq_codes; J.zq_sf_in = zq_sf;
+    parallel_for(T, nthreads, layer_rows, &J);
+    if (out->counts && out->idx) {
+        memset(out->counts, 0, sizeof(int32_t) * L->E);
+        for (int64_t i = 0; i < T * L->k; ++i) out->counts[out->idx[i]]++;
     }
     return J.error ? -1 : 0;
 }

@@ -142,6 +142,14 @@ typedef struct {               /* every pointer optional (NULL = not wanted)    
 int oracle_layer_forward(const oracle_layer *L, const float *x, int64_t T, int quant,
                          oracle_out *out, int nthreads);
 
+/* The NVFP4 layer (quant = 1) with each token's quantized z given (zq_codes [T][l/2],
+ * zq_sf [T][l/16]) instead of the quantization of the oracle's own z: routing, experts,
+ * combine, up-projection and shared expert are the steps above, applied to that zq.  For a z
+ * whose fp32 accumulation order differs (one bf16 ulp away), whose quantization is as correct.
+ * Returns 0, or -1 (missing expert weights / NULL zq). */
+int oracle_layer_forward_zq(const oracle_layer *L, const float *x, const uint8_t *zq_codes,
+                            const uint8_t *zq_sf, int64_t T, oracle_out *out, int nthreads);
+
 /* The shared expert alone on token rows x [T][d] (outputs as in oracle_out; each optional).
  * quant = 0: fp64 with the master weights, no quantization and no rounding. */
 int oracle_shared_forward(const oracle_layer *L, const float *x, int64_t T, int quant,

@@ -2,6 +2,9 @@
 library (through its C ABI binding) and to the CPU oracle."""
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -9,6 +12,19 @@ import lmoe_synth
 import oracle
 
 E4M3 = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def stored_calib(name):
+    """The stored static activation scales of a named workload (written by
+    tests/golden/make_calibration.py, which calls only the oracle): (amax_z, amax_h, amax_xs,
+    amax_hs), the last two 0 without a shared expert."""
+    with open(os.path.join(GOLDEN, "calibration.json")) as f:
+        c = json.load(f)[name]
+    assert c["calib_T"] == lmoe_synth.CONFIGS[name]["calib_T"], "stale calibration record"
+    return (c["amax_z"], c["amax_h"], c.get("amax_xs", 0.0), c.get("amax_hs", 0.0))
 
 
 def w_tol(T):
@@ -30,6 +46,58 @@ def real_rows(counts, nrows):
     return mask
 
 
+def check_routing_all_tokens(case, T, x, idx, counts, w=None):
+    """Expert indices and per-expert counts of every token against the oracle's router (exact),
+    routing weights within their tolerance."""
+    d = case.dims
+    _, oidx, ow, ocounts = case.ol.route(x.float().cpu().numpy())
+    bad = np.flatnonzero(np.any(idx != oidx, axis=1))
+    assert bad.size == 0, f"T={T}: {bad.size} tokens routed differently, first {bad[:8]}"
+    assert np.array_equal(counts, ocounts)
+    assert counts.sum() == T * d.k
+    if w is not None:
+        assert np.allclose(w, ow, **w_tol(T))
+
+
+def sample_tokens(T, n=256, seed=0):
+    """n sorted token indices including the first and the last (the ragged M tile)."""
+    if T <= n:
+        return np.arange(T)
+    s = np.sort(np.random.default_rng(seed).choice(np.arange(1, T - 1), n - 2, replace=False))
+    return np.concatenate([[0], s, [T - 1]])
+
+
+def check_outputs_all_tokens(case, x, zq_codes, zq_sf, outs, ref, tol=2e-2, max_moved=0.1):
+    """Every sampled token's float outputs at the layer's tolerance.  x: the sampled tokens
+    [n][d]; zq_codes / zq_sf: the GPU's quantized z of those tokens; outs: {name: GPU values
+    [n][...]} for names among c, y; ref: the oracle's forward of x with want >= outs, zq_codes,
+    zq_sf.  z is the bf16 rounding of a sum whose fp32 accumulation order the method leaves
+    open, so the GPU's z may sit one bf16 ulp from the oracle's at a quantization boundary and
+    its zq take a neighbouring code (or block scale); one E2M1 step of one element is up to a
+    third of its value, which moves c and y by a few percent.  Those tokens are checked against
+    the oracle's layer fed the GPU's zq (oracle_layer_forward_zq); they must be rare, and their
+    zq must differ from the oracle's in a few bytes only.  Returns (moved, worst error of a
+    moved token against the plain oracle) as a measurement."""
+    n = x.shape[0]
+    same = np.all(zq_codes == ref["zq_codes"], axis=1) & np.all(zq_sf == ref["zq_sf"], axis=1)
+    moved = np.flatnonzero(~same)
+    assert moved.size <= max(1, max_moved * n), f"{moved.size} of {n} tokens with another zq"
+    for name, got in outs.items():
+        err = rel_l2_rows(got[same], ref[name][same]) if same.any() else np.zeros(1)
+        assert err.max() <= tol, (name, float(err.max()))
+    worst = 0.0
+    if moved.size:
+        assert np.all((zq_codes[moved] != ref["zq_codes"][moved]).sum(axis=1) <= 16)
+        assert np.all((zq_sf[moved] != ref["zq_sf"][moved]).sum(axis=1) <= 2)
+        alt = case.ol.forward(np.asarray(x)[moved], quant=True, want=tuple(outs),
+                              zq=(zq_codes[moved], zq_sf[moved]))
+        for name, got in outs.items():
+            err = rel_l2_rows(got[moved], alt[name])
+            assert err.max() <= tol, (name, "zq-fed", float(err.max()))
+            worst = max(worst, float(rel_l2_rows(got[moved], ref[name][moved]).max()))
+    return moved.size, worst
+
+
 def rel_l2_rows(a, b):
     a = np.asarray(a, np.float64).reshape(a.shape[0], -1)
     b = np.asarray(b, np.float64).reshape(b.shape[0], -1)
@@ -48,7 +116,7 @@ def atoms_to_rows(atoms: np.ndarray, rows: int, K: int) -> np.ndarray:
 class Case:
     """A layer (dims, seed, routing skew) with its calibration, on the GPU and in the oracle."""
 
-    def __init__(self, dims: lmoe_synth.Dims, seed: int, zipf: float = 0.0, calib_T: int = 64,
+    def __init__(self, dims: lmoe_synth.Dims, seed: int, zipf: float = 0.0, calib_T: int = 1024,
                  gen_device: str = "cpu", weight_blocks_2d: bool = False, w4a16: bool = False,
                  calib=None):
         """calib: stored static scales (amax_z, amax_h, amax_xs, amax_hs) instead of the

@@ -9,7 +9,7 @@ import torch
 
 import lmoe_synth
 import oracle
-from lmoe_cases import Case, rel_l2_rows, w_tol
+from lmoe_cases import Case, rel_l2_rows, w_tol, check_outputs_all_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -72,7 +72,7 @@ def test_forward_2d_matches_oracle(tiny2d, T):
     x = tiny2d.tokens(T, seed_offset=500 + T)
     y = moe.forward(x.cuda())
     moe.check()
-    ref = tiny2d.ol.forward(x.float().numpy(), quant=True, want=("z", "zq_codes", "c", "y"))
+    ref = tiny2d.ol.forward(x.float().numpy(), quant=True, want=("z", "zq_codes", "zq_sf", "c", "y"))
     idx = moe.stage("idx", T, torch.int32).view(T, d.k).cpu().numpy()
     assert np.array_equal(idx, ref["idx"])
     w = moe.stage("w", T, torch.float32).view(T, d.k).cpu().numpy()
@@ -80,8 +80,9 @@ def test_forward_2d_matches_oracle(tiny2d, T):
     z = moe.stage("z", T, torch.bfloat16).view(T, d.l).float().cpu().numpy()
     assert rel_l2_rows(z, ref["z"]).max() <= TOL_INTER
     zc = moe.stage("zq_codes", T).view(T, d.l // 2).cpu().numpy()
-    same = np.all(zc == ref["zq_codes"], axis=1)            # see the mid-size stage test
-    assert same.mean() >= 0.95
+    zs = moe.stage("zq_sf", T).view(T, d.l // 16).cpu().numpy()
     c = moe.stage("c", T, torch.bfloat16).view(T, d.l).float().cpu().numpy()
-    assert rel_l2_rows(c[same], ref["c"][same]).max() <= TOL_OUT
-    assert rel_l2_rows(y.float().cpu().numpy()[same], ref["y"][same]).max() <= TOL_OUT
+    moved, worst = check_outputs_all_tokens(tiny2d, x.float().numpy(), zc, zs,
+                                            {"c": c, "y": y.float().cpu().numpy()}, ref, TOL_OUT)
+    print(f"T={T}: {moved} of {T} tokens took a neighbouring zq code (worst rel L2 against the "
+          f"oracle's own zq: {worst:.3e})")

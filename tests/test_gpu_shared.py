@@ -13,7 +13,7 @@ import torch
 
 import lmoe_synth
 import oracle
-from lmoe_cases import Case, rel_l2_rows
+from lmoe_cases import Case, rel_l2_rows, stored_calib, check_routing_all_tokens, sample_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -139,16 +139,17 @@ def test_create_rejects_bad_shared_arguments(tiny_shared):
 @pytest.fixture(scope="module")
 def ultra_shared():
     cfg = lmoe_synth.CONFIGS["ultra_long_T32768_shared"]
-    case = Case(cfg["dims"], seed=cfg["seed"], zipf=cfg["zipf"], calib_T=cfg["calib_T"],
-                gen_device="cuda")
+    case = Case(cfg["dims"], seed=cfg["seed"], zipf=cfg["zipf"], gen_device="cuda",
+                calib=stored_calib("ultra_long_T32768_shared"))
     yield case
     case.close()
 
 
 @pytest.mark.slow
 def test_ultra_long_prompt_with_shared_expert(ultra_shared):
-    """T = 32768 (one long prompt), Ultra dims, shared expert d = ffn = 8192: routing counts on
-    every token, everything else on a token sample."""
+    """T = 32768 (one long prompt), Ultra dims, shared expert d = ffn = 8192: expert indices and
+    per-expert counts against the oracle's router on every token; the shared expert's stages
+    and y on 64 sampled tokens (the first and the last among them)."""
     T = lmoe_synth.CONFIGS["ultra_long_T32768_shared"]["T"]
     moe = ultra_shared.gpu(debug=True)
     d = ultra_shared.dims
@@ -157,10 +158,6 @@ def test_ultra_long_prompt_with_shared_expert(ultra_shared):
     moe.check()
     idx = moe.stage("idx", T, torch.int32).view(T, d.k).cpu().numpy()
     counts = moe.stage("counts", T, torch.int32).cpu().numpy()
-    assert counts.sum() == T * d.k
-    assert np.array_equal(counts, np.bincount(idx.ravel(), minlength=d.E))
-    sample = np.sort(np.random.default_rng(3).choice(T, 6, replace=False))
-    sample[-1] = T - 1                                   # the last (ragged) M tile
+    check_routing_all_tokens(ultra_shared, T, x, idx, counts)
+    sample = sample_tokens(T, 64, seed=3)
     _check_shared(ultra_shared, T, x, y, sample)
-    _, oidx, _, _ = ultra_shared.ol.route(x[sample].float().cpu().numpy())
-    assert np.array_equal(idx[sample], oidx)

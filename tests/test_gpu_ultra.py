@@ -2,9 +2,11 @@
 NVIDIA AI releases Nemotron 3 Ultra, architecture paragraph; l = d/4 from the shengxinai.com
 Nemotron 3 blog, section 2.2), in the launch configuration the benchmark times.
 
-Decode (T = 8, uniform routing): every token against the oracle.  Prefill (T = 4096,
-Zipf(1.1) router bias): routing on a token sample plus the count invariants on all tokens,
-and full outputs on a token sample (tokens are independent under static scales).
+Both workloads use the benchmark's layer (weights of seed 1) and its stored static activation
+scales (calibrated by the oracle on 1024 tokens).  Decode (T = 8, uniform routing): every token
+against the oracle.  Prefill (T = 4096, Zipf(1.1) router bias): expert indices and per-expert
+counts against the oracle's router on every token, the other stages on 256 sampled tokens
+(tokens are independent under static scales), every sampled token at the layer's tolerance.
 """
 import numpy as np
 import pytest
@@ -12,7 +14,8 @@ import torch
 
 import lmoe_synth
 import oracle
-from lmoe_cases import Case, real_rows, rel_l2_rows, w_tol
+from lmoe_cases import (Case, check_outputs_all_tokens, check_routing_all_tokens, real_rows,
+                        rel_l2_rows, sample_tokens, stored_calib, w_tol)
 
 pytestmark = pytest.mark.gpu
 
@@ -20,16 +23,26 @@ TOL_INTER = 5e-3
 TOL_OUT = 2e-2
 
 
+DECODE = "ultra_decode_T8"
+PREFILL = "ultra_prefill_T4096_zipf1.1"
+
+
+def _case(name):
+    cfg = lmoe_synth.CONFIGS[name]
+    return Case(cfg["dims"], seed=cfg["seed"], zipf=cfg["zipf"], gen_device="cuda",
+                calib=stored_calib(name))
+
+
 @pytest.fixture(scope="module")
 def ultra_uniform():
-    case = Case(lmoe_synth.ULTRA, seed=1, zipf=0.0, calib_T=8, gen_device="cuda")
+    case = _case(DECODE)
     yield case
     case.close()
 
 
 @pytest.fixture(scope="module")
 def ultra_zipf():
-    case = Case(lmoe_synth.ULTRA, seed=2, zipf=1.1, calib_T=8, gen_device="cuda")
+    case = _case(PREFILL)
     yield case
     case.close()
 
@@ -39,10 +52,10 @@ def _check_tokens(case, T, x, y, sample):
     moe = case.moe
     idx = moe.stage("idx", T, torch.int32).view(T, d.k).cpu().numpy()
     counts = moe.stage("counts", T, torch.int32).cpu().numpy()
-    assert counts.sum() == T * d.k
-    assert np.array_equal(counts, np.bincount(idx.ravel(), minlength=d.E))
+    w = moe.stage("w", T, torch.float32).view(T, d.k).cpu().numpy()
+    check_routing_all_tokens(case, T, x, idx, counts, w)
     xs = x[sample].float().cpu().numpy()
-    ref = case.ol.forward(xs, quant=True, want=("z", "c", "y"))
+    ref = case.ol.forward(xs, quant=True, want=("z", "zq_codes", "zq_sf", "c", "y"))
     assert np.array_equal(idx[sample], ref["idx"])
     w = moe.stage("w", T, torch.float32).view(T, d.k).cpu().numpy()
     assert np.allclose(w[sample], ref["w"], **w_tol(T))
@@ -53,8 +66,10 @@ def _check_tokens(case, T, x, y, sample):
     oc, os_, _ = oracle.quantize_nvfp4(z, case.amax_z)
     assert np.array_equal(zs, os_) and np.array_equal(zc, oc)
     c = moe.stage("c", T, torch.bfloat16).view(T, d.l).float().cpu().numpy()[sample]
-    assert rel_l2_rows(c, ref["c"]).max() <= TOL_OUT
-    assert rel_l2_rows(y[sample].float().cpu().numpy(), ref["y"]).max() <= TOL_OUT
+    moved, worst = check_outputs_all_tokens(case, xs, zc, zs, {"c": c, "y": y[sample].float().cpu().numpy()},
+                                            ref, TOL_OUT)
+    print(f"T={T}: {moved} of {len(sample)} sampled tokens took a neighbouring zq code "
+          f"(their worst rel L2 against the oracle's own zq: {worst:.3e})")
 
 
 def test_ultra_expert_weights_sampled(ultra_uniform):
@@ -92,17 +107,22 @@ def test_ultra_prefill_T4096_zipf(ultra_zipf):
     moe.check()
     counts = moe.stage("counts", T, torch.int32).cpu().numpy()
     assert (counts == 0).sum() > 0 and counts.max() > 1000      # the skew the workload asks for
-    rng = np.random.default_rng(0)
-    sample = np.sort(rng.choice(T, 12, replace=False))
-    sample[0] = 0
-    sample[-1] = T - 1
-    _check_tokens(case, T, x, y, sample)
+    # saturation under the static scales (calibrated on 1024 other tokens): |z| > amax_z, h > amax_h
+    d = case.dims
+    z = moe.stage("z", T, torch.bfloat16).view(T, d.l).float()
+    nrows = int(moe.stage("nrows", T, torch.int32).cpu()[0])
+    R = moe.stage("rows", T, torch.int32).numel()
+    live = torch.from_numpy(real_rows(counts, nrows)).cuda()
+    h = moe.stage("h", T, torch.bfloat16).view(R, d.ffn)[:nrows][live].float()
+    print(f"saturation at T={T}: z {float((z.abs() > case.amax_z).float().mean()):.3e}, "
+          f"h {float((h > case.amax_h).float().mean()):.3e} (amax_z {case.amax_z}, amax_h {case.amax_h})")
+    _check_tokens(case, T, x, y, sample_tokens(T))
 
 
 def test_ultra_router_margin_and_routing_on_many_tokens(ultra_zipf):
-    """T = 4096: routing of 256 sampled tokens against the oracle, and the tensor-core logits
-    against the canonical ones: the observed error must sit far inside the certified margin
-    (whose floor is 2^-16 |x| max|w_e|)."""
+    """T = 4096: routing of every token against the oracle, and the tensor-core logits of 256
+    sampled tokens against the canonical ones: the observed error must sit far inside the
+    certified margin (whose floor is 2^-16 |x| max|w_e|)."""
     case = ultra_zipf
     moe = case.gpu(debug=True)
     d = case.dims
@@ -110,6 +130,8 @@ def test_ultra_router_margin_and_routing_on_many_tokens(ultra_zipf):
     x = case.tokens(T, seed_offset=31).cuda()
     moe.forward(x)
     moe.check()
+    check_routing_all_tokens(case, T, x, moe.stage("idx", T, torch.int32).view(T, d.k).cpu().numpy(),
+                             moe.stage("counts", T, torch.int32).cpu().numpy())
     sample = np.sort(np.random.default_rng(1).choice(T, 256, replace=False))
     xs = x[sample].float().cpu().numpy()
     logits, oidx, ow, _ = oracle.router(xs, case.ol.w_router, case.ol.b_router, d.k)
@@ -163,9 +185,9 @@ def test_ultra_drift_against_bf16_experts(ultra_uniform):
 @pytest.mark.parametrize("which,T", [("uniform", 8), ("zipf", 4096)])
 def test_ultra_timed_configuration(ultra_uniform, ultra_zipf, which, T):
     """The benchmark times the layer with debug copies off; that forward (same kernels, no
-    intermediate copies) gives the oracle's routing on all sampled tokens and its outputs on
-    every sampled token whose zq equals the oracle's (a z on a rounding boundary can take the
-    neighbouring code, as in the stage-by-stage tests; such tokens must be rare)."""
+    intermediate copies) gives the oracle's routing on every token and its output y on every
+    sampled token (256 at T = 4096) within the layer's tolerance.  A z on a rounding boundary
+    can take the neighbouring zq code (counted and printed; such tokens must be rare)."""
     case = ultra_uniform if which == "uniform" else ultra_zipf
     moe = case.gpu(debug=True)
     d = case.dims
@@ -180,10 +202,12 @@ def test_ultra_timed_configuration(ultra_uniform, ultra_zipf, which, T):
         zs = moe.stage("zq_sf", T).view(T, d.l // 16).cpu().numpy()
     finally:
         case.lm.lmoe_set_debug(moe.ctx, True)
-    assert np.array_equal(counts, np.bincount(idx.ravel(), minlength=d.E))
-    sample = np.arange(T) if T <= 8 else np.array([0, 1, 777, 2048, 3001, T - 1])
-    ref = case.ol.forward(x[sample].float().cpu().numpy(), quant=True, want=("zq_codes", "zq_sf", "y"))
+    check_routing_all_tokens(case, T, x, idx, counts)
+    sample = sample_tokens(T, seed=5)
+    xs = x[sample].float().cpu().numpy()
+    ref = case.ol.forward(xs, quant=True, want=("zq_codes", "zq_sf", "y"))
     assert np.array_equal(idx[sample], ref["idx"])
-    same_zq = np.all(zc[sample] == ref["zq_codes"], axis=1) & np.all(zs[sample] == ref["zq_sf"], axis=1)
-    assert same_zq.sum() >= len(sample) - 1
-    assert rel_l2_rows(y[sample].float().cpu().numpy()[same_zq], ref["y"][same_zq]).max() <= TOL_OUT
+    moved, worst = check_outputs_all_tokens(case, xs, zc[sample], zs[sample],
+                                            {"y": y[sample].float().cpu().numpy()}, ref, TOL_OUT)
+    print(f"T={T}: {moved} of {len(sample)} sampled tokens took a neighbouring zq code "
+          f"(their worst rel L2 against the oracle's own zq: {worst:.3e})")

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import lmoe_synth
-from lmoe_cases import Case, real_rows, rel_l2_rows, w_tol
+from lmoe_cases import Case, real_rows, rel_l2_rows, w_tol, stored_calib
 
 pytestmark = pytest.mark.gpu
 
@@ -61,7 +61,8 @@ def test_forward_w4a16_matches_oracle(w4, T):
 
 @pytest.fixture(scope="module")
 def ultra_w4():
-    case = Case(lmoe_synth.ULTRA, seed=1, zipf=0.0, calib_T=8, gen_device="cuda", w4a16=True)
+    case = Case(lmoe_synth.ULTRA, seed=1, zipf=0.0, gen_device="cuda", w4a16=True,
+                calib=stored_calib("ultra_decode_T8"))
     yield case
     case.close()
 

@@ -148,3 +148,35 @@ def test_storage_arithmetic_ultra():
     per = 2 * (d.l * d.ffn // 2 + d.l * d.ffn // 16 + 4)
     assert per == 4_718_600
     assert abs(per * d.E / 1e9 - 2.416) < 1e-3
+
+
+def test_forward_from_a_given_zq(tiny):
+    """The layer fed a given zq: with the oracle's own zq it reproduces the plain forward bit for
+    bit; with a zq one neighbouring code away in some tokens (a z one bf16 ulp away can quantize
+    so), its expert stage equals the dense products of that zq's independently decoded values,
+    and the outputs of the untouched tokens do not change."""
+    dims, ol, mats, x, res = tiny
+    want = ("zq_codes", "zq_sf", "hq_codes", "hq_sf", "c64", "c", "y")
+    same = ol.forward(x, quant=True, want=want, zq=(res["zq_codes"], res["zq_sf"]))
+    for k in want + ("idx", "w", "counts"):
+        assert np.array_equal(same[k], res[k]), k
+    zc = res["zq_codes"].copy()
+    moved = [3, 17, 40]
+    for t in moved:                    # raise the magnitude code of one element by one step
+        lo = int(zc[t, 5]) & 15
+        zc[t, 5] = (zc[t, 5] & 0xF0) | ((lo & 8) | min((lo & 7) + 1, 7))
+    alt = ol.forward(x, quant=True, want=("c64", "y"), zq=(zc, res["zq_sf"]))
+    keep = np.setdiff1d(np.arange(x.shape[0]), moved)
+    assert np.array_equal(alt["y"][keep], res["y"][keep])
+    assert not np.array_equal(alt["c64"][moved], res["c64"][moved])
+    s_z = np.float32(ol.amax_z) / np.float32(2688.0)
+    s_h = np.float32(ol.amax_h) / np.float32(2688.0)
+    zq = dequant(zc, res["zq_sf"], 1.0) * float(s_z)
+    for t in moved:
+        c = np.zeros(dims.l)
+        for j, e in enumerate(res["idx"][t]):
+            c1, s1, d1, c2, s2, d2 = ol.quantized(int(e))
+            h = _bf16(np.maximum(dequant(c1, s1, d1) @ zq[t], 0.0) ** 2)
+            hc, hs, _ = oracle.quantize_nvfp4(h[None], amax=ol.amax_h)
+            c += float(res["w"][t, j]) * (dequant(c2, s2, d2) @ (dequant(hc, hs, 1.0)[0] * float(s_h)))
+        assert np.allclose(alt["c64"][t], c, rtol=1e-6, atol=1e-6 * np.abs(c).max())
