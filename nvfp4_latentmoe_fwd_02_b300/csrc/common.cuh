@@ -237,6 +237,85 @@ __host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
 }
 
 // ------------------------------------------------------------------------------------
+// Warp-converged issue.  The pipeline roles (TMA producer, MMA issuer, scale copiers) run
+// their loops with all 32 lanes of the warp, so every address, coordinate and descriptor is
+// computed identically by the whole warp; each issuing instruction is predicated on one
+// elected lane (`leader`), so it is issued once.  Waits are made by all lanes.
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t elect_leader() {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx_p(uint32_t leader, uint64_t *bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+        "@q mbarrier.arrive.expect_tx.shared::cta.b64 _, [%1], %2;\n\t}" ::"r"(leader),
+        "r"(smem_u32(bar)), "r"(bytes)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_p(uint32_t leader, uint32_t smem_dst, const CUtensorMap *map,
+                                              uint64_t *bar, int x, int y) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+        "@q cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%1], [%2, {%4, %5}], [%3];\n\t}" ::"r"(leader),
+        "r"(smem_dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_load_p(uint32_t leader, uint32_t smem_dst, const void *gsrc,
+                                            uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+        "@q cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%1], [%2], %3, [%4];\n\t}" ::"r"(
+            leader),
+        "r"(smem_dst), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void mma_nvf4_p(uint32_t leader, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %6, 0;\n\tsetp.ne.b32 q, %7, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"(leader)
+        : "memory");
+}
+__device__ __forceinline__ void mma_bf16_p(uint32_t leader, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(leader)
+        : "memory");
+}
+__device__ __forceinline__ void mma_f8_p(uint32_t leader, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(leader)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit_p(uint32_t leader, uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];\n\t}" ::"r"(leader),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tmem_cp_sf_p(uint32_t leader, uint32_t taddr, uint64_t sdesc) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+        "@q tcgen05.cp.cta_group::1.32x128b.warpx4 [%1], %2;\n\t}" ::"r"(leader),
+        "r"(taddr), "l"(sdesc)
+        : "memory");
+}
+
+// ------------------------------------------------------------------------------------
 // programmatic dependent launch: every kernel of the forward is launched so that its CTAs may
 // start while the previous kernel drains; pdl_wait() blocks until the previous grid has
 // completed and its writes are visible, so it comes before the first global access.

@@ -603,145 +603,145 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
 
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t issued = 0, issued_phase = 0;   // per stage: ever issued / phase of last issue
-            const uint32_t sA0 = smem_u32(sA), sB0 = smem_u32(sB);
-            const uint32_t sSFA0 = smem_u32(sSFA), sSFB0 = smem_u32(sSFB);
-            for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x) {
-                const Tile tl = decode_tile(g, tb, t);
-                const uint8_t *sfa_tile = NVF4 ? g.sfa + static_cast<size_t>(tl.a_row0 >> 7) * K64 * 512 : nullptr;
-                const uint8_t *sfb_tile = (NVF4 || W4) ? g.sfb + (static_cast<size_t>(tl.e) * g.NB + (tl.n0 >> 7)) * K64 * 512 : nullptr;
-                for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
-                    if (!role_wait(&empty[stage], phase ^ 1, s_abort, g.err, g.wait_limit)) break;
-                    const int kb0 = kt * KB;
-                    uint64_t *fb = &full[stage];
-                    const uint32_t a_st = sA0 + stage * C::kAStage, b_st = sB0 + stage * C::kBStage;
-                    if constexpr (W4) {
-                        // activations (bf16), raw E2M1 codes and the scale atom of each 64-element block
-                        const int nb = min(KB, K64 - kb0);
-                        mbar_arrive_expect_tx(fb, nb * (C::kACol + C::kRawBlock));
-                        const uint32_t r_st = smem_u32(sRaw) + stage * C::kRawStage;
-                        for (int b = 0; b < nb; ++b) {
-                            tma_load_2d_u32(a_st + b * C::kACol, &tmA, fb, (kb0 + b) * 64, tl.a_row0);
-                            // 32 code bytes of 64-element block kb0 + b: a quarter of a tiled box row
-                            const int kb = kb0 + b;
-                            tma_load_2d_u32(r_st + b * C::kRawBlock, &tmB, fb, (kb & 3) * 32,
-                                            ((tl.e * g.NB + (tl.n0 >> 7)) * g.b_kt + (kb >> 2)) * 128);
-                            bulk_load_u32(r_st + b * C::kRawBlock + 4096, sfb_tile + (kb0 + b) * 512, 512, fb);
-                        }
-                        issued |= 1u << stage;
-                        issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-                        if (++stage == STAGES) { stage = 0; phase ^= 1; }
-                        continue;
-                    }
-                    const int nsteps = NVF4 ? min(4 * KB, K64 - 4 * kb0) : 4 * KB;
-                    if (NVF4) {
-                        // the scale atoms first, on their own barrier: they land ahead of the
-                        // operand tiles, so their smem -> TMEM copies are off the critical path
-                        uint64_t *sb = &sffull[stage];
-                        mbar_arrive_expect_tx(sb, 2 * nsteps * 512);
-                        bulk_load_u32(sSFA0 + stage * C::kSfStage, sfa_tile + kb0 * 2048, nsteps * 512, sb);
-                        bulk_load_u32(sSFB0 + stage * C::kSfStage, sfb_tile + kb0 * 2048, nsteps * 512, sb);
-                    }
-                    mbar_arrive_expect_tx(fb, KB * (C::kACol + BN * 128));
-#pragma unroll
-                    for (int b = 0; b < KB; ++b) {
-                        const int kx = (kb0 + b) * C::kTmaXPerBlock;
-                        const int kxa = g.a_kwrap > 0 ? kx % g.a_kwrap : kx;
-                        tma_load_2d_u32(a_st + b * C::kACol, &tmA, fb, kxa, tl.a_row0);
-                        if (NVF4)   // weight codes in tile order: box (expert, row block, column block)
-                            tma_load_2d_u32(b_st + b * (BN * 128), &tmB, fb, 0,
-                                            ((tl.e * g.NB + (tl.n0 >> 7)) * g.b_kt + kb0 + b) * 128);
-                        else
-                            tma_load_2d_u32(b_st + b * (BN * 128), &tmB, fb, kx, tl.b_row0);
+        // (all lanes run the loop; the elected lane issues: see elect_leader)
+        const uint32_t leader = elect_leader();
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued = 0, issued_phase = 0;   // per stage: ever issued / phase of last issue
+        const uint32_t sA0 = smem_u32(sA), sB0 = smem_u32(sB);
+        const uint32_t sSFA0 = smem_u32(sSFA), sSFB0 = smem_u32(sSFB);
+        for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x) {
+            const Tile tl = decode_tile(g, tb, t);
+            const uint8_t *sfa_tile = NVF4 ? g.sfa + static_cast<size_t>(tl.a_row0 >> 7) * K64 * 512 : nullptr;
+            const uint8_t *sfb_tile = (NVF4 || W4) ? g.sfb + (static_cast<size_t>(tl.e) * g.NB + (tl.n0 >> 7)) * K64 * 512 : nullptr;
+            for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
+                if (!role_wait(&empty[stage], phase ^ 1, s_abort, g.err, g.wait_limit)) break;
+                const int kb0 = kt * KB;
+                uint64_t *fb = &full[stage];
+                const uint32_t a_st = sA0 + stage * C::kAStage, b_st = sB0 + stage * C::kBStage;
+                if constexpr (W4) {
+                    // activations (bf16), raw E2M1 codes and the scale atom of each 64-element block
+                    const int nb = min(KB, K64 - kb0);
+                    mbar_arrive_expect_tx_p(leader, fb, nb * (C::kACol + C::kRawBlock));
+                    const uint32_t r_st = smem_u32(sRaw) + stage * C::kRawStage;
+                    for (int b = 0; b < nb; ++b) {
+                        tma_load_2d_p(leader, a_st + b * C::kACol, &tmA, fb, (kb0 + b) * 64, tl.a_row0);
+                        // 32 code bytes of 64-element block kb0 + b: a quarter of a tiled box row
+                        const int kb = kb0 + b;
+                        tma_load_2d_p(leader, r_st + b * C::kRawBlock, &tmB, fb, (kb & 3) * 32,
+                                      ((tl.e * g.NB + (tl.n0 >> 7)) * g.b_kt + (kb >> 2)) * 128);
+                        bulk_load_p(leader, r_st + b * C::kRawBlock + 4096, sfb_tile + (kb0 + b) * 512, 512, fb);
                     }
                     issued |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    continue;
                 }
+                const int nsteps = NVF4 ? min(4 * KB, K64 - 4 * kb0) : 4 * KB;
+                if (NVF4) {
+                    // the scale atoms first, on their own barrier: they land ahead of the
+                    // operand tiles, so their smem -> TMEM copies are off the critical path
+                    uint64_t *sb = &sffull[stage];
+                    mbar_arrive_expect_tx_p(leader, sb, 2 * nsteps * 512);
+                    bulk_load_p(leader, sSFA0 + stage * C::kSfStage, sfa_tile + kb0 * 2048, nsteps * 512, sb);
+                    bulk_load_p(leader, sSFB0 + stage * C::kSfStage, sfb_tile + kb0 * 2048, nsteps * 512, sb);
+                }
+                mbar_arrive_expect_tx_p(leader, fb, KB * (C::kACol + BN * 128));
+#pragma unroll
+                for (int b = 0; b < KB; ++b) {
+                    const int kx = (kb0 + b) * C::kTmaXPerBlock;
+                    const int kxa = g.a_kwrap > 0 ? kx % g.a_kwrap : kx;
+                    tma_load_2d_p(leader, a_st + b * C::kACol, &tmA, fb, kxa, tl.a_row0);
+                    if (NVF4)   // weight codes in tile order: box (expert, row block, column block)
+                        tma_load_2d_p(leader, b_st + b * (BN * 128), &tmB, fb, 0,
+                                      ((tl.e * g.NB + (tl.n0 >> 7)) * g.b_kt + kb0 + b) * 128);
+                    else
+                        tma_load_2d_p(leader, b_st + b * (BN * 128), &tmB, fb, kx, tl.b_row0);
+                }
+                issued |= 1u << stage;
+                issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
-            if (*s_abort) {
-                // the last load issued to each stage has landed before the CTA leaves (bounded)
-                for (int s = 0; s < STAGES; ++s) {
-                    if (!((issued >> s) & 1u)) continue;
-                    const uint32_t p = (issued_phase >> s) & 1u;
-                    const long long t0 = clock64();
-                    while (!mbar_try_wait(&full[s], p) && clock64() - t0 < kWaitLimitCycles / 8) {}
-                    while (NVF4 && !mbar_try_wait(&sffull[s], p) && clock64() - t0 < kWaitLimitCycles / 8) {}
-                }
+        }
+        if (*s_abort) {
+            // the last load issued to each stage has landed before the CTA leaves (bounded)
+            for (int s = 0; s < STAGES; ++s) {
+                if (!((issued >> s) & 1u)) continue;
+                const uint32_t p = (issued_phase >> s) & 1u;
+                const long long t0 = clock64();
+                while (!mbar_try_wait(&full[s], p) && clock64() - t0 < kWaitLimitCycles / 8) {}
+                while (NVF4 && !mbar_try_wait(&sffull[s], p) && clock64() - t0 < kWaitLimitCycles / 8) {}
             }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = NVF4 ? idesc_nvf4(kBM, BN)
-                                        : (KIND == kKindFp8 ? idesc_f8(kBM, BN) : idesc_bf16(kBM, BN));
-            // descriptors of stage 0; a stage adds its byte offset >> 4 to the start address
-            const uint64_t adesc0 = sdesc_sw128(smem_u32(sA)), bdesc0 = sdesc_sw128(smem_u32(sB));
-            int stage = 0;
-            uint32_t phase = 0;
-            int it = 0;
-            // Injected fault: `drain` gets its only arrival from the commit after the tile
-            // loop, so this wait cannot succeed; it runs out after g.wait_limit cycles and
-            // takes the CTA down the timeout path.
-            if (g.inject_wait) role_wait(drain, 0, s_abort, g.err, g.wait_limit);
-            for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x, ++it) {
-                const Tile tl = decode_tile(g, tb, t);
-                const int acc = it & 1;
-                const uint32_t aphase = (it >> 1) & 1;
-                if (!role_wait(&tempty[acc], aphase ^ 1, s_abort, g.err, g.wait_limit)) break;
+        // (all lanes run the loop; the elected lane issues)
+        const uint32_t leader = elect_leader();
+        const uint32_t idesc = NVF4 ? idesc_nvf4(kBM, BN)
+                                    : (KIND == kKindFp8 ? idesc_f8(kBM, BN) : idesc_bf16(kBM, BN));
+        // descriptors of stage 0; a stage adds its byte offset >> 4 to the start address
+        const uint64_t adesc0 = sdesc_sw128(smem_u32(sA)), bdesc0 = sdesc_sw128(smem_u32(sB));
+        int stage = 0;
+        uint32_t phase = 0;
+        int it = 0;
+        // Injected fault: `drain` gets its only arrival from the commit after the tile loop, so
+        // this wait cannot succeed; it runs out after g.wait_limit cycles and takes the CTA
+        // down the timeout path.
+        if (g.inject_wait) role_wait(drain, 0, s_abort, g.err, g.wait_limit);
+        for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x, ++it) {
+            const Tile tl = decode_tile(g, tb, t);
+            const int acc = it & 1;
+            const uint32_t aphase = (it >> 1) & 1;
+            if (!role_wait(&tempty[acc], aphase ^ 1, s_abort, g.err, g.wait_limit)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem + acc * kAccCols;
+            bool ok = true;
+            for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
+                if (!role_wait(&full[stage], phase, s_abort, g.err, g.wait_limit)) { ok = false; break; }
+                if ((NVF4 || W4) && !role_wait(&sfready[stage], phase, s_abort, g.err, g.wait_limit)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem + acc * kAccCols;
-                bool ok = true;
-                for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
-                    if (!role_wait(&full[stage], phase, s_abort, g.err, g.wait_limit)) { ok = false; break; }
-                    if ((NVF4 || W4) && !role_wait(&sfready[stage], phase, s_abort, g.err, g.wait_limit)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint64_t ad = adesc0 + ((stage * C::kAStage) >> 4);
-                    const uint64_t bd = bdesc0 + ((stage * C::kBStage) >> 4);
-                    const uint32_t acc_flag0 = kt > tl.kt0 ? 1u : 0u;
-                    if constexpr (NVF4) {
-                        const int nsteps = min(4 * KB, K64 - 4 * kt * KB);
-                        const uint32_t sf_t = tmem + kSfCol0 + stage * C::kSfCols;
+                const uint64_t ad = adesc0 + ((stage * C::kAStage) >> 4);
+                const uint64_t bd = bdesc0 + ((stage * C::kBStage) >> 4);
+                const uint32_t acc_flag0 = kt > tl.kt0 ? 1u : 0u;
+                if constexpr (NVF4) {
+                    const int nsteps = min(4 * KB, K64 - 4 * kt * KB);
+                    const uint32_t sf_t = tmem + kSfCol0 + stage * C::kSfCols;
 #pragma unroll
-                        for (int kk = 0; kk < 4 * KB; ++kk) {
-                            if (kk < nsteps)
-                                mma_nvf4(d_tmem, ad + (((kk >> 2) * C::kACol + (kk & 3) * 32) >> 4),
-                                         bd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4), idesc,
-                                         sf_t + kk * 4, sf_t + 16 * KB + kk * 4, (acc_flag0 | kk) ? 1u : 0u);
-                        }
-                    } else if constexpr (W4) {
-                        const int nb = min(KB, K64 - kt * KB);    // 64-element blocks present
-                        for (int kk = 0; kk < 4 * nb; ++kk)
-                            mma_bf16(d_tmem, ad + (((kk >> 2) * C::kACol + (kk & 3) * 32) >> 4),
-                                     bd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4), idesc,
-                                     (acc_flag0 | kk) ? 1u : 0u);
-                    } else if constexpr (KIND == kKindFp8) {
-#pragma unroll
-                        for (int kk = 0; kk < 4 * KB; ++kk)
-                            mma_f8(d_tmem, ad + (((kk >> 2) * C::kACol + (kk & 3) * 32) >> 4),
+                    for (int kk = 0; kk < 4 * KB; ++kk) {
+                        if (kk < nsteps)
+                            mma_nvf4_p(leader, d_tmem, ad + (((kk >> 2) * C::kACol + (kk & 3) * 32) >> 4),
+                                       bd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4), idesc,
+                                       sf_t + kk * 4, sf_t + 16 * KB + kk * 4, (acc_flag0 | kk) ? 1u : 0u);
+                    }
+                } else if constexpr (W4) {
+                    const int nb = min(KB, K64 - kt * KB);    // 64-element blocks present
+                    for (int kk = 0; kk < 4 * nb; ++kk)
+                        mma_bf16_p(leader, d_tmem, ad + (((kk >> 2) * C::kACol + (kk & 3) * 32) >> 4),
                                    bd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4), idesc,
                                    (acc_flag0 | kk) ? 1u : 0u);
-                    } else {
+                } else if constexpr (KIND == kKindFp8) {
 #pragma unroll
-                        for (int kk = 0; kk < 4 * KB; ++kk)
-                            mma_bf16(d_tmem, ad + (((kk >> 2) * C::kACol + (kk & 3) * 32) >> 4),
-                                     bd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4), idesc,
-                                     (acc_flag0 | kk) ? 1u : 0u);
-                    }
-                    mma_commit(&empty[stage]);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    for (int kk = 0; kk < 4 * KB; ++kk)
+                        mma_f8_p(leader, d_tmem, ad + (((kk >> 2) * C::kACol + (kk & 3) * 32) >> 4),
+                                 bd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4), idesc,
+                                 (acc_flag0 | kk) ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 4 * KB; ++kk)
+                        mma_bf16_p(leader, d_tmem, ad + (((kk >> 2) * C::kACol + (kk & 3) * 32) >> 4),
+                                   bd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4), idesc,
+                                   (acc_flag0 | kk) ? 1u : 0u);
                 }
-                if (!ok) break;
-                mma_commit(&tfull[acc]);
+                mma_commit_p(leader, &empty[stage]);
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
-            // all tensor-core work of this CTA is complete before TMEM is released
-            mma_commit(drain);
-            const long long t0 = clock64();
-            while (!mbar_try_wait(drain, 0) && clock64() - t0 < kWaitLimitCycles) {}
+            if (!ok) break;
+            mma_commit_p(leader, &tfull[acc]);
         }
+        // all tensor-core work of this CTA is complete before TMEM is released
+        mma_commit_p(leader, drain);
+        const long long t0 = clock64();
+        while (!mbar_try_wait(drain, 0) && clock64() - t0 < kWaitLimitCycles) {}
     } else if (W4 && warp < kEpi0) {
         // ---------------------------------------------------------------- weight decoders
         const int ct = (warp - 2) * 32 + lane;
@@ -765,7 +765,9 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
         }
     } else if (warp == 2 || warp == 3) {
         // ---------------------------------------------------------------- scale copiers
-        if (NVF4 && lane == 0) {
+        // (all lanes run the loop; the elected lane issues)
+        if (NVF4) {
+            const uint32_t leader = elect_leader();
             const bool is_b = warp == 3;
             const uint64_t sfdesc0 = sdesc_sf(smem_u32(is_b ? sSFB : sSFA));
             const uint32_t col_off = is_b ? 16 * KB : 0;
@@ -782,14 +784,14 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
                     const uint64_t sfd = sfdesc0 + ((stage * C::kSfStage) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 4 * KB; ++kk)
-                        if (kk < nsteps) tmem_cp_sf(sf_t + kk * 4, sfd + kk * (512 >> 4));
-                    mma_commit(&sfready[stage]);
+                        if (kk < nsteps) tmem_cp_sf_p(leader, sf_t + kk * 4, sfd + kk * (512 >> 4));
+                    mma_commit_p(leader, &sfready[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
             }
-            // every copy this thread issued is complete before TMEM is released
-            mma_commit(&cdrain[is_b ? 1 : 0]);
+            // every copy this warp issued is complete before TMEM is released
+            mma_commit_p(leader, &cdrain[is_b ? 1 : 0]);
             const long long t0 = clock64();
             while (!mbar_try_wait(&cdrain[is_b ? 1 : 0], 0) && clock64() - t0 < kWaitLimitCycles) {}
         }

@@ -8,6 +8,7 @@
 // reads device memory inside lmoe_forward.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cmath>
@@ -35,7 +36,11 @@ namespace {
 // and scale-copy commits per byte (T = 4096, Zipf 1.1: 424 -> 381 us).
 constexpr int kKbF4Up = 2;
 constexpr int kStagesF4 = 3;
-constexpr int kStagesF4Stg = 5;       // NVFP4 prefill, latent-down: + 16 KB of combine staging
+// NVFP4 prefill, latent-down: one column block per stage, five stages, + 16 KB of combine
+// staging (two blocks per stage fit only without the staging, which costs more: 431 -> 487 us)
+constexpr int kKbF4Dn = 1;
+constexpr int kStagesF4Stg = 5;
+constexpr bool kStgF4Dn = true;
 constexpr int kStagesBF16 = 6;
 constexpr int kStagesF4Small = 4;     // decode (T <= 32): 4 KB A boxes, 2 column blocks per stage
 constexpr int kStagesBF16Small = 5;
@@ -47,6 +52,7 @@ constexpr int kBNNarrow = 64;         // bf16 GEMMs at decode whose 128-column t
 constexpr int kStagesW4 = 5;          // W4A16: bf16 A + decoded bf16 B + raw E2M1 block per stage
 constexpr int kStagesW4Small = 4;
 constexpr int kSmallAMaxT = 32;
+
 inline int kb_for(bool small_a) { return small_a ? 2 : 1; }   // column blocks per stage
 // tile width of the dense (bf16 / fp8) GEMMs: 256 outside decode (fewer operand bytes per output)
 inline int bn_for(bool small_a) { return small_a ? 128 : 256; }
@@ -174,6 +180,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// One NVTX range around the host side of a forward (its launches), for timeline tools.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
 
 struct WsLayout {
     size_t idx, w, counts, seg, mt, slot_off, nrows, row_slot, router, zacc, zq_codes, zq_sf, z_dbg,
@@ -349,7 +361,7 @@ cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const Gemm
                         bool small_a, cudaStream_t s) {
     if (KIND == kKindNvf4)
         return small_a ? launch_gemm_cfg<kKindNvf4, true, 2, kStagesF4Small>(ta, tb, g, grid, s)
-               : g.epi == EPI_COMBINE ? launch_gemm_cfg<kKindNvf4, false, 1, kStagesF4Stg, kBN, true>(ta, tb, g, grid, s)
+               : g.epi == EPI_COMBINE ? launch_gemm_cfg<kKindNvf4, false, kKbF4Dn, kStagesF4Stg, kBN, kStgF4Dn>(ta, tb, g, grid, s)
                                       : launch_gemm_cfg<kKindNvf4, false, kKbF4Up, kStagesF4>(ta, tb, g, grid, s);
     if (KIND == kKindFp8)
         return small_a ? launch_gemm_cfg<kKindFp8, true, 2, kStagesF8Small>(ta, tb, g, grid, s)
@@ -386,7 +398,10 @@ int grid_for(int64_t tiles, int num_sms) {
 }
 
 // Record the end of the kernel just launched (profiling mode only).
+// Also an NVTX mark with the kernel's name (free unless a tracing tool is attached), so a
+// timeline shows which stage each launch of the forward belongs to.
 inline void prof_mark(lmoe_ctx *c, const char *name, cudaStream_t s) {
+    nvtxMarkA(name);
     if (!c->profile || c->nprof >= 32) return;
     c->prof_name[c->nprof] = name;
     cudaEventRecord(c->ev[c->nprof + 1], s);
@@ -673,7 +688,7 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
         static cudaError_t attr_err = cudaSuccess;
         std::call_once(once, [] {
             cudaError_t a = set_smem_attr<kKindNvf4, false, kKbF4Up, kStagesF4>();
-            if (a == cudaSuccess) a = set_smem_attr<kKindNvf4, false, 1, kStagesF4Stg, kBN, true>();
+            if (a == cudaSuccess) a = set_smem_attr<kKindNvf4, false, kKbF4Dn, kStagesF4Stg, kBN, kStgF4Dn>();
             cudaError_t b = set_smem_attr<kKindBf16, false, 1, kStagesBF16>();
             if (a == cudaSuccess) a = set_smem_attr<kKindNvf4, true, 2, kStagesF4Small>();
             if (b == cudaSuccess) b = set_smem_attr<kKindBf16, true, 2, kStagesBF16Small>();
@@ -997,6 +1012,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         return LMOE_EINVAL;
     FaultScope fault_scope;
     const Fault &fault = fault_scope.f;
+    NvtxRange nvtx_range("lmoe_forward");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t *W = static_cast<uint8_t *>(ws);
     auto at = [&](size_t off) { return static_cast<void *>(W + off); };
@@ -1160,7 +1176,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
             g.alpha = c->w2_sdec;
             LMOE_CUDA((launch_gemm<kKindW4A16>(ta, c->tm_w2raw, g, c->num_sms, small_a, s)));
         } else {
-            g.k_tiles = static_cast<int>(cdiv(F, 256 * kb_for(small_a)));
+            g.k_tiles = static_cast<int>(cdiv(F, 256 * (small_a ? kb_for(true) : kKbF4Dn)));
             g.sfa = h_sf;
             g.alpha = c->alpha2;
             LMOE_CUDA((launch_gemm<kKindNvf4>(ta, c->tm_w2, g, c->num_sms, small_a, s)));
