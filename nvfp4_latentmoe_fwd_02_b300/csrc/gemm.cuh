@@ -404,6 +404,60 @@ __device__ __forceinline__ void hquant_pair(const GemmArgs &g, const Tile &tl, c
         s[0] | (s[1] << 8) | (s[2] << 16) | (s[3] << 24);
 }
 
+// The h quantization of hquant_pair from 64 accumulator values (two 32-column chunks), one
+// 16-element block at a time (only one block's temporaries live), with the same results:
+// u = alpha acc and h = u^2 as packed fp32 pairs (each lane the __fmul_rn product), h rounded
+// to bf16; h >= 0, so the block amax is the maximum of the bf16 values (max.bf16x2, exact);
+// then the block scale, its reciprocal from the table, and the E2M1 codes of h * rcp.
+__device__ __forceinline__ void hquant_from_acc(const GemmArgs &g, const Tile &tl, int row, int c0, float a,
+                                                const uint32_t (&r0)[32], const uint32_t (&r1)[32],
+                                                const float *rcp_of) {
+    const int64_t grow = static_cast<int64_t>(tl.a_row0) + row;
+    const int col = tl.n0 + c0;
+    const uint64_t a2 = f2_pack(a, a);
+    uint32_t w[8], s[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const uint32_t *rb = (b < 2 ? r0 : r1) + 16 * (b & 1);
+        uint32_t hb[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float u0, u1, h0, h1;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1])), a2), u0, u1);
+            const uint64_t q = f2_pack(fmaxf(u0, 0.0f), fmaxf(u1, 0.0f));
+            f2_unpack(f2_mul(q, q), h0, h1);
+            hb[i] = cvt_bf16x2(h0, h1);
+        }
+        if (g.dbg) {
+            uint4 *o = reinterpret_cast<uint4 *>(g.dbg + grow * g.N + col + 16 * b);
+            o[0] = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+            o[1] = make_uint4(hb[4], hb[5], hb[6], hb[7]);
+        }
+        if (g.q.zero) { w[2 * b] = w[2 * b + 1] = 0u; s[b] = 0u; continue; }
+        const uint32_t m = max_bf16x2(max_bf16x2(max_bf16x2(hb[0], hb[1]), max_bf16x2(hb[2], hb[3])),
+                                      max_bf16x2(max_bf16x2(hb[4], hb[5]), max_bf16x2(hb[6], hb[7])));
+        const float amax_b = __uint_as_float(max(m & 0xFFFFu, m >> 16) << 16);
+        const uint32_t sf = f32_to_e4m3_satfinite(__fmul_rn(amax_b, g.q.s_enc6));
+        const float rcp = rcp_of[sf];
+        const uint64_t r2 = f2_pack(rcp, rcp);
+        uint32_t by[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float y0, y1;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(hb[i] << 16), __uint_as_float(hb[i] & 0xFFFF0000u)), r2), y0, y1);
+            by[i] = f32x2_to_e2m1x2(y0, y1);
+        }
+        w[2 * b] = (by[0] | (by[1] << 8)) | ((by[2] << 16) | (by[3] << 24));
+        w[2 * b + 1] = (by[4] | (by[5] << 8)) | ((by[6] << 16) | (by[7] << 24));
+        s[b] = sf;
+    }
+    uint4 *qc = reinterpret_cast<uint4 *>(g.q_codes + grow * (g.N / 2) + col / 2);
+    qc[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    qc[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    *reinterpret_cast<uint32_t *>(g.q_sf + sf_atom_offset(grow, col / 16, g.N / 64)) =
+        s[0] | (s[1] << 8) | (s[2] << 16) | (s[3] << 24);
+}
+
 // The output row of each of the eight rows this lane reduces (rows it * 4 + lane / 8), or -1
 // for padding: exchanged once per tile and shared by the tile's chunks.
 __device__ __forceinline__ void combine_rows(const EpiRow &er, int lane, int32_t (&orow)[8]) {
@@ -456,21 +510,29 @@ struct GemmCfg {
     static constexpr int kRawBlock = W4 ? 128 * 32 + 512 : 0;         // E2M1 codes + one scale atom per block
     static constexpr int kRawStage = KB * kRawBlock;
     static constexpr int kEpi0 = W4 ? 8 : 4;                          // first epilogue warp
-    // epilogue warps: 4 for the grouped NVFP4 GEMMs at prefill (one per TMEM lane quadrant,
-    // four 32-column chunks each), 8 otherwise.  At prefill the MMA issuer and the TMA
-    // producer, not the epilogue, set the pace, and every epilogue warp competes with them for
-    // its SM sub-partition's issue slots: 4 warps run the grouped GEMMs faster than 8 or 16.
-    static constexpr int kEpiWarps = NVF4 && !SMALLA ? 4 : 8;
+    // epilogue warps: 4 for the grouped NVFP4 GEMMs at prefill with 128-column tiles (one per
+    // TMEM lane quadrant, four 32-column chunks each: with the MMA issue setting the pace,
+    // more warps only compete with the pipeline threads for issue slots); 8 otherwise (two per
+    // quadrant; for the 256-column NVFP4 tile each holds its 128 accumulator columns in
+    // registers: 16 warps would cap registers at 96 and spill).
+    static constexpr int kEpiWarps = NVF4 && !SMALLA && BN == 128 ? 4 : 8;
+    // NVFP4 tiles 256 columns wide: one accumulator (two of 256 columns would leave no TMEM for
+    // the scale factors); its epilogue copies the accumulator to registers and releases it
+    // before any arithmetic, so the next tile's MMAs wait only for those TMEM loads.
+    static constexpr int kNumAcc = NVF4 && BN == 256 ? 1 : 2;
     static constexpr int kThreads = 32 * (kEpi0 + kEpiWarps);
     static constexpr int kACol = SMALLA ? kABoxBytes : kTileBytes;   // A bytes per column block
     static constexpr int kAStage = KB * kACol;
     static constexpr int kBStage = KB * BN * 128;                     // B tile: BN rows of 128 bytes
-    static constexpr int kSfStage = NVF4 ? KB * kSfStageBytes : 0;   // per operand
+    static constexpr int kSfStageA = NVF4 ? KB * kSfStageBytes : 0;              // A scale atoms
+    static constexpr int kSfStageB = NVF4 ? KB * kSfStageBytes * (BN / 128) : 0; // B: one atom per 128 rows
     static constexpr int kSlack = SMALLA ? kTileBytes - kABoxBytes : 0;
     static constexpr int kElemsPerBlock = NVF4 ? 256 : (KIND == kKindFp8 ? 128 : 64);
     static constexpr int kTmaXPerBlock = (KIND == kKindBf16 || W4) ? 64 : 128;  // tensor-map x units per block
     static constexpr int kStepsPerBlock = 4;                          // MMA K steps per block
-    static constexpr int kSfCols = NVF4 ? 32 * KB : 0;                // TMEM columns per stage
+    // TMEM columns per stage: 4 per K step for A (128 rows), 4 per 128 rows of B
+    static constexpr int kSfColsA = NVF4 ? 16 * KB : 0;
+    static constexpr int kSfCols = NVF4 ? 16 * KB * (1 + BN / 128) : 0;
     static constexpr bool kStagedCombine = NVF4 && !SMALLA && STG;    // combine via smem staging
     static constexpr int kStgBytes = kStagedCombine ? kEpiWarps * 4096 : 0;   // one 4 KB buffer per epilogue warp
 };
@@ -478,7 +540,7 @@ struct GemmCfg {
 template <int KIND, bool SMALLA, int KB, int BN = kBN, bool STG = false>
 constexpr int gemm_smem_bytes(int stages) {
     using C = GemmCfg<KIND, SMALLA, KB, BN, STG>;
-    return 1024 + stages * (C::kAStage + C::kBStage + 2 * C::kSfStage) + C::kSlack + 256 +
+    return 1024 + stages * (C::kAStage + C::kBStage + C::kSfStageA + C::kSfStageB) + C::kSlack + 256 +
            stages * C::kRawStage +
            (C::kTables ? static_cast<int>((sizeof(SmemTables) + 15) & ~static_cast<size_t>(15)) : 0) +
            C::kStgBytes + (C::W4 ? 1024 : 0);
@@ -533,6 +595,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
                 const GemmArgs g) {
     using C = GemmCfg<KIND, SMALLA, KB, BN, STG>;
     static_assert(BN == 128 || (BN == 256 && (KIND == kKindBf16 || KIND == kKindFp8)) ||
+                      (BN == 256 && KIND == kKindNvf4 && !SMALLA && !STG) ||
                       (BN == 64 && KIND == kKindBf16 && SMALLA), "tile width");
     constexpr bool NVF4 = C::NVF4;
     constexpr bool W4 = C::W4;
@@ -543,8 +606,8 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
     uint8_t *sA = smem;
     uint8_t *sB = sA + STAGES * C::kAStage + C::kSlack;
     uint8_t *sSFA = sB + STAGES * C::kBStage;
-    uint8_t *sSFB = sSFA + STAGES * C::kSfStage;
-    uint8_t *sRaw = sSFB + STAGES * C::kSfStage;              // W4A16: raw weight blocks
+    uint8_t *sSFB = sSFA + STAGES * C::kSfStageA;
+    uint8_t *sRaw = sSFB + STAGES * C::kSfStageB;             // W4A16: raw weight blocks
     uint64_t *bars = reinterpret_cast<uint64_t *>(sRaw + STAGES * C::kRawStage);
     uint64_t *full = bars, *empty = bars + STAGES, *sfready = bars + 2 * STAGES;
     uint64_t *sffull = bars + 3 * STAGES;   // NVFP4: the stage's scale atoms have landed
@@ -559,7 +622,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
 
     constexpr uint32_t kAccCols = BN;
     constexpr uint32_t kTmemCols = NVF4 ? 512 : 2 * BN;
-    constexpr uint32_t kSfCol0 = 2 * kAccCols;
+    constexpr uint32_t kSfCol0 = C::kNumAcc * kAccCols;
     static_assert(!NVF4 || kSfCol0 + STAGES * C::kSfCols <= 512, "TMEM budget");
     static_assert(4 * STAGES + 8 <= 32, "barrier area");
     static_assert(!W4 || kEpi0 == 2 + kConvWarps, "warp roles");
@@ -595,7 +658,9 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *s_tmem;
+    // A CTA that allocates all 512 columns (the NVFP4 kernels) always gets lane 0, column 0:
+    // a compile-time base lets every TMEM operand stay warp-uniform.
+    const uint32_t tmem = kTmemCols == 512 ? 0u : *s_tmem;
 
     const int num_tiles = g.grouped ? tb->mt[g.E] * g.n_tiles
                                     : g.m_tiles * g.n_tiles * g.k_splits;
@@ -641,10 +706,18 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
                 if (NVF4) {
                     // the scale atoms first, on their own barrier: they land ahead of the
                     // operand tiles, so their smem -> TMEM copies are off the critical path
+                    // (B: the atoms of each 128-row block of the tile, [block][K step][512 B])
                     uint64_t *sb = &sffull[stage];
-                    mbar_arrive_expect_tx_p(leader, sb, 2 * nsteps * 512);
-                    bulk_load_p(leader, sSFA0 + stage * C::kSfStage, sfa_tile + kb0 * 2048, nsteps * 512, sb);
-                    bulk_load_p(leader, sSFB0 + stage * C::kSfStage, sfb_tile + kb0 * 2048, nsteps * 512, sb);
+                    mbar_arrive_expect_tx_p(leader, sb, (1 + BN / 128) * nsteps * 512);
+                    bulk_load_p(leader, sSFA0 + stage * C::kSfStageA, sfa_tile + kb0 * 2048, nsteps * 512, sb);
+                    // (a 256-column tile whose second half lies past N re-reads the last block,
+                    // so no copy leaves the expert's weights; those columns are never stored)
+#pragma unroll
+                    for (int h = 0; h < BN / 128; ++h)
+                        bulk_load_p(leader, sSFB0 + stage * C::kSfStageB + h * (4 * KB * 512),
+                                    sfb_tile + static_cast<size_t>(min(h, g.NB - 1 - (tl.n0 >> 7))) * K64 * 512 +
+                                        kb0 * 2048,
+                                    nsteps * 512, sb);
                 }
                 mbar_arrive_expect_tx_p(leader, fb, KB * (C::kACol + BN * 128));
 #pragma unroll
@@ -652,10 +725,12 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
                     const int kx = (kb0 + b) * C::kTmaXPerBlock;
                     const int kxa = g.a_kwrap > 0 ? kx % g.a_kwrap : kx;
                     tma_load_2d_p(leader, a_st + b * C::kACol, &tmA, fb, kxa, tl.a_row0);
-                    if (NVF4)   // weight codes in tile order: box (expert, row block, column block)
-                        tma_load_2d_p(leader, b_st + b * (BN * 128), &tmB, fb, 0,
-                                      ((tl.e * g.NB + (tl.n0 >> 7)) * g.b_kt + kb0 + b) * 128);
-                    else
+                    if (NVF4) {   // weight codes in tile order: box (expert, row block, column block)
+#pragma unroll
+                        for (int h = 0; h < BN / 128; ++h)
+                            tma_load_2d_p(leader, b_st + b * (BN * 128) + h * kTileBytes, &tmB, fb, 0,
+                                          ((tl.e * g.NB + min((tl.n0 >> 7) + h, g.NB - 1)) * g.b_kt + kb0 + b) * 128);
+                    } else
                         tma_load_2d_p(leader, b_st + b * (BN * 128), &tmB, fb, kx, tl.b_row0);
                 }
                 issued |= 1u << stage;
@@ -690,8 +765,8 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
         if (g.inject_wait) role_wait(drain, 0, s_abort, g.err, g.wait_limit);
         for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x, ++it) {
             const Tile tl = decode_tile(g, tb, t);
-            const int acc = it & 1;
-            const uint32_t aphase = (it >> 1) & 1;
+            const int acc = C::kNumAcc == 2 ? (it & 1) : 0;
+            const uint32_t aphase = C::kNumAcc == 2 ? ((it >> 1) & 1) : (it & 1);
             if (!role_wait(&tempty[acc], aphase ^ 1, s_abort, g.err, g.wait_limit)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem + acc * kAccCols;
@@ -711,7 +786,8 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
                         if (kk < nsteps)
                             mma_nvf4_p(leader, d_tmem, ad + (((kk >> 2) * C::kACol + (kk & 3) * 32) >> 4),
                                        bd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4), idesc,
-                                       sf_t + kk * 4, sf_t + 16 * KB + kk * 4, (acc_flag0 | kk) ? 1u : 0u);
+                                       sf_t + kk * 4, sf_t + C::kSfColsA + kk * 4 * (BN / 128),
+                                       (acc_flag0 | kk) ? 1u : 0u);
                     }
                 } else if constexpr (W4) {
                     const int nb = min(KB, K64 - kt * KB);    // 64-element blocks present
@@ -770,7 +846,9 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
             const uint32_t leader = elect_leader();
             const bool is_b = warp == 3;
             const uint64_t sfdesc0 = sdesc_sf(smem_u32(is_b ? sSFB : sSFA));
-            const uint32_t col_off = is_b ? 16 * KB : 0;
+            const uint32_t col_off = is_b ? C::kSfColsA : 0;
+            const int nblk = is_b ? BN / 128 : 1;              // 128-row atoms per K step
+            const int sf_stage = is_b ? C::kSfStageB : C::kSfStageA;
             int stage = 0;
             uint32_t phase = 0;
             for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x) {
@@ -781,10 +859,14 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
                     tc_fence_after();
                     const int nsteps = min(4 * KB, K64 - 4 * kt * KB);
                     const uint32_t sf_t = tmem + kSfCol0 + stage * C::kSfCols + col_off;
-                    const uint64_t sfd = sfdesc0 + ((stage * C::kSfStage) >> 4);
+                    const uint64_t sfd = sfdesc0 + ((stage * sf_stage) >> 4);
+                    // K step kk of 128-row block h: 4 columns at kk * 4 * nblk + 4 h (so a step's
+                    // scales of B rows 0..255 sit in 8 consecutive columns), from smem atom (h, kk)
 #pragma unroll
                     for (int kk = 0; kk < 4 * KB; ++kk)
-                        if (kk < nsteps) tmem_cp_sf_p(leader, sf_t + kk * 4, sfd + kk * (512 >> 4));
+                        for (int h = 0; h < nblk; ++h)
+                            if (kk < nsteps)
+                                tmem_cp_sf_p(leader, sf_t + kk * 4 * nblk + h * 4, sfd + (h * 4 * KB + kk) * (512 >> 4));
                     mma_commit_p(leader, &sfready[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
@@ -833,8 +915,8 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
                 tn = decode_tile(g, tb, t + gridDim.x);
                 en = epilogue_row(g, tn, row);
             }
-            const int acc = it & 1;
-            const uint32_t aphase = (it >> 1) & 1;
+            const int acc = C::kNumAcc == 2 ? (it & 1) : 0;
+            const uint32_t aphase = C::kNumAcc == 2 ? ((it >> 1) & 1) : (it & 1);
             // A warp whose 32 rows are all past the tile's valid rows reads nothing; it still
             // waits for the accumulator before releasing it, which keeps the release phases
             // of all four warps in step.
@@ -842,6 +924,30 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
             if (!role_wait(&tfull[acc], aphase, s_abort, g.err, g.wait_limit)) break;
             tc_fence_after();
             const uint32_t taddr = tmem + acc * kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
+            if constexpr (C::kNumAcc == 1) {
+                // 256-column NVFP4 tile (latent-up only): this warp's accumulator columns go to
+                // registers and the accumulator is released at once (the next tile's MMAs wait
+                // only for these loads); then h = bf16(relu(alpha acc)^2) and its quantization
+                uint32_t r[kChunks][32];
+                if (live) {
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c) tmem_ld32(taddr + (ch0 + c) * 32, r[c]);
+                    tmem_wait_ld();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[acc]);
+                if (live && er.valid) {
+#pragma unroll
+                    for (int c = 0; c < kChunks; c += 2) {
+                        if ((ch0 + c + 2) * 32 <= tl.cols)
+                            hquant_from_acc(g, tl, row, (ch0 + c) * 32, er.alpha, r[c], r[c + 1], rcp_of);
+                    }
+                }
+                tl = tn;
+                er = en;
+                continue;
+            }
             if (live) {
                 if (C::kStagedCombine && g.epi == EPI_COMBINE) combine_rows(er, lane, orow);
                 if constexpr (kChunks == 1) {

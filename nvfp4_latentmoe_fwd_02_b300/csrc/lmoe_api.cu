@@ -31,11 +31,13 @@ using namespace lmoe;
 
 namespace {
 
-// NVFP4 prefill, latent-up: two 128-byte column blocks (72 KB) per stage, three stages.  The
-// same bytes in flight as six one-block stages, but half the barrier handshakes, MMA commits
-// and scale-copy commits per byte (T = 4096, Zipf 1.1: 424 -> 381 us).
-constexpr int kKbF4Up = 2;
-constexpr int kStagesF4 = 3;
+// NVFP4 prefill, latent-up: 128 x 256 tiles, one N = 256 MMA per K step (each tcgen05.mma
+// costs its issuing thread ~85 cycles whatever its N, so wider MMAs feed the tensor core
+// faster); one accumulator, one 128-byte column block (54 KB with the scale atoms) per stage,
+// four stages.
+constexpr int kKbF4Up = 1;
+constexpr int kStagesF4 = 4;
+constexpr int kBNF4Up = 256;
 // NVFP4 prefill, latent-down: one column block per stage, five stages, + 16 KB of combine
 // staging (two blocks per stage fit only without the staging, which costs more: 431 -> 487 us)
 constexpr int kKbF4Dn = 1;
@@ -362,7 +364,7 @@ cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const Gemm
     if (KIND == kKindNvf4)
         return small_a ? launch_gemm_cfg<kKindNvf4, true, 2, kStagesF4Small>(ta, tb, g, grid, s)
                : g.epi == EPI_COMBINE ? launch_gemm_cfg<kKindNvf4, false, kKbF4Dn, kStagesF4Stg, kBN, kStgF4Dn>(ta, tb, g, grid, s)
-                                      : launch_gemm_cfg<kKindNvf4, false, kKbF4Up, kStagesF4>(ta, tb, g, grid, s);
+                                      : launch_gemm_cfg<kKindNvf4, false, kKbF4Up, kStagesF4, kBNF4Up>(ta, tb, g, grid, s);
     if (KIND == kKindFp8)
         return small_a ? launch_gemm_cfg<kKindFp8, true, 2, kStagesF8Small>(ta, tb, g, grid, s)
                        : launch_gemm_cfg<kKindFp8, false, 1, kStagesWide, kBNWide>(ta, tb, g, grid, s);
@@ -687,7 +689,7 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
         static std::once_flag once;
         static cudaError_t attr_err = cudaSuccess;
         std::call_once(once, [] {
-            cudaError_t a = set_smem_attr<kKindNvf4, false, kKbF4Up, kStagesF4>();
+            cudaError_t a = set_smem_attr<kKindNvf4, false, kKbF4Up, kStagesF4, kBNF4Up>();
             if (a == cudaSuccess) a = set_smem_attr<kKindNvf4, false, kKbF4Dn, kStagesF4Stg, kBN, kStgF4Dn>();
             cudaError_t b = set_smem_attr<kKindBf16, false, 1, kStagesBF16>();
             if (a == cudaSuccess) a = set_smem_attr<kKindNvf4, true, 2, kStagesF4Small>();
@@ -1133,8 +1135,8 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         GemmArgs g;
         std::memset(&g, 0, sizeof(g));
         g.M = static_cast<int>(L.R); g.N = F; g.K = l;
-        g.bn = kBN;
-        g.n_tiles = static_cast<int>(cdiv(F, kBN));
+        g.bn = (c->w4a16 || small_a) ? kBN : kBNF4Up;   // the launch_gemm configuration's tile width
+        g.n_tiles = static_cast<int>(cdiv(F, g.bn));
         g.grouped = 1; g.E = E; g.mt_start = mt; g.seg_start = seg; g.counts = counts;
         g.sfb = c->w1_sf; g.NB = static_cast<int>(cdiv(F, 128));
         g.b_kt = static_cast<int>(cdiv(l, 256));
