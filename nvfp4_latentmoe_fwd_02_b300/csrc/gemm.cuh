@@ -595,7 +595,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
                 const GemmArgs g) {
     using C = GemmCfg<KIND, SMALLA, KB, BN, STG>;
     static_assert(BN == 128 || (BN == 256 && (KIND == kKindBf16 || KIND == kKindFp8)) ||
-                      (BN == 256 && KIND == kKindNvf4 && !SMALLA && !STG) ||
+                      (BN == 256 && KIND == kKindNvf4 && !SMALLA) ||
                       (BN == 64 && KIND == kKindBf16 && SMALLA), "tile width");
     constexpr bool NVF4 = C::NVF4;
     constexpr bool W4 = C::W4;
@@ -925,9 +925,10 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
             tc_fence_after();
             const uint32_t taddr = tmem + acc * kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
             if constexpr (C::kNumAcc == 1) {
-                // 256-column NVFP4 tile (latent-up only): this warp's accumulator columns go to
-                // registers and the accumulator is released at once (the next tile's MMAs wait
-                // only for these loads); then h = bf16(relu(alpha acc)^2) and its quantization
+                // 256-column NVFP4 tile: this warp's accumulator columns go to registers and
+                // the accumulator is released at once (the next tile's MMAs wait only for these
+                // loads); then the latent-up's h = bf16(relu(alpha acc)^2) and its quantization,
+                // or the latent-down's weighted combine
                 uint32_t r[kChunks][32];
                 if (live) {
 #pragma unroll
@@ -937,7 +938,14 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[acc]);
-                if (live && er.valid) {
+                if constexpr (C::kStagedCombine) {
+                    if (live) {
+                        combine_rows(er, lane, orow);
+#pragma unroll
+                        for (int c = 0; c < kChunks; ++c)
+                            if ((ch0 + c) * 32 < tl.cols) combine_staged(g, tl, er, (ch0 + c) * 32, r[c], stg, lane, orow);
+                    }
+                } else if (live && er.valid) {
 #pragma unroll
                     for (int c = 0; c < kChunks; c += 2) {
                         if ((ch0 + c + 2) * 32 <= tl.cols)

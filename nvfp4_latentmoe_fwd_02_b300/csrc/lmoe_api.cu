@@ -38,11 +38,12 @@ namespace {
 constexpr int kKbF4Up = 1;
 constexpr int kStagesF4 = 4;
 constexpr int kBNF4Up = 256;
-// NVFP4 prefill, latent-down: one column block per stage, five stages, + 16 KB of combine
-// staging (two blocks per stage fit only without the staging, which costs more: 431 -> 487 us)
+// NVFP4 prefill, latent-down: 128 x 256 tiles like the latent-up, three 54 KB stages + 32 KB
+// of combine staging (8 epilogue warps x 4 KB)
 constexpr int kKbF4Dn = 1;
-constexpr int kStagesF4Stg = 5;
+constexpr int kStagesF4Stg = 3;
 constexpr bool kStgF4Dn = true;
+constexpr int kBNF4Dn = 256;
 constexpr int kStagesBF16 = 6;
 constexpr int kStagesF4Small = 4;     // decode (T <= 32): 4 KB A boxes, 2 column blocks per stage
 constexpr int kStagesBF16Small = 5;
@@ -363,7 +364,7 @@ cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const Gemm
                         bool small_a, cudaStream_t s) {
     if (KIND == kKindNvf4)
         return small_a ? launch_gemm_cfg<kKindNvf4, true, 2, kStagesF4Small>(ta, tb, g, grid, s)
-               : g.epi == EPI_COMBINE ? launch_gemm_cfg<kKindNvf4, false, kKbF4Dn, kStagesF4Stg, kBN, kStgF4Dn>(ta, tb, g, grid, s)
+               : g.epi == EPI_COMBINE ? launch_gemm_cfg<kKindNvf4, false, kKbF4Dn, kStagesF4Stg, kBNF4Dn, kStgF4Dn>(ta, tb, g, grid, s)
                                       : launch_gemm_cfg<kKindNvf4, false, kKbF4Up, kStagesF4, kBNF4Up>(ta, tb, g, grid, s);
     if (KIND == kKindFp8)
         return small_a ? launch_gemm_cfg<kKindFp8, true, 2, kStagesF8Small>(ta, tb, g, grid, s)
@@ -690,7 +691,7 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
         static cudaError_t attr_err = cudaSuccess;
         std::call_once(once, [] {
             cudaError_t a = set_smem_attr<kKindNvf4, false, kKbF4Up, kStagesF4, kBNF4Up>();
-            if (a == cudaSuccess) a = set_smem_attr<kKindNvf4, false, kKbF4Dn, kStagesF4Stg, kBN, kStgF4Dn>();
+            if (a == cudaSuccess) a = set_smem_attr<kKindNvf4, false, kKbF4Dn, kStagesF4Stg, kBNF4Dn, kStgF4Dn>();
             cudaError_t b = set_smem_attr<kKindBf16, false, 1, kStagesBF16>();
             if (a == cudaSuccess) a = set_smem_attr<kKindNvf4, true, 2, kStagesF4Small>();
             if (b == cudaSuccess) b = set_smem_attr<kKindBf16, true, 2, kStagesBF16Small>();
@@ -1165,8 +1166,8 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         GemmArgs g;
         std::memset(&g, 0, sizeof(g));
         g.M = static_cast<int>(L.R); g.N = l; g.K = F;
-        g.bn = kBN;
-        g.n_tiles = static_cast<int>(cdiv(l, kBN));
+        g.bn = (c->w4a16 || small_a) ? kBN : kBNF4Dn;   // the launch_gemm configuration's tile width
+        g.n_tiles = static_cast<int>(cdiv(l, g.bn));
         g.grouped = 1; g.E = E; g.mt_start = mt; g.seg_start = seg; g.counts = counts;
         g.sfb = c->w2_sf; g.NB = static_cast<int>(cdiv(l, 128));
         g.b_kt = static_cast<int>(cdiv(F, 256));
