@@ -102,6 +102,10 @@ struct GemmArgs {
     long long wait_limit;        // SM cycles a pipeline wait may take before the CTA gives up
     int inject_wait;             // fault injection: the MMA role first waits on a barrier that
                                  // nothing arrives at, so the wait runs out (LMOE_FAULT=wait)
+    int preload;                 // decode launches: issue the weight (B) loads of the first
+                                 // ring pass before waiting on the previous grid (the weights,
+                                 // and for grouped launches the segment tables, are complete
+                                 // before that grid began)
 };
 
 struct Tile {
@@ -644,17 +648,58 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
     }
     if (warp == 0 && lane == 0) { prefetch_tmap(&tmA); prefetch_tmap(&tmB); }
     if (warp == 1) { tmem_alloc(s_tmem, kTmemCols); tmem_relinquish(); }
+    auto load_tables = [&]() {
+        if (C::kTables && g.grouped) {
+            for (int i = threadIdx.x; i <= g.E; i += blockDim.x) {
+                tb->mt[i] = __ldg(g.mt_start + i);
+                if (i < g.E) tb->cnt[i] = __ldg(g.counts + i);
+            }
+        }
+    };
+    constexpr bool kPreload = SMALLA && !W4;
+    int npre = 0;           // stages of this CTA's first tile whose B was issued before the wait
+    if (kPreload && g.preload) {
+        load_tables();
+        __syncthreads();    // tables and barrier initialisation visible to the producer warp
+        if (warp == 0) {
+            const uint32_t leader = elect_leader();
+            const int ntiles = g.grouped ? tb->mt[g.E] * g.n_tiles : g.m_tiles * g.n_tiles * g.k_splits;
+            if (static_cast<int>(blockIdx.x) < ntiles) {
+                const Tile tl = decode_tile(g, tb, blockIdx.x);
+                const int K64p = g.K / 64;
+                npre = min(STAGES, tl.kt1 - tl.kt0);
+                for (int s = 0; s < npre; ++s) {
+                    const int kb0 = (tl.kt0 + s) * KB;
+                    const uint32_t b_st = smem_u32(sB) + s * C::kBStage;
+                    if constexpr (NVF4) {
+                        // the stage's arrival, counting the scale atoms of A still to come
+                        const int nsteps = min(4 * KB, K64p - 4 * kb0);
+                        mbar_arrive_expect_tx_p(leader, &sffull[s], (1 + BN / 128) * nsteps * 512);
+                        const uint8_t *sfb_tile = g.sfb + (static_cast<size_t>(tl.e) * g.NB + (tl.n0 >> 7)) * K64p * 512;
+                        bulk_load_p(leader, smem_u32(sSFB) + s * C::kSfStageB, sfb_tile + kb0 * 2048, nsteps * 512,
+                                    &sffull[s]);
+                    }
+                    // the stage's arrival, counting the A bytes still to come
+                    mbar_arrive_expect_tx_p(leader, &full[s], KB * (C::kACol + BN * 128));
+#pragma unroll
+                    for (int b = 0; b < KB; ++b) {
+                        if constexpr (NVF4)
+                            tma_load_2d_p(leader, b_st + b * (BN * 128), &tmB, &full[s], 0,
+                                          ((tl.e * g.NB + (tl.n0 >> 7)) * g.b_kt + kb0 + b) * 128);
+                        else
+                            tma_load_2d_p(leader, b_st + b * (BN * 128), &tmB, &full[s],
+                                          (kb0 + b) * C::kTmaXPerBlock, tl.b_row0);
+                    }
+                }
+            }
+        }
+    }
     pdl_wait();      // the previous kernel's outputs (tables, activations) are complete
     pdl_trigger();
     if (W4)
         for (int i = threadIdx.x; i < 256; i += blockDim.x)
             lut[i] = e2m1_bf16_bits(i & 15u) | (e2m1_bf16_bits(i >> 4) << 16);
-    if (C::kTables && g.grouped) {
-        for (int i = threadIdx.x; i <= g.E; i += blockDim.x) {
-            tb->mt[i] = __ldg(g.mt_start + i);
-            if (i < g.E) tb->cnt[i] = __ldg(g.counts + i);
-        }
-    }
+    if (!(kPreload && g.preload)) load_tables();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -672,11 +717,13 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
         const uint32_t leader = elect_leader();
         int stage = 0;
         uint32_t phase = 0;
-        uint32_t issued = 0, issued_phase = 0;   // per stage: ever issued / phase of last issue
+        // per stage: ever issued / phase of last issue (a preloaded stage counts as issued)
+        uint32_t issued = (1u << npre) - 1u, issued_phase = 0;
         const uint32_t sA0 = smem_u32(sA), sB0 = smem_u32(sB);
         const uint32_t sSFA0 = smem_u32(sSFA), sSFB0 = smem_u32(sSFB);
         for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x) {
             const Tile tl = decode_tile(g, tb, t);
+            const bool first = t == static_cast<int>(blockIdx.x);
             const uint8_t *sfa_tile = NVF4 ? g.sfa + static_cast<size_t>(tl.a_row0 >> 7) * K64 * 512 : nullptr;
             const uint8_t *sfb_tile = (NVF4 || W4) ? g.sfb + (static_cast<size_t>(tl.e) * g.NB + (tl.n0 >> 7)) * K64 * 512 : nullptr;
             for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
@@ -703,28 +750,32 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
                     continue;
                 }
                 const int nsteps = NVF4 ? min(4 * KB, K64 - 4 * kb0) : 4 * KB;
+                // a stage whose B went out before the grid dependency wait (first tile only):
+                // its arrivals are made, only A (and A's scale atoms) remain
+                const bool pre = first && kt - tl.kt0 < npre;
                 if (NVF4) {
                     // the scale atoms first, on their own barrier: they land ahead of the
                     // operand tiles, so their smem -> TMEM copies are off the critical path
                     // (B: the atoms of each 128-row block of the tile, [block][K step][512 B])
                     uint64_t *sb = &sffull[stage];
-                    mbar_arrive_expect_tx_p(leader, sb, (1 + BN / 128) * nsteps * 512);
+                    if (!pre) mbar_arrive_expect_tx_p(leader, sb, (1 + BN / 128) * nsteps * 512);
                     bulk_load_p(leader, sSFA0 + stage * C::kSfStageA, sfa_tile + kb0 * 2048, nsteps * 512, sb);
                     // (a 256-column tile whose second half lies past N re-reads the last block,
                     // so no copy leaves the expert's weights; those columns are never stored)
 #pragma unroll
-                    for (int h = 0; h < BN / 128; ++h)
+                    for (int h = 0; h < BN / 128 && !pre; ++h)
                         bulk_load_p(leader, sSFB0 + stage * C::kSfStageB + h * (4 * KB * 512),
                                     sfb_tile + static_cast<size_t>(min(h, g.NB - 1 - (tl.n0 >> 7))) * K64 * 512 +
                                         kb0 * 2048,
                                     nsteps * 512, sb);
                 }
-                mbar_arrive_expect_tx_p(leader, fb, KB * (C::kACol + BN * 128));
+                if (!pre) mbar_arrive_expect_tx_p(leader, fb, KB * (C::kACol + BN * 128));
 #pragma unroll
                 for (int b = 0; b < KB; ++b) {
                     const int kx = (kb0 + b) * C::kTmaXPerBlock;
                     const int kxa = g.a_kwrap > 0 ? kx % g.a_kwrap : kx;
                     tma_load_2d_p(leader, a_st + b * C::kACol, &tmA, fb, kxa, tl.a_row0);
+                    if (pre) continue;
                     if (NVF4) {   // weight codes in tile order: box (expert, row block, column block)
 #pragma unroll
                         for (int h = 0; h < BN / 128; ++h)

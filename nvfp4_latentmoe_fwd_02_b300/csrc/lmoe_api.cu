@@ -360,8 +360,13 @@ cudaError_t launch_gemm_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const 
 // small_a: every tile has at most 32 valid A rows (T <= 32); such launches use two column
 // blocks per stage, and g.k_tiles must count stages of kb_for(true) blocks.
 template <int KIND>
-cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g, int grid,
+cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &g_in, int grid,
                         bool small_a, cudaStream_t s) {
+    // decode launches issue their first weight stages before waiting on the previous kernel:
+    // the weights are static and every grouped launch's segment tables come from the router,
+    // which completed before the previous kernel of the forward began
+    GemmArgs g = g_in;
+    g.preload = small_a && KIND != kKindW4A16 ? 1 : 0;
     if (KIND == kKindNvf4)
         return small_a ? launch_gemm_cfg<kKindNvf4, true, 2, kStagesF4Small>(ta, tb, g, grid, s)
                : g.epi == EPI_COMBINE ? launch_gemm_cfg<kKindNvf4, false, kKbF4Dn, kStagesF4Stg, kBNF4Dn, kStgF4Dn>(ta, tb, g, grid, s)
