@@ -95,7 +95,8 @@ typedef struct {
     int weight_blocks_2d;
     /* Expert arithmetic: 0 = W4A4 (z and h quantized to NVFP4, native FP4 MMAs); 1 = W4A16
      * (NVIDIA AI releases Nemotron 3 Ultra, quantization paragraph: the Hopper form of the
-     * checkpoint): NVFP4 weights decoded to bf16 in shared memory and bf16 z and h, with
+     * checkpoint): NVFP4 weights decoded to bf16 on chip (in tensor memory at T <= 32, in
+     * shared memory above) and bf16 z and h, with
      * u = s_w1 (z . dq(W1q)), h = bf16(relu(u)^2), o = s_w2 (h . dq(W2q)). */
     int expert_w4a16;
 } lmoe_weights;

@@ -41,8 +41,9 @@
 namespace lmoe {
 
 // Operand kinds (template argument KIND).
-// kKindW4A16: bf16 activations times NVFP4 weights that converter warps decode into bf16 tiles
-// in shared memory (E2M1 x E4M3 is exact in bf16), then kind::f16 MMAs.
+// kKindW4A16 (above decode size; decode has its own kernel, w4dec.cuh): bf16 activations times
+// NVFP4 weights that converter warps decode into bf16 tiles in shared memory (E2M1 x E4M3 is
+// exact in bf16), then kind::f16 MMAs.
 constexpr int kKindBf16 = 0, kKindNvf4 = 1, kKindFp8 = 2, kKindW4A16 = 3;
 
 enum EpiMode : int {
@@ -159,14 +160,15 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &g, const SmemTables 
 }
 
 // Pipeline wait: gives up after `limit` SM cycles (recording LMOE_ETIMEOUT and telling the
-// other roles to stop), or as soon as another role of the CTA has given up.
+// other roles to stop), or as soon as another role of the CTA has given up.  sleep_ns > 0: the
+// waiting thread is suspended between polls (mbar_try_wait_sleep).
 __device__ __forceinline__ bool role_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          unsigned *err, long long limit) {
+                                          unsigned *err, long long limit, uint32_t sleep_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     if (limit <= 0) limit = kWaitLimitCycles;       // unset: the library's default bound
     const long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (sleep_ns ? mbar_try_wait_sleep(bar, parity, sleep_ns) : mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
         if (clock64() - t0 > limit) {
             *abort = 1;

@@ -26,6 +26,7 @@
 #include "moe.cuh"
 #include "nvfp4.cuh"
 #include "router.cuh"
+#include "w4dec.cuh"
 
 using namespace lmoe;
 
@@ -52,8 +53,7 @@ constexpr int kStagesF8Small = 5;
 constexpr int kStagesWide = 4;        // bf16 / fp8 with 256-column tiles: 48 KB per stage
 constexpr int kBNWide = 256;
 constexpr int kBNNarrow = 64;         // bf16 GEMMs at decode whose 128-column tiles leave SMs idle
-constexpr int kStagesW4 = 5;          // W4A16: bf16 A + decoded bf16 B + raw E2M1 block per stage
-constexpr int kStagesW4Small = 4;
+constexpr int kStagesW4 = 5;          // W4A16 above decode: bf16 A + decoded bf16 B + raw E2M1 block per stage
 constexpr int kSmallAMaxT = 32;
 
 inline int kb_for(bool small_a) { return small_a ? 2 : 1; }   // column blocks per stage
@@ -374,13 +374,26 @@ cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const Gemm
     if (KIND == kKindFp8)
         return small_a ? launch_gemm_cfg<kKindFp8, true, 2, kStagesF8Small>(ta, tb, g, grid, s)
                        : launch_gemm_cfg<kKindFp8, false, 1, kStagesWide, kBNWide>(ta, tb, g, grid, s);
-    if (KIND == kKindW4A16)
-        return small_a ? launch_gemm_cfg<kKindW4A16, true, 2, kStagesW4Small>(ta, tb, g, grid, s)
-                       : launch_gemm_cfg<kKindW4A16, false, 1, kStagesW4>(ta, tb, g, grid, s);
+    if (KIND == kKindW4A16)   // (decode: launch_w4dec)
+        return small_a ? cudaErrorInvalidValue : launch_gemm_cfg<kKindW4A16, false, 1, kStagesW4>(ta, tb, g, grid, s);
     if (small_a && g.bn == kBNNarrow)
         return launch_gemm_cfg<kKindBf16, true, 2, kStagesBF16Small, kBNNarrow>(ta, tb, g, grid, s);
     return small_a ? launch_gemm_cfg<kKindBf16, true, 2, kStagesBF16Small>(ta, tb, g, grid, s)
                    : launch_gemm_cfg<kKindBf16, false, 1, kStagesWide, kBNWide>(ta, tb, g, grid, s);
+}
+
+// W4A16 expert GEMM at decode (every expert segment has at most nt <= 32 rows): tx is the bf16
+// activation map with nt-row boxes, tw the expert codes' tile-order map (128-byte swizzle).
+cudaError_t launch_w4dec(const CUtensorMap &tx, const CUtensorMap &tw, const GemmArgs &g_in, int grid, int nt,
+                         cudaStream_t s) {
+    static_assert(w4dec_smem_bytes<16>() <= 232448 && w4dec_smem_bytes<32>() <= 232448, "shared memory budget");
+    GemmArgs g = g_in;
+    g.preload = 1;
+    g.k_tiles = static_cast<int>(cdiv(g.K, 256));   // 256-element chunks per tile
+    return nt <= 16 ? launch_pdl(w4_decode_kernel<16>, dim3(grid), dim3(W4Cfg<16>::kThreads), w4dec_smem_bytes<16>(), s,
+                                 tx, tw, g)
+                    : launch_pdl(w4_decode_kernel<32>, dim3(grid), dim3(W4Cfg<32>::kThreads), w4dec_smem_bytes<32>(), s,
+                                 tx, tw, g);
 }
 
 // K elements per 128-byte column block: 64 (bf16) or 128 (fp8).
@@ -705,8 +718,13 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
             if (a == cudaSuccess) a = set_smem_attr<kKindBf16, false, 1, kStagesWide, kBNWide>();
             if (a == cudaSuccess) a = set_smem_attr<kKindBf16, true, 2, kStagesBF16Small, kBNNarrow>();
             if (a == cudaSuccess) a = set_smem_attr<kKindFp8, false, 1, kStagesWide, kBNWide>();
-            if (a == cudaSuccess) a = set_smem_attr<kKindW4A16, true, 2, kStagesW4Small>();
             if (a == cudaSuccess) a = set_smem_attr<kKindFp8, true, 2, kStagesF8Small>();
+            if (a == cudaSuccess)
+                a = cudaFuncSetAttribute(w4_decode_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         w4dec_smem_bytes<16>());
+            if (a == cudaSuccess)
+                a = cudaFuncSetAttribute(w4_decode_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         w4dec_smem_bytes<32>());
             cudaError_t r = cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  kRouterSmallSmem);
             attr_err = a != cudaSuccess ? a : (b != cudaSuccess ? b : r);
@@ -1053,6 +1071,9 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     const int d = c->d, l = c->l, E = c->E, k = c->k, F = c->ffn;
     const bool small_a = T <= kSmallAMaxT;   // no GEMM tile then has more than 32 valid rows
     const uint32_t a_box = small_a ? kABoxRows : kBM;   // rows of the activation TMA box
+    // W4A16 expert GEMMs: at decode the token rows are the MMA's N (16 or 32; an expert segment
+    // has at most T rows, since a token's k experts are distinct)
+    const uint32_t w4_box = small_a ? (T <= 16 ? 16u : 32u) : kBM;
     if (c->profile) {
         c->nprof = 0;
         cudaEventRecord(c->ev[0], s);
@@ -1135,7 +1156,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     // 5. latent-up grouped GEMM + relu^2 (+ requantize to NVFP4; W4A16: bf16 h)
     {
         CUtensorMap ta;
-        const bool ok = c->w4a16 ? make_map(&ta, true, a_bf16, l, L.R, static_cast<uint64_t>(l) * 2, a_box)
+        const bool ok = c->w4a16 ? make_map(&ta, true, a_bf16, l, L.R, static_cast<uint64_t>(l) * 2, w4_box)
                                  : make_map(&ta, false, a_codes, l / 2, L.R, l / 2, a_box);
         if (!ok) return LMOE_ECUDA;
         GemmArgs g;
@@ -1152,7 +1173,10 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         if (c->w4a16) {
             g.k_tiles = static_cast<int>(cdiv(l / 64, kb_for(small_a)));
             g.epi = EPI_H_BF16; g.out = h_bf16; g.alpha = c->w1_sdec;
-            LMOE_CUDA((launch_gemm<kKindW4A16>(ta, c->tm_w1raw, g, c->num_sms, small_a, s)));
+            if (small_a)
+                LMOE_CUDA(launch_w4dec(ta, c->tm_w1, g, c->num_sms, static_cast<int>(w4_box), s));
+            else
+                LMOE_CUDA((launch_gemm<kKindW4A16>(ta, c->tm_w1raw, g, c->num_sms, small_a, s)));
         } else {
             g.k_tiles = static_cast<int>(cdiv(l, 256 * (small_a ? kb_for(true) : kKbF4Up)));
             g.sfa = a_sf;
@@ -1165,7 +1189,7 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     // 6. latent-down grouped GEMM, routing weight, combine into c_acc
     {
         CUtensorMap ta;
-        const bool ok = c->w4a16 ? make_map(&ta, true, h_bf16, F, L.R, static_cast<uint64_t>(F) * 2, a_box)
+        const bool ok = c->w4a16 ? make_map(&ta, true, h_bf16, F, L.R, static_cast<uint64_t>(F) * 2, w4_box)
                                  : make_map(&ta, false, h_codes, F / 2, L.R, F / 2, a_box);
         if (!ok) return LMOE_ECUDA;
         GemmArgs g;
@@ -1182,7 +1206,10 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         if (c->w4a16) {
             g.k_tiles = static_cast<int>(cdiv(F / 64, kb_for(small_a)));
             g.alpha = c->w2_sdec;
-            LMOE_CUDA((launch_gemm<kKindW4A16>(ta, c->tm_w2raw, g, c->num_sms, small_a, s)));
+            if (small_a)
+                LMOE_CUDA(launch_w4dec(ta, c->tm_w2, g, c->num_sms, static_cast<int>(w4_box), s));
+            else
+                LMOE_CUDA((launch_gemm<kKindW4A16>(ta, c->tm_w2raw, g, c->num_sms, small_a, s)));
         } else {
             g.k_tiles = static_cast<int>(cdiv(F, 256 * (small_a ? kb_for(true) : kKbF4Dn)));
             g.sfa = h_sf;

@@ -62,11 +62,14 @@ def _compare(case, T, seed):
     # the routing weights above 64 tokens and z at small T come from fp32 reductions with
     # atomics: between two runs they may differ in the last bits (and z then in a rare code)
     assert np.allclose(clean["w"], poisoned["w"], rtol=1e-4, atol=1e-6)
-    zc_a, zc_b = clean["zq_codes"].reshape(T, -1), poisoned["zq_codes"].reshape(T, -1)
-    zs_a, zs_b = clean["zq_sf"].reshape(T, -1), poisoned["zq_sf"].reshape(T, -1)
-    same = np.all(zc_a == zc_b, axis=1) & np.all(zs_a == zs_b, axis=1)
-    assert same.mean() >= 0.95
-    assert np.all((zc_a != zc_b).sum(axis=1) <= 16) and np.all((zs_a != zs_b).sum(axis=1) <= 2)
+    if case.w4a16:
+        same = np.ones(T, dtype=bool)       # no activation quantizer in the W4A16 form
+    else:
+        zc_a, zc_b = clean["zq_codes"].reshape(T, -1), poisoned["zq_codes"].reshape(T, -1)
+        zs_a, zs_b = clean["zq_sf"].reshape(T, -1), poisoned["zq_sf"].reshape(T, -1)
+        same = np.all(zc_a == zc_b, axis=1) & np.all(zs_a == zs_b, axis=1)
+        assert same.mean() >= 0.95
+        assert np.all((zc_a != zc_b).sum(axis=1) <= 16) and np.all((zs_a != zs_b).sum(axis=1) <= 2)
     for k in ("y", "c"):
         a, b = clean[k].reshape(T, -1), poisoned[k].reshape(T, -1)
         assert np.isfinite(a).all() and np.isfinite(b).all(), k
@@ -109,3 +112,17 @@ def test_poisoned_workspace_mid(mid, T):
 @pytest.mark.parametrize("T", [8, 4096])
 def test_poisoned_workspace_ultra(ultra, T):
     _compare(ultra, T, 900 + T)
+
+
+@pytest.fixture(scope="module")
+def mid_w4():
+    case = Case(lmoe_synth.Dims(d=1024, l=512, E=32, k=4, ffn=512), seed=9, zipf=1.1, w4a16=True)
+    yield case
+    case.close()
+
+
+# W4A16: the decode kernel (T <= 32) reads 16 or 32 token rows of each expert segment, past the
+# segment's count, into accumulator columns it never stores; T = 40 takes the shared-memory path
+@pytest.mark.parametrize("T", [1, 8, 20, 40])
+def test_poisoned_workspace_w4a16(mid_w4, T):
+    _compare(mid_w4, T, 850 + T)
