@@ -408,73 +408,108 @@ __device__ __forceinline__ void segments_if_last(int units, int *done, const int
     }
 }
 
-// Small T: one block of 256 threads per token (at decode there are few tokens, so the work of
-// one token is spread over eight warps).  G: group sums [T][E][NG] (router_small_kernel); a
-// logit is their sum in ascending group order plus the bias (the canonical order).  Each warp
-// sorts 128 selection keys (4 per lane; E <= 1024), the per-warp top-32 lists are merged
-// pairwise through shared memory, and warp 0 emits the top k (softmax, counts, slot offsets);
-// the last block lays out the segments (when `done` is given).
-constexpr int kTopkThreads = 256;
+// The expert segments laid out by the last of `units` blocks to finish (a whole block: one or
+// two experts per thread, E <= 2 blockDim), the same layout as segments_if_last.
+__device__ __forceinline__ void segments_block_if_last(int units, int *done, const int32_t *counts, int E,
+                                                       int32_t *seg_start, int32_t *mt_start, int32_t *nrows,
+                                                       int *s_flag, int32_t *s_wsum) {
+    __threadfence();                                       // this block's counts are visible
+    __syncthreads();
+    if (threadIdx.x == 0) *s_flag = atomicAdd(done, 1) == units - 1;
+    __syncthreads();
+    if (!*s_flag) return;
+    __threadfence();
+    const int nthr = blockDim.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = nthr >> 5;
+    // expert e = threadIdx.x + j nthr: padded count, block-wide exclusive scan in expert order
+    int p[2], incl[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int e = threadIdx.x + j * nthr;
+        p[j] = e < E ? ((__ldcg(counts + e) + 127) & ~127) : 0;
+        incl[j] = p[j];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl[j], o);
+            if (lane >= o) incl[j] += v;
+        }
+        if (lane == 31) s_wsum[j * nw + warp] = incl[j];
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {                                // 2 nw warp totals, in expert order
+        int run = 0;
+        for (int i = 0; i < 2 * nw; ++i) { const int v = s_wsum[i]; s_wsum[i] = run; run += v; }
+        seg_start[E] = run;
+        mt_start[E] = run >> 7;
+        *nrows = run;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int e = threadIdx.x + j * nthr;
+        if (e < E) {
+            const int st = s_wsum[j * nw + warp] + incl[j] - p[j];
+            seg_start[e] = st;
+            mt_start[e] = st >> 7;
+        }
+    }
+}
+
+// Small T: one block of 512 threads per token, one or two experts per thread (E <= 1024,
+// k <= 32).  G: group sums [T][E][NG] (router_small_kernel); a logit is their sum in ascending
+// group order plus the bias (the canonical order).  Selection by tournament: each warp sorts its
+// keys into a top-32 list in registers (warp_top32), the sixteen lists are merged pairwise to
+// the top 32 of the token (merge_top32, four rounds through shared memory), and warp 0 emits the
+// first k (emit_selection).  The last block lays out the segments (when `done` is given).
+constexpr int kTopkThreads = 512;
 __global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(
     const float *__restrict__ G, int NG, const float *__restrict__ bias, int T, int E, int k,
     int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts,
     int32_t *__restrict__ slot_off, int *__restrict__ done, int32_t *__restrict__ seg_start,
     int32_t *__restrict__ mt_start, int32_t *__restrict__ nrows) {
-    __shared__ uint64_t lists[8][32];
+    constexpr int nw = kTopkThreads / 32;
+    __shared__ uint64_t lists[nw][32];
+    __shared__ int32_t wsum[2 * nw];
+    __shared__ int s_flag;
     pdl_wait();
     pdl_trigger();
     const int t = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // the group sums of one expert are contiguous: every load of this thread is independent
     const float *gt = G + static_cast<int64_t>(t) * E * NG;
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    if (NG % 4 == 0) {
-        for (int g0 = 0; g0 < NG; g0 += 4) {
-            float4 v[4];
+    uint64_t key[2];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int e = warp * 128 + 4 * lane + r;
-                v[r] = e < E ? __ldg(reinterpret_cast<const float4 *>(gt + static_cast<int64_t>(e) * NG + g0))
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < 2; ++j) {
+        const int e = threadIdx.x + j * kTopkThreads;
+        float acc = 0.0f;
+        if (e < E) {
+            if (NG % 4 == 0) {
+                for (int g0 = 0; g0 < NG; g0 += 4) {
+                    const float4 v = __ldg(reinterpret_cast<const float4 *>(gt + static_cast<int64_t>(e) * NG + g0));
+                    acc = __fadd_rn(acc, v.x); acc = __fadd_rn(acc, v.y);
+                    acc = __fadd_rn(acc, v.z); acc = __fadd_rn(acc, v.w);
+                }
+            } else {
+                for (int g = 0; g < NG; ++g) acc = __fadd_rn(acc, __ldg(gt + static_cast<int64_t>(e) * NG + g));
             }
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                acc[r] = __fadd_rn(acc[r], v[r].x); acc[r] = __fadd_rn(acc[r], v[r].y);
-                acc[r] = __fadd_rn(acc[r], v[r].z); acc[r] = __fadd_rn(acc[r], v[r].w);
-            }
-        }
-    } else {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int e = warp * 128 + 4 * lane + r;
-            if (e < E)
-                for (int g = 0; g < NG; ++g) acc[r] = __fadd_rn(acc[r], __ldg(gt + static_cast<int64_t>(e) * NG + g));
+            key[j] = topk_key(__fadd_rn(acc, bias ? __ldg(bias + e) : 0.0f), e);
+        } else {
+            key[j] = 0ull;                                 // below every real key
         }
     }
-    uint64_t key[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int e = warp * 128 + 4 * lane + r;
-        key[r] = e < E ? topk_key(__fadd_rn(acc[r], bias ? __ldg(bias + e) : 0.0f), e) : 0ull;
-    }
-    warp_sort128_desc(key, lane);
-    if (lane < 8) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) lists[warp][4 * lane + r] = key[r];
-    }
+    lists[warp][lane] = warp_top32<2>(key, lane);
     __syncthreads();
 #pragma unroll
-    for (int n = 8; n > 1; n >>= 1) {
+    for (int n = nw; n > 1; n >>= 1) {
         uint64_t res = 0;
         if (warp < n / 2) res = merge_top32(lists[2 * warp][lane], lists[2 * warp + 1][31 - lane], lane);
         __syncthreads();
         if (warp < n / 2) lists[warp][lane] = res;
         __syncthreads();
     }
-    if (warp != 0) return;
-    const uint64_t best = lists[0][lane];
-    emit_selection(t, k, lane < k, key_index(best), key_value(best), lane, idx_out, w_out, counts, slot_off);
-    if (done) segments_if_last(T, done, counts, E, seg_start, mt_start, nrows, lane);
+    if (warp == 0) {
+        const uint64_t best = lists[0][lane];
+        emit_selection(t, k, lane < k, key_index(best), key_value(best), lane, idx_out, w_out, counts, slot_off);
+    }
+    if (done) segments_block_if_last(T, done, counts, E, seg_start, mt_start, nrows, &s_flag, wsum);
 }
 
 // One warp per token (kSelWarps tokens per block).  approx: [T][E] fp32 sums of the tensor-core
