@@ -149,8 +149,10 @@ def test_ultra_router_margin_and_routing_on_many_tokens(ultra_zipf):
 def test_ultra_drift_against_bf16_experts(ultra_uniform):
     """Layer-level drift at Ultra dims, T = 8: the GPU's NVFP4 layer against the oracle's
     BF16-expert layer (unquantized mode: fp64, bf16 master weights, no quantization), with the
-    flush-to-zero rates of the GPU's z and h.  A measurement; the bounds only catch a broken
-    quantized path."""
+    flush-to-zero rates of the GPU's z and h.  The inputs, weights and static scales are
+    seeded, so these are reproducible measurements (on a B300: y rel L2 mean 0.1965, max
+    0.2038, c 0.1955, FTZ z 0.0649, FTZ h 0.2750); the bounds sit about 15% around them, so a
+    quantizer that rounds, scales or flushes differently fails here."""
     case = ultra_uniform
     moe = case.gpu(debug=True)
     d = case.dims
@@ -178,8 +180,9 @@ def test_ultra_drift_against_bf16_experts(ultra_uniform):
          "ftz_rate_h": float((((hn & 7) == 0) & (h != 0)).sum() / max(1, (h != 0).sum()))}
     print("drift ultra T=8:", r)
     assert r["routing_agreement"] == 1.0
-    assert 0.05 < r["y_rel_l2_mean"] < 0.35 and r["y_rel_l2_max"] < 0.6
-    assert r["ftz_rate_z"] < 0.15 and r["ftz_rate_h"] < 0.5
+    assert 0.17 < r["y_rel_l2_mean"] < 0.23 and r["y_rel_l2_max"] < 0.24
+    assert 0.17 < r["c_rel_l2_mean"] < 0.23
+    assert 0.055 < r["ftz_rate_z"] < 0.075 and 0.235 < r["ftz_rate_h"] < 0.315
 
 
 @pytest.mark.parametrize("which,T", [("uniform", 8), ("zipf", 4096)])
