@@ -166,21 +166,38 @@ cudaError_t dev_malloc_async(void **p, size_t bytes, cudaStream_t s) {
 // Launch with programmatic stream serialization: the kernel's CTAs may be scheduled while the
 // previous kernel on the stream drains; each kernel of this library calls pdl_wait() before
 // its first global access (see common.cuh), so results are the same as a plain launch.
+// prio != 0: the launch's scheduling priority (a stream priority value; lower = more urgent),
+// which graph capture keeps with the kernel node.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                       Args &&...args) {
+cudaError_t launch_pdl_prio(int prio, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, Args &&...args) {
     if (injected_launch_failure()) return cudaErrorLaunchFailure;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributePriority;
+    attr[1].val.priority = prio;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = prio != 0 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args) {
+    return launch_pdl_prio(0, kernel, grid, block, smem, s, std::forward<Args>(args)...);
+}
+// The most urgent launch priority of this device (0 if it has a single priority level).
+int urgent_priority() {
+    static int p = [] {
+        int least = 0, greatest = 0;
+        return cudaDeviceGetStreamPriorityRange(&least, &greatest) == cudaSuccess ? greatest : 0;
+    }();
+    return p;
 }
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -205,7 +222,7 @@ struct lmoe_ctx {
     int d, l, E, k, ffn;
     int dev, num_sms;
     __nv_bfloat16 *w_down, *w_up;
-    float *w_router, *b_router;   // w_router transposed: [d][E] (small-T router)
+    float *w_router, *b_router;   // w_router in 32-expert panels [ceil(E/32)][d][32] (small-T router)
     // large-T router: bf16 planes [E][2d] (hi | lo) for the tensor-core logits, fp32 rows [E][d]
     // for the canonical recompute, per-expert norm bounds; host copies of max norm and max |b|
     __nv_bfloat16 *w_split;
@@ -455,12 +472,16 @@ lmoe_status launch_router(lmoe_ctx *c, const __nv_bfloat16 *x, int64_t T, float 
     const int C = c->d / kChunk;
     const int NG = static_cast<int>(cdiv(C, kGroupChunks));
     if (small) {
-        LMOE_CUDA(launch_pdl(router_small_kernel,
+        // the router and the split-K down-projection (forked stream) each want about 128 SMs
+        // at the start of a forward; the router's chain (top-k, segments) is the longer one,
+        // so its kernels are scheduled first
+        LMOE_CUDA(launch_pdl_prio(urgent_priority(), router_small_kernel,
                              dim3(static_cast<unsigned>(cdiv(c->E, kSmallEG)), static_cast<unsigned>(cdiv(C, kSmallCG))),
                              dim3(kSmallEG * kSmallCG), kRouterSmallSmem, s, x,
-                             static_cast<const float *>(c->w_router), static_cast<int>(T), c->d, c->E, scratch, zr));
+                             static_cast<const float *>(c->w_router), static_cast<int>(T), c->d, c->E, scratch, zr,
+                             c->err));
         prof_mark(c, "router_small", s);
-        LMOE_CUDA(launch_pdl(router_topk_kernel, dim3(static_cast<unsigned>(T)), dim3(kTopkThreads), 0, s,
+        LMOE_CUDA(launch_pdl_prio(urgent_priority(), router_topk_kernel, dim3(static_cast<unsigned>(T)), dim3(kTopkThreads), 0, s,
                              static_cast<const float *>(scratch), NG, static_cast<const float *>(c->b_router),
                              static_cast<int>(T), c->E, c->k, idx, w, counts, slot_off, so.done, so.seg, so.mt,
                              so.nrows));
@@ -756,7 +777,7 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
     const size_t w2_sf_bytes = static_cast<size_t>(E) * NB2 * (ffn / 64) * 512;
     CREATE_CUDA(dev_malloc(&c->w_down, static_cast<size_t>(l) * d * 2));
     CREATE_CUDA(dev_malloc(&c->w_up, static_cast<size_t>(d) * l * 2));
-    CREATE_CUDA(dev_malloc(&c->w_router, static_cast<size_t>(E) * d * 4));
+    CREATE_CUDA(dev_malloc(&c->w_router, static_cast<size_t>(cdiv(E, 32)) * 32 * d * 4));
     CREATE_CUDA(dev_malloc(&c->b_router, static_cast<size_t>(E) * 4));
     CREATE_CUDA(dev_malloc(&c->w_split, static_cast<size_t>(E) * 2 * d * 2));
     CREATE_CUDA(dev_malloc(&c->w_rows, static_cast<size_t>(E) * d * 4));
@@ -778,7 +799,8 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
     CREATE_CUDA(cudaMemsetAsync(c->err, 0, sizeof(unsigned), s));
     CREATE_CUDA(cudaMemcpyAsync(c->w_down, w->w_down, static_cast<size_t>(l) * d * 2, cudaMemcpyDeviceToDevice, s));
     CREATE_CUDA(cudaMemcpyAsync(c->w_up, w->w_up, static_cast<size_t>(d) * l * 2, cudaMemcpyDeviceToDevice, s));
-    transpose_f32_kernel<<<dim3(static_cast<unsigned>(cdiv(d, 32)), static_cast<unsigned>(cdiv(E, 32))),
+    CREATE_CUDA(cudaMemsetAsync(c->w_router, 0, static_cast<size_t>(cdiv(E, 32)) * 32 * d * 4, s));
+    router_panels_kernel<<<dim3(static_cast<unsigned>(cdiv(d, 32)), static_cast<unsigned>(cdiv(E, 32))),
                            dim3(32, 8), 0, s>>>(w->w_router, E, d, c->w_router);
     CREATE_CUDA(cudaGetLastError());
     if (w->b_router)

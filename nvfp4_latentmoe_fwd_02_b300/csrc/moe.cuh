@@ -137,19 +137,20 @@ __global__ void __launch_bounds__(256) scatter_rows_kernel(
     }
 }
 
-// out[c][r] = in[r][c] for an [R][Cn] fp32 matrix (router weights, once at create).
-__global__ void transpose_f32_kernel(const float *__restrict__ in, int64_t R, int64_t Cn,
-                                     float *__restrict__ out) {
+// Router weights [E][d] -> 32-expert panels [ceil(E/32)][d][32] (expert e of panel e / 32 at
+// lane e % 32; the panels' unused lanes are left as they are, zero after the allocation's clear):
+// one block of the small-T router reads a contiguous slab of one panel.
+__global__ void router_panels_kernel(const float *__restrict__ in, int64_t E, int64_t d, float *__restrict__ out) {
     __shared__ float tile[32][33];
-    const int64_t c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+    const int64_t c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;   // d columns, expert rows (one panel)
     for (int j = threadIdx.y; j < 32; j += blockDim.y) {
         const int64_t r = r0 + j, c = c0 + threadIdx.x;
-        if (r < R && c < Cn) tile[j][threadIdx.x] = in[r * Cn + c];
+        if (r < E && c < d) tile[j][threadIdx.x] = in[r * d + c];
     }
     __syncthreads();
     for (int j = threadIdx.y; j < 32; j += blockDim.y) {
         const int64_t c = c0 + j, r = r0 + threadIdx.x;
-        if (r < R && c < Cn) out[c * R + r] = tile[threadIdx.x][j];
+        if (r < E && c < d) out[((r0 / 32) * d + c) * 32 + threadIdx.x] = tile[threadIdx.x][j];
     }
 }
 

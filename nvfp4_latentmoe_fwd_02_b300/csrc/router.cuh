@@ -45,20 +45,26 @@ __global__ void zero_kernel(ZeroRanges z) {
 }
 
 // Small T: group sums G[t][e][g].  Block: 32 experts (lanes) x the 16 chunks of group g
-// (warps); thread (e, c) loads its 64 weights once (one coalesced 128-byte load per element
-// across the warp) and runs one fmaf chain per token; the block then adds its 16 chunk
-// partials in order per (token, expert) from shared memory.  Tokens are staged 16 at a time
+// (warps).  The block's router weights, rows [64 c0, 64 (c0 + 16)) of one 32-expert panel
+// (Wp: [ceil(E/32)][d][32], router_panels_kernel), are one contiguous slab of up to 128 KB: a
+// single bulk copy brings it into shared memory, issued before the wait on the previous grid
+// (the weights are static).  Thread (e, c) runs one fmaf chain over its chunk per token, reading
+// the weights from shared memory (lane = expert: conflict free); the block then adds its 16
+// chunk partials in order per (token, expert) from shared memory.  Tokens are staged 16 at a time
 // in shared memory as fp32 (all lanes of a warp read the same element: a broadcast).
 // grid = (ceil(E / 32), ceil(C / 16)); T <= 64.
 constexpr int kSmallMaxT = 64;
 constexpr int kSmallEG = 32, kSmallCG = 16, kSmallTG = 16;
 constexpr int kGroupChunks = 16;
-constexpr int kRouterSmallSmem = kSmallTG * kSmallCG * kChunk * 4 + kSmallTG * kSmallCG * kSmallEG * 4;
+constexpr int kRouterSmallSmem = kSmallCG * kChunk * kSmallEG * 4 + kSmallTG * kSmallCG * kChunk * 4 +
+                                 kSmallTG * kSmallCG * kSmallEG * 4 + 16;
 __global__ void __launch_bounds__(kSmallEG * kSmallCG) router_small_kernel(
-    const __nv_bfloat16 *__restrict__ x, const float *__restrict__ Wt, int T, int d, int E,
-    float *__restrict__ G, ZeroRanges zr) {
-    extern __shared__ __align__(16) float xs[];        // [kSmallTG][kSmallCG][64], then ps
+    const __nv_bfloat16 *__restrict__ x, const float *__restrict__ Wp, int T, int d, int E,
+    float *__restrict__ G, ZeroRanges zr, unsigned *err) {
+    extern __shared__ __align__(16) float wsm[];        // [kSmallCG * 64][32], then xs, ps, the barrier
+    float *xs = wsm + kSmallCG * kChunk * kSmallEG;     // [kSmallTG][kSmallCG][64]
     float *ps = xs + kSmallTG * kSmallCG * kChunk;      // [kSmallTG][kSmallCG][32]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(ps + kSmallTG * kSmallCG * kSmallEG);
     const int C = d / kChunk;
     const int ng = (C + kGroupChunks - 1) / kGroupChunks;
     const int lane = threadIdx.x & 31, cl = threadIdx.x >> 5;
@@ -66,16 +72,21 @@ __global__ void __launch_bounds__(kSmallEG * kSmallCG) router_small_kernel(
     const int c0 = blockIdx.y * kSmallCG;
     const int c = c0 + cl;
     const bool active = e < E && c < C;
+    const int ncg = min(kSmallCG, C - c0);
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        const uint32_t bytes = static_cast<uint32_t>(ncg * kChunk * kSmallEG * 4);
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_load(wsm, Wp + (static_cast<int64_t>(blockIdx.x) * d + static_cast<int64_t>(c0) * kChunk) * kSmallEG,
+                  bytes, bar);
+    }
     pdl_wait();
     pdl_trigger();
     zero_ranges(zr);
-    float w[kChunk];
-    if (active) {
-#pragma unroll
-        for (int i = 0; i < kChunk; ++i) w[i] = __ldg(Wt + static_cast<int64_t>(c * kChunk + i) * E + e);
-    }
-    const int ncg = min(kSmallCG, C - c0);
     const int per_tok = ncg * (kChunk / 8);            // uint4 per token
+    bool have_w = false;
+    float w[kChunk];
     for (int t0 = 0; t0 < T; t0 += kSmallTG) {
         const int nt = min(kSmallTG, T - t0);
         __syncthreads();
@@ -87,6 +98,13 @@ __global__ void __launch_bounds__(kSmallEG * kSmallCG) router_small_kernel(
                                  __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
             dst[1] = make_float4(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xFFFF0000u),
                                  __uint_as_float(u.w << 16), __uint_as_float(u.w & 0xFFFF0000u));
+        }
+        if (!have_w) {                                  // the weight slab has landed (bounded); the
+            if (!mbar_wait(bar, 0)) raise_error(err, kErrTimeout);   // thread's 64 weights to registers
+            const float *wr = wsm + cl * kChunk * kSmallEG + lane;
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) w[i] = wr[i * kSmallEG];
+            have_w = true;
         }
         __syncthreads();
         if (active) {
@@ -113,6 +131,7 @@ __global__ void __launch_bounds__(kSmallEG * kSmallCG) router_small_kernel(
             G[(static_cast<int64_t>(t0 + tt) * E + e) * ng + blockIdx.y] = gs;
         }
     }
+    if (!have_w && !mbar_wait(bar, 0)) raise_error(err, kErrTimeout);   // no copy in flight at exit
 }
 
 // Top-k by sorting.  A selection key packs (logit, expert) into 64 bits so that a larger key
