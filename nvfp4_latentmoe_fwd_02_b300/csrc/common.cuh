@@ -382,6 +382,19 @@ __device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
     return d;
 }
 
+// An L2 policy that keeps the lines it touches ahead of other traffic (evict_last), and a vector
+// reduction that carries it: the combine accumulator's lines then survive the weight stream
+// between the contributions of a token's experts.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void red_add_v4_f32_hint(float *p, float a, float b, float c, float d, uint64_t pol) {
+    asm volatile("red.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(a), "f"(b),
+                 "f"(c), "f"(d), "l"(pol)
+                 : "memory");
+}
 __device__ __forceinline__ void red_add_f32(float *p, float v) {
     asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }

@@ -491,13 +491,14 @@ __device__ __forceinline__ void combine_staged(const GemmArgs &g, const Tile &tl
     __syncwarp();
     const int col = tl.n0 + c0;
     const int cc = lane & 7;
+    const uint64_t pol = policy_evict_last();
 #pragma unroll
     for (int it = 0; it < 8; ++it) {
         const int rr = it * 4 + (lane >> 3);
         const float4 v = stg[rr * 8 + (cc ^ (rr & 7))];
         if (orow[it] >= 0)
-            red_add_v4_f32(static_cast<float *>(g.out) + static_cast<int64_t>(orow[it]) * g.ld_out + col + 4 * cc,
-                           v.x, v.y, v.z, v.w);
+            red_add_v4_f32_hint(static_cast<float *>(g.out) + static_cast<int64_t>(orow[it]) * g.ld_out + col + 4 * cc,
+                                v.x, v.y, v.z, v.w, pol);
     }
     __syncwarp();
 }

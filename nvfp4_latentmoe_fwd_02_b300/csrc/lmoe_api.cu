@@ -467,7 +467,8 @@ struct SegOut {
 };
 lmoe_status launch_router(lmoe_ctx *c, const __nv_bfloat16 *x, int64_t T, float *scratch,
                           int32_t *idx, float *w, int32_t *counts, int32_t *slot_off,
-                          const ZeroRanges &zr, cudaStream_t s, SegOut so = {nullptr, nullptr, nullptr, nullptr}) {
+                          const ZeroRanges &zr, cudaStream_t s, SegOut so = {nullptr, nullptr, nullptr, nullptr},
+                          cudaEvent_t after_logits = nullptr) {
     const bool small = T <= kSmallMaxT;
     const int C = c->d / kChunk;
     const int NG = static_cast<int>(cdiv(C, kGroupChunks));
@@ -481,6 +482,7 @@ lmoe_status launch_router(lmoe_ctx *c, const __nv_bfloat16 *x, int64_t T, float 
                              static_cast<const float *>(c->w_router), static_cast<int>(T), c->d, c->E, scratch, zr,
                              c->err));
         prof_mark(c, "router_small", s);
+        if (after_logits) LMOE_CUDA(cudaEventRecord(after_logits, s));
         LMOE_CUDA(launch_pdl_prio(urgent_priority(), router_topk_kernel, dim3(static_cast<unsigned>(T)), dim3(kTopkThreads), 0, s,
                              static_cast<const float *>(scratch), NG, static_cast<const float *>(c->b_router),
                              static_cast<int>(T), c->E, c->k, idx, w, counts, slot_off, so.done, so.seg, so.mt,
@@ -1123,17 +1125,12 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         prof_mark(c, "down_proj", ds);
         return LMOE_OK;
     };
-    if (fork) {
-        LMOE_CUDA(cudaEventRecord(c->ev_fork, s));
-        LMOE_CUDA(cudaStreamWaitEvent(c->aux, c->ev_fork, 0));
-        ZeroRanges zz;
-        std::memset(&zz, 0, sizeof(zz));
-        zz.p[0] = reinterpret_cast<uint4 *>(zacc); zz.n16[0] = T * l * 4 / 16;
-        LMOE_CUDA(launch_pdl(zero_kernel, dim3(c->num_sms), dim3(256), 0, c->aux, zz));
-        lmoe_status st = down_proj(c->aux);
-        if (st != LMOE_OK) return st;
-        LMOE_CUDA(cudaEventRecord(c->ev_join, c->aux));
-    }
+    // The split-K down-projection runs on the second stream beside the router.  At small T it
+    // forks after the router's logit kernel: both want about 128 SMs, and the router's chain
+    // (logits, top-k, segments) is the longer one, so it streams its weights first on an idle
+    // GPU; that kernel also clears the down-projection's accumulator.
+    const bool fork_late = fork && T <= kSmallMaxT;
+    if (fork && !fork_late) LMOE_CUDA(cudaEventRecord(c->ev_fork, s));
 
     // 1. router (its first kernel also clears the histogram and the fp32 accumulators)
     {
@@ -1141,12 +1138,25 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         std::memset(&z, 0, sizeof(z));
         z.p[0] = reinterpret_cast<uint4 *>(counts); z.n16[0] = cdiv(E * 4 + 16, 16);   // counts + done
         z.p[1] = reinterpret_cast<uint4 *>(c_acc); z.n16[1] = T * l * 4 / 16;
-        if (L.split_down && !fork) { z.p[2] = reinterpret_cast<uint4 *>(zacc); z.n16[2] = T * l * 4 / 16; }
+        if (L.split_down && (!fork || fork_late)) { z.p[2] = reinterpret_cast<uint4 *>(zacc); z.n16[2] = T * l * 4 / 16; }
         if (L.split_up) { z.p[3] = reinterpret_cast<uint4 *>(yacc); z.n16[3] = T * d * 4 / 16; }
         SegOut so = {counts + E, seg, mt, nrows};
         lmoe_status st = launch_router(c, static_cast<const __nv_bfloat16 *>(x), T,
-                                       static_cast<float *>(at(L.router)), idx, rw, counts, slot_off, z, s, so);
+                                       static_cast<float *>(at(L.router)), idx, rw, counts, slot_off, z, s, so,
+                                       fork_late ? c->ev_fork : nullptr);
         if (st != LMOE_OK) return st;
+    }
+    if (fork) {
+        LMOE_CUDA(cudaStreamWaitEvent(c->aux, c->ev_fork, 0));
+        if (!fork_late) {
+            ZeroRanges zz;
+            std::memset(&zz, 0, sizeof(zz));
+            zz.p[0] = reinterpret_cast<uint4 *>(zacc); zz.n16[0] = T * l * 4 / 16;
+            LMOE_CUDA(launch_pdl(zero_kernel, dim3(c->num_sms), dim3(256), 0, c->aux, zz));
+        }
+        lmoe_status st = down_proj(c->aux);
+        if (st != LMOE_OK) return st;
+        LMOE_CUDA(cudaEventRecord(c->ev_join, c->aux));
     }
     // 3. down-projection z = x Wd^T, quantized to NVFP4
     {
@@ -1399,10 +1409,12 @@ int lmoe_forward_kernel_count(const lmoe_ctx *c, int64_t T) {
     if (!c || T <= 0) return 0;
     const WsLayout L = layout(c, T);
     // router (small T: chunk sums, top-k; large T: clearing, tensor-core logits, selection;
-    // its last warp lays out the segments), down-proj, expert-up, expert-down, combine cast, up-proj, plus one finalize per split projection (and, for a split down-projection run
-    // beside the router, the clearing of its accumulator), plus the shared expert's
-    // quantization of x and its two GEMMs
-    return 7 + (T > kSmallMaxT ? 1 : 0) + (L.split_down ? 2 : 1) + (L.split_up ? 1 : 0) + (c->shared_ffn ? 3 : 0);
+    // its last warp lays out the segments), down-proj, expert-up, expert-down, combine cast,
+    // up-proj, plus one finalize per split projection or the row scatter (and, for a split
+    // down-projection forked before a large-T router, the clearing of its accumulator), plus
+    // the shared expert's quantization of x and its two GEMMs
+    const int down_extra = L.split_down && T > kSmallMaxT && !c->profile ? 1 : 0;
+    return 7 + (T > kSmallMaxT ? 1 : 0) + 1 + down_extra + (L.split_up ? 1 : 0) + (c->shared_ffn ? 3 : 0);
 }
 
 lmoe_status lmoe_set_profile(lmoe_ctx *c, int on) {
