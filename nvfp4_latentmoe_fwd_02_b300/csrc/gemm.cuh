@@ -61,6 +61,7 @@ constexpr int kBM = 128, kBN = 128;
 constexpr int kTileBytes = kBM * 128;     // 16 KB per operand per stage
 constexpr int kABoxRows = 32;             // decode: A is loaded as one 32-row box per column block
 constexpr int kABoxBytes = kABoxRows * 128;
+constexpr int kAF32Rows = 8;              // decode, A staged as fp32: one 8-row box per column block
 constexpr int kSfStageBytes = 4 * 512;    // 4 scale atoms (4 x K64) per operand per stage
 
 struct GemmArgs {
@@ -103,6 +104,9 @@ struct GemmArgs {
     long long wait_limit;        // SM cycles a pipeline wait may take before the CTA gives up
     int inject_wait;             // fault injection: the MMA role first waits on a barrier that
                                  // nothing arrives at, so the wait runs out (LMOE_FAULT=wait)
+    __nv_bfloat16 *a_copy;       // A staged as fp32 (bf16 GEMM at decode, STG): the bf16 rounding
+                                 // of A's first a_rows rows, [a_rows][K], written by the CTAs of n-tile 0
+    int a_rows;
     int preload;                 // decode launches: issue the weight (B) loads of the first
                                  // ring pass before waiting on the previous grid (the weights,
                                  // and for grouped launches the segment tables, are complete
@@ -514,7 +518,11 @@ struct GemmCfg {
     static constexpr bool NVF4 = KIND == kKindNvf4;
     static constexpr bool W4 = KIND == kKindW4A16;
     static constexpr bool kTables = NVF4 || W4;                       // grouped launches: tables in smem
-    static constexpr int kRawBlock = W4 ? 128 * 32 + 512 : 0;         // E2M1 codes + one scale atom per block
+    // bf16 at decode with STG (T <= 8): A arrives as fp32 (the combine accumulator) in 8-row x
+    // 64-element boxes, and warps 2-3 round it to bf16 into the SW128 A slot (no cast kernel)
+    static constexpr bool kAF32 = KIND == kKindBf16 && SMALLA && STG;
+    static constexpr int kRawBlock = W4 ? 128 * 32 + 512                // E2M1 codes + one scale atom per block
+                                        : (kAF32 ? kAF32Rows * 64 * 4 : 0);   // or the fp32 A box
     static constexpr int kRawStage = KB * kRawBlock;
     static constexpr int kEpi0 = W4 ? 8 : 4;                          // first epilogue warp
     // epilogue warps: 4 for the grouped NVFP4 GEMMs at prefill with 128-column tiles (one per
@@ -595,7 +603,8 @@ __device__ __forceinline__ void w4_convert_block(const uint8_t *raw, uint8_t *ds
 // the bf16 up-projection at decode: twice the CTAs stream the weights, with no split-K.  (NVFP4
 // stays at 128: two 256-column accumulators would fill TMEM and leave no room for the scale
 // factors, and one accumulator serialises each tile's epilogue with the next tile's MMAs.)
-// STG: the staged combine (grouped NVFP4 latent-down at prefill; 16 KB of smem).
+// STG: the staged combine (grouped NVFP4 latent-down at prefill; 32 KB of smem); for the bf16
+// GEMM at decode, A staged as fp32 and rounded to bf16 by warps 2-3 (GemmCfg::kAF32).
 template <int KIND, bool SMALLA, int KB, int STAGES, int BN = kBN, bool STG = false>
 __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -683,7 +692,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
                                     &sffull[s]);
                     }
                     // the stage's arrival, counting the A bytes still to come
-                    mbar_arrive_expect_tx_p(leader, &full[s], KB * (C::kACol + BN * 128));
+                    mbar_arrive_expect_tx_p(leader, &full[s], KB * ((C::kAF32 ? C::kRawBlock : C::kACol) + BN * 128));
 #pragma unroll
                     for (int b = 0; b < KB; ++b) {
                         if constexpr (NVF4)
@@ -772,12 +781,16 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
                                         kb0 * 2048,
                                     nsteps * 512, sb);
                 }
-                if (!pre) mbar_arrive_expect_tx_p(leader, fb, KB * (C::kACol + BN * 128));
+                if (!pre) mbar_arrive_expect_tx_p(leader, fb, KB * ((C::kAF32 ? C::kRawBlock : C::kACol) + BN * 128));
 #pragma unroll
                 for (int b = 0; b < KB; ++b) {
                     const int kx = (kb0 + b) * C::kTmaXPerBlock;
                     const int kxa = g.a_kwrap > 0 ? kx % g.a_kwrap : kx;
-                    tma_load_2d_p(leader, a_st + b * C::kACol, &tmA, fb, kxa, tl.a_row0);
+                    if constexpr (C::kAF32)
+                        tma_load_2d_p(leader, smem_u32(sRaw) + stage * C::kRawStage + b * C::kRawBlock, &tmA, fb, kx,
+                                      tl.a_row0);
+                    else
+                        tma_load_2d_p(leader, a_st + b * C::kACol, &tmA, fb, kxa, tl.a_row0);
                     if (pre) continue;
                     if (NVF4) {   // weight codes in tile order: box (expert, row block, column block)
 #pragma unroll
@@ -827,7 +840,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
             bool ok = true;
             for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
                 if (!role_wait(&full[stage], phase, s_abort, g.err, g.wait_limit)) { ok = false; break; }
-                if ((NVF4 || W4) && !role_wait(&sfready[stage], phase, s_abort, g.err, g.wait_limit)) { ok = false; break; }
+                if ((NVF4 || W4 || C::kAF32) && !role_wait(&sfready[stage], phase, s_abort, g.err, g.wait_limit)) { ok = false; break; }
                 tc_fence_after();
                 const uint64_t ad = adesc0 + ((stage * C::kAStage) >> 4);
                 const uint64_t bd = bdesc0 + ((stage * C::kBStage) >> 4);
@@ -930,6 +943,41 @@ __global__ void __launch_bounds__(GemmCfg<KIND, SMALLA, KB, BN, STG>::kThreads, 
             mma_commit_p(leader, &cdrain[is_b ? 1 : 0]);
             const long long t0 = clock64();
             while (!mbar_try_wait(&cdrain[is_b ? 1 : 0], 0) && clock64() - t0 < kWaitLimitCycles) {}
+        } else if constexpr (C::kAF32) {
+            // ------------------------------------------------------------ A converters (fp32 -> bf16)
+            // A stage = KB boxes of 8 rows x 64 fp32 (256-byte rows, unswizzled) -> the SW128 bf16
+            // A slot (16-byte chunk c of row r at c ^ (r % 8)), round to nearest even as the
+            // combine's cast; then the async proxy is fenced and the MMA told ("sfready")
+            const int ct = (warp - 2) * 32 + lane;
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int t = blockIdx.x; t < num_tiles && !*s_abort; t += gridDim.x) {
+                const Tile tl = decode_tile(g, tb, t);
+                const bool copy = g.a_copy != nullptr && tl.n0 == 0;
+                bool ok = true;
+                for (int kt = tl.kt0; kt < tl.kt1; ++kt) {
+                    if (!role_wait(&full[stage], phase, s_abort, g.err, g.wait_limit)) { ok = false; break; }
+                    const uint8_t *src = sRaw + stage * C::kRawStage;
+                    uint8_t *dst = sA + stage * C::kAStage;
+                    for (int u = ct; u < KB * kAF32Rows * 8; u += 64) {
+                        const int b = u / (kAF32Rows * 8), rem = u - b * (kAF32Rows * 8);
+                        const int r = rem >> 3, c = rem & 7;
+                        const float4 *f = reinterpret_cast<const float4 *>(src + b * C::kRawBlock + r * 256 + c * 32);
+                        const float4 x0 = f[0], x1 = f[1];
+                        const uint4 o = make_uint4(pack_bf16x2(x0.x, x0.y), pack_bf16x2(x0.z, x0.w),
+                                                   pack_bf16x2(x1.x, x1.y), pack_bf16x2(x1.z, x1.w));
+                        *reinterpret_cast<uint4 *>(dst + b * C::kACol + r * 128 + ((c ^ (r & 7)) << 4)) = o;
+                        const int k0 = (kt * KB + b) * 64 + c * 8;
+                        if (copy && r < g.a_rows && k0 < g.K)
+                            *reinterpret_cast<uint4 *>(g.a_copy + static_cast<int64_t>(tl.a_row0 + r) * g.K + k0) = o;
+                    }
+                    fence_proxy_async();      // the tensor core reads what these threads wrote
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sfready[stage]);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+            }
         }
     } else {
         // ---------------------------------------------------------------- epilogue

@@ -55,6 +55,10 @@ constexpr int kBNWide = 256;
 constexpr int kBNNarrow = 64;         // bf16 GEMMs at decode whose 128-column tiles leave SMs idle
 constexpr int kStagesW4 = 5;          // W4A16 above decode: bf16 A + decoded bf16 B + raw E2M1 block per stage
 constexpr int kSmallAMaxT = 32;
+// up-projection at T <= 8 reading the fp32 combine accumulator (A staged as fp32, 4 KB more per
+// stage): 64-column tiles 6 stages, 128-column tiles 4
+constexpr int kStagesUpF32N = 6, kStagesUpF32W = 4;
+constexpr int kUpF32MaxT = 8;
 
 inline int kb_for(bool small_a) { return small_a ? 2 : 1; }   // column blocks per stage
 // tile width of the dense (bf16 / fp8) GEMMs: 256 outside decode (fewer operand bytes per output)
@@ -92,6 +96,20 @@ bool make_map(CUtensorMap *m, bool bf16, const void *ptr, uint64_t inner, uint64
     CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
                     const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// fp32 [rows][inner] map, unswizzled, box of 64 elements (256 bytes) x box_rows.
+bool make_map_f32(CUtensorMap *m, const float *ptr, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * 4};
+    cuuint32_t box[2] = {64u, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(ptr), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -742,6 +760,8 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
             if (a == cudaSuccess) a = set_smem_attr<kKindBf16, true, 2, kStagesBF16Small, kBNNarrow>();
             if (a == cudaSuccess) a = set_smem_attr<kKindFp8, false, 1, kStagesWide, kBNWide>();
             if (a == cudaSuccess) a = set_smem_attr<kKindFp8, true, 2, kStagesF8Small>();
+            if (a == cudaSuccess) a = set_smem_attr<kKindBf16, true, 2, kStagesUpF32N, kBNNarrow, true>();
+            if (a == cudaSuccess) a = set_smem_attr<kKindBf16, true, 2, kStagesUpF32W, kBN, true>();
             if (a == cudaSuccess)
                 a = cudaFuncSetAttribute(w4_decode_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          w4dec_smem_bytes<16>());
@@ -1250,8 +1270,9 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         }
         prof_mark(c, "expert_down", s);
     }
-    // 7. c = bf16(c_acc)
-    {
+    // 7. c = bf16(c_acc) (at T <= 8 the up-projection rounds c_acc itself, below)
+    const bool up_f32 = T <= kUpF32MaxT;
+    if (!up_f32) {
         const int grid = static_cast<int>(std::min<int64_t>(cdiv(T * l / 8, 256), c->num_sms * 8));
         LMOE_CUDA(launch_pdl(f32_to_bf16_kernel, dim3(grid), dim3(256), 0, s, static_cast<const float *>(c_acc),
                              T * l, cb, static_cast<const __nv_bfloat16 *>(nullptr)));
@@ -1286,15 +1307,28 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     // 8. up-projection y = c Wu^T (+ s)
     {
         CUtensorMap tc;
-        if (!make_map(&tc, true, cb, l, T, static_cast<uint64_t>(l) * 2, a_box)) return LMOE_ECUDA;
+        // T <= 8: A is the fp32 combine accumulator, rounded to bf16 inside the GEMM (which also
+        // writes the bf16 c); otherwise the bf16 c of step 7
+        const bool ok = up_f32 ? make_map_f32(&tc, static_cast<const float *>(c_acc), l, T, kAF32Rows)
+                               : make_map(&tc, true, cb, l, T, static_cast<uint64_t>(l) * 2, a_box);
+        if (!ok) return LMOE_ECUDA;
         GemmArgs g = dense_args(static_cast<int>(T), d, l, L.up_splits,
                                 L.split_up ? EPI_RED_F32 : EPI_STORE_BF16, c, kb_for(small_a), 64, L.up_bn);
         g.out = L.split_up ? static_cast<void *>(yacc) : y;
         g.ld_out = d;
         if (!L.split_up) g.addend = y_add;
         const CUtensorMap &twu = !small_a ? c->tm_wu_w : (L.up_bn == kBNNarrow ? c->tm_wu_n : c->tm_wu);
-        LMOE_CUDA((launch_gemm<kKindBf16>(tc, twu, g,
-                                                   grid_for(int64_t(g.m_tiles) * g.n_tiles * g.k_splits, c->num_sms), small_a, s)));
+        const int grid = grid_for(int64_t(g.m_tiles) * g.n_tiles * g.k_splits, c->num_sms);
+        if (up_f32) {
+            g.a_copy = cb;
+            g.a_rows = static_cast<int>(T);
+            g.preload = 1;
+            LMOE_CUDA((L.up_bn == kBNNarrow
+                           ? launch_gemm_cfg<kKindBf16, true, 2, kStagesUpF32N, kBNNarrow, true>(tc, twu, g, grid, s)
+                           : launch_gemm_cfg<kKindBf16, true, 2, kStagesUpF32W, kBN, true>(tc, twu, g, grid, s)));
+        } else {
+            LMOE_CUDA((launch_gemm<kKindBf16>(tc, twu, g, grid, small_a, s)));
+        }
         prof_mark(c, "up_proj", s);
         if (L.split_up) {
             const int grid = static_cast<int>(std::min<int64_t>(cdiv(T * d / 8, 256), c->num_sms * 8));
@@ -1414,7 +1448,8 @@ int lmoe_forward_kernel_count(const lmoe_ctx *c, int64_t T) {
     // down-projection forked before a large-T router, the clearing of its accumulator), plus
     // the shared expert's quantization of x and its two GEMMs
     const int down_extra = L.split_down && T > kSmallMaxT && !c->profile ? 1 : 0;
-    return 7 + (T > kSmallMaxT ? 1 : 0) + 1 + down_extra + (L.split_up ? 1 : 0) + (c->shared_ffn ? 3 : 0);
+    const int cast = T > kUpF32MaxT ? 1 : 0;       // at T <= 8 the up-projection rounds c itself
+    return 6 + cast + (T > kSmallMaxT ? 1 : 0) + 1 + down_extra + (L.split_up ? 1 : 0) + (c->shared_ffn ? 3 : 0);
 }
 
 lmoe_status lmoe_set_profile(lmoe_ctx *c, int on) {
