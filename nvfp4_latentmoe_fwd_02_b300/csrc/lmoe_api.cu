@@ -270,7 +270,7 @@ struct lmoe_ctx {
     size_t route_ws_bytes;
     // second stream: the split-K down-projection runs beside the router (fork / join events)
     cudaStream_t aux;
-    cudaEvent_t ev_fork, ev_join;
+    cudaEvent_t ev_fork, ev_join, ev_join_s;   // ev_join_s: the shared expert, run on the second stream
     // lmoe_forward_host: its copy-in, forward and copy-out as one CUDA graph, replayed while a
     // call's arguments (and the debug flag) equal those it was captured with
     cudaGraphExec_t host_exec;
@@ -818,6 +818,7 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
     CREATE_CUDA(cudaStreamCreateWithFlags(&c->aux, cudaStreamNonBlocking));
     CREATE_CUDA(cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming));
     CREATE_CUDA(cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming));
+    CREATE_CUDA(cudaEventCreateWithFlags(&c->ev_join_s, cudaEventDisableTiming));
     CREATE_CUDA(cudaMemsetAsync(c->err, 0, sizeof(unsigned), s));
     CREATE_CUDA(cudaMemcpyAsync(c->w_down, w->w_down, static_cast<size_t>(l) * d * 2, cudaMemcpyDeviceToDevice, s));
     CREATE_CUDA(cudaMemcpyAsync(c->w_up, w->w_up, static_cast<size_t>(d) * l * 2, cudaMemcpyDeviceToDevice, s));
@@ -969,6 +970,7 @@ void lmoe_destroy(lmoe_ctx *c) {
         if (e) cudaEventDestroy(e);
     if (c->ev_fork) cudaEventDestroy(c->ev_fork);
     if (c->ev_join) cudaEventDestroy(c->ev_join);
+    if (c->ev_join_s) cudaEventDestroy(c->ev_join_s);
     if (c->aux) cudaStreamDestroy(c->aux);
     if (c->host_exec) cudaGraphExecDestroy(c->host_exec);
     delete c;
@@ -1279,14 +1281,18 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
         prof_mark(c, "combine_cast", s);
     }
     // 7b. shared expert at width d (FP8): xs = q8(x); hs = q8(bf16(relu(alpha_s1 xs Ws1q^T)^2));
-    //     s = bf16(alpha_s2 hs Ws2q^T), added to the up-projection before its rounding
+    //     s = bf16(alpha_s2 hs Ws2q^T), added to the up-projection before its rounding.  It needs
+    //     only x: when the forward forks, it runs on the second stream after the down-projection,
+    //     beside the routed experts, and joins before the up-projection.
+    const bool shared_aux = c->shared_ffn && fork;
     if (c->shared_ffn) {
+        const cudaStream_t ss = shared_aux ? c->aux : s;
         const int FS = c->shared_ffn;
         const int qg = static_cast<int>(std::min<int64_t>(cdiv(T * d / 16, 256), c->num_sms * 16));
-        LMOE_CUDA(launch_pdl(quantize_fp8_kernel<__nv_bfloat16>, dim3(qg), dim3(256), 0, s,
+        LMOE_CUDA(launch_pdl(quantize_fp8_kernel<__nv_bfloat16>, dim3(qg), dim3(256), 0, ss,
                              static_cast<const __nv_bfloat16 *>(x), T * d, c->amax_xs,
                              static_cast<const unsigned *>(nullptr), xs_q));
-        prof_mark(c, "shared_quant_x", s);
+        prof_mark(c, "shared_quant_x", ss);
         CUtensorMap txs, ths;
         if (!make_map(&txs, false, xs_q, d, T, d, a_box) || !make_map(&ths, false, hs_q, FS, T, FS, a_box))
             return LMOE_ECUDA;
@@ -1294,14 +1300,18 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
                                  bn_for(small_a));
         g1.alpha_s = c->alpha_s1; g1.s_enc8 = c->s_enc_hs; g1.q_codes = hs_q; g1.dbg = hs_dbg;
         LMOE_CUDA((launch_gemm<kKindFp8>(txs, small_a ? c->tm_ws1 : c->tm_ws1_w, g1, grid_for(int64_t(g1.m_tiles) * g1.n_tiles, c->num_sms),
-                                         small_a, s)));
-        prof_mark(c, "shared_up", s);
+                                         small_a, ss)));
+        prof_mark(c, "shared_up", ss);
         GemmArgs g2 = dense_args(static_cast<int>(T), d, FS, 1, EPI_STORE_SCALED, c, kb_for(small_a), 128,
                                  bn_for(small_a));
         g2.alpha_s = c->alpha_s2; g2.out = s_out; g2.ld_out = d;
         LMOE_CUDA((launch_gemm<kKindFp8>(ths, small_a ? c->tm_ws2 : c->tm_ws2_w, g2, grid_for(int64_t(g2.m_tiles) * g2.n_tiles, c->num_sms),
-                                         small_a, s)));
-        prof_mark(c, "shared_down", s);
+                                         small_a, ss)));
+        prof_mark(c, "shared_down", ss);
+        if (shared_aux) {
+            LMOE_CUDA(cudaEventRecord(c->ev_join_s, c->aux));
+            LMOE_CUDA(cudaStreamWaitEvent(s, c->ev_join_s, 0));
+        }
     }
     const __nv_bfloat16 *y_add = c->shared_ffn ? s_out : nullptr;
     // 8. up-projection y = c Wu^T (+ s)
