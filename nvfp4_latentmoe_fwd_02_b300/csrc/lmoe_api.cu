@@ -1197,10 +1197,12 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
             prof_mark(c, "scatter", s);
         }
         if (L.split_down) {
-            // whole tokens per block: 256 threads cover 256 / (l/16) tokens (l <= 4096, k * tokens <= 256)
+            // whole tokens per block: 256 threads cover 256 / (l/16) tokens (l <= 4096, k * tokens <= 256);
+            // at T <= 16 one token per block and its k copies in four groups of blocks
             const int nb = l / 16;
-            const int tpb = std::max(1, std::min(256 / nb, 256 / k));
-            LMOE_CUDA(launch_pdl(z_finalize_kernel, dim3(static_cast<unsigned>(cdiv(T, tpb))), dim3(tpb * nb), 0, s,
+            const int tpb = T <= 16 ? 1 : std::max(1, std::min(256 / nb, 256 / k));
+            const unsigned groups = T <= 16 ? 4u : 1u;
+            LMOE_CUDA(launch_pdl(z_finalize_kernel, dim3(static_cast<unsigned>(cdiv(T, tpb)), groups), dim3(tpb * nb), 0, s,
                                  static_cast<const float *>(zacc), T, l, c->qz, zq_codes, zq_sf, z_dbg,
                                  static_cast<const int32_t *>(idx), static_cast<const int32_t *>(slot_off),
                                  static_cast<const int32_t *>(seg), k, row_slot, a_codes, a_sf, a_bf16));

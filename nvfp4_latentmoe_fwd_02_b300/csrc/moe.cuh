@@ -22,22 +22,26 @@ __device__ __forceinline__ int slot_row(const int32_t *idx, const int32_t *slot_
 // Split-K finalize of the down-projection, one thread per (token, 16-block): z = bf16(zacc),
 // zq = NVFP4(z) into the row-major buffers and into the token's k segment rows (codes and
 // scale atoms; or, for W4A16, the bf16 z itself); row_slot records the slot of each row.  A block covers whole tokens
-// (blockDim / (l/16) of them); their k segment rows are looked up once into shared memory.
+// (blockDim / (l/16) of them) and one group of their slots (blockIdx.y of gridDim.y groups: at
+// small T the copies are spread over more SMs, so the stores drain sooner); the group's segment
+// rows are looked up once into shared memory.  The row-major zq is written by group 0.
 __global__ void __launch_bounds__(256) z_finalize_kernel(
     const float *__restrict__ zacc, int64_t T, int l, QScale q, uint8_t *__restrict__ codes,
     uint8_t *__restrict__ sf, __nv_bfloat16 *__restrict__ z_out, const int32_t *__restrict__ idx,
     const int32_t *__restrict__ slot_off, const int32_t *__restrict__ seg_start, int k,
     int32_t *__restrict__ row_slot, uint8_t *__restrict__ a_codes, uint8_t *__restrict__ a_sf,
     __nv_bfloat16 *__restrict__ a_bf16) {
-    __shared__ int rows_s[256];   // [tokens per block][k]
+    __shared__ int rows_s[256];   // [tokens per block][slots of the group]
     pdl_wait();
     pdl_trigger();
     const int nb = l / 16, K64 = l / 64;
     const int tpb = blockDim.x / nb;                   // tokens per block (>= 1)
     const int64_t t_first = static_cast<int64_t>(blockIdx.x) * tpb;
-    for (int i = threadIdx.x; i < tpb * k; i += blockDim.x) {
-        const int64_t slot = t_first * k + i;
-        if (t_first + i / k < T) {
+    const int spg = (k + gridDim.y - 1) / gridDim.y;   // slots per group
+    const int j0 = blockIdx.y * spg, nj = max(0, min(k, j0 + spg) - j0);
+    for (int i = threadIdx.x; i < tpb * nj; i += blockDim.x) {
+        const int64_t slot = (t_first + i / nj) * k + j0 + i % nj;
+        if (t_first + i / nj < T) {
             const int row = slot_row(idx, slot_off, seg_start, slot);
             rows_s[i] = row;
             row_slot[row] = static_cast<int32_t>(slot);
@@ -55,17 +59,19 @@ __global__ void __launch_bounds__(256) z_finalize_kernel(
     uint32_t zb[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) zb[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
-    if (z_out) {
+    if (z_out && blockIdx.y == 0) {
         uint4 *zo = reinterpret_cast<uint4 *>(z_out + i * 16);
         zo[0] = make_uint4(zb[0], zb[1], zb[2], zb[3]);
         zo[1] = make_uint4(zb[4], zb[5], zb[6], zb[7]);
     }
     uint32_t lo, hi;
     const uint32_t s = quant_block16(x, q, lo, hi);
-    reinterpret_cast<uint2 *>(codes)[i] = make_uint2(lo, hi);
-    sf[i] = static_cast<uint8_t>(s);
-    for (int j = 0; j < k; ++j) {
-        const int row = rows_s[tl * k + j];
+    if (blockIdx.y == 0) {
+        reinterpret_cast<uint2 *>(codes)[i] = make_uint2(lo, hi);
+        sf[i] = static_cast<uint8_t>(s);
+    }
+    for (int j = 0; j < nj; ++j) {
+        const int row = rows_s[tl * nj + j];
         if (a_bf16) {       // W4A16: the bf16 z itself goes to the expert segments
             uint4 *o = reinterpret_cast<uint4 *>(a_bf16 + static_cast<int64_t>(row) * l + b * 16);
             o[0] = make_uint4(zb[0], zb[1], zb[2], zb[3]);

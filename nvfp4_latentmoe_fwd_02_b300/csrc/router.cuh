@@ -157,42 +157,6 @@ __device__ __forceinline__ uint64_t shfl_xor64(uint64_t v, int m) {
     return (static_cast<uint64_t>(hi) << 32) | lo;
 }
 
-// Descending bitonic sort of the warp's 128 keys, 4 per lane; key r of lane L sits at position
-// 4L + r.
-__device__ __forceinline__ void warp_sort128_desc(uint64_t (&a)[4], int lane) {
-#pragma unroll
-    for (int k = 2; k <= 128; k <<= 1) {
-#pragma unroll
-        for (int j = k >> 1; j >= 1; j >>= 1) {
-            if (j >= 4) {
-                const int m = j >> 2;                      // partner lane distance
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int i = 4 * lane + r;
-                    const uint64_t o = shfl_xor64(a[r], m);
-                    const bool lower = (i & j) == 0;       // i < partner
-                    const bool desc = (i & k) == 0;        // this run sorts descending
-                    const bool keep_max = (lower == desc);
-                    a[r] = keep_max ? (a[r] > o ? a[r] : o) : (a[r] < o ? a[r] : o);
-                }
-            } else {
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int pr = r ^ j;
-                    if (pr > r) {
-                        const int i = 4 * lane + r;
-                        const bool desc = (i & k) == 0;
-                        const uint64_t x = a[r], y = a[pr];
-                        const bool swap = desc ? (x < y) : (x > y);
-                        a[r] = swap ? y : x;
-                        a[pr] = swap ? x : y;
-                    }
-                }
-            }
-        }
-    }
-}
-
 // Two descending 32-lists (lane i holds element i of each): the top 32 of their union,
 // descending, lane i holding element i.
 __device__ __forceinline__ uint64_t merge_top32(uint64_t a_i, uint64_t b_rev_i, int lane) {
