@@ -18,6 +18,8 @@
 //              spend their time in flight from HBM, not waiting for the decode;
 //   act ring:  per chunk the NT x 64 bf16 activation boxes of the four 64-element blocks (read
 //              by the MMAs, released by their commit).
+// Both rings have a multiple of G stages, so that each stage is filled for and consumed by one
+// group only (see W4Cfg).
 //
 // G converter groups (G = 3 for NT = 16, 2 for NT = 32).  Chunk q of the CTA's sequence goes
 // to group q % G: its four converter warps (one per TMEM lane quadrant) decode the chunk into
@@ -54,8 +56,14 @@ struct W4Cfg {
     static constexpr int kActBlock = NT * 128;              // NT rows x 64 bf16 (one SW128 box)
     static constexpr int kActStage = 4 * kActBlock;
     static constexpr int kStagesC = NT == 16 ? 9 : 8;
-    static constexpr int kStagesA = NT == 16 ? 5 : 4;
+    static constexpr int kStagesA = NT == 16 ? 6 : 4;
     static constexpr int kBarBytes = 512;
+    // Chunk q fills stage q % S of a ring and is consumed by group q % G.  With S a multiple of G
+    // every stage belongs to one group, whose consumers take its fills in order.  Otherwise a
+    // consumer that is ahead could wait on a stage whose previous fill (another group's chunk)
+    // has not landed yet: the barrier is then one phase short, its parity reads as "complete",
+    // and the MMA would read the stage before its data arrived.
+    static_assert(kStagesC % G == 0 && kStagesA % G == 0, "each ring stage belongs to one group");
     static_assert(kCodeStage % 1024 == 0 && kActStage % 1024 == 0, "stages keep the 1024-byte alignment of the swizzled boxes");
     static_assert(kSlotCol0 + G * 128 <= 512, "TMEM budget");
 };

@@ -26,6 +26,20 @@ def w4(request):
     case.close()
 
 
+def gpu_h_rows(case, T, sample):
+    """The GPU's h rows of the sampled tokens in (token, slot) order, from the expert segments."""
+    d = case.dims
+    moe = case.moe
+    nrows = int(moe.stage("nrows", T, torch.int32).cpu()[0])
+    R = moe.stage("rows", T, torch.int32).numel()
+    rows = moe.stage("rows", T, torch.int32).cpu().numpy()[:nrows]
+    h = moe.stage("h", T, torch.bfloat16).view(R, d.ffn)[:nrows].float().cpu().numpy()
+    counts = moe.stage("counts", T, torch.int32).cpu().numpy()
+    live = real_rows(counts, nrows)
+    pos = {int(sl): i for i, sl in enumerate(rows) if live[i]}
+    return np.stack([h[pos[int(t) * d.k + j]] for t in sample for j in range(d.k)])
+
+
 def check_w4a16(case, T, x, y, sample):
     d = case.dims
     moe = case.moe
@@ -36,14 +50,7 @@ def check_w4a16(case, T, x, y, sample):
     assert np.allclose(w, ref["w"], **w_tol(T))
     z = moe.stage("z", T, torch.bfloat16).view(T, d.l).float().cpu().numpy()[sample]
     assert rel_l2_rows(z, ref["z"]).max() <= TOL_INTER
-    nrows = int(moe.stage("nrows", T, torch.int32).cpu()[0])
-    R = moe.stage("rows", T, torch.int32).numel()
-    rows = moe.stage("rows", T, torch.int32).cpu().numpy()[:nrows]
-    h = moe.stage("h", T, torch.bfloat16).view(R, d.ffn)[:nrows].float().cpu().numpy()
-    counts = moe.stage("counts", T, torch.int32).cpu().numpy()
-    live = real_rows(counts, nrows)
-    pos = {int(sl): i for i, sl in enumerate(rows) if live[i]}
-    hr = np.stack([h[pos[int(t) * d.k + j]] for t in sample for j in range(d.k)])
+    hr = gpu_h_rows(case, T, sample)
     assert rel_l2_rows(hr, ref["h"].reshape(-1, d.ffn)).max() <= TOL_INTER
     c = moe.stage("c", T, torch.bfloat16).view(T, d.l).float().cpu().numpy()[sample]
     assert rel_l2_rows(c, ref["c"]).max() <= TOL_OUT
@@ -75,3 +82,22 @@ def test_ultra_decode_w4a16(ultra_w4, T):
     y = moe.forward(x)
     moe.check()
     check_w4a16(ultra_w4, T, x, y, np.arange(T))
+
+
+@pytest.mark.parametrize("T", [8, 16])
+def test_ultra_decode_w4a16_repeated(ultra_w4, T):
+    """The 16-token-tile decode kernel (three converter groups sharing the rings) run 24 times on
+    the same tokens: every run completes with no bounded wait running out, and every run's h rows
+    and y match the oracle.  An MMA that read a ring stage before its fill had landed would show
+    up here as a wrong h row, or as a timeout, in some run."""
+    moe = ultra_w4.gpu(debug=True)
+    d = ultra_w4.dims
+    x = ultra_w4.tokens(T, seed_offset=900 + T).cuda()
+    sample = np.arange(T)
+    ref = ultra_w4.ol.forward(x.float().cpu().numpy(), quant="w4a16", want=("h", "y"))
+    href = ref["h"].reshape(-1, d.ffn)
+    for run in range(24):
+        y = moe.forward(x)
+        moe.check()
+        assert rel_l2_rows(gpu_h_rows(ultra_w4, T, sample), href).max() <= TOL_INTER, f"run {run}"
+        assert rel_l2_rows(y.float().cpu().numpy(), ref["y"]).max() <= TOL_OUT, f"run {run}"
