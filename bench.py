@@ -616,7 +616,7 @@ def main():
         "csrc_hash": csrc_hash(),
     }
 
-    # ---- the W4A16 form of the same decode step (NVFP4 weights decoded in smem, bf16 z and h)
+    # ---- the W4A16 form of the same decode step (NVFP4 weights decoded on chip, bf16 z and h)
     if not a.no_w4a16:
         import nvfp4_latentmoe_fwd_02_b300 as lm2
         Lw = lmoe_synth.layer(cfg["dims"], cfg["seed"], "cuda", cfg["zipf"])
