@@ -59,6 +59,7 @@ constexpr int kSmallAMaxT = 32;
 // stage): 64-column tiles 6 stages, 128-column tiles 4
 constexpr int kStagesUpF32N = 6, kStagesUpF32W = 4;
 constexpr int kUpF32MaxT = 8;
+constexpr int64_t kSharedFirstMaxT = 1;   // forking forwards up to this T put the shared expert first
 
 inline int kb_for(bool small_a) { return small_a ? 2 : 1; }   // column blocks per stage
 // tile width of the dense (bf16 / fp8) GEMMs: 256 outside decode (fewer operand bytes per output)
@@ -204,10 +205,18 @@ cudaError_t launch_pdl_prio(int prio, void (*kernel)(KArgs...), dim3 grid, dim3 
     cfg.numAttrs = prio != 0 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
+// The priority launch_pdl gives its kernels on this thread (0: the stream's own), set for a
+// stretch of launches by PrioScope.
+thread_local int t_launch_prio = 0;
+struct PrioScope {
+    int saved;
+    explicit PrioScope(int prio) : saved(t_launch_prio) { t_launch_prio = prio; }
+    ~PrioScope() { t_launch_prio = saved; }
+};
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                        Args &&...args) {
-    return launch_pdl_prio(0, kernel, grid, block, smem, s, std::forward<Args>(args)...);
+    return launch_pdl_prio(t_launch_prio, kernel, grid, block, smem, s, std::forward<Args>(args)...);
 }
 // The most urgent launch priority of this device (0 if it has a single priority level).
 int urgent_priority() {
@@ -1288,6 +1297,9 @@ lmoe_status lmoe_forward(lmoe_ctx *c, const void *x, int64_t T, void *y, void *w
     //     beside the routed experts, and joins before the up-projection.
     const bool shared_aux = c->shared_ffn && fork;
     if (c->shared_ffn) {
+        // at T = 1 its 134 MB of FP8 weights outweigh the routed experts' 104 MB: its kernels
+        // are scheduled first (at T = 8 and 64 that ordering was slower)
+        PrioScope shared_prio(shared_aux && T <= kSharedFirstMaxT ? urgent_priority() : 0);
         const cudaStream_t ss = shared_aux ? c->aux : s;
         const int FS = c->shared_ffn;
         const int qg = static_cast<int>(std::min<int64_t>(cdiv(T * d / 16, 256), c->num_sms * 16));
