@@ -22,19 +22,24 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "lmoe_oracle.c")
 _HDR = os.path.join(_HERE, "lmoe_oracle.h")
 _LIB = os.path.join(_HERE, "liboracle.so")
+# A library built from a modified copy of lmoe_oracle.c, loaded in place of liboracle.so: the
+# mutation tests plant one mistake in such a copy and check that a pin fails.
+LIB_ENV = "LMOE_ORACLE_LIB"
 _lock = threading.Lock()
 _lib = None
 
 
-def build(force: bool = False) -> str:
-    """Compile liboracle.so with gcc (no fast-math, no FMA contraction)."""
-    stale = (not os.path.exists(_LIB)) or any(
-        os.path.getmtime(p) > os.path.getmtime(_LIB) for p in (_SRC, _HDR))
+def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
+    """Compile the oracle source `src` (liboracle.so from lmoe_oracle.c by default) with gcc (no
+    fast-math, no FMA contraction); lmoe_oracle.h is taken from beside `src`."""
+    hdr = os.path.join(os.path.dirname(os.path.abspath(src)), "lmoe_oracle.h")
+    stale = (not os.path.exists(out)) or any(
+        os.path.getmtime(p) > os.path.getmtime(out) for p in (src, hdr))
     if force or stale:
         cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
-               "-Wall", "-o", _LIB, _SRC, "-lm", "-lpthread"]
+               "-Wall", "-o", out, src, "-lm", "-lpthread"]
         subprocess.run(cmd, check=True)
-    return _LIB
+    return out
 
 
 class _Layer(C.Structure):
@@ -64,8 +69,7 @@ def lib():
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            L = C.CDLL(_LIB)
+            L = C.CDLL(os.environ.get(LIB_ENV) or build())
             L.oracle_e2m1_value.restype = C.c_double
             L.oracle_e2m1_value.argtypes = [C.c_uint8]
             L.oracle_e4m3_value.restype = C.c_double

@@ -1,0 +1,123 @@
+"""Mutation checks of the oracle's pins (CPU only).
+
+Each case copies oracle/lmoe_oracle.c, plants one plausible mistake in the copy (a wrong
+constant, exponent bias or rounding, a dropped term, a swapped operand or index, a flipped
+sign or tie-break), builds it with the oracle's own compiler flags, and runs the pin files
+that cover that step against the mutant (the oracle package loads the library named by
+oracle.LIB_ENV).  The pins must fail: a mistake they let through would be a gap in what pins
+the oracle to the pages and the mathematics.  A control case builds the unmodified copy the
+same way and must pass the same files.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "lmoe_oracle.c")
+HDR = os.path.join(ROOT, "oracle", "lmoe_oracle.h")
+
+FORMATS = ["tests/test_oracle_formats.py"]
+QUANT = ["tests/test_oracle_quant.py"]
+QUANT2D = ["tests/test_oracle_quant2d.py"]
+ROUTER = ["tests/test_oracle_router.py"]
+LAYER = ["tests/test_oracle_layer.py"]
+SHARED = ["tests/test_oracle_shared.py"]
+W4A16 = ["tests/test_oracle_w4a16.py"]
+
+# (name, text in lmoe_oracle.c (unique), its replacement, pin files that must catch it)
+MUTANTS = [
+    ("e2m1_exponent_bias",
+     "ldexp(1.0 + 0.5 * m, e - 1);", "ldexp(1.0 + 0.5 * m, e);", FORMATS),
+    ("e2m1_ties_away_from_zero",
+     "double q = (a < 2.0) ? 0.5 : (a < 4.0 ? 1.0 : 2.0);\n    double r = nearbyint(a / q) * q;",
+     "double q = (a < 2.0) ? 0.5 : (a < 4.0 ? 1.0 : 2.0);\n    double r = floor(a / q + 0.5) * q;", FORMATS),
+    ("e4m3_exponent_bias",
+     "return sign | (uint8_t)(((E + 7) << 3) | m);", "return sign | (uint8_t)(((E + 8) << 3) | m);", FORMATS),
+    ("bf16_nine_significant_bits",
+     "int qe = (e - 1) - 7;", "int qe = (e - 1) - 8;", FORMATS),
+    ("nvfp4_tensor_scale_without_e2m1_max",
+     "const float S = 2688.0f;\n    float s_enc = S / amax;\n    float s_dec = amax / S;\n    quant_job j",
+     "const float S = 448.0f;\n    float s_enc = S / amax;\n    float s_dec = amax / S;\n    quant_job j", QUANT),
+    ("nvfp4_nibble_order",
+     "codes[8 * b + i / 2] = (uint8_t)(q0 | (q1 << 4));", "codes[8 * b + i / 2] = (uint8_t)(q1 | (q0 << 4));",
+     QUANT),
+    ("nvfp4_block_dot_factor",
+     "acc += (double)dot * 0.25 * g_e4m3[sfa[b]] * g_e4m3[sfb[b]];",
+     "acc += (double)dot * 0.5 * g_e4m3[sfa[b]] * g_e4m3[sfb[b]];", QUANT),
+    ("nvfp4_2d_amax_over_half_the_rows",
+     "for (int r = 0; r < 16; ++r)\n                for (int i = 0; i < 16; ++i) {",
+     "for (int r = 0; r < 8; ++r)\n                for (int i = 0; i < 16; ++i) {", QUANT2D),
+    ("router_ties_to_higher_index",
+     "if (best < 0 || lg[e] > lg[best]) best = e;", "if (best < 0 || lg[e] >= lg[best]) best = e;", ROUTER),
+    ("router_weights_not_normalised",
+     "double v = exp((double)lg[idx[j]] - m) / s;", "double v = exp((double)lg[idx[j]] - m);", ROUTER),
+    ("router_logit_unfused_multiply_add",
+     "for (int i = c; i < c + 64; ++i) p = fmaf(x[i], w[i], p);",
+     "for (int i = c; i < c + 64; ++i) p = p + x[i] * w[i];", ROUTER),
+    ("layer_down_projection_transposed",
+     "for (int i = 0; i < d; ++i) s += (double)xt[i] * (double)wr[i];\n            z64[j]",
+     "for (int i = 0; i < d; ++i) s += (double)xt[i] * (double)L->w_down[(int64_t)i * l + j];\n            z64[j]",
+     LAYER),
+    ("layer_latent_up_without_relu",
+     "L->w1_sf[e] + (int64_t)f * (l / 16), l);\n                    double r = u > 0.0 ? u : 0.0;\n"
+     "                    hf[f] = (float)oracle_round_bf16(r * r);\n                    if (hf[f] > hmax)",
+     "L->w1_sf[e] + (int64_t)f * (l / 16), l);\n                    double r = u;\n"
+     "                    hf[f] = (float)oracle_round_bf16(r * r);\n                    if (hf[f] > hmax)", LAYER),
+    ("layer_combine_without_routing_weight",
+     "L->w2_sf[e] + (int64_t)j * (F / 16), F);\n                    c64[j] += w64[jj] * o;\n                }\n                if (O->hq_codes)",
+     "L->w2_sf[e] + (int64_t)j * (F / 16), F);\n                    c64[j] += o;\n                }\n                if (O->hq_codes)",
+     LAYER),
+    ("layer_shared_output_subtracted",
+     "s += ss64[j];", "s -= ss64[j];", SHARED),
+    ("shared_up_without_relu",
+     "double u = a1 * oracle_fp8_dot(xq, L->ws1_codes + (int64_t)f * d, d);\n            double r = u > 0.0 ? u : 0.0;",
+     "double u = a1 * oracle_fp8_dot(xq, L->ws1_codes + (int64_t)f * d, d);\n            double r = u;", SHARED),
+    ("fp8_scale_from_wrong_maximum",
+     "fp8_job j = {src, 448.0f / amax, codes};", "fp8_job j = {src, 240.0f / amax, codes};", SHARED),
+    ("w4a16_block_scale_dropped",
+     "acc += blk * g_e4m3[sfb[b]];", "acc += blk;", W4A16),
+]
+
+
+def _build_variant(tmp_path, text):
+    d = tmp_path / "src"
+    d.mkdir()
+    shutil.copy(HDR, d / "lmoe_oracle.h")
+    src = d / "lmoe_oracle.c"
+    src.write_text(text)
+    return oracle.build(force=True, src=str(src), out=str(tmp_path / "liboracle_variant.so"))
+
+
+def _run_pins(lib_path, files):
+    env = dict(os.environ)
+    env[oracle.LIB_ENV] = lib_path
+    cmd = [sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", "-m", "not gpu", *files]
+    return subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+
+
+def test_mutation_sites_are_unique():
+    text = open(SRC).read()
+    for name, before, _, _ in MUTANTS:
+        assert text.count(before) == 1, name
+
+
+def test_unmodified_copy_passes_the_pins(tmp_path):
+    lib = _build_variant(tmp_path, open(SRC).read())
+    files = sorted({f for *_, fs in MUTANTS for f in fs})
+    r = _run_pins(lib, files)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
+
+@pytest.mark.parametrize("name,before,after,files", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(tmp_path, name, before, after, files):
+    text = open(SRC).read()
+    assert text.count(before) == 1
+    lib = _build_variant(tmp_path, text.replace(before, after))
+    r = _run_pins(lib, files)
+    # exit status 1: the run completed and at least one pin failed (a crash would be another status)
+    assert r.returncode == 1, f"mutant {name} passed the pins:\n" + r.stdout[-3000:] + r.stderr[-2000:]

@@ -76,6 +76,20 @@ def test_canonical_two_level_order_worked_example():
     assert lg[0, 0] == 1.0
 
 
+def test_chunk_chain_is_fused_multiply_add_worked_example():
+    # One chunk: p = fma(1, -1, 0) = -1, then fma(x1, w1, p) with x1 = w1 = 1 + 2^-12.  The exact
+    # product is 1 + 2^-11 + 2^-24, and a fused multiply-add adds it to -1 with a single
+    # rounding: 2^-11 + 2^-24, exact in fp32.  Rounding the product first (2^-24 is half an ulp
+    # of 1, and the tie goes to the even neighbour 1 + 2^-11) and then adding would give 2^-11.
+    # Worked by hand from the definition of the chunk's fmaf chain.
+    x = np.zeros((1, 64), np.float32)
+    W = np.zeros((1, 64), np.float32)
+    x[0, 0], W[0, 0] = 1.0, -1.0
+    x[0, 1] = W[0, 1] = 1.0 + 2.0 ** -12
+    lg, _, _, _ = oracle.router(x, W, None, 1)
+    assert lg[0, 0] == np.float32(2.0 ** -11 + 2.0 ** -24)
+
+
 def test_canonical_chunked_fp32_order_worked_example():
     # d = 192: three chunks of 64.  Chunk sums p0 = 2^24, p1 = 1, p2 = -2^24 (each exact).
     # Canonical order ((0 + p0) + p1) + p2 = (2^24 + 1 -> 2^24 in fp32) - 2^24 = 0, whereas
