@@ -98,3 +98,17 @@ def test_bf16_rounding_matches_torch():
     want = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
     got = np.array([oracle.round_bf16(float(x)) for x in v])
     assert np.array_equal(got, want)
+
+
+def test_bf16_rounding_at_the_ends_of_its_range_matches_torch():
+    # the largest bf16 value (255/128) 2^127, whose ulp is 2^120: a quarter ulp above it rounds
+    # down to it, half an ulp above is a tie that goes to the even neighbour 2^128 (overflow to
+    # inf); and the subnormal ties around the smallest bf16 subnormal 2^-133
+    top = 255.0 / 128.0 * 2.0 ** 127
+    vals = [top, top + 2.0 ** 118, top + 2.0 ** 119, top + 3 * 2.0 ** 118, 3.4028234663852886e38,
+            2.0 ** -133, 2.0 ** -134, 3 * 2.0 ** -134, 5 * 2.0 ** -134, 2.0 ** -127, 2.0 ** -126 - 2.0 ** -140]
+    v = np.array(vals + [-x for x in vals], np.float32)
+    want = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([oracle.round_bf16(float(x)) for x in v])
+    assert np.array_equal(got, want)
+    assert want[0] == top and want[1] == top and np.isinf(want[2]) and want[6] == 0.0

@@ -63,6 +63,22 @@ def test_identity_projections_reduce_to_textbook_moe():
     assert np.allclose(res["y64"], y_ref, rtol=1e-5, atol=1e-6 * np.abs(y_ref).max())
 
 
+def test_router_bias_decides_the_selection():
+    # A bias of +1000 on two experts (k = 2) outweighs every logit of this layer (all below 100
+    # in magnitude), so every token selects exactly those two; moving the bias moves the choice.
+    dims = lmoe_synth.Dims(d=64, l=64, E=8, k=2, ffn=32)
+    _, (wd, wu, Wr, b, w1, w2) = _layer(dims, 13)
+    x = lmoe_synth.tokens(16, dims.d, 13).float().numpy()
+    assert np.abs(x.astype(np.float64) @ Wr.T).max() < 100
+    for hot in ((2, 5), (0, 7)):
+        bias = np.zeros(dims.E, np.float32)
+        bias[list(hot)] = 1000.0
+        ol = oracle.OracleLayer(dims.d, dims.l, dims.E, dims.k, dims.ffn, wd, wu, Wr.astype(np.float32),
+                                bias, lambda e: (w1[e], w2[e]))
+        res = ol.forward(x, quant=False, want=("y64",))
+        assert np.array_equal(res["idx"], np.tile(np.array(hot, np.int32), (16, 1)))
+
+
 def test_single_expert_reduces_to_plain_relu2_ffn():
     dims = lmoe_synth.Dims(d=128, l=32, E=1, k=1, ffn=64)
     ol, (wd, wu, Wr, b, w1, w2) = _layer(dims, 12)

@@ -81,6 +81,39 @@ MUTANTS = [
      "fp8_job j = {src, 448.0f / amax, codes};", "fp8_job j = {src, 240.0f / amax, codes};", SHARED),
     ("w4a16_block_scale_dropped",
      "acc += blk * g_e4m3[sfb[b]];", "acc += blk;", W4A16),
+    ("w4a16_h_not_rounded_to_bf16",
+     "hf[f] = (float)oracle_round_bf16(r * r);\n                }\n                for (int j = 0; j < l; ++j) {\n"
+     "                    double o = (double)L->w2_sdec[e] *",
+     "hf[f] = (float)(r * r);\n                }\n                for (int j = 0; j < l; ++j) {\n"
+     "                    double o = (double)L->w2_sdec[e] *", W4A16),
+    ("e4m3_subnormal_spacing",
+     "q = ldexp(1.0, -9);", "q = ldexp(1.0, -10);", FORMATS),
+    ("bf16_overflow_threshold",
+     "const double bf16_max = ldexp(255.0 / 128.0, 127);", "const double bf16_max = ldexp(254.0 / 128.0, 127);",
+     FORMATS),
+    ("router_slots_in_rank_order",
+     "if (taken[e]) idx[n++] = e;", "if (taken[e]) idx[n++] = sel[n];", ROUTER),
+    ("router_counts_drop_the_last_slot",
+     "for (int64_t i = 0; i < T * k; ++i) counts[idx[i]]++;",
+     "for (int64_t i = 0; i + 1 < T * k; ++i) counts[idx[i]]++;", ROUTER),
+    ("layer_router_bias_dropped",
+     "(L->b_router ? L->b_router[e] : 0.0f);", "0.0f;", LAYER),
+    ("layer_z_quantized_with_a_per_token_amax",
+     "oracle_quantize_nvfp4(zf, 1, l, J->amax_z, zc, zs, &sd, 1);",
+     "oracle_quantize_nvfp4(zf, 1, l, -1.0f, zc, zs, &sd, 1);", LAYER),
+    ("layer_h_requantized_with_the_z_scale",
+     "oracle_quantize_nvfp4(hf, 1, F, J->amax_h, hc, hs, NULL, 1);",
+     "oracle_quantize_nvfp4(hf, 1, F, J->amax_z, hc, hs, NULL, 1);", LAYER),
+    ("layer_c_not_rounded_to_bf16",
+     "cin[j] = J->quant ? oracle_round_bf16(c64[j]) : c64[j];", "cin[j] = c64[j];", LAYER),
+    ("layer_up_projection_transposed",
+     "for (int i = 0; i < l; ++i) s += cin[i] * (double)wr[i];",
+     "for (int i = 0; i < l; ++i) s += cin[i] * (double)L->w_up[(int64_t)i * d + j];", LAYER),
+    ("fp8_dot_units",
+     "return ldexp((double)acc, -18);", "return ldexp((double)acc, -17);", SHARED),
+    ("shared_h_quantized_with_the_x_scale",
+     "oracle_quantize_fp8(hf, F, amax_hs, hq, &sdh, 1);", "oracle_quantize_fp8(hf, F, amax_xs, hq, &sdh, 1);",
+     SHARED),
 ]
 
 

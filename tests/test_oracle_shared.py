@@ -68,7 +68,7 @@ def test_fp8_dot_is_exact():
     assert oracle.fp8_dot(a, a) == 8192 * 448.0 ** 2
 
 
-def _selection_case(d=64, F=40, T=12, seed=5):
+def _selection_case(d=64, F=40, T=12, seed=5, amax_xs=7.0, amax_hs=7.0):
     """Closed-form shared expert: returns (layer, x, expected h, expected s)."""
     rng = np.random.default_rng(seed)
     pi1 = rng.permutation(d - 1)[:F]                  # f -> column of x (never d - 1)
@@ -92,7 +92,7 @@ def _selection_case(d=64, F=40, T=12, seed=5):
     ol = oracle.OracleLayer(d, 16, 4, 2, 32, L.w_down.float().numpy(), L.w_up.float().numpy(),
                             L.w_router.numpy(), None,
                             lambda e: (L.w1[e].float().numpy(), L.w2[e].float().numpy()),
-                            amax_z=4.0, amax_h=16.0, shared=(ws1, ws2), amax_xs=7.0, amax_hs=7.0)
+                            amax_z=4.0, amax_h=16.0, shared=(ws1, ws2), amax_xs=amax_xs, amax_hs=amax_hs)
     return ol, x, h, s
 
 
@@ -109,6 +109,18 @@ def test_shared_expert_selection_closed_form():
     # the unquantized path gives the same exact values here
     r0 = ol.shared_forward(x, quant=False)
     assert np.array_equal(r0["s"], s.astype(np.float32))
+
+
+def test_shared_expert_activation_scales_are_separate():
+    # amax_xs = 3.5 (s_enc 128, s_dec 2^-7) and amax_hs = 7 (s_enc 64, s_dec 2^-6): x * 128 and
+    # h * 64 still lie on the E4M3 grid, so xs_q, hs_q and s stay exact.  Quantizing h with the
+    # x scale instead would saturate h = 4 at 448 / 128 = 3.5.
+    ol, x, h, s = _selection_case(amax_xs=3.5, amax_hs=7.0)
+    assert h.max() == 4.0
+    r = ol.shared_forward(x, quant=True)
+    assert np.array_equal(E4M3[r["xs_q"]] * 2.0 ** -7, x.astype(np.float64))
+    assert np.array_equal(E4M3[r["hs_q"]] * 2.0 ** -6, h)
+    assert np.array_equal(r["s"], s.astype(np.float32))
 
 
 def test_calibrate_shared_closed_form():
