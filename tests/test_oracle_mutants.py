@@ -111,6 +111,27 @@ MUTANTS = [
      "for (int i = 0; i < l; ++i) s += cin[i] * (double)L->w_up[(int64_t)i * d + j];", LAYER),
     ("fp8_dot_units",
      "return ldexp((double)acc, -18);", "return ldexp((double)acc, -17);", SHARED),
+    ("e2m1_saturates_to_four",
+     "if (!(a < 6.0)) return sign | 7;", "if (!(a < 6.0)) return sign | 6;", FORMATS),
+    ("nvfp4_block_amax_without_abs",
+     "float a = fabsf(xb[i]);", "float a = xb[i];", QUANT),
+    ("nvfp4_2d_scale_on_the_first_row_only",
+     "j->sf[(g * 16 + r) * (K / 16) + b] = s;", "if (r == 0) j->sf[(g * 16 + r) * (K / 16) + b] = s;", QUANT2D),
+    ("router_groups_of_eight_chunks",
+     "for (int g = 0; g < d; g += 16 * 64) {\n        float gs = 0.0f;\n        for (int c = g; c < g + 16 * 64 && c < d; c += 64) {",
+     "for (int g = 0; g < d; g += 8 * 64) {\n        float gs = 0.0f;\n        for (int c = g; c < g + 8 * 64 && c < d; c += 64) {",
+     ROUTER),
+    ("router_flat_sum_of_chunks",
+     "            gs = gs + p;\n        }\n        acc = acc + gs;",
+     "            acc = acc + p;\n        }\n        (void)gs;", ROUTER),
+    ("layer_z_not_rounded_to_bf16",
+     "z64[j] = J->quant ? oracle_round_bf16(s) : s;", "z64[j] = s;", LAYER),
+    ("layer_y_not_rounded_to_bf16",
+     "if (O->y) O->y[t * d + j] = (float)(J->quant ? oracle_round_bf16(s) : s);",
+     "if (O->y) O->y[t * d + j] = (float)s;", LAYER),
+    ("w4a16_low_nibble_read_as_high",
+     "blk += (double)a[16 * b + 2 * i] * (0.5 * g_e2m1x2[c & 15]) +",
+     "blk += (double)a[16 * b + 2 * i] * (0.5 * g_e2m1x2[c >> 4]) +", W4A16),
     ("shared_h_quantized_with_the_x_scale",
      "oracle_quantize_fp8(hf, F, amax_hs, hq, &sdh, 1);", "oracle_quantize_fp8(hf, F, amax_xs, hq, &sdh, 1);",
      SHARED),

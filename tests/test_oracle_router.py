@@ -76,6 +76,21 @@ def test_canonical_two_level_order_worked_example():
     assert lg[0, 0] == 1.0
 
 
+def test_group_is_sixteen_chunks_worked_example():
+    # d = 1024: one group of 16 chunks.  Chunks 0, 8 and 9 give 2^24, 1 and -2^24.  In the
+    # group's left-to-right sum 2^24 + 1 rounds back to 2^24 (a tie, to even), then -2^24:
+    # the logit is 0.  Groups of 8 chunks would give G0 = 2^24 and G1 = 1 - 2^24 (exact in
+    # fp32), logit 1.  Worked by hand from the order.
+    d = 1024
+    x = np.zeros((1, d), np.float32)
+    W = np.zeros((1, d), np.float32)
+    x[0, 0], W[0, 0] = 2.0 ** 12, 2.0 ** 12
+    x[0, 8 * 64], W[0, 8 * 64] = 1.0, 1.0
+    x[0, 9 * 64], W[0, 9 * 64] = -(2.0 ** 12), 2.0 ** 12
+    lg, _, _, _ = oracle.router(x, W, None, 1)
+    assert lg[0, 0] == 0.0
+
+
 def test_chunk_chain_is_fused_multiply_add_worked_example():
     # One chunk: p = fma(1, -1, 0) = -1, then fma(x1, w1, p) with x1 = w1 = 1 + 2^-12.  The exact
     # product is 1 + 2^-11 + 2^-24, and a fused multiply-add adds it to -1 with a single
