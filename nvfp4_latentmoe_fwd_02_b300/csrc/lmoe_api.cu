@@ -273,6 +273,7 @@ struct lmoe_ctx {
     float alpha_s1, alpha_s2, s_enc_hs;
     CUtensorMap tm_ws1, tm_ws2, tm_ws1_w, tm_ws2_w;
     unsigned *err;
+    unsigned *err_host;               // pinned: the error word as lmoe_forward_host's graph copied it
     long long wait_limit;             // SM cycles a GEMM pipeline wait may take (<= 0: default)
     int debug;
     void *route_ws;
@@ -480,6 +481,13 @@ lmoe_status check_error_word(lmoe_ctx *c) {
     if (v & kErrTimeout) return LMOE_ETIMEOUT;
     if (v) return LMOE_EDEVICE;
     return LMOE_OK;
+}
+// After a replay of lmoe_forward_host's graph has completed: its last node copied the error
+// word to pinned host memory, so a clear word needs no further device round trip.
+lmoe_status host_error_word(lmoe_ctx *c) {
+    if (*static_cast<volatile unsigned *>(c->err_host) == 0) return LMOE_OK;
+    *c->err_host = 0;
+    return check_error_word(c);
 }
 
 // The router on x.  Small T: canonical chunk-group sums into `scratch`, then top-k, softmax and
@@ -824,6 +832,8 @@ lmoe_status lmoe_create(int d, int l, int E, int k, int ffn, const lmoe_weights 
     CREATE_CUDA(dev_malloc(&c->alpha2, E * 4));
     CREATE_CUDA(dev_malloc(&c->amax_bits, 2 * E * 4));
     CREATE_CUDA(dev_malloc(&c->err, sizeof(unsigned)));
+    CREATE_CUDA(cudaMallocHost(reinterpret_cast<void **>(&c->err_host), sizeof(unsigned)));
+    *c->err_host = 0;
     CREATE_CUDA(cudaStreamCreateWithFlags(&c->aux, cudaStreamNonBlocking));
     CREATE_CUDA(cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming));
     CREATE_CUDA(cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming));
@@ -982,6 +992,7 @@ void lmoe_destroy(lmoe_ctx *c) {
     if (c->ev_join_s) cudaEventDestroy(c->ev_join_s);
     if (c->aux) cudaStreamDestroy(c->aux);
     if (c->host_exec) cudaGraphExecDestroy(c->host_exec);
+    if (c->err_host) cudaFreeHost(c->err_host);
     delete c;
 }
 
@@ -1398,9 +1409,9 @@ lmoe_status lmoe_forward_host(lmoe_ctx *c, const void *x_host, int64_t T, void *
         c->host_wait_limit == c->wait_limit) {
         LMOE_CUDA(cudaGraphLaunch(c->host_exec, s));
         LMOE_CUDA(cudaStreamSynchronize(s));
-        return check_error_word(c);
+        return host_error_word(c);
     }
-    // capture copy-in + forward + copy-out; if the capture cannot be made (e.g. pageable host
+    // capture copy-in + forward + copy-out (and the error word); if the capture cannot be made (e.g. pageable host
     // memory), run the same work directly
     cudaGraph_t graph = nullptr;
     if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
@@ -1410,6 +1421,8 @@ lmoe_status lmoe_forward_host(lmoe_ctx *c, const void *x_host, int64_t T, void *
     cudaError_t e = cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s);
     lmoe_status st = e == cudaSuccess ? lmoe_forward(c, xd, T, yd, ws, main, stream) : LMOE_ECUDA;
     if (st == LMOE_OK) e = cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s);
+    if (st == LMOE_OK && e == cudaSuccess)
+        e = cudaMemcpyAsync(c->err_host, c->err, sizeof(unsigned), cudaMemcpyDeviceToHost, s);
     const cudaError_t ec = cudaStreamEndCapture(s, &graph);
     if (st == LMOE_EINVAL || st == LMOE_ENOMEM) {        // argument errors: nothing ran
         if (graph) cudaGraphDestroy(graph);
@@ -1426,7 +1439,7 @@ lmoe_status lmoe_forward_host(lmoe_ctx *c, const void *x_host, int64_t T, void *
         c->host_wait_limit = c->wait_limit;
         LMOE_CUDA(cudaGraphLaunch(c->host_exec, s));
         LMOE_CUDA(cudaStreamSynchronize(s));
-        return check_error_word(c);
+        return host_error_word(c);
     }
     if (graph) cudaGraphDestroy(graph);
     cudaGetLastError();                                    // the failed capture's error
