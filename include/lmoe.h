@@ -203,7 +203,8 @@ size_t lmoe_host_workspace_size(const lmoe_ctx *ctx, int64_t T);
 
 /* The forward from and to HOST memory: copies x_host (bf16 [T][d], pinned for best speed) to
  * the device, runs lmoe_forward, copies y back to y_host and synchronizes `stream`.  On a
- * created (non-default) stream the three steps are captured as one CUDA graph, kept in the
+ * created (non-default) stream the three steps, and a copy of the context's error word to
+ * pinned host memory (read after the synchronization), are captured as one CUDA graph, kept in the
  * context and replayed by later calls with the same T, x_host, y_host, ws, ws_bytes, stream,
  * debug flag and wait limit (the host buffers' contents are read and written at each
  * replay); any other call captures anew.  A call with LMOE_FAULT set runs the steps directly
