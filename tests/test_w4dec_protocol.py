@@ -24,6 +24,8 @@ import re
 
 import pytest
 
+from protocol_model import Bar, Violation, schedule
+
 HDR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                    "nvfp4_latentmoe_fwd_02_b300", "csrc", "w4dec.cuh")
 
@@ -38,36 +40,6 @@ def kernel_config(nt):
         return int(m.group(1) if nt == 16 else m.group(2))
 
     return pick("G"), pick("kStagesC"), pick("kStagesA")
-
-
-class Violation(Exception):
-    pass
-
-
-class Bar:
-    """An mbarrier: `count` arrivals and a zero transaction count complete a phase."""
-
-    def __init__(self, count):
-        self.count, self.pending, self.tx, self.done = count, count, 0, 0
-
-    def arrive(self, n=1, tx=0):
-        self.tx += tx
-        self.pending -= n
-        if self.pending < 0:
-            raise Violation("more arrivals than the barrier's count in one phase")
-        self._step()
-
-    def complete_tx(self, n):
-        self.tx -= n
-        self._step()
-
-    def _step(self):
-        if self.pending == 0 and self.tx == 0:
-            self.done += 1
-            self.pending = self.count
-
-    def passed(self, parity):
-        return (self.done & 1) != parity
 
 
 def run(G, SC, SA, nch, ntiles, rng):
@@ -174,30 +146,7 @@ def run(G, SC, SA, nch, ntiles, rng):
 
     roles = [code_producer(), act_producer()] + [converters(g) for g in range(G)] + \
             [mma(g) for g in range(G)] + [epilogue()]
-    waits = [None] * len(roles)
-
-    def advance(i):
-        try:
-            waits[i] = next(roles[i])
-        except StopIteration:
-            waits[i] = "done"
-
-    for i in range(len(roles)):
-        advance(i)
-    while True:
-        cands = [("role", i) for i, w in enumerate(waits) if w != "done" and w[0].passed(w[1])]
-        cands += [("tma", k) for k in range(len(tma))] + [("mma", g) for g in range(G) if mmaq[g]]
-        if not cands:
-            if all(w == "done" for w in waits):
-                return
-            raise Violation("deadlock: every role waits and nothing is in flight")
-        kind, k = rng.choice(cands)
-        if kind == "role":
-            advance(k)
-        elif kind == "tma":
-            tma.pop(k)()
-        else:
-            mmaq[k].pop(0)()
+    schedule(roles, tma, mmaq, rng)
 
 
 @pytest.mark.parametrize("nt", [16, 32])
