@@ -132,6 +132,12 @@ MUTANTS = [
     ("w4a16_low_nibble_read_as_high",
      "blk += (double)a[16 * b + 2 * i] * (0.5 * g_e2m1x2[c & 15]) +",
      "blk += (double)a[16 * b + 2 * i] * (0.5 * g_e2m1x2[c >> 4]) +", W4A16),
+    ("calibration_amax_z_signed",
+     "float v = (float)fabs(oracle_round_bf16(s));", "float v = (float)oracle_round_bf16(s);", LAYER),
+    ("calibration_amax_h_from_the_unquantized_layer",
+     "J.L = &Lc; J.x = x; J.quant = 1; J.out = &none;", "J.L = &Lc; J.x = x; J.quant = 0; J.out = &none;", LAYER),
+    ("calibration_shared_amax_x_signed",
+     "float a = fabsf(x[i]);", "float a = x[i];", SHARED),
     ("shared_h_quantized_with_the_x_scale",
      "oracle_quantize_fp8(hf, F, amax_hs, hq, &sdh, 1);", "oracle_quantize_fp8(hf, F, amax_xs, hq, &sdh, 1);",
      SHARED),

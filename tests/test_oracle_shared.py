@@ -130,6 +130,15 @@ def test_calibrate_shared_closed_form():
     assert ah == float(h.max())
 
 
+def test_calibrate_shared_uses_magnitudes():
+    # amax_xs = max |x|: one entry of -3, beyond every other |x| <= 2, sets it
+    ol, x, _, _ = _selection_case(T=20, seed=8)
+    x = x.copy()
+    x[4, 7] = -3.0
+    ax, _ = ol.calibrate_shared(x)
+    assert ax == 3.0
+
+
 def test_layer_composition_with_shared_expert():
     ol, x, _, s = _selection_case(T=10, seed=9)
     # w_up = 0: c Wu^T = 0 and y = bf16(0 + s) = s (s already holds bf16 values)
